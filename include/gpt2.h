@@ -1,0 +1,229 @@
+/* gpt2.h - C ABI of libgpt2.so: one GPT-2 pretraining step on one B300 (sm_103a).
+ *
+ * What the step computes (the pages this follows, by title and section):
+ *   - token + position embedding, pre-LN blocks (LayerNorm -> QKV -> causal
+ *     softmax attention -> projection + residual -> LayerNorm -> 4C GELU MLP +
+ *     residual), final LayerNorm, lm_head tied to wte over a vocabulary padded
+ *     50257 -> 50304, mean cross-entropy over all B*T positions:
+ *     "Let's reproduce GPT-2 (124M)" wiki page, "Training recipe details"
+ *     (weight tying, 1/sqrt(2N) residual init) and "GPU optimisation ladder"
+ *     (FlashAttention, vocab padding); qntz.me nanoGPT page (block contents,
+ *     init loss ln V); llm.c 1558M article run log (parameter layout, bf16
+ *     params/grads with fp32 master weights and AdamW state);
+ *   - global-norm gradient clip and AdamW(beta1, beta2, eps) with decoupled weight
+ *     decay on the 2-D matrices only: wiki page "Training recipe details";
+ *     llm.c article "Parameter guide" (-c 0.1 decays 2-D weights only).
+ *
+ * Conventions for every call:
+ *   - Pointers named d_* or documented as device pointers are CUDA device
+ *     addresses; h_* are host addresses.  The library never allocates device
+ *     memory: the caller owns the arena and all I/O buffers.
+ *   - All GPU work is enqueued on the caller's stream (a cudaStream_t passed
+ *     as void*; NULL = legacy default stream).  Calls do not synchronise except
+ *     where a host output (h_loss, h_norm, gpt2_get_tensor to host,
+ *     gpt2_sync_status) is requested.
+ *   - Every function returns GPT2_OK (0) or a negative status below; shape and
+ *     pointer errors are detected on the host before anything is enqueued.
+ *   - Results are bitwise reproducible run to run on the same device.
+ *
+ * Parameter order (canonical flat fp32 vector, Linear weights [out, in]):
+ *   wte[Vpad,C] wpe[T,C] ln1w[L,C] ln1b[L,C] qkvw[L,3C,C] qkvb[L,3C]
+ *   attprojw[L,C,C] attprojb[L,C] ln2w[L,C] ln2b[L,C] fcw[L,4C,C] fcb[L,4C]
+ *   fcprojw[L,C,4C] fcprojb[L,C] lnfw[C] lnfb[C]
+ *   total N = Vpad*C + T*C + L*(12C^2 + 13C) + 2C  (1557686400 for L=48, C=1600,
+ *   Vpad=50304, T=1024, as printed in the llm.c 1558M run log).
+ */
+#ifndef GPT2_B300_H
+#define GPT2_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum gpt2_status {
+  GPT2_OK = 0,
+  GPT2_E_INVAL = -1,      /* bad shape, size, alignment or null pointer */
+  GPT2_E_STATE = -2,      /* call out of order (forward -> backward -> clip_adamw) */
+  GPT2_E_TOKEN = -3,      /* a token or target id was outside [0, V); it was clamped to 0 */
+  GPT2_E_CUDA = -4,       /* a CUDA runtime call failed (see gpt2_last_cuda_error) */
+  GPT2_E_TIMEOUT = -5,    /* a bounded wait inside a pipelined kernel expired */
+  GPT2_E_NONFINITE = -6,  /* the loss or the gradient norm is not finite */
+  GPT2_E_UNSUPPORTED = -7 /* shape valid but outside what this build handles */
+};
+
+enum gpt2_precision {
+  GPT2_FP32 = 0, /* fp32 params, activations and grads; CUDA-core GEMMs (parity mode) */
+  GPT2_BF16 = 1  /* bf16 params/activations/grads, fp32 master + AdamW state; tcgen05 GEMMs */
+};
+
+enum gpt2_tensor {
+  GPT2_PARAMS = 0, /* working parameters (bf16 in GPT2_BF16 mode) */
+  GPT2_GRADS = 1,  /* parameter gradients of the last backward */
+  GPT2_ADAM_M = 2, /* AdamW first moment (fp32) */
+  GPT2_ADAM_V = 3, /* AdamW second moment (fp32) */
+  GPT2_MASTER = 4  /* fp32 master weights (same as PARAMS in GPT2_FP32 mode) */
+};
+
+/* Kernel classes of the per-region timing (gpt2_profile). */
+enum gpt2_kernel_class {
+  GPT2_K_GEMM = 0,      /* every Linear incl. the fused classifier logits (tensor cores) */
+  GPT2_K_SPLITK = 1,    /* fp32 split-K partial reduction of the weight-gradient GEMMs */
+  GPT2_K_ATTN_FWD = 2,  /* fused causal attention forward */
+  GPT2_K_ATTN_BWD = 3,  /* rowsum(dO*O) + dK/dV + dQ kernels */
+  GPT2_K_LN_FWD = 4,
+  GPT2_K_LN_BWD = 5,    /* incl. the fixed-order dgamma/dbeta reduction */
+  GPT2_K_CE = 6,        /* statistics merge, mean loss, dlogits in place */
+  GPT2_K_ENCODER = 7,   /* id checks + gather (forward), sort + scatter (backward) */
+  GPT2_K_BIAS_GRAD = 8, /* bias gradients (column sums) */
+  GPT2_K_NORM = 9,      /* global gradient norm */
+  GPT2_K_ADAMW = 10,    /* fused clip + AdamW + bf16 copy */
+  GPT2_K_COUNT = 11
+};
+
+typedef struct gpt2 gpt2_t;
+
+/* Number of parameters N (canonical order above). */
+size_t gpt2_num_params(int L, int C, int Vpad, int T);
+
+/* Bytes of device memory gpt2_create needs for this shape (B = sequences per
+ * step, T = sequence length = number of positions in wpe).  Constant for the
+ * life of the handle: nothing is allocated afterwards. 0 on invalid shape. */
+size_t gpt2_arena_bytes(int L, int H, int C, int V, int Vpad, int T, int B, int precision);
+
+/* Create a step driver over a caller-owned device arena of >= gpt2_arena_bytes
+ * bytes (256-byte aligned).  Requirements: C % H == 0, C % 8 == 0, Vpad >= V,
+ * Vpad % 8 == 0, B*T <= 16384; GPT2_BF16 additionally needs head size C/H == 64
+ * and C <= 2048; GPT2_FP32 needs C/H <= 128 and C <= 1024.  Parameters start
+ * at zero: call gpt2_set_params before the first step. */
+int gpt2_create(int L, int H, int C, int V, int Vpad, int T, int B, int precision, void* d_arena,
+                size_t arena_bytes, void* stream, gpt2_t** out);
+void gpt2_destroy(gpt2_t* h);
+int gpt2_set_stream(gpt2_t* h, void* stream);
+
+/* Load N fp32 parameters (canonical order) from host (on_device = 0) or device
+ * memory; in GPT2_BF16 mode they become the fp32 master copy and the working
+ * bf16 copy is their round-to-nearest-even.  Zeroes the AdamW moments. */
+int gpt2_set_params(gpt2_t* h, const float* params, int on_device);
+
+/* Copy one state tensor (enum gpt2_tensor) as N fp32 values to dst (host or device). */
+int gpt2_get_tensor(gpt2_t* h, int which, float* dst, int dst_on_device);
+
+/* Forward pass and loss.  d_tokens / d_targets: device int32 [B, T] (copied
+ * into the arena, so they may be reused after the call is enqueued).  The
+ * fused classifier also turns the logits into dlogits in place, so the next
+ * gpt2_backward needs no other input.  The mean loss lands in device memory
+ * (gpt2_device_loss); h_loss, if not NULL, receives it after a stream sync,
+ * and then a clamped token id is reported as GPT2_E_TOKEN. */
+int gpt2_forward(gpt2_t* h, const int32_t* d_tokens, const int32_t* d_targets, float* h_loss);
+
+/* Backward pass of the last forward: writes every parameter gradient. */
+int gpt2_backward(gpt2_t* h);
+
+/* Global-norm clip to max_norm (scale = max_norm / norm when norm > max_norm)
+ * followed by AdamW at step t (step_t >= 1; step_t = 0 takes t from a device
+ * counter that each call increments and gpt2_set_params resets, so a CUDA
+ * graph of the step stays correct across replays): m = b1 m + (1-b1) g, v = b2 v + (1-b2) g^2,
+ * w -= lr (m/(1-b1^t) / (sqrt(v/(1-b2^t)) + eps) + weight_decay * w) with the
+ * decay applied to wte, wpe, qkvw, attprojw, fcw, fcprojw only.  The norm
+ * stays on the device; h_norm, if not NULL, receives it after a stream sync. */
+int gpt2_clip_adamw(gpt2_t* h, float lr, float beta1, float beta2, float eps, float weight_decay,
+                    float max_norm, int step_t, float* h_norm);
+
+/* One whole step from host buffers: copies h_tokens / h_targets (int32 [B, T],
+ * preferably pinned) to the device, runs forward, backward, clip + AdamW, and
+ * copies the loss and gradient norm back (h_loss / h_norm may be NULL).
+ * Synchronises the stream. */
+int gpt2_train_step_host(gpt2_t* h, const int32_t* h_tokens, const int32_t* h_targets, float lr,
+                         float beta1, float beta2, float eps, float weight_decay, float max_norm,
+                         int step_t, float* h_loss, float* h_norm);
+
+/* Device addresses of the last loss (fp32) and of {norm, clip scale} (fp32[2]). */
+const float* gpt2_device_loss(gpt2_t* h);
+const float* gpt2_device_norm(gpt2_t* h);
+
+/* Per-region timing: while on, every kernel group the step issues is bracketed
+ * by CUDA events on the stream (do not capture a graph while it is on).  `on`
+ * clears earlier records.  gpt2_profile_read synchronises and returns, for one
+ * enum gpt2_kernel_class, the number of regions, their summed milliseconds and
+ * their summed algorithmic flops and bytes. */
+int gpt2_profile(gpt2_t* h, int on);
+int gpt2_profile_read(gpt2_t* h, int kernel_class, int* regions, double* ms, double* flops,
+                      double* bytes);
+
+/* Synchronise the stream, read and clear the device status word; returns
+ * GPT2_OK, GPT2_E_TOKEN, GPT2_E_TIMEOUT or GPT2_E_NONFINITE. */
+int gpt2_sync_status(gpt2_t* h);
+
+const char* gpt2_strerror(int status);
+/* Text of the last CUDA error seen by any call in this process. */
+const char* gpt2_last_cuda_error(void);
+
+/* ---------------------------------------------------------------- standalone kernels
+ * Causal attention over bf16 tensors, head size d = 64, fp32 accumulation,
+ * softmax scale `scale`.  Element (b, h, t, i) of q, k, v, dq, dk, dv is at
+ * b*sb + h*sh + t*st + i; of o and dO at b*osb + h*osh + t*ost + i (elements;
+ * all strides multiples of 8, pointers 16-byte aligned).  lse: fp32 [B, H, T],
+ * natural-log sum of exp of the scaled, masked scores (keys j <= query t).
+ * The T x T matrix is never stored. */
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int T,
+             int d, long long sb, long long sh, long long st, long long osb, long long osh,
+             long long ost, float scale, void* stream);
+/* Gradients of attn_fwd; workspace >= attn_workspace_bytes(B, H, T) device bytes. */
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+             const void* dO, void* dq, void* dk, void* dv, int B, int H, int T, int d, long long sb,
+             long long sh, long long st, long long osb, long long osh, long long ost, float scale,
+             void* workspace, size_t workspace_bytes, void* stream);
+size_t attn_workspace_bytes(int B, int H, int T);
+
+/* Tied lm_head + mean cross-entropy, fused: logits = x w^T (x bf16 [M, C],
+ * w bf16 [Vpad, C]; columns >= V excluded from the softmax), loss = mean over
+ * rows of lse - logit[target]; then dlogits = (softmax - onehot) / M,
+ * dx = dlogits w (bf16 [M, C]) and dw = dlogits^T x (bf16 [Vpad, C], pad rows 0).
+ * d_loss: device fp32 scalar.  targets: device int32 [M] in [0, V).
+ * workspace >= classifier_workspace_bytes(M, C, Vpad) (holds the bf16 logits). */
+int classifier_fwd_bwd(const void* x, const void* w, const int32_t* targets, int M, int C, int V,
+                       int Vpad, float* d_loss, void* dx, void* dw, void* workspace,
+                       size_t workspace_bytes, void* stream);
+size_t classifier_workspace_bytes(int M, int C, int Vpad);
+
+/* Token + position embedding on its own (the gather of the forward pass):
+ * x0[b, t, :] = wte[tok[b, t], :] + wpe[t, :] with one fp32 addition and one
+ * rounding to the storage type (precision: GPT2_FP32 -> float, GPT2_BF16 -> bf16
+ * tensors).  tok: device int32 [B, T]; ids outside [0, V) are clamped to 0 and
+ * bit 0 of *d_status (device uint32, may be NULL) is set.  Bit-exact. */
+int gpt2_encoder_fwd(const int32_t* tok, const void* wte, const void* wpe, void* x0, int B, int T,
+                     int C, int V, int precision, void* d_status, void* stream);
+/* The scatter of the backward pass: for every vocab id v, acc = 0; add dx0 rows
+ * (fp32 [B, T, C]) of the positions holding v in ascending position order;
+ * then dwte[v] = dwte[v] + acc (one rounding).  dwpe[t] = sum over b ascending
+ * of dx0[b, t] (written, not accumulated).  workspace >= 8*B*T bytes.  Bit-exact
+ * and deterministic. */
+int gpt2_encoder_bwd(const int32_t* tok, const float* dx0, void* dwte, void* dwpe, int B, int T,
+                     int C, int V, int precision, void* workspace, size_t workspace_bytes,
+                     void* stream);
+
+/* The tensor-core GEMM engine on its own (bf16 in, fp32 accumulate):
+ * D[m, n] = sum_k A(m, k) B(n, k), A(m, k) = A[m*lda + k] (a_mn = 0) or
+ * A[k*lda + m] (a_mn = 1), likewise B(n, k) with b_mn; D bf16 (d_f32 = 0) or
+ * fp32 (d_f32 = 1) with leading dimension ldd.  N, lda, ldb, ldd multiples of 8.
+ * splits > 1 divides K and needs workspace >= splits*M*N*4 bytes (0 = choose). */
+int gemm_bf16(const void* A, const void* B, void* D, int M, int N, int K, long long lda,
+              long long ldb, long long ldd, int a_mn, int b_mn, int d_f32, int splits,
+              void* workspace, size_t workspace_bytes, void* stream);
+
+/* Test hook for the bounded waits: while on, the GEMM's TMA producer skips its
+ * first shared-memory stage, so the MMA thread's wait expires (~2 s) and the
+ * call's status word reports GPT2_E_TIMEOUT.  gemm_bf16_status runs one GEMM
+ * like gemm_bf16 and returns that status after a stream sync. */
+int gpt2_test_set_gemm_poison(int on);
+int gemm_bf16_status(const void* A, const void* B, void* D, int M, int N, int K, long long lda,
+                     long long ldb, long long ldd, int a_mn, int b_mn, void* d_status_word,
+                     void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -109,14 +109,14 @@ def attention_forward(q, k, v, scale):
     O = P v.  Returns (O, P, lse) where lse[b, h, i] = log sum_j exp S[i, j].
     """
     T = q.shape[2]
-    s = np.einsum("bhid,bhjd->bhij", q, k) * scale
+    s = np.matmul(q, np.swapaxes(k, -1, -2)) * scale
     mask = np.triu(np.ones((T, T), dtype=bool), k=1)
     s = np.where(mask, -np.inf, s)
     smax = s.max(axis=-1, keepdims=True)
     e = np.exp(s - smax)
     ssum = e.sum(axis=-1, keepdims=True)
     p = e / ssum
-    o = np.einsum("bhij,bhjd->bhid", p, v)
+    o = np.matmul(p, v)
     lse = (smax + np.log(ssum))[..., 0]
     return o, p, lse
 
@@ -127,11 +127,12 @@ def attention_backward(do, q, k, v, p, scale):
     dV = P^T dO; dP = dO v^T; dS = P * (dP - rowsum(P * dP)); dQ = dS k scale;
     dK = dS^T q scale.  (rowsum(P * dP) equals rowsum(dO * O).)
     """
-    dv = np.einsum("bhij,bhid->bhjd", p, do)
-    dp = np.einsum("bhid,bhjd->bhij", do, v)
+    pt = np.swapaxes(p, -1, -2)
+    dv = np.matmul(pt, do)
+    dp = np.matmul(do, np.swapaxes(v, -1, -2))
     ds = p * (dp - (p * dp).sum(axis=-1, keepdims=True))
-    dq = np.einsum("bhij,bhjd->bhid", ds, k) * scale
-    dk = np.einsum("bhij,bhid->bhjd", ds, q) * scale
+    dq = np.matmul(ds, k) * scale
+    dk = np.matmul(np.swapaxes(ds, -1, -2), q) * scale
     return dq, dk, dv
 
 

@@ -1,0 +1,570 @@
+// bf16 GEMM on the 5th-generation tensor cores (tcgen05) for sm_103a.
+//
+// D[m, n] = sum_k A(m, k) B(n, k), fp32 accumulation in tensor memory.
+// Every Linear of the GPT-2 step maps onto it:
+//   forward   Y  = X W^T      A = X  (K-major), B = W  (K-major)
+//   backward  dX = dY W      A = dY (K-major), B = W  (MN-major)
+//             dW = dY^T X    A = dY (MN-major), B = X (MN-major), split over the rows
+//
+// Structure (one persistent CTA per SM, 6 warps):
+//   warp 0      TMA producer: 128B-swizzled A (128 x 64) and B (256 x 64) tiles
+//               into a 4-stage shared-memory ring, completion on mbarriers;
+//   warp 1      owns 512 TMEM columns (two 128 x 256 fp32 accumulators) and one
+//               thread issues tcgen05.mma (M=128, N=256, K=16) per 16-wide k step,
+//               releasing ring stages and finished accumulators with tcgen05.commit;
+//   warps 2-5   epilogue: tcgen05.ld 32 lanes x 32 columns at a time, fused
+//               bias / residual / GELU / GELU' / cross-entropy statistics, stores.
+// The accumulator double buffer lets the epilogue of tile i overlap the
+// mainloop of tile i+1.  Every wait is bounded (about 2 s of %globaltimer);
+// on expiry the CTA latches ST_TIMEOUT in the status word, the other roles
+// stop, outstanding TMA copies and MMAs are drained and TMEM is freed.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace gpt2k {
+
+namespace {
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int A_TILE = BM * BK * 2;  // 16 KB
+constexpr int B_TILE = BN * BK * 2;  // 32 KB
+constexpr int STAGE_BYTES = A_TILE + B_TILE;
+constexpr int TMEM_COLS = 2 * BN;
+constexpr int NUM_THREADS = 192;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;
+
+struct TcParams {
+  GemmArgs g;
+  int mt, nt, splits, kps, total_kb;
+  uint32_t idesc;
+  float* ws;
+  unsigned* status;
+  int poison;
+};
+
+int g_poison = 0;
+
+// ------------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, "
+      "p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait: false when the CTA aborted or the limit expired (then latches ST_TIMEOUT).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          unsigned* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+      if (status) atomicOr(status, ST_TIMEOUT);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+// Drain wait used on the way out: bounded, ignores the abort flag.
+__device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
+  const unsigned long long t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) return;
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm, uint32_t bar,
+                                            int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+      "%3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\ntcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, "
+      "%3, p;\n}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+        "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+        "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05 format): start address, leading /
+// stride byte offsets (16-byte units), descriptor version 1, 128B swizzle.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo & 0x3FFFFu) >> 4) << 16;
+  d |= (uint64_t)((sbo & 0x3FFFFu) >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// K-major tile: rows of 64 bf16 (128 B), 8-row swizzle atoms 1024 B apart; a
+// 16-wide k step advances the start by 32 B inside the atom.
+// MN-major tile: boxes of 64 MN x 64 K (8 KB) side by side along MN; within a
+// box each K row is 128 B, 8 K rows form a 1024 B atom; LBO = 8 KB (next 64 MN),
+// SBO = 1 KB (next 8 K rows); a 16-wide k step advances the start by 2 KB.
+__device__ __forceinline__ uint64_t operand_desc(uint32_t tile, int mn_major, int kstep) {
+  return mn_major ? sdesc(tile + kstep * 2048, 8192, 1024) : sdesc(tile + kstep * 32, 16, 1024);
+}
+
+__device__ __forceinline__ void store8_bf16(bf16* p, const float* v) {
+  uint4 u;
+  __nv_bfloat162 a = __floats2bfloat162_rn(v[0], v[1]), b = __floats2bfloat162_rn(v[2], v[3]),
+                 c = __floats2bfloat162_rn(v[4], v[5]), d = __floats2bfloat162_rn(v[6], v[7]);
+  u.x = *reinterpret_cast<uint32_t*>(&a);
+  u.y = *reinterpret_cast<uint32_t*>(&b);
+  u.z = *reinterpret_cast<uint32_t*>(&c);
+  u.w = *reinterpret_cast<uint32_t*>(&d);
+  *reinterpret_cast<uint4*>(p) = u;
+}
+__device__ __forceinline__ void load8_bf16(const bf16* p, float* v) {
+  uint4 u = *reinterpret_cast<const uint4*>(p);
+  const bf16* h = reinterpret_cast<const bf16*>(&u);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __bfloat162float(h[i]);
+}
+
+// Epilogue of 32 consecutive columns [n0, n0+32) of row m.
+__device__ __forceinline__ void epilogue_chunk(const TcParams& p, int sp, int m, int n0, float* v,
+                                               float& ce_m, float& ce_s, float& ce_t) {
+  const GemmArgs& g = p.g;
+  const bool row_ok = m < g.M;
+  if (p.splits > 1) {
+    if (!row_ok) return;
+    float* dst = p.ws + ((long long)sp * g.M + m) * g.N;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      int n = n0 + q * 4;
+      if (n < g.N)
+        *reinterpret_cast<float4*>(dst + n) = make_float4(v[q * 4], v[q * 4 + 1], v[q * 4 + 2], v[q * 4 + 3]);
+    }
+    return;
+  }
+  if (g.epi == EPI_CE) {
+    // logits rounded to bf16 are stored and used for the statistics
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = __bfloat162float(__float2bfloat16_rn(v[j]));
+    float cm = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (n0 + j < g.V) cm = fmaxf(cm, v[j]);
+    if (cm > -INFINITY) {
+      float mn = fmaxf(ce_m, cm);
+      float s = (ce_m > -INFINITY) ? ce_s * __expf(ce_m - mn) : 0.f;
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (n0 + j < g.V) s += __expf(v[j] - mn);
+      ce_m = mn;
+      ce_s = s;
+    }
+    if (row_ok) {
+      const int t = g.targets[m];
+      if (t >= n0 && t < n0 + 32) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (n0 + j == t) ce_t = v[j];
+      }
+    }
+  }
+  if (!row_ok) return;
+  if (g.epi == EPI_F32) {
+    float* dst = static_cast<float*>(g.D) + (long long)m * g.ldd;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      int n = n0 + q * 4;
+      if (n < g.N)
+        *reinterpret_cast<float4*>(dst + n) = make_float4(v[q * 4], v[q * 4 + 1], v[q * 4 + 2], v[q * 4 + 3]);
+    }
+    return;
+  }
+  bf16* dst = static_cast<bf16*>(g.D) + (long long)m * g.ldd;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int n = n0 + q * 8;
+    if (n >= g.N) continue;
+    float* w = v + q * 8;
+    if (g.epi == EPI_BIAS || g.epi == EPI_BIAS_RESID || g.epi == EPI_BIAS_GELU) {
+      float b[8];
+      load8_bf16(static_cast<const bf16*>(g.bias) + n, b);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) w[i] += b[i];
+    }
+    if (g.epi == EPI_BIAS_RESID) {
+      float r[8];
+      load8_bf16(static_cast<const bf16*>(g.resid) + (long long)m * g.ldr + n, r);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) w[i] += r[i];
+    }
+    if (g.epi == EPI_GELU_BWD) {
+      float h[8];
+      load8_bf16(static_cast<const bf16*>(g.aux) + (long long)m * g.ldaux + n, h);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) w[i] *= gelu_grad_f(h[i]);
+    }
+    store8_bf16(dst + n, w);
+    if (g.epi == EPI_BIAS_GELU) {
+      float a[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) a[i] = gelu_f(w[i]);
+      store8_bf16(static_cast<bf16*>(g.D2) + (long long)m * g.ldd + n, a);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+              const TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t s_tiles = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], done
+  const uint32_t b_full = smem_u32(bars), b_empty = b_full + 8 * STAGES;
+  const uint32_t b_tfull = b_empty + 8 * STAGES, b_tempty = b_tfull + 16, b_done = b_tempty + 16;
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bars + 2 * STAGES + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * STAGES + 6);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const GemmArgs& g = p.g;
+  const int ntiles = p.mt * p.nt * p.splits;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(b_full + 8 * i, 1);
+      mbar_init(b_empty + 8 * i, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(b_tfull + 8 * i, 1);
+      mbar_init(b_tempty + 8 * i, 128);
+    }
+    mbar_init(b_done, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer
+      int stage = 0;
+      uint32_t phase = 0;
+      int last_par[STAGES];
+#pragma unroll
+      for (int i = 0; i < STAGES; ++i) last_par[i] = -1;
+      bool first = true;
+      for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+        const int n_t = tile % p.nt, m_t = (tile / p.nt) % p.mt, sp = tile / (p.nt * p.mt);
+        const int kb0 = sp * p.kps, kb1 = min(p.total_kb, kb0 + p.kps);
+        bool stop = false;
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait(b_empty + 8 * stage, phase ^ 1, abort_flag, p.status)) { stop = true; break; }
+          if (!(p.poison && first)) {
+            const uint32_t sa = s_tiles + stage * STAGE_BYTES, sb = sa + A_TILE;
+            const uint32_t fb = b_full + 8 * stage;
+            mbar_expect_tx(fb, STAGE_BYTES);
+            if (!g.a_mn) {
+              tma_load_2d(sa, &tmA, fb, kb * BK, m_t * BM);
+            } else {
+              tma_load_2d(sa, &tmA, fb, m_t * BM, kb * BK);
+              tma_load_2d(sa + 8192, &tmA, fb, m_t * BM + 64, kb * BK);
+            }
+            if (!g.b_mn) {
+              tma_load_2d(sb, &tmB, fb, kb * BK, n_t * BN);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 4; ++j) tma_load_2d(sb + j * 8192, &tmB, fb, n_t * BN + j * 64, kb * BK);
+            }
+            last_par[stage] = (int)phase;
+          }
+          first = false;
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+        if (stop) break;
+      }
+      // drain: never leave the CTA with bulk copies still landing in its shared memory
+#pragma unroll
+      for (int i = 0; i < STAGES; ++i)
+        if (last_par[i] >= 0) mbar_wait_drain(b_full + 8 * i, (uint32_t)last_par[i]);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer
+      int stage = 0;
+      uint32_t phase = 0;
+      int abuf = 0;
+      uint32_t aphase = 0;
+      for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+        const int sp = tile / (p.nt * p.mt);
+        const int kb0 = sp * p.kps, kb1 = min(p.total_kb, kb0 + p.kps);
+        if (!mbar_wait(b_tempty + 8 * abuf, aphase ^ 1, abort_flag, p.status)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + abuf * BN;
+        bool stop = false;
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait(b_full + 8 * stage, phase, abort_flag, p.status)) { stop = true; break; }
+          tc_fence_after();
+          const uint32_t sa = s_tiles + stage * STAGE_BYTES, sb = sa + A_TILE;
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            mma_bf16(d_tmem, operand_desc(sa, g.a_mn, k), operand_desc(sb, g.b_mn, k), p.idesc,
+                     (kb > kb0 || k > 0) ? 1u : 0u);
+          }
+          mma_commit(b_empty + 8 * stage);
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+        if (stop) break;
+        mma_commit(b_tfull + 8 * abuf);
+        if (++abuf == 2) { abuf = 0; aphase ^= 1; }
+      }
+      // all MMAs issued by this thread have completed once b_done flips
+      mma_commit(b_done);
+      mbar_wait_drain(b_done, 0);
+    }
+  } else {
+    // ---------------- epilogue warps 2..5 (TMEM lane quadrant = warp % 4)
+    const int quad = warp & 3;
+    const int r_in_tile = quad * 32 + lane;
+    int abuf = 0;
+    uint32_t aphase = 0;
+    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+      const int n_t = tile % p.nt, m_t = (tile / p.nt) % p.mt, sp = tile / (p.nt * p.mt);
+      if (!mbar_wait(b_tfull + 8 * abuf, aphase, abort_flag, p.status)) break;
+      tc_fence_after();
+      const int m = m_t * BM + r_in_tile;
+      float ce_m = -INFINITY, ce_s = 0.f, ce_t = 0.f;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tmem_base + ((uint32_t)(quad * 32) << 16) + abuf * BN + c * 32, r);
+        tmem_ld_wait();
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+        epilogue_chunk(p, sp, m, n_t * BN + c * 32, v, ce_m, ce_s, ce_t);
+      }
+      if (g.epi == EPI_CE && p.splits == 1 && m < g.M) {
+        g.ce_max[(long long)m * g.ce_ld + n_t] = ce_m;
+        g.ce_sum[(long long)m * g.ce_ld + n_t] = ce_s;
+        const int t = g.targets[m];
+        if (t >= n_t * BN && t < n_t * BN + BN) g.ce_tgt[m] = ce_t;
+      }
+      tc_fence_before();
+      mbar_arrive(b_tempty + 8 * abuf);
+      if (++abuf == 2) { abuf = 0; aphase ^= 1; }
+    }
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+typedef CUresult (*PFN_encodeTiled_t)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                      const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                      const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                      CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+PFN_encodeTiled_t get_encode() {
+  static PFN_encodeTiled_t fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_encodeTiled_t>(ptr);
+  }
+  return fn;
+}
+
+// 2-D bf16 tensor map over a row-major [outer, inner] matrix with leading dimension ld.
+bool make_tmap(CUtensorMap* tm, const void* base, long long inner, long long outer, long long ld,
+               int box_inner, int box_outer) {
+  PFN_encodeTiled_t enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_outer};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                   box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+int num_sms() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
+int gemm_tc_poison(int on) {
+  int old = g_poison;
+  g_poison = on;
+  return old;
+}
+
+size_t gemm_tc_ws_bytes(int M, int N, int splits) {
+  return splits > 1 ? (size_t)splits * M * N * sizeof(float) : 0;
+}
+
+int gemm_tc_pick_splits(int M, int N, int K, int sms) {
+  const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+  const int total_kb = (K + BK - 1) / BK;
+  if (tiles >= sms) return 1;
+  int best = 1;
+  double best_score = -1.0;
+  for (int s = 1; s <= 16; ++s) {
+    const int kps = (total_kb + s - 1) / s;
+    if (s > 1 && kps < 4) break;
+    const int work = tiles * s;
+    const int waves = (work + sms - 1) / sms;
+    const double eff = (double)work / ((double)waves * sms);
+    const double score = eff - 0.02 * s;
+    if (score > best_score) { best_score = score; best = s; }
+  }
+  return best;
+}
+
+int gemm_tc_effective_splits(int K, int splits) {
+  const int total_kb = (K + BK - 1) / BK;
+  if (splits < 1) splits = 1;
+  if (splits > total_kb) splits = total_kb;
+  const int kps = (total_kb + splits - 1) / splits;
+  return (total_kb + kps - 1) / kps;
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+int gemm_tc(const GemmArgs& g, int splits, void* ws, size_t ws_bytes, unsigned* status,
+            cudaStream_t s, int reduce) {
+  if (g.M <= 0 || g.N <= 0 || g.K <= 0) return (int)cudaErrorInvalidValue;
+  if (g.N % 8 || g.lda % 8 || g.ldb % 8 || g.ldd % 8) return (int)cudaErrorInvalidValue;
+  if (!aligned16(g.A) || !aligned16(g.B) || !aligned16(g.D)) return (int)cudaErrorInvalidValue;
+  if (g.epi == EPI_BIAS_RESID && (g.ldr % 8 || !aligned16(g.resid))) return (int)cudaErrorInvalidValue;
+  if (g.epi == EPI_GELU_BWD && (g.ldaux % 8 || !aligned16(g.aux))) return (int)cudaErrorInvalidValue;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return (int)e;
+    attr_set = true;
+  }
+  CUtensorMap tmA, tmB;
+  bool ok = g.a_mn ? make_tmap(&tmA, g.A, g.M, g.K, g.lda, 64, 64)
+                   : make_tmap(&tmA, g.A, g.K, g.M, g.lda, 64, BM);
+  ok = ok && (g.b_mn ? make_tmap(&tmB, g.B, g.N, g.K, g.ldb, 64, 64)
+                     : make_tmap(&tmB, g.B, g.K, g.N, g.ldb, 64, BN));
+  if (!ok) return (int)cudaErrorInvalidValue;
+  TcParams p;
+  p.g = g;
+  p.mt = (g.M + BM - 1) / BM;
+  p.nt = (g.N + BN - 1) / BN;
+  p.total_kb = (g.K + BK - 1) / BK;
+  if (splits < 1) splits = 1;
+  if (splits > p.total_kb) splits = p.total_kb;
+  p.kps = (p.total_kb + splits - 1) / splits;
+  p.splits = (p.total_kb + p.kps - 1) / p.kps;
+  if (p.splits > 1) {
+    if (g.epi != EPI_STORE && g.epi != EPI_F32) return (int)cudaErrorInvalidValue;
+    if (!ws || ws_bytes < gemm_tc_ws_bytes(g.M, g.N, p.splits)) return (int)cudaErrorInvalidValue;
+  }
+  p.ws = static_cast<float*>(ws);
+  p.status = status;
+  p.poison = g_poison;
+  // kind::f16 instruction descriptor: D fp32, A/B bf16, operand majors, N >> 3, M >> 4
+  p.idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)g.a_mn << 15) |
+            ((uint32_t)g.b_mn << 16) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+  const int ntiles = p.mt * p.nt * p.splits;
+  int grid = num_sms();
+  if (grid > ntiles) grid = ntiles;
+  k_gemm_tc<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(tmA, tmB, p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return (int)e;
+  if (p.splits > 1 && reduce) {
+    splitk_reduce(g.D, g.epi == EPI_F32, g.ldd, p.ws, p.splits, g.M, g.N, s);
+    e = cudaGetLastError();
+  }
+  return (int)e;
+}
+
+}  // namespace gpt2k

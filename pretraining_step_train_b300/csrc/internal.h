@@ -1,0 +1,128 @@
+// Host-side launchers of the GPT-2 step kernels (internal to libgpt2.so).
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace gpt2k {
+
+// ------------------------------------------------------------------ GEMM
+// D[m, n] = sum_k A(m, k) * B(n, k), fp32 accumulation, then an epilogue.
+// A(m, k) = A[m * lda + k] when a_mn == 0 (K-major), A[k * lda + m] when 1.
+// B(n, k) = B[n * ldb + k] when b_mn == 0 (K-major), B[k * ldb + n] when 1.
+enum EpiKind {
+  EPI_STORE = 0,       // D = acc                          (storage type)
+  EPI_BIAS = 1,        // D = acc + bias[n]
+  EPI_BIAS_RESID = 2,  // D = acc + bias[n] + resid[m, n]
+  EPI_BIAS_GELU = 3,   // D = h = acc + bias[n];  D2 = gelu(h)
+  EPI_GELU_BWD = 4,    // D = acc * gelu'(aux[m, n])
+  EPI_CE = 5,          // D = z = acc; per (row, N tile) max / sum exp over n < V; target logit
+  EPI_F32 = 6,         // D (float*) = acc
+};
+
+struct GemmArgs {
+  const void* A = nullptr; long long lda = 0; int a_mn = 0;
+  const void* B = nullptr; long long ldb = 0; int b_mn = 0;
+  int M = 0, N = 0, K = 0;
+  int epi = EPI_STORE;
+  void* D = nullptr; long long ldd = 0;
+  const void* bias = nullptr;
+  const void* resid = nullptr; long long ldr = 0;
+  void* D2 = nullptr;
+  const void* aux = nullptr; long long ldaux = 0;
+  float* ce_max = nullptr; float* ce_sum = nullptr; int ce_ld = 0;
+  float* ce_tgt = nullptr; const int32_t* targets = nullptr; int V = 0;
+};
+
+// bf16 operands on tcgen05 tensor cores (TMA -> smem ring -> MMA -> TMEM -> epilogue).
+// `splits` > 1 splits K; partials go to `ws` as fp32 [splits][M][N] and a
+// reduction kernel applies EPI_STORE / EPI_F32 (skipped when reduce == 0; the
+// caller then runs splitk_reduce itself).  Returns 0 or a cudaError_t.
+int gemm_tc(const GemmArgs& g, int splits, void* ws, size_t ws_bytes, unsigned* status,
+            cudaStream_t s, int reduce = 1);
+// Splits the call above will actually use for this K (every split non-empty).
+int gemm_tc_effective_splits(int K, int splits);
+size_t gemm_tc_ws_bytes(int M, int N, int splits);
+int gemm_tc_pick_splits(int M, int N, int K, int num_sms);
+int gemm_tc_poison(int on);  // test hook: the TMA producer skips its first stage when on
+int num_sms();
+
+// fp32 operands on CUDA cores (the fp32 parity mode).
+int gemm_simt(const GemmArgs& g, cudaStream_t s);
+
+// ------------------------------------------------------------------ attention
+struct AttnArgs {
+  const void *q = nullptr, *k = nullptr, *v = nullptr;
+  void* o = nullptr; float* lse = nullptr;
+  const void* dO = nullptr;
+  void *dq = nullptr, *dk = nullptr, *dv = nullptr;
+  float* Dbuf = nullptr;  // [B, H, T] rowsum(dO * O)
+  int B = 0, H = 0, T = 0, d = 0;
+  long long sb = 0, sh = 0, st = 0;     // q, k, v, dq, dk, dv (elements)
+  long long osb = 0, osh = 0, ost = 0;  // o, dO
+  float scale = 0.f;
+};
+int attn_fwd_bf16(const AttnArgs& a, cudaStream_t s);
+int attn_bwd_bf16(const AttnArgs& a, cudaStream_t s);
+int attn_fwd_f32(const AttnArgs& a, cudaStream_t s);
+int attn_bwd_f32(const AttnArgs& a, cudaStream_t s);
+
+// ------------------------------------------------------------------ memory-bound
+void check_ids(int32_t* ids, int n, int V, unsigned* status, cudaStream_t s);
+template <typename T>
+void encoder_fwd(T* x0, const int32_t* tok, const T* wte, const T* wpe, int B, int Tn, int C, int V,
+                 unsigned* status, cudaStream_t s);
+template <typename T>
+void layernorm_fwd(T* y, float* mean, float* rstd, const T* x, const T* w, const T* b, int M, int C,
+                   cudaStream_t s);
+// dres (+)= LNbwd(dy); dres_b (optional) = storage copy of dres; dw/db partials then reduced.
+template <typename T>
+void layernorm_bwd(float* dres, T* dres_b, const T* dy, const T* x, const float* mean,
+                   const float* rstd, const T* w, T* dw, T* db, float* partials, int M, int C,
+                   int accumulate, cudaStream_t s);
+size_t layernorm_bwd_partials_floats(int C);
+template <typename T>
+void colsum(T* out, const T* x, int M, int N, long long ld, float* partials, cudaStream_t s);
+size_t colsum_partials_floats(int N);
+template <typename T> void gelu_fwd(T* y, const T* x, long long n, cudaStream_t s);
+template <typename T> void gelu_bwd(T* dx, const T* dy, const T* x, long long n, cudaStream_t s);
+template <typename T> void residual_add(T* y, const T* a, const T* b, long long n, cudaStream_t s);
+template <typename T> void to_storage(T* dst, const float* src, long long n, cudaStream_t s);
+template <typename T> void to_f32(float* dst, const T* src, long long n, cudaStream_t s);
+
+// Cross-entropy pieces.
+template <typename T>
+void ce_rowstats(const T* z, long long ldz, const int32_t* tgt, int M, int V, float* lse,
+                 float* loss_rows, cudaStream_t s);
+void ce_reduce_partials(const float* pmax, const float* psum, int ntiles, int ld, const float* ztgt,
+                        int M, float* lse, float* loss_rows, cudaStream_t s);
+template <typename T>
+void ce_dlogits(T* z, long long ldz, const float* lse, const int32_t* tgt, int M, int V, int Vpad,
+                float inv_scale, cudaStream_t s);
+void mean_reduce(float* out, const float* rows, int M, unsigned* status, cudaStream_t s);
+
+// Encoder backward: fixed-order scatter of dx0 (fp32) into dwte, and dwpe.
+void sort_tokens(uint32_t* order, const int32_t* tok, int M, int V, cudaStream_t s);
+template <typename T>
+void encoder_bwd(T* dwte, T* dwpe, const float* dx0, const uint32_t* order, const int32_t* tok,
+                 int B, int Tn, int C, cudaStream_t s);
+
+// Split-K reduction: out = sum over splits of ws[s][m][n].
+void splitk_reduce(void* out, int out_f32, long long ldo, const float* ws, int splits, int M, int N,
+                   cudaStream_t s);
+
+// Optimizer.
+struct Segment { long long begin, end; int decay; };
+constexpr int kMaxSegments = 16;
+template <typename G>
+void grad_sumsq_partials(float* partials, int nparts, const G* g, long long n, cudaStream_t s);
+void grad_norm_finalize(float* norm_scale, const float* partials, int nparts, float max_norm,
+                        unsigned* status, int* counter, int host_t, float b1, float b2,
+                        cudaStream_t s);
+// bf16 mode: master/m/v fp32 with a bf16 copy of the parameters; fp32 mode: param_copy null.
+template <typename G, typename P>
+void adamw(float* master, P* param_copy, const G* grad, float* m, float* v, long long n,
+           const Segment* segs, int nsegs, const float* norm_scale, float lr, float beta1,
+           float beta2, float eps, float wd, cudaStream_t s);
+
+}  // namespace gpt2k

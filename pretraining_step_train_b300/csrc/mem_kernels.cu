@@ -1,0 +1,841 @@
+// Memory-bound kernels of the GPT-2 step: encoder, LayerNorm, GELU, residual,
+// bias-gradient column sums, cross-entropy pieces, fixed-order encoder
+// backward, split-K reduction, global gradient norm and AdamW.
+//
+// All of them stream 16-byte vectors (4 fp32 or 8 bf16 per access) with
+// consecutive threads on consecutive addresses, reduce with warp shuffles,
+// and keep every reduction in a fixed order so results are bitwise
+// reproducible run to run.
+#include "common.cuh"
+#include "internal.h"
+
+#include <math.h>
+
+namespace gpt2k {
+
+static inline int grid_for(long long work, int block, int cap = 148 * 16) {
+  long long g = (work + block - 1) / block;
+  if (g < 1) g = 1;
+  if (g > cap) g = cap;
+  return (int)g;
+}
+
+// ------------------------------------------------------------------ encoder
+// x0[b, t, :] = wte[tok[b, t], :] + wpe[t, :]   (one fp32 add, then one rounding)
+template <typename T>
+__global__ void k_encoder_fwd(T* __restrict__ x0, const int32_t* __restrict__ tok,
+                              const T* __restrict__ wte, const T* __restrict__ wpe, int M, int Tn,
+                              int C, int V, unsigned* status) {
+  constexpr int N = V16<T>::N;
+  const int cv = C / N;
+  const long long nvec = (long long)M * cv;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < nvec;
+       i += (long long)gridDim.x * blockDim.x) {
+    int m = (int)(i / cv), c = (int)(i % cv) * N;
+    int t = m % Tn;
+    int id = tok[m];
+    if (id < 0 || id >= V) {
+      if (status) atomicOr(status, ST_TOKEN);
+      id = 0;
+    }
+    float a[N], b[N];
+    load16(wte + (long long)id * C + c, a);
+    load16(wpe + (long long)t * C + c, b);
+#pragma unroll
+    for (int j = 0; j < N; ++j) a[j] = a[j] + b[j];
+    store16(x0 + (long long)m * C + c, a);
+  }
+}
+
+template <typename T>
+void encoder_fwd(T* x0, const int32_t* tok, const T* wte, const T* wpe, int B, int Tn, int C, int V,
+                 unsigned* status, cudaStream_t s) {
+  long long nvec = (long long)B * Tn * C / V16<T>::N;
+  k_encoder_fwd<T><<<grid_for(nvec, 256), 256, 0, s>>>(x0, tok, wte, wpe, B * Tn, Tn, C, V, status);
+}
+
+// Clamp ids outside [0, V) to 0 in place and latch ST_TOKEN.
+__global__ void k_check_ids(int32_t* __restrict__ ids, int n, int V, unsigned* status) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+    int t = ids[i];
+    if (t < 0 || t >= V) {
+      ids[i] = 0;
+      if (status) atomicOr(status, ST_TOKEN);
+    }
+  }
+}
+void check_ids(int32_t* ids, int n, int V, unsigned* status, cudaStream_t s) {
+  k_check_ids<<<grid_for(n, 256, 148), 256, 0, s>>>(ids, n, V, status);
+}
+
+// ------------------------------------------------------------------ LayerNorm forward
+// One warp per row; the row stays in registers (two-pass mean / biased variance).
+template <typename T, int MAXV>
+__global__ void k_layernorm_fwd(T* __restrict__ y, float* __restrict__ mean,
+                                float* __restrict__ rstd, const T* __restrict__ x,
+                                const T* __restrict__ w, const T* __restrict__ b, int M, int C) {
+  constexpr int N = V16<T>::N;
+  const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (row >= M) return;
+  const int nv = C / N;
+  const T* xr = x + (long long)row * C;
+  float v[MAXV][N];
+  float s = 0.f;
+#pragma unroll
+  for (int j = 0; j < MAXV; ++j) {
+    int vi = lane + j * 32;
+    if (vi < nv) {
+      load16(xr + vi * N, v[j]);
+#pragma unroll
+      for (int e = 0; e < N; ++e) s += v[j][e];
+    }
+  }
+  s = warp_sum(s);
+  const float mu = s / (float)C;
+  float ss = 0.f;
+#pragma unroll
+  for (int j = 0; j < MAXV; ++j) {
+    int vi = lane + j * 32;
+    if (vi < nv) {
+#pragma unroll
+      for (int e = 0; e < N; ++e) {
+        float d = v[j][e] - mu;
+        ss += d * d;
+      }
+    }
+  }
+  ss = warp_sum(ss);
+  const float rs = 1.0f / sqrtf(ss / (float)C + 1e-5f);
+  T* yr = y + (long long)row * C;
+#pragma unroll
+  for (int j = 0; j < MAXV; ++j) {
+    int vi = lane + j * 32;
+    if (vi < nv) {
+      float wv[N], bv[N], o[N];
+      load16(w + vi * N, wv);
+      load16(b + vi * N, bv);
+#pragma unroll
+      for (int e = 0; e < N; ++e) o[e] = (v[j][e] - mu) * rs * wv[e] + bv[e];
+      store16(yr + vi * N, o);
+    }
+  }
+  if (lane == 0) {
+    mean[row] = mu;
+    rstd[row] = rs;
+  }
+}
+
+template <typename T>
+void layernorm_fwd(T* y, float* mean, float* rstd, const T* x, const T* w, const T* b, int M, int C,
+                   cudaStream_t s) {
+  const int nv = C / V16<T>::N;
+  const int per = (nv + 31) / 32;
+  const int block = 256;
+  const int grid = (M * 32 + block - 1) / block;
+  if (per <= 1) k_layernorm_fwd<T, 1><<<grid, block, 0, s>>>(y, mean, rstd, x, w, b, M, C);
+  else if (per <= 2) k_layernorm_fwd<T, 2><<<grid, block, 0, s>>>(y, mean, rstd, x, w, b, M, C);
+  else if (per <= 3) k_layernorm_fwd<T, 3><<<grid, block, 0, s>>>(y, mean, rstd, x, w, b, M, C);
+  else if (per <= 4) k_layernorm_fwd<T, 4><<<grid, block, 0, s>>>(y, mean, rstd, x, w, b, M, C);
+  else k_layernorm_fwd<T, 8><<<grid, block, 0, s>>>(y, mean, rstd, x, w, b, M, C);
+}
+
+// ------------------------------------------------------------------ LayerNorm backward
+// dx = rstd * (g - mean(g) - xhat * mean(g * xhat)),  g = dy * w.
+// dres = (accumulate ? dres : 0) + dx in fp32; dres_b (if given) = storage copy.
+// dw = sum_rows dy * xhat, db = sum_rows dy: per-lane register accumulators,
+// combined across the block's warps in a fixed order, then across blocks.
+constexpr int kLnbBlocks = 256;
+constexpr int kLnbWarps = 8;
+
+template <typename T, int MAXV>
+__global__ void __launch_bounds__(kLnbWarps * 32)
+    k_layernorm_bwd(float* __restrict__ dres, T* __restrict__ dres_b, const T* __restrict__ dy,
+                    const T* __restrict__ x, const float* __restrict__ mean,
+                    const float* __restrict__ rstd, const T* __restrict__ w,
+                    float* __restrict__ partials, int M, int C, int accumulate, int rows_per_block) {
+  constexpr int N = V16<T>::N;
+  extern __shared__ float sred[];  // [2C]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nv = C / N;
+  float wv[MAXV][N], adw[MAXV][N], adb[MAXV][N];
+#pragma unroll
+  for (int j = 0; j < MAXV; ++j) {
+    int vi = lane + j * 32;
+#pragma unroll
+    for (int e = 0; e < N; ++e) adw[j][e] = adb[j][e] = 0.f;
+    if (vi < nv) load16(w + vi * N, wv[j]);
+  }
+  const int r0 = blockIdx.x * rows_per_block;
+  const int r1 = min(M, r0 + rows_per_block);
+  for (int r = r0 + warp; r < r1; r += kLnbWarps) {
+    const float mu = mean[r], rs = rstd[r];
+    float g[MAXV][N], xh[MAXV][N], dyv[MAXV][N];
+    float sg = 0.f, sgx = 0.f;
+#pragma unroll
+    for (int j = 0; j < MAXV; ++j) {
+      int vi = lane + j * 32;
+      if (vi < nv) {
+        float xv[N];
+        load16(dy + (long long)r * C + vi * N, dyv[j]);
+        load16(x + (long long)r * C + vi * N, xv);
+#pragma unroll
+        for (int e = 0; e < N; ++e) {
+          xh[j][e] = (xv[e] - mu) * rs;
+          g[j][e] = dyv[j][e] * wv[j][e];
+          sg += g[j][e];
+          sgx += g[j][e] * xh[j][e];
+        }
+      }
+    }
+    sg = warp_sum(sg) / (float)C;
+    sgx = warp_sum(sgx) / (float)C;
+#pragma unroll
+    for (int j = 0; j < MAXV; ++j) {
+      int vi = lane + j * 32;
+      if (vi < nv) {
+        float d[N];
+        float* dp = dres + (long long)r * C + vi * N;
+        if (accumulate) {
+#pragma unroll
+          for (int e = 0; e < N; e += 4) {
+            float4 o = *reinterpret_cast<const float4*>(dp + e);
+            d[e] = o.x; d[e + 1] = o.y; d[e + 2] = o.z; d[e + 3] = o.w;
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < N; ++e) d[e] = 0.f;
+        }
+#pragma unroll
+        for (int e = 0; e < N; ++e) {
+          d[e] += rs * (g[j][e] - sg - xh[j][e] * sgx);
+          adw[j][e] += dyv[j][e] * xh[j][e];
+          adb[j][e] += dyv[j][e];
+        }
+#pragma unroll
+        for (int e = 0; e < N; e += 4)
+          *reinterpret_cast<float4*>(dp + e) = make_float4(d[e], d[e + 1], d[e + 2], d[e + 3]);
+        if (dres_b) store16(dres_b + (long long)r * C + vi * N, d);
+      }
+    }
+  }
+  // fixed-order combination of the warps' accumulators
+  for (int i = threadIdx.x; i < 2 * C; i += blockDim.x) sred[i] = 0.f;
+  __syncthreads();
+  for (int ww = 0; ww < kLnbWarps; ++ww) {
+    if (warp == ww) {
+#pragma unroll
+      for (int j = 0; j < MAXV; ++j) {
+        int vi = lane + j * 32;
+        if (vi < nv) {
+#pragma unroll
+          for (int e = 0; e < N; ++e) {
+            sred[vi * N + e] += adw[j][e];
+            sred[C + vi * N + e] += adb[j][e];
+          }
+        }
+      }
+    }
+    __syncthreads();
+  }
+  for (int i = threadIdx.x; i < 2 * C; i += blockDim.x)
+    partials[(long long)blockIdx.x * 2 * C + i] = sred[i];
+}
+
+template <typename T>
+__global__ void k_sum_partials_2(T* __restrict__ dw, T* __restrict__ db,
+                                 const float* __restrict__ partials, int nblocks, int C) {
+  int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= 2 * C) return;
+  float s = 0.f;
+  for (int b = 0; b < nblocks; ++b) s += partials[(long long)b * 2 * C + c];
+  if (c < C) dw[c] = from_f<T>(s);
+  else db[c - C] = from_f<T>(s);
+}
+
+size_t layernorm_bwd_partials_floats(int C) { return (size_t)kLnbBlocks * 2 * C; }
+
+template <typename T>
+void layernorm_bwd(float* dres, T* dres_b, const T* dy, const T* x, const float* mean,
+                   const float* rstd, const T* w, T* dw, T* db, float* partials, int M, int C,
+                   int accumulate, cudaStream_t s) {
+  const int nv = C / V16<T>::N;
+  const int per = (nv + 31) / 32;
+  int nblocks = (M + kLnbWarps - 1) / kLnbWarps;
+  if (nblocks > kLnbBlocks) nblocks = kLnbBlocks;
+  const int rpb = (M + nblocks - 1) / nblocks;
+  const size_t sm = 2 * C * sizeof(float);
+#define LNB(P)                                                                                  \
+  k_layernorm_bwd<T, P><<<nblocks, kLnbWarps * 32, sm, s>>>(dres, dres_b, dy, x, mean, rstd, w, \
+                                                            partials, M, C, accumulate, rpb)
+  if (per <= 1) LNB(1);
+  else if (per <= 2) LNB(2);
+  else if (per <= 3) LNB(3);
+  else if (per <= 4) LNB(4);
+  else LNB(8);
+#undef LNB
+  k_sum_partials_2<T><<<(2 * C + 255) / 256, 256, 0, s>>>(dw, db, partials, nblocks, C);
+}
+
+// ------------------------------------------------------------------ column sums (bias grads)
+constexpr int kColsumRowBlocks = 128;
+
+template <typename T>
+__global__ void __launch_bounds__(256)
+    k_colsum_partial(float* __restrict__ partials, const T* __restrict__ x, int M, int N,
+                     long long ld, int rows_per_block) {
+  constexpr int NV = V16<T>::N;
+  __shared__ float sred[32 * NV];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c = (blockIdx.x * 32 + lane) * NV;
+  float acc[NV];
+#pragma unroll
+  for (int e = 0; e < NV; ++e) acc[e] = 0.f;
+  const int r0 = blockIdx.y * rows_per_block, r1 = min(M, r0 + rows_per_block);
+  if (c < N) {
+    for (int r = r0 + warp; r < r1; r += 8) {
+      float v[NV];
+      load16(x + (long long)r * ld + c, v);
+#pragma unroll
+      for (int e = 0; e < NV; ++e) acc[e] += v[e];
+    }
+  }
+  for (int i = threadIdx.x; i < 32 * NV; i += 256) sred[i] = 0.f;
+  __syncthreads();
+  for (int ww = 0; ww < 8; ++ww) {
+    if (warp == ww) {
+#pragma unroll
+      for (int e = 0; e < NV; ++e) sred[lane * NV + e] += acc[e];
+    }
+    __syncthreads();
+  }
+  for (int i = threadIdx.x; i < 32 * NV; i += 256) {
+    int cc = blockIdx.x * 32 * NV + i;
+    if (cc < N) partials[(long long)blockIdx.y * N + cc] = sred[i];
+  }
+}
+
+template <typename T>
+__global__ void k_colsum_final(T* __restrict__ out, const float* __restrict__ partials, int nrb,
+                               int N) {
+  int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= N) return;
+  float s = 0.f;
+  for (int b = 0; b < nrb; ++b) s += partials[(long long)b * N + c];
+  out[c] = from_f<T>(s);
+}
+
+size_t colsum_partials_floats(int N) { return (size_t)kColsumRowBlocks * N; }
+
+template <typename T>
+void colsum(T* out, const T* x, int M, int N, long long ld, float* partials, cudaStream_t s) {
+  constexpr int NV = V16<T>::N;
+  int nrb = (M + 63) / 64;
+  if (nrb > kColsumRowBlocks) nrb = kColsumRowBlocks;
+  const int rpb = (M + nrb - 1) / nrb;
+  dim3 grid((N + 32 * NV - 1) / (32 * NV), nrb);
+  k_colsum_partial<T><<<grid, 256, 0, s>>>(partials, x, M, N, ld, rpb);
+  k_colsum_final<T><<<(N + 255) / 256, 256, 0, s>>>(out, partials, nrb, N);
+}
+
+// ------------------------------------------------------------------ elementwise
+template <typename T>
+__global__ void k_gelu_fwd(T* __restrict__ y, const T* __restrict__ x, long long n) {
+  constexpr int N = V16<T>::N;
+  for (long long i = (blockIdx.x * (long long)blockDim.x + threadIdx.x) * N; i < n;
+       i += (long long)gridDim.x * blockDim.x * N) {
+    float v[N];
+    load16(x + i, v);
+#pragma unroll
+    for (int e = 0; e < N; ++e) v[e] = gelu_f(v[e]);
+    store16(y + i, v);
+  }
+}
+template <typename T>
+__global__ void k_gelu_bwd(T* __restrict__ dx, const T* __restrict__ dy, const T* __restrict__ x,
+                           long long n) {
+  constexpr int N = V16<T>::N;
+  for (long long i = (blockIdx.x * (long long)blockDim.x + threadIdx.x) * N; i < n;
+       i += (long long)gridDim.x * blockDim.x * N) {
+    float a[N], b[N];
+    load16(dy + i, a);
+    load16(x + i, b);
+#pragma unroll
+    for (int e = 0; e < N; ++e) a[e] = a[e] * gelu_grad_f(b[e]);
+    store16(dx + i, a);
+  }
+}
+template <typename T>
+__global__ void k_residual(T* __restrict__ y, const T* __restrict__ a, const T* __restrict__ b,
+                           long long n) {
+  constexpr int N = V16<T>::N;
+  for (long long i = (blockIdx.x * (long long)blockDim.x + threadIdx.x) * N; i < n;
+       i += (long long)gridDim.x * blockDim.x * N) {
+    float u[N], v[N];
+    load16(a + i, u);
+    load16(b + i, v);
+#pragma unroll
+    for (int e = 0; e < N; ++e) u[e] = u[e] + v[e];
+    store16(y + i, u);
+  }
+}
+template <typename T>
+__global__ void k_to_storage(T* __restrict__ dst, const float* __restrict__ src, long long n) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x)
+    dst[i] = from_f<T>(src[i]);
+}
+template <typename T>
+__global__ void k_to_f32(float* __restrict__ dst, const T* __restrict__ src, long long n) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x)
+    dst[i] = to_f(src[i]);
+}
+
+template <typename T> void gelu_fwd(T* y, const T* x, long long n, cudaStream_t s) {
+  k_gelu_fwd<T><<<grid_for(n / V16<T>::N, 256), 256, 0, s>>>(y, x, n);
+}
+template <typename T> void gelu_bwd(T* dx, const T* dy, const T* x, long long n, cudaStream_t s) {
+  k_gelu_bwd<T><<<grid_for(n / V16<T>::N, 256), 256, 0, s>>>(dx, dy, x, n);
+}
+template <typename T> void residual_add(T* y, const T* a, const T* b, long long n, cudaStream_t s) {
+  k_residual<T><<<grid_for(n / V16<T>::N, 256), 256, 0, s>>>(y, a, b, n);
+}
+template <typename T> void to_storage(T* dst, const float* src, long long n, cudaStream_t s) {
+  k_to_storage<T><<<grid_for(n, 256), 256, 0, s>>>(dst, src, n);
+}
+template <typename T> void to_f32(float* dst, const T* src, long long n, cudaStream_t s) {
+  k_to_f32<T><<<grid_for(n, 256), 256, 0, s>>>(dst, src, n);
+}
+
+// ------------------------------------------------------------------ cross-entropy
+__device__ __forceinline__ float block_reduce(float v, float* sh, bool is_max) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  v = is_max ? warp_max(v) : warp_sum(v);
+  __syncthreads();
+  if (lane == 0) sh[warp] = v;
+  __syncthreads();
+  float r = (lane < nw) ? sh[lane] : (is_max ? -INFINITY : 0.f);
+  r = is_max ? warp_max(r) : warp_sum(r);
+  return r;
+}
+
+// One block per row: lse = log sum_{n<V} exp z[n]; loss_row = lse - z[target].
+template <typename T>
+__global__ void k_ce_rowstats(const T* __restrict__ z, long long ldz, const int32_t* __restrict__ tgt,
+                              int V, float* __restrict__ lse, float* __restrict__ loss_rows) {
+  __shared__ float sh[32];
+  const int r = blockIdx.x;
+  const T* zr = z + (long long)r * ldz;
+  float m = -INFINITY;
+  for (int c = threadIdx.x; c < V; c += blockDim.x) m = fmaxf(m, to_f(zr[c]));
+  m = block_reduce(m, sh, true);
+  float s = 0.f;
+  for (int c = threadIdx.x; c < V; c += blockDim.x) s += expf(to_f(zr[c]) - m);
+  s = block_reduce(s, sh, false);
+  if (threadIdx.x == 0) {
+    int t = tgt[r];
+    t = (t < 0 || t >= V) ? 0 : t;
+    float l = m + logf(s);
+    lse[r] = l;
+    loss_rows[r] = l - to_f(zr[t]);
+  }
+}
+template <typename T>
+void ce_rowstats(const T* z, long long ldz, const int32_t* tgt, int M, int V, float* lse,
+                 float* loss_rows, cudaStream_t s) {
+  k_ce_rowstats<T><<<M, 256, 0, s>>>(z, ldz, tgt, V, lse, loss_rows);
+}
+
+// One warp per row: combine per-tile (max, sum exp) partials into lse.
+__global__ void k_ce_reduce_partials(const float* __restrict__ pmax, const float* __restrict__ psum,
+                                     int ntiles, int ld, const float* __restrict__ ztgt, int M,
+                                     float* __restrict__ lse, float* __restrict__ loss_rows) {
+  const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (row >= M) return;
+  const float* pm = pmax + (long long)row * ld;
+  const float* ps = psum + (long long)row * ld;
+  float m = -INFINITY;
+  for (int i = lane; i < ntiles; i += 32) m = fmaxf(m, pm[i]);
+  m = warp_max(m);
+  float s = 0.f;
+  for (int i = lane; i < ntiles; i += 32) {
+    float mi = pm[i];
+    if (mi > -INFINITY) s += ps[i] * expf(mi - m);
+  }
+  s = warp_sum(s);
+  if (lane == 0) {
+    float l = m + logf(s);
+    lse[row] = l;
+    loss_rows[row] = l - ztgt[row];
+  }
+}
+void ce_reduce_partials(const float* pmax, const float* psum, int ntiles, int ld, const float* ztgt,
+                        int M, float* lse, float* loss_rows, cudaStream_t s) {
+  k_ce_reduce_partials<<<(M * 32 + 255) / 256, 256, 0, s>>>(pmax, psum, ntiles, ld, ztgt, M, lse,
+                                                           loss_rows);
+}
+
+// dz = (softmax(z) - onehot(target)) * inv_scale on n < V, 0 on the pad columns; in place.
+template <typename T>
+__global__ void __launch_bounds__(256)
+    k_ce_dlogits(T* __restrict__ z, long long ldz, const float* __restrict__ lse,
+                 const int32_t* __restrict__ tgt, int V, int Vpad, float inv_scale) {
+  constexpr int N = V16<T>::N;
+  const int r = blockIdx.x;
+  T* zr = z + (long long)r * ldz;
+  const float l = lse[r];
+  int t = tgt[r];
+  t = (t < 0 || t >= V) ? 0 : t;
+  for (int c0 = threadIdx.x * N; c0 < Vpad; c0 += blockDim.x * N) {
+    float v[N];
+    load16(zr + c0, v);
+#pragma unroll
+    for (int e = 0; e < N; ++e) {
+      int c = c0 + e;
+      float p = (c < V) ? expf(v[e] - l) : 0.f;
+      if (c == t) p -= 1.0f;
+      v[e] = p * inv_scale;
+    }
+    store16(zr + c0, v);
+  }
+}
+template <typename T>
+void ce_dlogits(T* z, long long ldz, const float* lse, const int32_t* tgt, int M, int V, int Vpad,
+                float inv_scale, cudaStream_t s) {
+  k_ce_dlogits<T><<<M, 256, 0, s>>>(z, ldz, lse, tgt, V, Vpad, inv_scale);
+}
+
+// Mean of M per-row values in a fixed order; flags a non-finite result.
+__global__ void k_mean_reduce(float* out, const float* __restrict__ rows, int M, unsigned* status) {
+  __shared__ double sh[32];
+  double s = 0.0;
+  for (int i = threadIdx.x; i < M; i += blockDim.x) s += (double)rows[i];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) sh[warp] = s;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double t = 0.0;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += sh[w];
+    float r = (float)(t / (double)M);
+    out[0] = r;
+    if (!isfinite(r) && status) atomicOr(status, ST_NONFINITE);
+  }
+}
+void mean_reduce(float* out, const float* rows, int M, unsigned* status, cudaStream_t s) {
+  k_mean_reduce<<<1, 1024, 0, s>>>(out, rows, M, status);
+}
+
+// ------------------------------------------------------------------ encoder backward
+// Single-block bitonic sort of (token, position) keys: order[] lists positions
+// grouped by token, ascending position within a token.  Keys live in shared
+// memory (8 bytes each, M <= 16384).
+__global__ void __launch_bounds__(1024) k_sort_tokens(uint32_t* __restrict__ order,
+                                                      const int32_t* __restrict__ tok, int M, int V,
+                                                      int P) {
+  extern __shared__ unsigned long long keys[];
+  for (int i = threadIdx.x; i < P; i += blockDim.x) {
+    unsigned long long k = ~0ull;
+    if (i < M) {
+      int t = tok[i];
+      t = (t < 0 || t >= V) ? 0 : t;
+      k = ((unsigned long long)(unsigned)t << 32) | (unsigned)i;
+    }
+    keys[i] = k;
+  }
+  __syncthreads();
+  for (int k = 2; k <= P; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < P; i += blockDim.x) {
+        int ixj = i ^ j;
+        if (ixj > i) {
+          unsigned long long a = keys[i], b = keys[ixj];
+          bool up = (i & k) == 0;
+          if ((a > b) == up) {
+            keys[i] = b;
+            keys[ixj] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int i = threadIdx.x; i < M; i += blockDim.x) {
+    order[i] = (uint32_t)(keys[i] & 0xffffffffull);
+    order[M + i] = (uint32_t)(keys[i] >> 32);  // sorted token ids
+  }
+}
+
+void sort_tokens(uint32_t* order, const int32_t* tok, int M, int V, cudaStream_t s) {
+  int P = 1;
+  while (P < M) P <<= 1;
+  size_t sm = (size_t)P * 8;
+  cudaFuncSetAttribute(k_sort_tokens, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  k_sort_tokens<<<1, 1024, sm, s>>>(order, tok, M, V, P);
+}
+
+// One block per segment head p of the sorted list: acc = sum over the
+// segment's positions in ascending order (fp32), then dwte[v] = dwte[v] + acc.
+template <typename T>
+__global__ void __launch_bounds__(256)
+    k_encoder_bwd_wte(T* __restrict__ dwte, const float* __restrict__ dx0,
+                      const uint32_t* __restrict__ order, int M, int C) {
+  const int p = blockIdx.x;
+  const uint32_t* stok = order + M;
+  const uint32_t v = stok[p];
+  if (p > 0 && stok[p - 1] == v) return;
+  // segment end: first q > p with stok[q] != v (binary search on the sorted ids)
+  int lo = p, hi = M;  // stok[lo] == v; find first index with stok > v
+  while (hi - lo > 1) {
+    int mid = (lo + hi) >> 1;
+    if (stok[mid] == v) lo = mid; else hi = mid;
+  }
+  const int q = hi;
+  for (int c = threadIdx.x * 4; c < C; c += blockDim.x * 4) {
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+    int r = p;
+    for (; r + 8 <= q; r += 8) {
+      float4 u[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) u[k] = *reinterpret_cast<const float4*>(dx0 + (long long)order[r + k] * C + c);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        a0 = a0 + u[k].x; a1 = a1 + u[k].y; a2 = a2 + u[k].z; a3 = a3 + u[k].w;
+      }
+    }
+    for (; r < q; ++r) {
+      float4 u = *reinterpret_cast<const float4*>(dx0 + (long long)order[r] * C + c);
+      a0 = a0 + u.x; a1 = a1 + u.y; a2 = a2 + u.z; a3 = a3 + u.w;
+    }
+    T* dst = dwte + (long long)v * C + c;
+    dst[0] = from_f<T>(to_f(dst[0]) + a0);
+    dst[1] = from_f<T>(to_f(dst[1]) + a1);
+    dst[2] = from_f<T>(to_f(dst[2]) + a2);
+    dst[3] = from_f<T>(to_f(dst[3]) + a3);
+  }
+}
+
+// dwpe[t, c] = sum over b ascending of dx0[b, t, c] (fp32), stored once.
+template <typename T>
+__global__ void k_encoder_bwd_wpe(T* __restrict__ dwpe, const float* __restrict__ dx0, int B, int Tn,
+                                  int C) {
+  long long n = (long long)Tn * C;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x) {
+    float acc = 0.f;
+    for (int b = 0; b < B; ++b) acc = acc + dx0[(long long)b * n + i];
+    dwpe[i] = from_f<T>(acc);
+  }
+}
+
+template <typename T>
+void encoder_bwd(T* dwte, T* dwpe, const float* dx0, const uint32_t* order, const int32_t* tok,
+                 int B, int Tn, int C, cudaStream_t s) {
+  const int M = B * Tn;
+  int threads = C / 4;
+  if (threads > 256) threads = 256;
+  if (threads < 32) threads = 32;
+  k_encoder_bwd_wte<T><<<M, threads, 0, s>>>(dwte, dx0, order, M, C);
+  k_encoder_bwd_wpe<T><<<grid_for((long long)Tn * C, 256), 256, 0, s>>>(dwpe, dx0, B, Tn, C);
+}
+
+// ------------------------------------------------------------------ split-K reduction
+__global__ void k_splitk_reduce(void* __restrict__ out, int out_f32, long long ldo,
+                                const float* __restrict__ ws, int splits, int M, int N) {
+  const long long nq = (long long)M * N / 4;
+  const long long plane = (long long)M * N;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < nq;
+       i += (long long)gridDim.x * blockDim.x) {
+    long long e = i * 4;
+    int m = (int)(e / N), n = (int)(e % N);
+    float4 a = *reinterpret_cast<const float4*>(ws + e);
+    for (int sp = 1; sp < splits; ++sp) {
+      float4 b = *reinterpret_cast<const float4*>(ws + sp * plane + e);
+      a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
+    }
+    if (out_f32) {
+      *reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + (long long)m * ldo + n) = a;
+    } else {
+      bf16* o = reinterpret_cast<bf16*>(out) + (long long)m * ldo + n;
+      __nv_bfloat162 lo = __floats2bfloat162_rn(a.x, a.y), hi = __floats2bfloat162_rn(a.z, a.w);
+      uint2 u;
+      u.x = *reinterpret_cast<uint32_t*>(&lo);
+      u.y = *reinterpret_cast<uint32_t*>(&hi);
+      *reinterpret_cast<uint2*>(o) = u;
+    }
+  }
+}
+void splitk_reduce(void* out, int out_f32, long long ldo, const float* ws, int splits, int M, int N,
+                   cudaStream_t s) {
+  k_splitk_reduce<<<grid_for((long long)M * N / 4, 256), 256, 0, s>>>(out, out_f32, ldo, ws, splits,
+                                                                     M, N);
+}
+
+// ------------------------------------------------------------------ global norm + AdamW
+template <typename G>
+__global__ void __launch_bounds__(512)
+    k_sumsq(float* __restrict__ partials, const G* __restrict__ g, long long n, long long chunk) {
+  constexpr int N = V16<G>::N;
+  __shared__ float sh[32];
+  const long long b0 = blockIdx.x * chunk;
+  const long long b1 = min(n, b0 + chunk);
+  float s = 0.f;
+  for (long long i = b0 + (long long)threadIdx.x * N; i < b1; i += (long long)blockDim.x * N) {
+    float v[N];
+    load16(g + i, v);
+#pragma unroll
+    for (int e = 0; e < N; ++e) s += v[e] * v[e];
+  }
+  s = block_reduce(s, sh, false);
+  if (threadIdx.x == 0) partials[blockIdx.x] = s;
+}
+template <typename G>
+void grad_sumsq_partials(float* partials, int nparts, const G* g, long long n, cudaStream_t s) {
+  constexpr int N = V16<G>::N;
+  long long chunk = (n + nparts - 1) / nparts;
+  chunk = (chunk + N - 1) / N * N;
+  k_sumsq<G><<<nparts, 512, 0, s>>>(partials, g, n, chunk);
+}
+
+// norm_scale[0] = ||g||, [1] = clip scale, [2] = 1 - b1^t, [3] = 1 - b2^t where
+// t = host_t when > 0, else the device step counter + 1 (the counter is stored).
+__global__ void k_norm_finalize(float* norm_scale, const float* __restrict__ partials, int nparts,
+                                float max_norm, unsigned* status, int* counter, int host_t,
+                                float b1, float b2) {
+  __shared__ double sh[32];
+  double s = 0.0;
+  for (int i = threadIdx.x; i < nparts; i += blockDim.x) s += (double)partials[i];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = s;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double t = 0.0;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += sh[w];
+    float norm = (float)sqrt(t);
+    norm_scale[0] = norm;
+    norm_scale[1] = (norm > max_norm) ? max_norm / norm : 1.0f;
+    if (!isfinite(norm) && status) atomicOr(status, ST_NONFINITE);
+    const int step = host_t > 0 ? host_t : counter[0] + 1;
+    counter[0] = step;
+    norm_scale[2] = 1.0f - powf(b1, (float)step);
+    norm_scale[3] = 1.0f - powf(b2, (float)step);
+  }
+}
+void grad_norm_finalize(float* norm_scale, const float* partials, int nparts, float max_norm,
+                        unsigned* status, int* counter, int host_t, float b1, float b2,
+                        cudaStream_t s) {
+  k_norm_finalize<<<1, 1024, 0, s>>>(norm_scale, partials, nparts, max_norm, status, counter,
+                                     host_t, b1, b2);
+}
+
+struct SegTable { Segment s[kMaxSegments]; int n; };
+
+template <typename G> struct G4;
+template <> struct G4<float> {
+  static __device__ __forceinline__ void ld(const float* p, float* o) {
+    float4 v = *reinterpret_cast<const float4*>(p);
+    o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w;
+  }
+  static __device__ __forceinline__ void st(float* p, const float* o) {
+    *reinterpret_cast<float4*>(p) = make_float4(o[0], o[1], o[2], o[3]);
+  }
+};
+template <> struct G4<bf16> {
+  static __device__ __forceinline__ void ld(const bf16* p, float* o) {
+    uint2 u = *reinterpret_cast<const uint2*>(p);
+    __nv_bfloat162 a = *reinterpret_cast<__nv_bfloat162*>(&u.x), b = *reinterpret_cast<__nv_bfloat162*>(&u.y);
+    o[0] = __low2float(a); o[1] = __high2float(a); o[2] = __low2float(b); o[3] = __high2float(b);
+  }
+  static __device__ __forceinline__ void st(bf16* p, const float* o) {
+    __nv_bfloat162 a = __floats2bfloat162_rn(o[0], o[1]), b = __floats2bfloat162_rn(o[2], o[3]);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t*>(&a);
+    u.y = *reinterpret_cast<uint32_t*>(&b);
+    *reinterpret_cast<uint2*>(p) = u;
+  }
+};
+
+// m = b1 m + (1-b1) g; v = b2 v + (1-b2) g^2; w -= lr (m/bc1 / (sqrt(v/bc2) + eps) + wd_seg w)
+// with g = grad * clip_scale; clip scale and bias corrections come from
+// norm_scale[1..3] on the device; one pass over 4-element vectors.
+template <typename G, typename P>
+__global__ void __launch_bounds__(256)
+    k_adamw(float* __restrict__ master, P* __restrict__ pcopy, const G* __restrict__ grad,
+            float* __restrict__ m, float* __restrict__ v, long long n, SegTable segs,
+            const float* __restrict__ norm_scale, float lr, float b1, float b2, float eps,
+            float wd) {
+  const float sc = norm_scale[1], bc1 = norm_scale[2], bc2 = norm_scale[3];
+  const long long n4 = n / 4;
+  for (long long q = blockIdx.x * (long long)blockDim.x + threadIdx.x; q < n4;
+       q += (long long)gridDim.x * blockDim.x) {
+    const long long i = q * 4;
+    float lam = 0.f;
+#pragma unroll 1
+    for (int k = 0; k < segs.n; ++k)
+      if (i >= segs.s[k].begin && i < segs.s[k].end) lam = segs.s[k].decay ? wd : 0.f;
+    float w[4], g[4], mm[4], vv[4];
+    G4<float>::ld(master + i, w);
+    G4<G>::ld(grad + i, g);
+    G4<float>::ld(m + i, mm);
+    G4<float>::ld(v + i, vv);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      float gg = g[e] * sc;
+      mm[e] = b1 * mm[e] + (1.0f - b1) * gg;
+      vv[e] = b2 * vv[e] + (1.0f - b2) * gg * gg;
+      float mh = mm[e] / bc1, vh = vv[e] / bc2;
+      w[e] = w[e] - lr * (mh / (sqrtf(vh) + eps) + lam * w[e]);
+    }
+    G4<float>::st(master + i, w);
+    G4<float>::st(m + i, mm);
+    G4<float>::st(v + i, vv);
+    if (pcopy) G4<P>::st(pcopy + i, w);
+  }
+}
+
+template <typename G, typename P>
+void adamw(float* master, P* param_copy, const G* grad, float* m, float* v, long long n,
+           const Segment* segs, int nsegs, const float* norm_scale, float lr, float beta1,
+           float beta2, float eps, float wd, cudaStream_t s) {
+  SegTable t;
+  t.n = nsegs;
+  for (int i = 0; i < nsegs && i < kMaxSegments; ++i) t.s[i] = segs[i];
+  k_adamw<G, P><<<grid_for(n / 4, 256, 148 * 8), 256, 0, s>>>(master, param_copy, grad, m, v, n, t,
+                                                             norm_scale, lr, beta1, beta2, eps, wd);
+}
+
+// ------------------------------------------------------------------ instantiations
+#define INST(T)                                                                                     \
+  template void encoder_fwd<T>(T*, const int32_t*, const T*, const T*, int, int, int, int,         \
+                               unsigned*, cudaStream_t);                                           \
+  template void layernorm_fwd<T>(T*, float*, float*, const T*, const T*, const T*, int, int,       \
+                                 cudaStream_t);                                                    \
+  template void layernorm_bwd<T>(float*, T*, const T*, const T*, const float*, const float*,       \
+                                 const T*, T*, T*, float*, int, int, int, cudaStream_t);           \
+  template void colsum<T>(T*, const T*, int, int, long long, float*, cudaStream_t);                \
+  template void gelu_fwd<T>(T*, const T*, long long, cudaStream_t);                                \
+  template void gelu_bwd<T>(T*, const T*, const T*, long long, cudaStream_t);                      \
+  template void residual_add<T>(T*, const T*, const T*, long long, cudaStream_t);                  \
+  template void to_storage<T>(T*, const float*, long long, cudaStream_t);                          \
+  template void to_f32<T>(float*, const T*, long long, cudaStream_t);                              \
+  template void ce_rowstats<T>(const T*, long long, const int32_t*, int, int, float*, float*,      \
+                               cudaStream_t);                                                      \
+  template void ce_dlogits<T>(T*, long long, const float*, const int32_t*, int, int, int, float,   \
+                              cudaStream_t);                                                       \
+  template void encoder_bwd<T>(T*, T*, const float*, const uint32_t*, const int32_t*, int, int,    \
+                               int, cudaStream_t);                                                 \
+  template void grad_sumsq_partials<T>(float*, int, const T*, long long, cudaStream_t);
+INST(float)
+INST(bf16)
+#undef INST
+template void adamw<float, float>(float*, float*, const float*, float*, float*, long long,
+                                  const Segment*, int, const float*, float, float, float, float,
+                                  float, cudaStream_t);
+template void adamw<bf16, bf16>(float*, bf16*, const bf16*, float*, float*, long long,
+                                const Segment*, int, const float*, float, float, float, float,
+                                float, cudaStream_t);
+
+}  // namespace gpt2k

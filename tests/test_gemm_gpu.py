@@ -1,0 +1,79 @@
+"""Parity of the tcgen05 GEMM engine (through the C ABI) with the plain
+definition D = A B^T evaluated in float64 on the same bf16 inputs."""
+import ctypes as ct
+
+import numpy as np
+import pytest
+
+from pretraining_step_train_b300 import binding, synth
+from tests._helpers import rel_l2, to_dev, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+def _operands(seed, M, N, K, a_mn, b_mn):
+    a = synth.round_to_bf16(synth.normal(seed, M * K)).reshape(M, K)
+    b = synth.round_to_bf16(synth.normal(seed + 1, N * K)).reshape(N, K)
+    pad = lambda n: (n + 7) // 8 * 8
+    if a_mn:
+        lda = pad(M)
+        As = np.zeros((K, lda), np.float32); As[:, :M] = a.T
+    else:
+        lda = pad(K)
+        As = np.zeros((M, lda), np.float32); As[:, :K] = a
+    if b_mn:
+        ldb = pad(N)
+        Bs = np.zeros((K, ldb), np.float32); Bs[:, :N] = b.T
+    else:
+        ldb = pad(K)
+        Bs = np.zeros((N, ldb), np.float32); Bs[:, :K] = b
+    return a, b, As, Bs, lda, ldb
+
+
+@pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 0), (1, 1)])
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (300, 520, 200), (1024, 768, 768), (64, 8, 16)])
+def test_gemm_majors_fp32_out(a_mn, b_mn, M, N, K):
+    import torch
+    a, b, As, Bs, lda, ldb = _operands(M + N + K, M, N, K, a_mn, b_mn)
+    A, B = to_dev(As), to_dev(Bs)
+    D = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    binding.check(binding.lib().gemm_bf16(A.data_ptr(), B.data_ptr(), D.data_ptr(), M, N, K, lda, ldb, N,
+                                          a_mn, b_mn, 1, 1, None, 0, None))
+    torch.cuda.synchronize()
+    ref = a.astype(np.float64) @ b.astype(np.float64).T
+    got = to_np(D)
+    assert np.isfinite(got).all()
+    np.testing.assert_allclose(got, ref, rtol=0, atol=2e-5 * np.sqrt(K) * 4)
+
+
+@pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (1, 1), (0, 1)])
+def test_gemm_bf16_out_and_splitk(a_mn, b_mn):
+    import torch
+    M, N, K = 256, 512, 4096
+    a, b, As, Bs, lda, ldb = _operands(7, M, N, K, a_mn, b_mn)
+    A, B = to_dev(As), to_dev(Bs)
+    ref = a.astype(np.float64) @ b.astype(np.float64).T
+    for splits in (1, 4, 7):
+        for f32 in (0, 1):
+            D = torch.empty((M, N), dtype=torch.float32 if f32 else torch.bfloat16, device="cuda")
+            ws = torch.empty(splits * M * N * 4 + 256, dtype=torch.uint8, device="cuda")
+            binding.check(binding.lib().gemm_bf16(A.data_ptr(), B.data_ptr(), D.data_ptr(), M, N, K, lda, ldb,
+                                                  N, a_mn, b_mn, f32, splits, ws.data_ptr(), ws.numel(), None))
+            torch.cuda.synchronize()
+            err = rel_l2(to_np(D), ref)
+            assert err < (1e-6 if f32 else 4e-3), (splits, f32, err)
+
+
+def test_gemm_deterministic():
+    import torch
+    M, N, K = 512, 768, 3072
+    a, b, As, Bs, lda, ldb = _operands(9, M, N, K, 1, 1)
+    A, B = to_dev(As), to_dev(Bs)
+    outs = []
+    for _ in range(2):
+        D = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        ws = torch.empty(8 * M * N * 4, dtype=torch.uint8, device="cuda")
+        binding.check(binding.lib().gemm_bf16(A.data_ptr(), B.data_ptr(), D.data_ptr(), M, N, K, lda, ldb, N,
+                                              1, 1, 1, 0, ws.data_ptr(), ws.numel(), None))
+        outs.append(to_np(D))
+    np.testing.assert_array_equal(outs[0], outs[1])

@@ -1,0 +1,141 @@
+"""Full training-step parity through the C ABI against the oracle:
+forward + mean CE + backward + global-norm clip + AdamW.
+
+fp32 mode (the tiny GPT step): loss within 1e-4 relative, every parameter
+gradient within 1e-4 relative L2, post-AdamW weights within 1e-4.
+bf16 mode: loss within 1e-2 relative, gradients within 3e-2 relative L2,
+post-AdamW weights within 1e-2 relative L2 (the oracle runs in float64 on the
+same bf16-rounded weights and tokens)."""
+import numpy as np
+import pytest
+
+from oracle import gpt2_oracle as O
+from pretraining_step_train_b300 import binding, synth
+from tests._helpers import rel_l2, to_dev
+
+pytestmark = pytest.mark.gpu
+
+LR, B1, B2, EPS, WD, CLIP = 6e-4, 0.9, 0.95, 1e-8, 0.1, 1.0
+
+
+def _gpu_step(cfg, B, prec, flat, tok, tgt, steps=1):
+    s = binding.Step(cfg.L, cfg.H, cfg.C, cfg.V, cfg.Vpad, cfg.T, B, precision=prec)
+    s.set_params(flat)
+    td, gd = to_dev(tok, "i32"), to_dev(tgt, "i32")
+    out = []
+    for t in range(1, steps + 1):
+        loss = s.forward(td, gd)
+        s.backward()
+        grads = s.get(binding.GPT2_GRADS)
+        norm = s.clip_adamw(LR, B1, B2, EPS, WD, CLIP, t)
+        out.append(dict(loss=loss, grads=grads, norm=norm, master=s.get(binding.GPT2_MASTER),
+                        params=s.get(binding.GPT2_PARAMS), m=s.get(binding.GPT2_ADAM_M)))
+    s.close()
+    return out
+
+
+def _compare(cfg, P, res, ref, loss_tol, grad_tol, w_tol, flat):
+    L, C, Vpad, T = cfg.L, cfg.C, cfg.Vpad, cfg.T
+    assert abs(res["loss"] - ref["loss"]) / abs(ref["loss"]) < loss_tol, (res["loss"], ref["loss"])
+    G = synth.unflatten_params(res["grads"], L, C, Vpad, T)
+    worst = {}
+    for k in G:
+        e = rel_l2(G[k], ref["grads"][k])
+        worst[k] = e
+    assert max(worst.values()) < grad_tol, worst
+    assert abs(res["norm"] - ref["norm"]) / ref["norm"] < grad_tol
+    W = synth.unflatten_params(res["master"], L, C, Vpad, T)
+    for k in W:
+        assert rel_l2(W[k], ref["params"][k]) < w_tol, k
+    return worst
+
+
+def test_tiny_fp32_step_parity():
+    """The tiny GPT step: L=4, H=4, C=64, V=256 (no padding), T=64, B=4, fp32."""
+    L, H, C, V, Vpad, T, B = 4, 4, 64, 256, 256, 64, 4
+    cfg = O.Config(L, H, C, V, Vpad, T)
+    P = synth.init_params(0, L, C, V, Vpad, T)
+    tok, tgt = synth.iid_token_batch(1, B, T, V)
+    flat = synth.flatten_params(P, L, C, Vpad, T)
+    res = _gpu_step(cfg, B, binding.GPT2_FP32, flat, tok, tgt)[0]
+    ref = O.train_step(P, tok, tgt, cfg, lr=LR, t=1, beta1=B1, beta2=B2, eps=EPS, wd=WD, max_norm=CLIP)
+    _compare(cfg, P, res, ref, 1e-4, 1e-4, 1e-4, flat)
+
+
+def test_tiny_fp32_two_steps_moments():
+    L, H, C, V, Vpad, T, B = 2, 2, 32, 64, 64, 16, 2
+    cfg = O.Config(L, H, C, V, Vpad, T)
+    P = synth.init_params(3, L, C, V, Vpad, T)
+    tok, tgt = synth.iid_token_batch(4, B, T, V)
+    flat = synth.flatten_params(P, L, C, Vpad, T)
+    res = _gpu_step(cfg, B, binding.GPT2_FP32, flat, tok, tgt, steps=2)
+    r1 = O.train_step(P, tok, tgt, cfg, lr=LR, t=1, beta1=B1, beta2=B2, eps=EPS, wd=WD, max_norm=CLIP)
+    r2 = O.train_step(r1["params"], tok, tgt, cfg, lr=LR, t=2, M_=r1["m"], V_=r1["v"], beta1=B1, beta2=B2,
+                      eps=EPS, wd=WD, max_norm=CLIP)
+    _compare(cfg, r1["params"], res[1], r2, 1e-4, 1e-4, 1e-4, flat)
+
+
+@pytest.mark.parametrize("L,H,C,V,Vpad,T,B", [(2, 2, 128, 1000, 1024, 128, 2), (1, 1, 64, 250, 256, 200, 1)])
+def test_bf16_step_parity_small(L, H, C, V, Vpad, T, B):
+    cfg = O.Config(L, H, C, V, Vpad, T)
+    P = synth.init_params(5, L, C, V, Vpad, T, bf16_representable=True)
+    tok, tgt = synth.token_batch(6, B, T, V)
+    flat = synth.flatten_params(P, L, C, Vpad, T)
+    res = _gpu_step(cfg, B, binding.GPT2_BF16, flat, tok, tgt)[0]
+    ref = O.train_step(P, tok, tgt, cfg, lr=LR, t=1, beta1=B1, beta2=B2, eps=EPS, wd=WD, max_norm=CLIP)
+    _compare(cfg, P, res, ref, 1e-2, 3e-2, 1e-2, flat)
+    # the working bf16 copy is the round-to-nearest-even of the fp32 master copy
+    np.testing.assert_array_equal(res["params"], synth.round_to_bf16(res["master"]))
+
+
+@pytest.mark.slow
+def test_bf16_step_parity_124m_shapes():
+    """GPT-2 124M shapes (L=12, H=12, C=768, V=50257 -> 50304, T=1024) at B=1."""
+    L, H, C, V, Vpad, T, B = 12, 12, 768, 50257, 50304, 1024, 1
+    cfg = O.Config(L, H, C, V, Vpad, T)
+    P = synth.init_params(7, L, C, V, Vpad, T, bf16_representable=True)
+    tok, tgt = synth.token_batch(8, B, T, V)
+    flat = synth.flatten_params(P, L, C, Vpad, T)
+    res = _gpu_step(cfg, B, binding.GPT2_BF16, flat, tok, tgt)[0]
+    ref = O.train_step(P, tok, tgt, cfg, lr=LR, t=1, beta1=B1, beta2=B2, eps=EPS, wd=WD, max_norm=CLIP,
+                       dtype=np.float64)
+    worst = _compare(cfg, P, res, ref, 1e-2, 3e-2, 1e-2, flat)
+    print("worst grad rel L2:", max(worst.items(), key=lambda kv: kv[1]))
+
+
+def test_bf16_step_deterministic():
+    L, H, C, V, Vpad, T, B = 2, 2, 128, 1000, 1024, 128, 2
+    cfg = O.Config(L, H, C, V, Vpad, T)
+    P = synth.init_params(9, L, C, V, Vpad, T, bf16_representable=True)
+    tok, tgt = synth.token_batch(10, B, T, V)
+    flat = synth.flatten_params(P, L, C, Vpad, T)
+    a = _gpu_step(cfg, B, binding.GPT2_BF16, flat, tok, tgt)[0]
+    b = _gpu_step(cfg, B, binding.GPT2_BF16, flat, tok, tgt)[0]
+    assert a["loss"] == b["loss"]
+    np.testing.assert_array_equal(a["grads"], b["grads"])
+    np.testing.assert_array_equal(a["master"], b["master"])
+
+
+def test_call_order_and_host_step():
+    L, H, C, V, Vpad, T, B = 1, 1, 64, 250, 256, 64, 2
+    cfg = O.Config(L, H, C, V, Vpad, T)
+    P = synth.init_params(11, L, C, V, Vpad, T, bf16_representable=True)
+    tok, tgt = synth.token_batch(12, B, T, V)
+    s = binding.Step(L, H, C, V, Vpad, T, B, precision=binding.GPT2_BF16)
+    s.set_params(synth.flatten_params(P, L, C, Vpad, T))
+    assert binding.lib().gpt2_backward(s.h) == binding.GPT2_E_STATE
+    loss, norm = s.train_step_host(tok, tgt)
+    ref = O.train_step(P, tok, tgt, cfg, lr=LR, t=1)
+    assert abs(loss - ref["loss"]) / ref["loss"] < 1e-2
+    assert abs(norm - ref["norm"]) / ref["norm"] < 3e-2
+    assert binding.lib().gpt2_clip_adamw(s.h, LR, B1, B2, EPS, WD, CLIP, 1, None) == binding.GPT2_E_STATE
+    # an out-of-range target is clamped and reported
+    bad = tgt.copy()
+    bad[0, 0] = V + 5
+    import ctypes as ct
+    lossv = ct.c_float()
+    r = binding.lib().gpt2_forward(s.h, to_dev(tok, "i32").data_ptr(), to_dev(bad, "i32").data_ptr(),
+                                   ct.byref(lossv))
+    assert r == binding.GPT2_E_TOKEN
+    assert s.sync_status() == binding.GPT2_OK  # the status word was read and cleared
+    s.close()
