@@ -197,6 +197,8 @@ def main():
     ap.add_argument("--config", default="124m", choices=sorted(CONFIGS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="eager launches instead of a CUDA graph")
+    ap.add_argument("--one-step", action="store_true",
+                    help="set up, run one eager step and exit (for profiler launch lists)")
     args = ap.parse_args()
     c = CONFIGS[args.config]
     if args.impl == "reference":
@@ -241,6 +243,10 @@ def main():
         src_tok.copy_(dev_tok[0]); src_tgt.copy_(dev_tgt[0])
         one_step()  # eager warm-up (one-time host set-up inside the library)
     stream.synchronize()
+    if args.one_step:
+        st = step.sync_status()
+        print(json.dumps({"one_step": True, "status": st}), flush=True)
+        sys.exit(0 if st == 0 else 1)
     graph = None
     n_kernels = None
     if not args.no_graph:

@@ -27,9 +27,11 @@ def test_encoder_forward_bit_exact(prec, B, T, C, V, Vpad):
         wte, wpe = synth.round_to_bf16(wte).reshape(Vpad, C), synth.round_to_bf16(wpe).reshape(T, C)
     x0 = torch.empty((B, T, C), dtype=torch.bfloat16 if dt == "bf16" else torch.float32, device="cuda")
     st = torch.zeros(4, dtype=torch.int32, device="cuda")
-    binding.check(binding.lib().gpt2_encoder_fwd(to_dev(tok, "i32").data_ptr(), to_dev(wte, dt).data_ptr(),
-                                                 to_dev(wpe, dt).data_ptr(), x0.data_ptr(), B, T, C, V, prec,
-                                                 st.data_ptr(), None))
+    # keep every device tensor referenced until the kernel has run
+    tok_d, wte_d, wpe_d = to_dev(tok, "i32"), to_dev(wte, dt), to_dev(wpe, dt)
+    binding.check(binding.lib().gpt2_encoder_fwd(tok_d.data_ptr(), wte_d.data_ptr(), wpe_d.data_ptr(),
+                                                 x0.data_ptr(), B, T, C, V, prec, st.data_ptr(), None))
+    torch.cuda.synchronize()
     ref = O.encoder_forward_f32(tok, wte, wpe)
     if prec == binding.GPT2_BF16:
         ref = synth.round_to_bf16(ref).reshape(ref.shape)
@@ -50,9 +52,11 @@ def test_encoder_backward_bit_exact(prec, B, T, C, V, Vpad):
     dwte = to_dev(din, dt)
     dwpe = torch.full((T, C), float("nan"), dtype=dwte.dtype, device="cuda")
     ws = torch.empty(8 * B * T, dtype=torch.uint8, device="cuda")
-    binding.check(binding.lib().gpt2_encoder_bwd(to_dev(tok, "i32").data_ptr(), to_dev(dx0, "f32").data_ptr(),
-                                                 dwte.data_ptr(), dwpe.data_ptr(), B, T, C, V, prec,
-                                                 ws.data_ptr(), ws.numel(), None))
+    tok_d, dx0_d = to_dev(tok, "i32"), to_dev(dx0, "f32")
+    binding.check(binding.lib().gpt2_encoder_bwd(tok_d.data_ptr(), dx0_d.data_ptr(), dwte.data_ptr(),
+                                                 dwpe.data_ptr(), B, T, C, V, prec, ws.data_ptr(), ws.numel(),
+                                                 None))
+    torch.cuda.synchronize()
     ref_wte, ref_wpe = O.encoder_backward_f32(tok, dx0, din, (T, C))
     if prec == binding.GPT2_BF16:
         ref_wte = synth.round_to_bf16(ref_wte).reshape(ref_wte.shape)
@@ -71,9 +75,11 @@ def test_encoder_out_of_range_tokens_flagged_and_clamped():
     wpe = synth.normal(2, T * C).astype(np.float32).reshape(T, C)
     x0 = torch.empty((B, T, C), dtype=torch.float32, device="cuda")
     st = torch.zeros(4, dtype=torch.int32, device="cuda")
-    binding.check(binding.lib().gpt2_encoder_fwd(to_dev(tok, "i32").data_ptr(), to_dev(wte, "f32").data_ptr(),
-                                                 to_dev(wpe, "f32").data_ptr(), x0.data_ptr(), B, T, C, V,
-                                                 binding.GPT2_FP32, st.data_ptr(), None))
+    tok_d, wte_d, wpe_d = to_dev(tok, "i32"), to_dev(wte, "f32"), to_dev(wpe, "f32")
+    binding.check(binding.lib().gpt2_encoder_fwd(tok_d.data_ptr(), wte_d.data_ptr(), wpe_d.data_ptr(),
+                                                 x0.data_ptr(), B, T, C, V, binding.GPT2_FP32, st.data_ptr(),
+                                                 None))
+    torch.cuda.synchronize()
     assert int(st[0].item()) & 1
     clamped = np.where((tok < 0) | (tok >= V), 0, tok)
     np.testing.assert_array_equal(to_np(x0), O.encoder_forward_f32(clamped, wte, wpe))

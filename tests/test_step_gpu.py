@@ -134,8 +134,8 @@ def test_call_order_and_host_step():
     bad[0, 0] = V + 5
     import ctypes as ct
     lossv = ct.c_float()
-    r = binding.lib().gpt2_forward(s.h, to_dev(tok, "i32").data_ptr(), to_dev(bad, "i32").data_ptr(),
-                                   ct.byref(lossv))
+    tok_d, bad_d = to_dev(tok, "i32"), to_dev(bad, "i32")
+    r = binding.lib().gpt2_forward(s.h, tok_d.data_ptr(), bad_d.data_ptr(), ct.byref(lossv))
     assert r == binding.GPT2_E_TOKEN
     assert s.sync_status() == binding.GPT2_OK  # the status word was read and cleared
     s.close()
