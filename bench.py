@@ -296,7 +296,19 @@ def main():
     with torch.cuda.stream(stream):
         one_step()
     prof = step.profile_read()
+    regions = step.profile_regions()
     step.profile(False)
+    shapes = {}
+    epi_names = ["store", "bias", "bias+resid", "bias+gelu", "gelu'", "ce", "f32"]
+    for cls, dims, rms, rfl, rby in regions:
+        if cls != "gemm":
+            continue
+        Mx, Nx, Kx, amn, bmn, epi = dims
+        key = f"{Mx}x{Nx}x{Kx} {'MN' if amn else 'K'}{'MN' if bmn else 'K'} {epi_names[epi]}"
+        e = shapes.setdefault(key, [0, 0.0, 0.0])
+        e[0] += 1; e[1] += rms; e[2] += rfl
+    gemm_shapes = {k: {"calls": v[0], "ms": round(v[1], 4), "tflops": round(v[2] / (v[1] / 1e3) / 1e12, 1)}
+                   for k, v in sorted(shapes.items(), key=lambda kv: -kv[1][1])}
 
     # end to end through the C ABI from pinned host buffers
     pin_tok = [torch.from_numpy(b[0]).pin_memory() for b in host_batches]
@@ -363,6 +375,7 @@ def main():
                      "peak_source": "MEASURED_PEAKS.json bf16_tflops_sustained (kernel timed inside a long step)",
                      "traffic": None},
         "kernels": kernels,
+        "gemm_shapes": gemm_shapes,
         "e2e": {"value": round(world * M / e2e_s, 1), "unit": "tokens/s", "h2d_bytes_per_step": 2 * M * 4,
                 "d2h_bytes_per_step": 8, "path": "gpt2_train_step_host, pinned host tokens, eager launches"},
         "gpu_launches": (n_kernels * args.steps) if n_kernels else None,

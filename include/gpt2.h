@@ -152,6 +152,12 @@ const float* gpt2_device_norm(gpt2_t* h);
 int gpt2_profile(gpt2_t* h, int on);
 int gpt2_profile_read(gpt2_t* h, int kernel_class, int* regions, double* ms, double* flops,
                       double* bytes);
+/* The recorded regions one by one (in issue order): count, then region i's
+ * class, dims (GEMM regions: M, N, K, A MN-major, B MN-major, epilogue kind;
+ * zeros otherwise; int[6]), milliseconds, flops and bytes. */
+int gpt2_profile_regions(gpt2_t* h);
+int gpt2_profile_region(gpt2_t* h, int i, int* kernel_class, int* dims, double* ms, double* flops,
+                        double* bytes);
 
 /* Synchronise the stream, read and clear the device status word; returns
  * GPT2_OK, GPT2_E_TOKEN, GPT2_E_TIMEOUT or GPT2_E_NONFINITE. */

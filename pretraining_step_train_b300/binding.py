@@ -42,6 +42,9 @@ SIGNATURES = {
     "gpt2_profile": (_i, [_p, _i]),
     "gpt2_profile_read": (_i, [_p, _i, ct.POINTER(_i), ct.POINTER(ct.c_double), ct.POINTER(ct.c_double),
                                ct.POINTER(ct.c_double)]),
+    "gpt2_profile_regions": (_i, [_p]),
+    "gpt2_profile_region": (_i, [_p, _i, ct.POINTER(_i), ct.POINTER(_i), ct.POINTER(ct.c_double),
+                                 ct.POINTER(ct.c_double), ct.POINTER(ct.c_double)]),
     "gpt2_sync_status": (_i, [_p]),
     "gpt2_strerror": (ct.c_char_p, [_i]),
     "gpt2_last_cuda_error": (ct.c_char_p, []),
@@ -199,6 +202,17 @@ class Step:
             check(lib().gpt2_profile_read(self.h, i, ct.byref(n), ct.byref(ms), ct.byref(fl), ct.byref(by)),
                   "gpt2_profile_read")
             out[name] = (n.value, ms.value, fl.value, by.value)
+        return out
+
+    def profile_regions(self):
+        """[(class name, dims tuple, ms, flops, bytes)] of every recorded region in issue order."""
+        out = []
+        for i in range(lib().gpt2_profile_regions(self.h)):
+            c, ms, fl, by = ct.c_int(), ct.c_double(), ct.c_double(), ct.c_double()
+            dims = (ct.c_int * 6)()
+            check(lib().gpt2_profile_region(self.h, i, ct.byref(c), dims, ct.byref(ms), ct.byref(fl),
+                                            ct.byref(by)), "gpt2_profile_region")
+            out.append((KERNEL_CLASSES[c.value], tuple(dims), ms.value, fl.value, by.value))
         return out
 
     def device_loss_ptr(self) -> int:

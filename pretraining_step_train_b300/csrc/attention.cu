@@ -434,10 +434,34 @@ int attn_fwd_bf16(const AttnArgs& a, cudaStream_t s) {
   return (int)cudaGetLastError();
 }
 
+// D[b, h, i] = sum_c dO[i, c] O[i, c] for d = 64: 8 threads per row, 16 B each.
+__global__ void __launch_bounds__(256) k_attn_rowdot64(AttnArgs a) {
+  const long long gid = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  const long long row = gid >> 3;
+  const int part = (int)(gid & 7);
+  const long long rows = (long long)a.B * a.H * a.T;
+  float s = 0.f;
+  if (row < rows) {
+    const int i = (int)(row % a.T);
+    const int bh = (int)(row / a.T);
+    const int b = bh / a.H, h = bh % a.H;
+    const long long off = b * a.osb + h * a.osh + (long long)i * a.ost + part * 8;
+    float o[8], g[8];
+    load16(static_cast<const bf16*>(a.o) + off, o);
+    load16(static_cast<const bf16*>(a.dO) + off, g);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) s += o[e] * g[e];
+  }
+  s += __shfl_xor_sync(0xffffffffu, s, 1);
+  s += __shfl_xor_sync(0xffffffffu, s, 2);
+  s += __shfl_xor_sync(0xffffffffu, s, 4);
+  if (row < rows && part == 0) a.Dbuf[row] = s;
+}
+
 int attn_bwd_bf16(const AttnArgs& a, cudaStream_t s) {
   if (!strides_ok(a)) return (int)cudaErrorInvalidValue;
   long long rows = (long long)a.B * a.H * a.T;
-  k_attn_rowdot<bf16><<<(unsigned)((rows * 32 + 255) / 256), 256, 0, s>>>(a);
+  k_attn_rowdot64<<<(unsigned)((rows * 8 + 255) / 256), 256, 0, s>>>(a);
   dim3 grid((a.T + 63) / 64, a.B * a.H);
   k_attn_bwd_dkdv_bf16<<<grid, 128, 0, s>>>(a);
   k_attn_bwd_dq_bf16<<<grid, 128, 0, s>>>(a);

@@ -176,6 +176,7 @@ int validate(const Shape& s) {
 struct ProfRec {
   int cls, ev0, ev1;
   double flops, bytes;
+  int dims[6];  // GEMM regions: M, N, K, a_mn, b_mn, epilogue
 };
 
 struct gpt2 {
@@ -203,10 +204,13 @@ int prof_begin(gpt2* h) {
   cudaEventRecord(h->evpool[h->evnext], h->stream);
   return h->evnext++;
 }
-void prof_end(gpt2* h, int i0, int cls, double flops, double bytes) {
+void prof_end(gpt2* h, int i0, int cls, double flops, double bytes, const int* dims = nullptr) {
   if (i0 < 0) return;
   cudaEventRecord(h->evpool[h->evnext], h->stream);
-  h->recs.push_back(ProfRec{cls, i0, h->evnext, flops, bytes});
+  ProfRec r{cls, i0, h->evnext, flops, bytes, {0, 0, 0, 0, 0, 0}};
+  if (dims)
+    for (int i = 0; i < 6; ++i) r.dims[i] = dims[i];
+  h->recs.push_back(r);
   h->evnext++;
 }
 // Run `stmt` as one timed region of kernel class `cls` with its algorithmic flops / bytes.
@@ -249,10 +253,12 @@ int linear(gpt2* h, GemmArgs g, int splits = 1) {
   const double flops = 2.0 * g.M * g.N * (double)g.K;
   const double bytes = ((double)g.M * g.K + (double)g.N * g.K + (double)g.M * g.N) * sizeof(T);
   int e = 0;
+  const int dims[6] = {g.M, g.N, g.K, g.a_mn, g.b_mn, g.epi};
   if (sizeof(T) == 2) {
     const int eff = gemm_tc_effective_splits(g.K, splits);
-    REGION(GPT2_K_GEMM, flops, bytes,
-           e = gemm_tc(g, eff, h->at<void>(h->p.splitk_ws), h->p.splitk_bytes, status, h->stream, 0));
+    const int pi = prof_begin(h);
+    e = gemm_tc(g, eff, h->at<void>(h->p.splitk_ws), h->p.splitk_bytes, status, h->stream, 0);
+    prof_end(h, pi, GPT2_K_GEMM, flops, bytes, dims);
     if (e) return e;
     if (eff > 1)
       REGION(GPT2_K_SPLITK, 0.0, (double)g.M * g.N * (4.0 * eff + 2.0),
@@ -260,7 +266,9 @@ int linear(gpt2* h, GemmArgs g, int splits = 1) {
                            h->stream));
     return (int)cudaGetLastError();
   }
-  REGION(GPT2_K_GEMM, flops, bytes, e = gemm_simt(g, h->stream));
+  const int pi = prof_begin(h);
+  e = gemm_simt(g, h->stream);
+  prof_end(h, pi, GPT2_K_GEMM, flops, bytes, dims);
   return e;
 }
 
@@ -386,14 +394,15 @@ int backward_impl(gpt2* h) {
   REGION(GPT2_K_LN_BWD, 0.0, lnb_first,
          layernorm_bwd<T>(dres, dres_b, dsmall, P.res(L), h->at<float>(h->p.lnf_mean),
                           h->at<float>(h->p.lnf_rstd), P.param(P_LNFW), P.grad(P_LNFW),
-                          P.grad(P_LNFB), lnbp, M, C, 0, st));
+                          P.grad(P_LNFB), L > 0 ? P.grad(P_FCPB, L - 1) : nullptr, lnbp, M, C, 0,
+                          st));
   for (int l = L - 1; l >= 0; --l) {
     // MLP projection: x2 = x1 + fca Wfcp^T + b
     g = GemmArgs();
     g.A = dcur; g.lda = C; g.a_mn = 1; g.B = P.fca(l); g.ldb = 4 * C; g.b_mn = 1;
     g.M = C; g.N = 4 * C; g.K = M; g.D = P.grad(P_FCPW, l); g.ldd = 4 * C;
     CKI(linear<T>(h, g, h->p.splits_fcp));
-    REGION(GPT2_K_BIAS_GRAD, 0.0, MC * E, colsum<T>(P.grad(P_FCPB, l), dcur, M, C, C, csp, st));
+    // the fcproj bias gradient (column sum of dcur) came out of the previous LayerNorm backward
     g = GemmArgs();
     g.A = dcur; g.lda = C; g.B = P.param(P_FCPW, l); g.ldb = 4 * C; g.b_mn = 1;
     g.M = M; g.N = 4 * C; g.K = C; g.epi = EPI_GELU_BWD; g.aux = P.fch(l); g.ldaux = 4 * C;
@@ -412,13 +421,12 @@ int backward_impl(gpt2* h) {
     REGION(GPT2_K_LN_BWD, 0.0, lnb_acc,
            layernorm_bwd<T>(dres, dres_b, dsmall, P.x1(l), P.stat(h->p.ln2_mean, l),
                             P.stat(h->p.ln2_rstd, l), P.param(P_LN2W, l), P.grad(P_LN2W, l),
-                            P.grad(P_LN2B, l), lnbp, M, C, 1, st));
+                            P.grad(P_LN2B, l), P.grad(P_APB, l), lnbp, M, C, 1, st));
     // attention projection: x1 = x + atty Wap^T + b
     g = GemmArgs();
     g.A = dcur; g.lda = C; g.a_mn = 1; g.B = P.atty(l); g.ldb = C; g.b_mn = 1;
     g.M = C; g.N = C; g.K = M; g.D = P.grad(P_APW, l); g.ldd = C;
     CKI(linear<T>(h, g, h->p.splits_ap));
-    REGION(GPT2_K_BIAS_GRAD, 0.0, MC * E, colsum<T>(P.grad(P_APB, l), dcur, M, C, C, csp, st));
     g = GemmArgs();
     g.A = dcur; g.lda = C; g.B = P.param(P_APW, l); g.ldb = C; g.b_mn = 1;
     g.M = M; g.N = C; g.K = C; g.D = dsmall; g.ldd = C;
@@ -449,7 +457,8 @@ int backward_impl(gpt2* h) {
     REGION(GPT2_K_LN_BWD, 0.0, lnb_acc,
            layernorm_bwd<T>(dres, dres_b, dsmall, P.res(l), P.stat(h->p.ln1_mean, l),
                             P.stat(h->p.ln1_rstd, l), P.param(P_LN1W, l), P.grad(P_LN1W, l),
-                            P.grad(P_LN1B, l), lnbp, M, C, 1, st));
+                            P.grad(P_LN1B, l), l > 0 ? P.grad(P_FCPB, l - 1) : nullptr, lnbp, M, C,
+                            1, st));
   }
   // encoder: dwte[tok] += dx0 in a fixed order, dwpe = sum over the batch
   uint32_t* order = h->at<uint32_t>(h->p.order);
@@ -559,6 +568,27 @@ int gpt2_profile(gpt2_t* h, int on) {
     h->evnext = 0;
   }
   h->prof_on = on != 0;
+  return GPT2_OK;
+}
+
+int gpt2_profile_regions(gpt2_t* h) {
+  if (!h) return GPT2_E_INVAL;
+  return (int)h->recs.size();
+}
+
+int gpt2_profile_region(gpt2_t* h, int i, int* kernel_class, int* dims, double* ms, double* flops,
+                        double* bytes) {
+  if (!h || i < 0 || i >= (int)h->recs.size()) return GPT2_E_INVAL;
+  CK(cudaStreamSynchronize(h->stream));
+  const ProfRec& r = h->recs[i];
+  float x = 0.f;
+  CK(cudaEventElapsedTime(&x, h->evpool[r.ev0], h->evpool[r.ev1]));
+  if (kernel_class) *kernel_class = r.cls;
+  if (dims)
+    for (int k = 0; k < 6; ++k) dims[k] = r.dims[k];
+  if (ms) *ms = x;
+  if (flops) *flops = r.flops;
+  if (bytes) *bytes = r.bytes;
   return GPT2_OK;
 }
 

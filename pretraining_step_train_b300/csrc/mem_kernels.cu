@@ -140,51 +140,84 @@ void layernorm_fwd(T* y, float* mean, float* rstd, const T* x, const T* w, const
   else k_layernorm_fwd<T, 8><<<grid, block, 0, s>>>(y, mean, rstd, x, w, b, M, C);
 }
 
+// ------------------------------------------------------------------ fixed-order partial sums
+// out_j[c] = sum over parts of partials[p][j * seg + c] for j = 0..2: each
+// block owns 32 columns, warp w sums parts w, w+8, ..., and the 8 warp sums
+// are then added in warp order.  Deterministic.
+template <typename T>
+__global__ void __launch_bounds__(256)
+    k_reduce_parts(T* __restrict__ o0, T* __restrict__ o1, T* __restrict__ o2,
+                   const float* __restrict__ partials, int nparts, int width, int seg) {
+  __shared__ float sh[8][33];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c = blockIdx.x * 32 + lane;
+  float acc = 0.f;
+  if (c < width)
+    for (int p = warp; p < nparts; p += 8) acc += partials[(long long)p * width + c];
+  sh[warp][lane] = acc;
+  __syncthreads();
+  if (warp == 0 && c < width) {
+    float t = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) t += sh[w][lane];
+    const int j = c / seg, cc = c % seg;
+    T* o = j == 0 ? o0 : (j == 1 ? o1 : o2);
+    if (o) o[cc] = from_f<T>(t);
+  }
+}
+
+template <typename T>
+static void reduce_parts(T* o0, T* o1, T* o2, const float* partials, int nparts, int width, int seg,
+                         cudaStream_t s) {
+  k_reduce_parts<T><<<(width + 31) / 32, 256, 0, s>>>(o0, o1, o2, partials, nparts, width, seg);
+}
+
 // ------------------------------------------------------------------ LayerNorm backward
 // dx = rstd * (g - mean(g) - xhat * mean(g * xhat)),  g = dy * w.
 // dres = (accumulate ? dres : 0) + dx in fp32; dres_b (if given) = storage copy.
-// dw = sum_rows dy * xhat, db = sum_rows dy: per-lane register accumulators,
-// combined across the block's warps in a fixed order, then across blocks.
-constexpr int kLnbBlocks = 256;
-constexpr int kLnbWarps = 8;
+// Column sums per block, each warp in its own shared-memory slice (no
+// atomics): dw = sum dy * xhat, db = sum dy and, when dsum is wanted, the
+// column sum of the new dres (the next projection's bias gradient).
+constexpr int kLnbBlocks = 592;
+constexpr int kLnbWarps = 4;
 
 template <typename T, int MAXV>
 __global__ void __launch_bounds__(kLnbWarps * 32)
     k_layernorm_bwd(float* __restrict__ dres, T* __restrict__ dres_b, const T* __restrict__ dy,
                     const T* __restrict__ x, const float* __restrict__ mean,
                     const float* __restrict__ rstd, const T* __restrict__ w,
-                    float* __restrict__ partials, int M, int C, int accumulate, int rows_per_block) {
+                    float* __restrict__ partials, int M, int C, int accumulate, int want_sum,
+                    int rows_per_block) {
   constexpr int N = V16<T>::N;
-  extern __shared__ float sred[];  // [2C]
+  extern __shared__ float sacc[];  // [kLnbWarps][3][C]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nv = C / N;
-  float wv[MAXV][N], adw[MAXV][N], adb[MAXV][N];
+  float* mine = sacc + warp * 3 * C;
+  for (int i = lane; i < 3 * C; i += 32) mine[i] = 0.f;
+  float wv[MAXV][N];
 #pragma unroll
   for (int j = 0; j < MAXV; ++j) {
     int vi = lane + j * 32;
-#pragma unroll
-    for (int e = 0; e < N; ++e) adw[j][e] = adb[j][e] = 0.f;
     if (vi < nv) load16(w + vi * N, wv[j]);
   }
   const int r0 = blockIdx.x * rows_per_block;
   const int r1 = min(M, r0 + rows_per_block);
   for (int r = r0 + warp; r < r1; r += kLnbWarps) {
     const float mu = mean[r], rs = rstd[r];
-    float g[MAXV][N], xh[MAXV][N], dyv[MAXV][N];
+    float dyv[MAXV][N], xh[MAXV][N];
     float sg = 0.f, sgx = 0.f;
 #pragma unroll
     for (int j = 0; j < MAXV; ++j) {
       int vi = lane + j * 32;
       if (vi < nv) {
-        float xv[N];
         load16(dy + (long long)r * C + vi * N, dyv[j]);
-        load16(x + (long long)r * C + vi * N, xv);
+        load16(x + (long long)r * C + vi * N, xh[j]);
 #pragma unroll
         for (int e = 0; e < N; ++e) {
-          xh[j][e] = (xv[e] - mu) * rs;
-          g[j][e] = dyv[j][e] * wv[j][e];
-          sg += g[j][e];
-          sgx += g[j][e] * xh[j][e];
+          xh[j][e] = (xh[j][e] - mu) * rs;
+          const float g = dyv[j][e] * wv[j][e];
+          sg += g;
+          sgx += g * xh[j][e];
         }
       }
     }
@@ -206,11 +239,13 @@ __global__ void __launch_bounds__(kLnbWarps * 32)
 #pragma unroll
           for (int e = 0; e < N; ++e) d[e] = 0.f;
         }
+        float* m0 = mine + vi * N;
 #pragma unroll
         for (int e = 0; e < N; ++e) {
-          d[e] += rs * (g[j][e] - sg - xh[j][e] * sgx);
-          adw[j][e] += dyv[j][e] * xh[j][e];
-          adb[j][e] += dyv[j][e];
+          d[e] += rs * (dyv[j][e] * wv[j][e] - sg - xh[j][e] * sgx);
+          m0[e] += dyv[j][e] * xh[j][e];
+          m0[C + e] += dyv[j][e];
+          if (want_sum) m0[2 * C + e] += d[e];
         }
 #pragma unroll
         for (int e = 0; e < N; e += 4)
@@ -219,62 +254,45 @@ __global__ void __launch_bounds__(kLnbWarps * 32)
       }
     }
   }
-  // fixed-order combination of the warps' accumulators
-  for (int i = threadIdx.x; i < 2 * C; i += blockDim.x) sred[i] = 0.f;
   __syncthreads();
-  for (int ww = 0; ww < kLnbWarps; ++ww) {
-    if (warp == ww) {
+  const int width = (want_sum ? 3 : 2) * C;
+  for (int i = threadIdx.x; i < width; i += blockDim.x) {
+    float t = 0.f;
 #pragma unroll
-      for (int j = 0; j < MAXV; ++j) {
-        int vi = lane + j * 32;
-        if (vi < nv) {
-#pragma unroll
-          for (int e = 0; e < N; ++e) {
-            sred[vi * N + e] += adw[j][e];
-            sred[C + vi * N + e] += adb[j][e];
-          }
-        }
-      }
-    }
-    __syncthreads();
+    for (int ww = 0; ww < kLnbWarps; ++ww) t += sacc[ww * 3 * C + i];
+    partials[(long long)blockIdx.x * width + i] = t;
   }
-  for (int i = threadIdx.x; i < 2 * C; i += blockDim.x)
-    partials[(long long)blockIdx.x * 2 * C + i] = sred[i];
 }
 
-template <typename T>
-__global__ void k_sum_partials_2(T* __restrict__ dw, T* __restrict__ db,
-                                 const float* __restrict__ partials, int nblocks, int C) {
-  int c = blockIdx.x * blockDim.x + threadIdx.x;
-  if (c >= 2 * C) return;
-  float s = 0.f;
-  for (int b = 0; b < nblocks; ++b) s += partials[(long long)b * 2 * C + c];
-  if (c < C) dw[c] = from_f<T>(s);
-  else db[c - C] = from_f<T>(s);
-}
-
-size_t layernorm_bwd_partials_floats(int C) { return (size_t)kLnbBlocks * 2 * C; }
+size_t layernorm_bwd_partials_floats(int C) { return (size_t)kLnbBlocks * 3 * C; }
 
 template <typename T>
 void layernorm_bwd(float* dres, T* dres_b, const T* dy, const T* x, const float* mean,
-                   const float* rstd, const T* w, T* dw, T* db, float* partials, int M, int C,
-                   int accumulate, cudaStream_t s) {
+                   const float* rstd, const T* w, T* dw, T* db, T* dsum, float* partials, int M,
+                   int C, int accumulate, cudaStream_t s) {
   const int nv = C / V16<T>::N;
   const int per = (nv + 31) / 32;
   int nblocks = (M + kLnbWarps - 1) / kLnbWarps;
   if (nblocks > kLnbBlocks) nblocks = kLnbBlocks;
   const int rpb = (M + nblocks - 1) / nblocks;
-  const size_t sm = 2 * C * sizeof(float);
-#define LNB(P)                                                                                  \
-  k_layernorm_bwd<T, P><<<nblocks, kLnbWarps * 32, sm, s>>>(dres, dres_b, dy, x, mean, rstd, w, \
-                                                            partials, M, C, accumulate, rpb)
+  const size_t sm = (size_t)kLnbWarps * 3 * C * sizeof(float);
+  const int want_sum = dsum != nullptr;
+#define LNB(P)                                                                                    \
+  do {                                                                                            \
+    if (sm > 48 * 1024)                                                                           \
+      cudaFuncSetAttribute(k_layernorm_bwd<T, P>, cudaFuncAttributeMaxDynamicSharedMemorySize,    \
+                           (int)sm);                                                              \
+    k_layernorm_bwd<T, P><<<nblocks, kLnbWarps * 32, sm, s>>>(dres, dres_b, dy, x, mean, rstd, w, \
+                                                              partials, M, C, accumulate,         \
+                                                              want_sum, rpb);                     \
+  } while (0)
   if (per <= 1) LNB(1);
   else if (per <= 2) LNB(2);
   else if (per <= 3) LNB(3);
   else if (per <= 4) LNB(4);
   else LNB(8);
 #undef LNB
-  k_sum_partials_2<T><<<(2 * C + 255) / 256, 256, 0, s>>>(dw, db, partials, nblocks, C);
+  reduce_parts<T>(dw, db, dsum, partials, nblocks, (want_sum ? 3 : 2) * C, C, s);
 }
 
 // ------------------------------------------------------------------ column sums (bias grads)
@@ -285,7 +303,7 @@ __global__ void __launch_bounds__(256)
     k_colsum_partial(float* __restrict__ partials, const T* __restrict__ x, int M, int N,
                      long long ld, int rows_per_block) {
   constexpr int NV = V16<T>::N;
-  __shared__ float sred[32 * NV];
+  __shared__ float sred[8][32 * NV];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = (blockIdx.x * 32 + lane) * NV;
   float acc[NV];
@@ -293,36 +311,31 @@ __global__ void __launch_bounds__(256)
   for (int e = 0; e < NV; ++e) acc[e] = 0.f;
   const int r0 = blockIdx.y * rows_per_block, r1 = min(M, r0 + rows_per_block);
   if (c < N) {
-    for (int r = r0 + warp; r < r1; r += 8) {
+    int r = r0 + warp;
+    for (; r + 8 < r1; r += 16) {
+      float v[NV], u[NV];
+      load16(x + (long long)r * ld + c, v);
+      load16(x + (long long)(r + 8) * ld + c, u);
+#pragma unroll
+      for (int e = 0; e < NV; ++e) acc[e] += v[e] + u[e];
+    }
+    for (; r < r1; r += 8) {
       float v[NV];
       load16(x + (long long)r * ld + c, v);
 #pragma unroll
       for (int e = 0; e < NV; ++e) acc[e] += v[e];
     }
   }
-  for (int i = threadIdx.x; i < 32 * NV; i += 256) sred[i] = 0.f;
-  __syncthreads();
-  for (int ww = 0; ww < 8; ++ww) {
-    if (warp == ww) {
 #pragma unroll
-      for (int e = 0; e < NV; ++e) sred[lane * NV + e] += acc[e];
-    }
-    __syncthreads();
-  }
+  for (int e = 0; e < NV; ++e) sred[warp][lane * NV + e] = acc[e];
+  __syncthreads();
   for (int i = threadIdx.x; i < 32 * NV; i += 256) {
     int cc = blockIdx.x * 32 * NV + i;
-    if (cc < N) partials[(long long)blockIdx.y * N + cc] = sred[i];
+    float t = 0.f;
+#pragma unroll
+    for (int ww = 0; ww < 8; ++ww) t += sred[ww][i];
+    if (cc < N) partials[(long long)blockIdx.y * N + cc] = t;
   }
-}
-
-template <typename T>
-__global__ void k_colsum_final(T* __restrict__ out, const float* __restrict__ partials, int nrb,
-                               int N) {
-  int c = blockIdx.x * blockDim.x + threadIdx.x;
-  if (c >= N) return;
-  float s = 0.f;
-  for (int b = 0; b < nrb; ++b) s += partials[(long long)b * N + c];
-  out[c] = from_f<T>(s);
 }
 
 size_t colsum_partials_floats(int N) { return (size_t)kColsumRowBlocks * N; }
@@ -330,12 +343,12 @@ size_t colsum_partials_floats(int N) { return (size_t)kColsumRowBlocks * N; }
 template <typename T>
 void colsum(T* out, const T* x, int M, int N, long long ld, float* partials, cudaStream_t s) {
   constexpr int NV = V16<T>::N;
-  int nrb = (M + 63) / 64;
+  int nrb = (M + 127) / 128;
   if (nrb > kColsumRowBlocks) nrb = kColsumRowBlocks;
   const int rpb = (M + nrb - 1) / nrb;
   dim3 grid((N + 32 * NV - 1) / (32 * NV), nrb);
   k_colsum_partial<T><<<grid, 256, 0, s>>>(partials, x, M, N, ld, rpb);
-  k_colsum_final<T><<<(N + 255) / 256, 256, 0, s>>>(out, partials, nrb, N);
+  reduce_parts<T>(out, (T*)nullptr, (T*)nullptr, partials, nrb, N, N, s);
 }
 
 // ------------------------------------------------------------------ elementwise
@@ -814,7 +827,7 @@ void adamw(float* master, P* param_copy, const G* grad, float* m, float* v, long
   template void layernorm_fwd<T>(T*, float*, float*, const T*, const T*, const T*, int, int,       \
                                  cudaStream_t);                                                    \
   template void layernorm_bwd<T>(float*, T*, const T*, const T*, const float*, const float*,       \
-                                 const T*, T*, T*, float*, int, int, int, cudaStream_t);           \
+                                 const T*, T*, T*, T*, float*, int, int, int, cudaStream_t);       \
   template void colsum<T>(T*, const T*, int, int, long long, float*, cudaStream_t);                \
   template void gelu_fwd<T>(T*, const T*, long long, cudaStream_t);                                \
   template void gelu_bwd<T>(T*, const T*, const T*, long long, cudaStream_t);                      \

@@ -61,7 +61,8 @@ def test_gemm_bf16_out_and_splitk(a_mn, b_mn):
                                                   N, a_mn, b_mn, f32, splits, ws.data_ptr(), ws.numel(), None))
             torch.cuda.synchronize()
             err = rel_l2(to_np(D), ref)
-            assert err < (1e-6 if f32 else 4e-3), (splits, f32, err)
+            # fp32 sums of K=4096 products: ~sqrt(K) * 2^-24 relative; bf16 output adds 2^-9
+            assert err < (2e-5 if f32 else 4e-3), (splits, f32, err)
 
 
 def test_gemm_deterministic():
@@ -72,7 +73,7 @@ def test_gemm_deterministic():
     outs = []
     for _ in range(2):
         D = torch.empty((M, N), dtype=torch.float32, device="cuda")
-        ws = torch.empty(8 * M * N * 4, dtype=torch.uint8, device="cuda")
+        ws = torch.empty(16 * M * N * 4, dtype=torch.uint8, device="cuda")
         binding.check(binding.lib().gemm_bf16(A.data_ptr(), B.data_ptr(), D.data_ptr(), M, N, K, lda, ldb, N,
                                               1, 1, 1, 0, ws.data_ptr(), ws.numel(), None))
         outs.append(to_np(D))

@@ -364,3 +364,15 @@ def test_encoder_fp32_references():
     np.add.at(ref, tok.reshape(-1), dx0.reshape(-1, C))
     np.testing.assert_array_equal(dwte, ref)
     np.testing.assert_array_equal(dwpe, dx0.sum(axis=0))
+
+
+def test_key_bias_gradient_vanishes():
+    """Softmax is invariant to a per-query shift of the scores, so the key part
+    of the QKV bias receives exactly zero gradient (up to rounding)."""
+    cfg, P, tok, tgt = tiny_case()
+    _, cache = O.forward(P, tok, tgt, cfg)
+    G = O.backward(cache, cfg)
+    C = cfg.C
+    gk = G["qkvb"][:, C:2 * C]
+    assert np.abs(gk).max() < 1e-14 * max(1.0, np.abs(G["qkvb"]).max()) + 1e-15
+    assert np.abs(G["qkvb"][:, :C]).max() > 1e-8 and np.abs(G["qkvb"][:, 2 * C:]).max() > 1e-8

@@ -34,19 +34,35 @@ def _gpu_step(cfg, B, prec, flat, tok, tgt, steps=1):
     return out
 
 
+ZERO_INIT = ("ln1b", "qkvb", "attprojb", "ln2b", "fcb", "fcprojb", "lnfb")
+
+
 def _compare(cfg, P, res, ref, loss_tol, grad_tol, w_tol, flat):
+    """Loss, every gradient tensor, the norm, and the post-AdamW weights.
+
+    Weights: relative L2 over the whole parameter vector and over every tensor
+    that does not start at zero.  A zero-initialised tensor holds only the
+    first AdamW update, about -lr * sign(g), which is ill-conditioned where
+    g sits at the rounding level (the key-bias gradient is exactly zero in
+    exact arithmetic because softmax ignores a per-query shift); those
+    tensors are compared on the elements whose gradient is well above it."""
     L, C, Vpad, T = cfg.L, cfg.C, cfg.Vpad, cfg.T
     assert abs(res["loss"] - ref["loss"]) / abs(ref["loss"]) < loss_tol, (res["loss"], ref["loss"])
     G = synth.unflatten_params(res["grads"], L, C, Vpad, T)
-    worst = {}
-    for k in G:
-        e = rel_l2(G[k], ref["grads"][k])
-        worst[k] = e
+    worst = {k: rel_l2(G[k], ref["grads"][k]) for k in G}
     assert max(worst.values()) < grad_tol, worst
     assert abs(res["norm"] - ref["norm"]) / ref["norm"] < grad_tol
+    ref_flat = np.concatenate([np.asarray(ref["params"][k]).reshape(-1) for k, _ in synth.param_shapes(L, C, Vpad, T)])
+    assert rel_l2(res["master"], ref_flat) < w_tol
     W = synth.unflatten_params(res["master"], L, C, Vpad, T)
     for k in W:
-        assert rel_l2(W[k], ref["params"][k]) < w_tol, k
+        if k in ZERO_INIT:
+            g = np.abs(ref["grads"][k])
+            big = g > 100 * grad_tol * (np.sqrt(np.mean(g ** 2)) + 1e-30)
+            if big.any():
+                assert rel_l2(W[k][big], ref["params"][k][big]) < w_tol, k
+        else:
+            assert rel_l2(W[k], ref["params"][k]) < w_tol, k
     return worst
 
 
