@@ -122,8 +122,12 @@ def count_graph_kernels(graph):
         return None
 
 
-def cpu_baseline(c, seconds_hint=True):
-    """The oracle (numpy float64) on one sequence of the workload: tokens/s on host cores."""
+def cpu_baseline(c, budget_s=20.0):
+    """The oracle (numpy float64) on a bounded sample of the workload: tokens/s on host cores.
+
+    The sample is a prefix of Ts positions of one sequence (causal, so a prefix
+    is a self-contained sub-problem) with Ts sized from a 64-position
+    calibration run so that the timed oracle step takes about budget_s."""
     import numpy as np
     from oracle import gpt2_oracle as O
     from pretraining_step_train_b300 import synth
@@ -136,11 +140,15 @@ def cpu_baseline(c, seconds_hint=True):
     P = synth.init_params(43, c["L"], c["C"], c["V"], c["Vpad"], c["T"], bf16_representable=True)
     tok, tgt = synth.token_batch(42, 1, c["T"], c["V"])
     t0 = time.perf_counter()
-    r = O.train_step(P, tok, tgt, cfg, lr=LR, t=1)
+    O.train_step(P, tok[:, :64], tgt[:, :64], cfg, lr=LR, t=1)  # calibration, untimed
+    per64 = time.perf_counter() - t0
+    Ts = int(max(64, min(c["T"], 64 * int(budget_s / per64))))
+    t0 = time.perf_counter()
+    r = O.train_step(P, tok[:, :Ts], tgt[:, :Ts], cfg, lr=LR, t=1)
     dt = time.perf_counter() - t0
-    return {"value": c["T"] / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": f"1 of {c['B']} sequences (T={c['T']}) of the step: forward+backward+clip+AdamW, "
-                      f"numpy float64, {dt:.1f} s", "loss": r["loss"]}
+    return {"value": round(Ts / dt, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"prefix of {Ts} positions of 1 of {c['B']} sequences (T={c['T']}): "
+                      f"forward+backward+clip+AdamW, numpy float64, {dt:.1f} s", "loss": r["loss"]}
 
 
 def run_reference(args, c):
@@ -199,8 +207,12 @@ def main():
     ap.add_argument("--no-graph", action="store_true", help="eager launches instead of a CUDA graph")
     ap.add_argument("--one-step", action="store_true",
                     help="set up, run one eager step and exit (for profiler launch lists)")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the sequences per step (smaller profiler captures)")
     args = ap.parse_args()
-    c = CONFIGS[args.config]
+    c = dict(CONFIGS[args.config])
+    if args.batch > 0:
+        c["B"] = args.batch
     if args.impl == "reference":
         run_reference(args, c)
         return
