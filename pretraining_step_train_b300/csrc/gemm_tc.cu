@@ -6,14 +6,19 @@
 //   backward  dX = dY W      A = dY (K-major), B = W  (MN-major)
 //             dW = dY^T X    A = dY (MN-major), B = X (MN-major), split over the rows
 //
-// Structure (one persistent CTA per SM, 6 warps):
+// Structure (one persistent CTA per SM, 10 warps):
 //   warp 0      TMA producer: 128B-swizzled A (128 x 64) and B (256 x 64) tiles
 //               into a 4-stage shared-memory ring, completion on mbarriers;
 //   warp 1      owns 512 TMEM columns (two 128 x 256 fp32 accumulators) and one
 //               thread issues tcgen05.mma (M=128, N=256, K=16) per 16-wide k step,
 //               releasing ring stages and finished accumulators with tcgen05.commit;
-//   warps 2-5   epilogue: tcgen05.ld 32 lanes x 32 columns at a time, fused
-//               bias / residual / GELU / GELU' / cross-entropy statistics, stores.
+//   warps 2-9   epilogue, two warps per TMEM lane quadrant (one per 128-column
+//               half): tcgen05.ld 32 rows x 32 columns at a time, fused bias /
+//               residual / GELU / GELU' / cross-entropy statistics, then the
+//               32 x 32 result is staged in 64B-swizzled shared memory and
+//               written by a TMA bulk tensor store (coalesced, asynchronous).
+//               Residual and pre-activation operands arrive the same way, by a
+//               TMA load of the matching 32 x 32 box, one chunk ahead.
 // The accumulator double buffer lets the epilogue of tile i overlap the
 // mainloop of tile i+1.  Every wait is bounded (about 2 s of %globaltimer);
 // on expiry the CTA latches ST_TIMEOUT in the status word, the other roles
@@ -30,18 +35,25 @@ constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
 constexpr int A_TILE = BM * BK * 2;  // 16 KB
 constexpr int B_TILE = BN * BK * 2;  // 32 KB
 constexpr int STAGE_BYTES = A_TILE + B_TILE;
+constexpr int RING_BYTES = STAGES * STAGE_BYTES;
 constexpr int TMEM_COLS = 2 * BN;
-constexpr int NUM_THREADS = 192;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+constexpr int EPI_WARPS = 8;
+constexpr int NUM_THREADS = 64 + 32 * EPI_WARPS;
+constexpr int BOX_BYTES = 2048;                 // one staged box: 32 rows x 64 bytes
+constexpr int STG_BYTES = 2 * BOX_BYTES;        // per epilogue warp
+constexpr int BAR_BYTES = 512;
+constexpr int SMEM_BYTES = 1024 + RING_BYTES + EPI_WARPS * STG_BYTES + BAR_BYTES;
 constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;
 
 struct TcParams {
   GemmArgs g;
   int mt, nt, splits, kps, total_kb;
   uint32_t idesc;
-  float* ws;
   unsigned* status;
   int poison;
+  int out_f32;  // D (or the split-K workspace) holds fp32
+  int load_x;   // the epilogue reads a [M, N] bf16 operand (residual or GELU pre-activation)
+  int m_fast;   // tile raster: consecutive tiles walk M (sharing a B tile) instead of N
 };
 
 int g_poison = 0;
@@ -166,122 +178,121 @@ __device__ __forceinline__ uint64_t operand_desc(uint32_t tile, int mn_major, in
   return mn_major ? sdesc(tile + kstep * 2048, 8192, 1024) : sdesc(tile + kstep * 32, 16, 1024);
 }
 
-__device__ __forceinline__ void store8_bf16(bf16* p, const float* v) {
-  uint4 u;
-  __nv_bfloat162 a = __floats2bfloat162_rn(v[0], v[1]), b = __floats2bfloat162_rn(v[2], v[3]),
-                 c = __floats2bfloat162_rn(v[4], v[5]), d = __floats2bfloat162_rn(v[6], v[7]);
-  u.x = *reinterpret_cast<uint32_t*>(&a);
-  u.y = *reinterpret_cast<uint32_t*>(&b);
-  u.z = *reinterpret_cast<uint32_t*>(&c);
-  u.w = *reinterpret_cast<uint32_t*>(&d);
-  *reinterpret_cast<uint4*>(p) = u;
-}
-__device__ __forceinline__ void load8_bf16(const bf16* p, float* v) {
-  uint4 u = *reinterpret_cast<const uint4*>(p);
-  const bf16* h = reinterpret_cast<const bf16*>(&u);
-#pragma unroll
-  for (int i = 0; i < 8; ++i) v[i] = __bfloat162float(h[i]);
+// Tile index -> (M tile, N tile, K split).  Consecutive tiles (one wave of
+// CTAs) share the tile of the larger operand, so it is read from DRAM about
+// once while the smaller operand is re-read from L2.
+__device__ __forceinline__ void tile_coords(const TcParams& p, int tile, int& m_t, int& n_t, int& sp) {
+  const int per = p.mt * p.nt;
+  sp = tile / per;
+  const int r = tile - sp * per;
+  if (p.m_fast) {
+    m_t = r % p.mt;
+    n_t = r / p.mt;
+  } else {
+    n_t = r % p.nt;
+    m_t = r / p.nt;
+  }
 }
 
-// Epilogue of 32 consecutive columns [n0, n0+32) of row m.
-__device__ __forceinline__ void epilogue_chunk(const TcParams& p, int sp, int m, int n0, float* v,
-                                               float& ce_m, float& ce_s, float& ce_t) {
-  const GemmArgs& g = p.g;
-  const bool row_ok = m < g.M;
-  if (p.splits > 1) {
-    if (!row_ok) return;
-    float* dst = p.ws + ((long long)sp * g.M + m) * g.N;
+
+// ------------------------------------------------------------------ epilogue helpers
+__device__ __forceinline__ void tma_load_x(uint32_t dst, const CUtensorMap* tm, uint32_t bar, int x,
+                                           int y) {
+  tma_load_2d(dst, tm, bar, x, y);
+}
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* tm, uint32_t src, int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(tm)),
+      "r"(src), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until at most N bulk groups of this thread are still reading shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// One staged box holds 32 rows of 64 bytes in the TMA 64-byte swizzle: the
+// 16-byte piece p of row r sits at r*64 + ((p ^ ((r >> 1) & 3)) << 4).  A
+// quarter-warp writing the same piece of 8 consecutive rows hits 8 distinct
+// 16-byte bank groups.
+__device__ __forceinline__ uint32_t box_addr(uint32_t box, int r, int p) {
+  return box + (uint32_t)(r * 64 + ((p ^ ((r >> 1) & 3)) << 4));
+}
+__device__ __forceinline__ void box_store_row(uint32_t box, int r, const uint32_t* w) {
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      int n = n0 + q * 4;
-      if (n < g.N)
-        *reinterpret_cast<float4*>(dst + n) = make_float4(v[q * 4], v[q * 4 + 1], v[q * 4 + 2], v[q * 4 + 3]);
-    }
-    return;
-  }
-  if (g.epi == EPI_CE) {
-    // logits rounded to bf16 are stored and used for the statistics
+  for (int p = 0; p < 4; ++p)
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(box_addr(box, r, p)), "r"(w[4 * p]),
+                 "r"(w[4 * p + 1]), "r"(w[4 * p + 2]), "r"(w[4 * p + 3])
+                 : "memory");
+}
+__device__ __forceinline__ void box_load_row_bf16(uint32_t box, int r, float* v) {
 #pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] = __bfloat162float(__float2bfloat16_rn(v[j]));
-    float cm = -INFINITY;
+  for (int p = 0; p < 4; ++p) {
+    uint32_t w0, w1, w2, w3;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
+                 : "r"(box_addr(box, r, p))
+                 : "memory");
+    const uint32_t w[4] = {w0, w1, w2, w3};
 #pragma unroll
-    for (int j = 0; j < 32; ++j)
-      if (n0 + j < g.V) cm = fmaxf(cm, v[j]);
-    if (cm > -INFINITY) {
-      float mn = fmaxf(ce_m, cm);
-      float s = (ce_m > -INFINITY) ? ce_s * __expf(ce_m - mn) : 0.f;
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (n0 + j < g.V) s += __expf(v[j] - mn);
-      ce_m = mn;
-      ce_s = s;
-    }
-    if (row_ok) {
-      const int t = g.targets[m];
-      if (t >= n0 && t < n0 + 32) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (n0 + j == t) ce_t = v[j];
-      }
-    }
-  }
-  if (!row_ok) return;
-  if (g.epi == EPI_F32) {
-    float* dst = static_cast<float*>(g.D) + (long long)m * g.ldd;
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      int n = n0 + q * 4;
-      if (n < g.N)
-        *reinterpret_cast<float4*>(dst + n) = make_float4(v[q * 4], v[q * 4 + 1], v[q * 4 + 2], v[q * 4 + 3]);
-    }
-    return;
-  }
-  bf16* dst = static_cast<bf16*>(g.D) + (long long)m * g.ldd;
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const int n = n0 + q * 8;
-    if (n >= g.N) continue;
-    float* w = v + q * 8;
-    if (g.epi == EPI_BIAS || g.epi == EPI_BIAS_RESID || g.epi == EPI_BIAS_GELU) {
-      float b[8];
-      load8_bf16(static_cast<const bf16*>(g.bias) + n, b);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) w[i] += b[i];
-    }
-    if (g.epi == EPI_BIAS_RESID) {
-      float r[8];
-      load8_bf16(static_cast<const bf16*>(g.resid) + (long long)m * g.ldr + n, r);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) w[i] += r[i];
-    }
-    if (g.epi == EPI_GELU_BWD) {
-      float h[8];
-      load8_bf16(static_cast<const bf16*>(g.aux) + (long long)m * g.ldaux + n, h);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) w[i] *= gelu_grad_f(h[i]);
-    }
-    store8_bf16(dst + n, w);
-    if (g.epi == EPI_BIAS_GELU) {
-      float a[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) a[i] = gelu_f(w[i]);
-      store8_bf16(static_cast<bf16*>(g.D2) + (long long)m * g.ldd + n, a);
+    for (int q = 0; q < 4; ++q) {
+      v[8 * p + 2 * q] = __uint_as_float(w[q] << 16);
+      v[8 * p + 2 * q + 1] = __uint_as_float(w[q] & 0xFFFF0000u);
     }
   }
+}
+__device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
+  __nv_bfloat162 t = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&t);
+}
+__device__ __forceinline__ void pack32_bf16(const float* v, uint32_t* w) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j) w[j] = pack2_bf16(v[2 * j], v[2 * j + 1]);
+}
+
+// Hardware tanh (MUFU, PTX tanh.approx.f32): relative error about 2^-11, far
+// below the bf16 rounding of the values it feeds.
+__device__ __forceinline__ float tanh_hw(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// tanh-form GELU and its derivative with the hardware tanh (bf16 epilogues only).
+__device__ __forceinline__ float gelu_hw(float x) {
+  const float u = x * (GELU_K + GELU_K * GELU_C * x * x);
+  const float hx = 0.5f * x;
+  return fmaf(hx, tanh_hw(u), hx);
+}
+__device__ __forceinline__ float gelu_grad_hw(float x) {
+  const float x2 = x * x;
+  const float th = tanh_hw(x * (GELU_K + GELU_K * GELU_C * x2));
+  const float du = GELU_K + 3.0f * GELU_K * GELU_C * x2;
+  return 0.5f * (1.0f + th) + 0.5f * x * (1.0f - th * th) * du;
 }
 
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-              const TcParams p) {
+              const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmD2,
+              const __grid_constant__ CUtensorMap tmX, const TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t s_tiles = smem_u32(smem);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
-  // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], done
+  const uint32_t s_stg = s_tiles + RING_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + RING_BYTES + EPI_WARPS * STG_BYTES);
+  // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], done, xload[EPI_WARPS][2]
   const uint32_t b_full = smem_u32(bars), b_empty = b_full + 8 * STAGES;
   const uint32_t b_tfull = b_empty + 8 * STAGES, b_tempty = b_tfull + 16, b_done = b_tempty + 16;
-  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bars + 2 * STAGES + 5);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * STAGES + 6);
+  const uint32_t b_xload = b_done + 8;
+  constexpr int NBARS = 2 * STAGES + 5 + 2 * EPI_WARPS;
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bars + NBARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + NBARS + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const GemmArgs& g = p.g;
@@ -294,14 +305,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(b_tfull + 8 * i, 1);
-      mbar_init(b_tempty + 8 * i, 128);
+      mbar_init(b_tempty + 8 * i, 32 * EPI_WARPS);
     }
     mbar_init(b_done, 1);
+    for (int i = 0; i < 2 * EPI_WARPS; ++i) mbar_init(b_xload + 8 * i, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmD)) : "memory");
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), TMEM_COLS);
@@ -322,7 +335,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int i = 0; i < STAGES; ++i) last_par[i] = -1;
       bool first = true;
       for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-        const int n_t = tile % p.nt, m_t = (tile / p.nt) % p.mt, sp = tile / (p.nt * p.mt);
+        int m_t, n_t, sp;
+        tile_coords(p, tile, m_t, n_t, sp);
         const int kb0 = sp * p.kps, kb1 = min(p.total_kb, kb0 + p.kps);
         bool stop = false;
         for (int kb = kb0; kb < kb1; ++kb) {
@@ -390,37 +404,192 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_wait_drain(b_done, 0);
     }
   } else {
-    // ---------------- epilogue warps 2..5 (TMEM lane quadrant = warp % 4)
-    const int quad = warp & 3;
-    const int r_in_tile = quad * 32 + lane;
+    // ---------------- epilogue warps 2..9: TMEM lane quadrant warp % 4, column half (warp-2)/4
+    const int ew = warp - 2, quad = warp & 3, hh = ew >> 2;
+    const uint32_t stg = s_stg + ew * STG_BYTES;   // two staged boxes
+    const uint32_t xbar = b_xload + 16 * ew;       // their load barriers
+    uint32_t xpar = 0;                             // bit b: parity of the next completion of xbar b
+    uint32_t xpend = 0;                            // bit b: a load into box b is in flight
+    int bx = 0;                                    // box of the current chunk
+    bool prev_stored = false;                      // the previous chunk issued a store
+    const int epi = g.epi;
+    const bool split = p.splits > 1;
+    // chunk (tile, c): rows m_t*BM + quad*32 .. +32, columns n_t*BN + hh*128 + c*32 .. +32
+    auto chunk_valid = [&](int tile, int c, int& x, int& y) {
+      if (tile >= ntiles) return false;
+      int m_t, n_t, sp;
+      tile_coords(p, tile, m_t, n_t, sp);
+      x = n_t * BN + hh * 128 + c * 32;
+      y = m_t * BM + quad * 32;
+      return x < g.N && y < g.M;
+    };
+    // Prefetch the x operand of chunk (tile, c) into box b (all lanes track the state).
+    auto x_issue = [&](int tile, int c, int b) {
+      int x, y;
+      if (!p.load_x || !chunk_valid(tile, c, x, y)) return;
+      if (lane == 0) {
+        bulk_wait_read<0>();  // the last store out of this box has finished reading it
+        mbar_expect_tx(xbar + 8 * b, BOX_BYTES);
+        tma_load_x(stg + b * BOX_BYTES, &tmX, xbar + 8 * b, x, y);
+      }
+      xpend |= 1u << b;
+    };
+    x_issue(blockIdx.x, 0, 0);
     int abuf = 0;
     uint32_t aphase = 0;
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-      const int n_t = tile % p.nt, m_t = (tile / p.nt) % p.mt, sp = tile / (p.nt * p.mt);
+      int m_t, n_t, sp;
+      tile_coords(p, tile, m_t, n_t, sp);
       if (!mbar_wait(b_tfull + 8 * abuf, aphase, abort_flag, p.status)) break;
       tc_fence_after();
-      const int m = m_t * BM + r_in_tile;
+      const int m = m_t * BM + quad * 32 + lane;
       float ce_m = -INFINITY, ce_s = 0.f, ce_t = 0.f;
+      bool stop = false;
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
+      for (int c = 0; c < 4; ++c) {
+        const int b = bx;
         uint32_t r[32];
-        tmem_ld32(tmem_base + ((uint32_t)(quad * 32) << 16) + abuf * BN + c * 32, r);
+        tmem_ld32(tmem_base + ((uint32_t)(quad * 32) << 16) + abuf * BN + hh * 128 + c * 32, r);
         tmem_ld_wait();
+        if (c == 3) {  // every TMEM read of this accumulator is done: hand it back to the MMA
+          tc_fence_before();
+          mbar_arrive(b_tempty + 8 * abuf);
+        }
+        // prefetch the next chunk's operand into the other box
+        if (c < 3) x_issue(tile, c + 1, b ^ 1);
+        else x_issue(tile + gridDim.x, 0, b ^ 1);
+        bx ^= 1;
+        int x0, y0;
+        if (!chunk_valid(tile, c, x0, y0)) { prev_stored = false; continue; }
         float v[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-        epilogue_chunk(p, sp, m, n_t * BN + c * 32, v, ce_m, ce_s, ce_t);
+        float xv[32];
+        if (p.load_x) {
+          if (!mbar_wait(xbar + 8 * b, (xpar >> b) & 1u, abort_flag, p.status)) { stop = true; break; }
+          xpar ^= 1u << b;
+          xpend &= ~(1u << b);
+          box_load_row_bf16(stg + b * BOX_BYTES, lane, xv);
+        }
+        const uint32_t box0 = stg + b * BOX_BYTES;
+        if (split || epi == EPI_F32) {
+          // fp32 result: two 16-column boxes (both staged boxes)
+          if (lane == 0) bulk_wait_read<0>();
+          __syncwarp();
+          box_store_row(stg, lane, r);
+          box_store_row(stg + BOX_BYTES, lane, r + 16);
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            const int z = split ? sp : 0;
+            tma_store_3d(&tmD, stg, x0, y0, z);
+            if (x0 + 16 < g.N) tma_store_3d(&tmD, stg + BOX_BYTES, x0 + 16, y0, z);
+            bulk_commit();
+          }
+          prev_stored = true;
+          continue;
+        }
+        if (epi == EPI_BIAS || epi == EPI_BIAS_RESID || epi == EPI_BIAS_GELU) {
+          const bf16* bias = static_cast<const bf16*>(g.bias);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            if (x0 + q * 8 < g.N) {
+              float bb[8];
+              load16<bf16>(bias + x0 + q * 8, bb);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) v[q * 8 + i] += bb[i];
+            }
+          }
+        }
+        if (epi == EPI_BIAS_RESID) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] += xv[j];
+        } else if (epi == EPI_GELU_BWD) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] *= gelu_grad_hw(xv[j]);
+        } else if (epi == EPI_CE) {
+          // logits rounded to bf16 are stored and used for the statistics
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = __bfloat162float(__float2bfloat16_rn(v[j]));
+          float cm = -INFINITY;
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (x0 + j < g.V) cm = fmaxf(cm, v[j]);
+          if (cm > -INFINITY) {
+            const float mn = fmaxf(ce_m, cm);
+            float s = (ce_m > -INFINITY) ? ce_s * __expf(ce_m - mn) : 0.f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (x0 + j < g.V) s += __expf(v[j] - mn);
+            ce_m = mn;
+            ce_s = s;
+          }
+          if (m < g.M) {
+            const int t = g.targets[m];
+            if (t >= x0 && t < x0 + 32) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (x0 + j == t) ce_t = v[j];
+            }
+          }
+        }
+        uint32_t w[16];
+        pack32_bf16(v, w);
+        if (epi == EPI_BIAS_GELU) {
+          // h and gelu(h): both staged boxes
+          float a[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) a[j] = gelu_hw(v[j]);
+          uint32_t wa[16];
+          pack32_bf16(a, wa);
+          if (lane == 0) bulk_wait_read<0>();
+          __syncwarp();
+          box_store_row(stg, lane, w);
+          box_store_row(stg + BOX_BYTES, lane, wa);
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(&tmD, stg, x0, y0, 0);
+            tma_store_3d(&tmD2, stg + BOX_BYTES, x0, y0, 0);
+            bulk_commit();
+          }
+          prev_stored = true;
+          continue;
+        }
+        if (!p.load_x) {
+          // box b was last read by the store two chunks back (or one, if the last chunk stored nothing)
+          if (lane == 0) {
+            if (prev_stored) bulk_wait_read<1>();
+            else bulk_wait_read<0>();
+          }
+          __syncwarp();
+        }
+        box_store_row(box0, lane, w);  // with load_x: in place over this row's operand
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_3d(&tmD, box0, x0, y0, 0);
+          bulk_commit();
+        }
+        prev_stored = true;
       }
-      if (g.epi == EPI_CE && p.splits == 1 && m < g.M) {
-        g.ce_max[(long long)m * g.ce_ld + n_t] = ce_m;
-        g.ce_sum[(long long)m * g.ce_ld + n_t] = ce_s;
+      if (stop) break;
+      // one statistics partial per row and 128-column half tile that starts inside N
+      if (epi == EPI_CE && !split && m < g.M && n_t * BN + hh * 128 < g.N) {
+        const int part = n_t * 2 + hh;
+        g.ce_max[(long long)m * g.ce_ld + part] = ce_m;
+        g.ce_sum[(long long)m * g.ce_ld + part] = ce_s;
         const int t = g.targets[m];
-        if (t >= n_t * BN && t < n_t * BN + BN) g.ce_tgt[m] = ce_t;
+        const int c0 = n_t * BN + hh * 128;
+        if (t >= c0 && t < c0 + 128) g.ce_tgt[m] = ce_t;
       }
-      tc_fence_before();
-      mbar_arrive(b_tempty + 8 * abuf);
       if (++abuf == 2) { abuf = 0; aphase ^= 1; }
     }
+    // never leave with bulk copies still reading or filling this warp's boxes
+    if (lane == 0) bulk_wait_all();
+    for (int b = 0; b < 2; ++b)
+      if (xpend & (1u << b)) mbar_wait_drain(xbar + 8 * b, (xpar >> b) & 1u);
+    __syncwarp();
   }
   __syncwarp();
   tc_fence_before();
@@ -450,7 +619,8 @@ PFN_encodeTiled_t get_encode() {
   return fn;
 }
 
-// 2-D bf16 tensor map over a row-major [outer, inner] matrix with leading dimension ld.
+// 2-D bf16 operand map over a row-major [outer, inner] matrix with leading
+// dimension ld (elements), 128-byte swizzle (the MMA's operand layout).
 bool make_tmap(CUtensorMap* tm, const void* base, long long inner, long long outer, long long ld,
                int box_inner, int box_outer) {
   PFN_encodeTiled_t enc = get_encode();
@@ -461,6 +631,38 @@ bool make_tmap(CUtensorMap* tm, const void* base, long long inner, long long out
   cuuint32_t es[2] = {1, 1};
   CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
                    box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// Epilogue box map: [depth][rows][cols] with leading dimension ld (elements) and
+// depth stride rows*ld, boxes of 64 bytes x 32 rows x 1, 64-byte swizzle.
+bool make_box_map(CUtensorMap* tm, const void* base, int f32, long long cols, long long rows,
+                  long long depth, long long ld) {
+  PFN_encodeTiled_t enc = get_encode();
+  if (!enc) return false;
+  const int es = f32 ? 4 : 2;
+  cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)depth};
+  cuuint64_t strides[2] = {(cuuint64_t)ld * es, (cuuint64_t)ld * es * rows};
+  cuuint32_t box[3] = {(cuuint32_t)(64 / es), 32, 1};
+  cuuint32_t el[3] = {1, 1, 1};
+  CUresult r = enc(tm, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                   const_cast<void*>(base), dims, strides, box, el, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// 2-D bf16 epilogue operand map (residual / pre-activation): 32 x 32 boxes, 64-byte swizzle.
+bool make_x_map(CUtensorMap* tm, const void* base, long long cols, long long rows, long long ld) {
+  PFN_encodeTiled_t enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t el[2] = {1, 1};
+  CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+                   el, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -483,6 +685,8 @@ int gemm_tc_poison(int on) {
   g_poison = on;
   return old;
 }
+
+int gemm_tc_stat_cols() { return BN / 2; }
 
 size_t gemm_tc_ws_bytes(int M, int N, int splits) {
   return splits > 1 ? (size_t)splits * M * N * sizeof(float) : 0;
@@ -523,18 +727,15 @@ int gemm_tc(const GemmArgs& g, int splits, void* ws, size_t ws_bytes, unsigned* 
   if (!aligned16(g.A) || !aligned16(g.B) || !aligned16(g.D)) return (int)cudaErrorInvalidValue;
   if (g.epi == EPI_BIAS_RESID && (g.ldr % 8 || !aligned16(g.resid))) return (int)cudaErrorInvalidValue;
   if (g.epi == EPI_GELU_BWD && (g.ldaux % 8 || !aligned16(g.aux))) return (int)cudaErrorInvalidValue;
+  if (g.epi == EPI_BIAS_GELU && !aligned16(g.D2)) return (int)cudaErrorInvalidValue;
+  if ((g.epi == EPI_BIAS || g.epi == EPI_BIAS_RESID || g.epi == EPI_BIAS_GELU) && !aligned16(g.bias))
+    return (int)cudaErrorInvalidValue;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return (int)e;
     attr_set = true;
   }
-  CUtensorMap tmA, tmB;
-  bool ok = g.a_mn ? make_tmap(&tmA, g.A, g.M, g.K, g.lda, 64, 64)
-                   : make_tmap(&tmA, g.A, g.K, g.M, g.lda, 64, BM);
-  ok = ok && (g.b_mn ? make_tmap(&tmB, g.B, g.N, g.K, g.ldb, 64, 64)
-                     : make_tmap(&tmB, g.B, g.K, g.N, g.ldb, 64, BN));
-  if (!ok) return (int)cudaErrorInvalidValue;
   TcParams p;
   p.g = g;
   p.mt = (g.M + BM - 1) / BM;
@@ -546,22 +747,45 @@ int gemm_tc(const GemmArgs& g, int splits, void* ws, size_t ws_bytes, unsigned* 
   p.splits = (p.total_kb + p.kps - 1) / p.kps;
   if (p.splits > 1) {
     if (g.epi != EPI_STORE && g.epi != EPI_F32) return (int)cudaErrorInvalidValue;
-    if (!ws || ws_bytes < gemm_tc_ws_bytes(g.M, g.N, p.splits)) return (int)cudaErrorInvalidValue;
+    if (!ws || !aligned16(ws) || ws_bytes < gemm_tc_ws_bytes(g.M, g.N, p.splits))
+      return (int)cudaErrorInvalidValue;
   }
-  p.ws = static_cast<float*>(ws);
   p.status = status;
   p.poison = g_poison;
+  p.out_f32 = (p.splits > 1 || g.epi == EPI_F32) ? 1 : 0;
+  p.load_x = (g.epi == EPI_BIAS_RESID || g.epi == EPI_GELU_BWD) ? 1 : 0;
+  p.m_fast = ((double)g.N * g.K > (double)g.M * g.K) ? 1 : 0;
+  CUtensorMap tmA, tmB, tmD, tmD2, tmX;
+  bool ok = g.a_mn ? make_tmap(&tmA, g.A, g.M, g.K, g.lda, 64, 64)
+                   : make_tmap(&tmA, g.A, g.K, g.M, g.lda, 64, BM);
+  ok = ok && (g.b_mn ? make_tmap(&tmB, g.B, g.N, g.K, g.ldb, 64, 64)
+                     : make_tmap(&tmB, g.B, g.K, g.N, g.ldb, 64, BN));
+  if (p.splits > 1)
+    ok = ok && make_box_map(&tmD, ws, 1, g.N, g.M, p.splits, g.N);
+  else
+    ok = ok && make_box_map(&tmD, g.D, p.out_f32, g.N, g.M, 1, g.ldd);
+  if (g.epi == EPI_BIAS_GELU)
+    ok = ok && make_box_map(&tmD2, g.D2, 0, g.N, g.M, 1, g.ldd);
+  else
+    tmD2 = tmD;
+  if (g.epi == EPI_BIAS_RESID)
+    ok = ok && make_x_map(&tmX, g.resid, g.N, g.M, g.ldr);
+  else if (g.epi == EPI_GELU_BWD)
+    ok = ok && make_x_map(&tmX, g.aux, g.N, g.M, g.ldaux);
+  else
+    tmX = tmA;
+  if (!ok) return (int)cudaErrorInvalidValue;
   // kind::f16 instruction descriptor: D fp32, A/B bf16, operand majors, N >> 3, M >> 4
   p.idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)g.a_mn << 15) |
             ((uint32_t)g.b_mn << 16) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
   const int ntiles = p.mt * p.nt * p.splits;
   int grid = num_sms();
   if (grid > ntiles) grid = ntiles;
-  k_gemm_tc<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(tmA, tmB, p);
+  k_gemm_tc<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(tmA, tmB, tmD, tmD2, tmX, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return (int)e;
   if (p.splits > 1 && reduce) {
-    splitk_reduce(g.D, g.epi == EPI_F32, g.ldd, p.ws, p.splits, g.M, g.N, s);
+    splitk_reduce(g.D, g.epi == EPI_F32, g.ldd, static_cast<float*>(ws), p.splits, g.M, g.N, s);
     e = cudaGetLastError();
   }
   return (int)e;

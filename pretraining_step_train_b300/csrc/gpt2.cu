@@ -85,7 +85,6 @@ struct Plan {
 };
 
 constexpr int kNormParts = 1024;
-constexpr int kCeTileN = 256;  // N tile of the tensor-core GEMM (one statistics partial per tile)
 
 size_t take(size_t& cur, size_t bytes) {
   size_t o = cur;
@@ -123,7 +122,7 @@ Plan make_plan(const Shape& s) {
   p.lnf_mean = take(cur, M * f);
   p.lnf_rstd = take(cur, M * f);
   p.logits = take(cur, M * (size_t)s.Vpad * e);
-  p.ce_tiles = (s.Vpad + kCeTileN - 1) / kCeTileN;
+  p.ce_tiles = (s.Vpad + gemm_tc_stat_cols() - 1) / gemm_tc_stat_cols();
   p.ce_max = take(cur, M * p.ce_tiles * f);
   p.ce_sum = take(cur, M * p.ce_tiles * f);
   p.ce_tgt = take(cur, M * f);
@@ -808,7 +807,7 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
 
 // workspace: logits bf16 [M, Vpad] | pmax, psum f32 [M, tiles] | ztgt, lse, rows f32 [M] | status
 static size_t cls_off(int M, int Vpad, int which) {
-  const int tiles = (Vpad + kCeTileN - 1) / kCeTileN;
+  const int tiles = (Vpad + gemm_tc_stat_cols() - 1) / gemm_tc_stat_cols();
   size_t cur = 0;
   size_t offs[8];
   offs[0] = take(cur, (size_t)M * Vpad * 2);
@@ -846,7 +845,7 @@ int classifier_fwd_bwd(const void* x, const void* w, const int32_t* targets, int
   float* lse = reinterpret_cast<float*>(ws + cls_off(M, Vpad, 4));
   float* rows = reinterpret_cast<float*>(ws + cls_off(M, Vpad, 5));
   unsigned* status = reinterpret_cast<unsigned*>(ws + cls_off(M, Vpad, 6));
-  const int tiles = (Vpad + kCeTileN - 1) / kCeTileN;
+  const int tiles = (Vpad + gemm_tc_stat_cols() - 1) / gemm_tc_stat_cols();
   GemmArgs g;
   g.A = x; g.lda = C; g.B = w; g.ldb = C; g.M = M; g.N = Vpad; g.K = C;
   g.epi = EPI_CE; g.D = logits; g.ldd = Vpad;

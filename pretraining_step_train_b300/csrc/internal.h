@@ -45,6 +45,9 @@ int gemm_tc_effective_splits(int K, int splits);
 size_t gemm_tc_ws_bytes(int M, int N, int splits);
 int gemm_tc_pick_splits(int M, int N, int K, int num_sms);
 int gemm_tc_poison(int on);  // test hook: the TMA producer skips its first stage when on
+// Columns covered by one EPI_CE statistics partial (row m's partial j covers
+// columns [j*cols, (j+1)*cols)).
+int gemm_tc_stat_cols();
 int num_sms();
 
 // fp32 operands on CUDA cores (the fp32 parity mode).
