@@ -184,6 +184,31 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
              void* workspace, size_t workspace_bytes, void* stream);
 size_t attn_workspace_bytes(int B, int H, int T);
 
+/* attn_bwd for callers that cannot allocate device memory; the pages have no
+ * counterpart of this call.  Some callers cannot hand the library a workspace:
+ * a host runtime that gives the whole device to its own memory pool and
+ * forbids library allocations, or a latency-critical loop that cannot afford
+ * cudaMalloc's implicit device synchronisation.  This call takes the same
+ * arguments as attn_bwd minus the workspace, computes the same gradients with
+ * the same kernels, and allocates nothing: its scratch (fp32 rowsum(dO * O),
+ * one float per (b, h, t)) is a fixed array in the library's static device
+ * memory, ATTN_BWD_NOALLOC_MAX_ROWS floats (4 MiB), which every GPU that
+ * loads the library holds until the process exits.
+ *   - B * H * T > ATTN_BWD_NOALLOC_MAX_ROWS returns GPT2_E_UNSUPPORTED before
+ *     anything is enqueued; other argument errors are those of attn_bwd.
+ *   - The first call on a device, made with that device current, looks up the
+ *     array's device address (cudaGetSymbolAddress) and caches it; make that
+ *     first call before any stream capture.  A failed lookup returns GPT2_E_CUDA.
+ *   - Every call on a device shares the one array.  Calls whose kernels may
+ *     overlap on the GPU (different streams with no ordering) race on it.  The
+ *     array keeps the last call's contents; nothing needs clearing, since
+ *     every row is written before it is read. */
+#define ATTN_BWD_NOALLOC_MAX_ROWS 1048576
+int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                     const void* dO, void* dq, void* dk, void* dv, int B, int H, int T, int d,
+                     long long sb, long long sh, long long st, long long osb, long long osh,
+                     long long ost, float scale, void* stream);
+
 /* Tied lm_head + mean cross-entropy, fused: logits = x w^T (x bf16 [M, C],
  * w bf16 [Vpad, C]; columns >= V excluded from the softmax), loss = mean over
  * rows of lse - logit[target]; then dlogits = (softmax - onehot) / M,

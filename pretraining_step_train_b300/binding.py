@@ -52,6 +52,8 @@ SIGNATURES = {
     "attn_bwd": (_i, [_p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _ll, _ll, _ll, _ll, _ll,
                       _ll, _f, _p, _sz, _p]),
     "attn_workspace_bytes": (_sz, [_i, _i, _i]),
+    "attn_bwd_noalloc": (_i, [_p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _ll, _ll, _ll, _ll, _ll,
+                              _ll, _f, _p]),
     "classifier_fwd_bwd": (_i, [_p, _p, _p, _i, _i, _i, _i, _p, _p, _p, _p, _sz, _p]),
     "classifier_workspace_bytes": (_sz, [_i, _i, _i]),
     "gpt2_encoder_fwd": (_i, [_p, _p, _p, _p, _i, _i, _i, _i, _i, _p, _p]),
