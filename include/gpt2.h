@@ -227,14 +227,15 @@ size_t classifier_workspace_bytes(int M, int C, int Vpad);
  * bit 0 of *d_status (device uint32, may be NULL) is set.  Bit-exact. */
 int gpt2_encoder_fwd(const int32_t* tok, const void* wte, const void* wpe, void* x0, int B, int T,
                      int C, int V, int precision, void* d_status, void* stream);
-/* The scatter of the backward pass: for every vocab id v, acc = 0; add dx0 rows
- * (fp32 [B, T, C]) of the positions holding v in ascending position order;
- * then dwte[v] = dwte[v] + acc (one rounding).  dwpe[t] = sum over b ascending
- * of dx0[b, t] (written, not accumulated).  workspace >= 8*B*T bytes.  Bit-exact
- * and deterministic. */
-int gpt2_encoder_bwd(const int32_t* tok, const float* dx0, void* dwte, void* dwpe, int B, int T,
-                     int C, int V, int precision, void* workspace, size_t workspace_bytes,
-                     void* stream);
+/* The scatter of the backward pass.  For every vocab id v: the positions
+ * holding v, in ascending order, are cut into runs of 64; each run's dx0 rows
+ * (fp32 [B, T, C]) are summed from zero in ascending order, the run sums are
+ * added in run order from zero, and dwte[v] = dwte[v] + total (one rounding).
+ * dwpe[t] = sum over b ascending of dx0[b, t] (written, not accumulated).
+ * dx0 is consumed: rows of it are overwritten with run sums.  workspace >=
+ * 8*B*T bytes.  Bit-exact and deterministic. */
+int gpt2_encoder_bwd(const int32_t* tok, float* dx0, void* dwte, void* dwpe, int B, int T, int C,
+                     int V, int precision, void* workspace, size_t workspace_bytes, void* stream);
 
 /* The tensor-core GEMM engine on its own (bf16 in, fp32 accumulate):
  * D[m, n] = sum_k A(m, k) B(n, k), A(m, k) = A[m*lda + k] (a_mn = 0) or

@@ -310,30 +310,30 @@ def encoder_forward_f32(tok, wte, wpe):
     return (wte[tok] + wpe[None, : tok.shape[1], :]).astype(np.float32)
 
 
-def encoder_backward_f32(tok, dx0, dwte_in, dwpe_shape):
+def encoder_backward_f32(tok, dx0, dwte_in, dwpe_shape, run=64):
     """Scatter of the encoder gradient in a fixed order, float32 throughout.
 
-    For every vocab id v: acc = 0; for each position i = b*T + t holding v, in
-    ascending i: acc += dx0[i]; then dwte[v] = dwte_in[v] + acc.  For every
-    position t: dwpe[t] = sum over b ascending of dx0[b, t], starting from 0.
-    Returns (dwte, dwpe) as float32.
+    For every vocab id v, its positions i = b*T + t in ascending order are cut
+    into runs of `run`; each run is summed from zero in ascending order, the
+    run sums are added in run order starting from zero, and
+    dwte[v] = dwte_in[v] + total.  For every position t: dwpe[t] = sum over b
+    ascending of dx0[b, t], starting from 0.  Returns (dwte, dwpe) as float32.
+    (The pages fix no order; this one is the reading both sides implement.)
     """
     B, T = tok.shape
     C = dx0.shape[-1]
     flat = np.asarray(dx0, np.float32).reshape(B * T, C)
     ids = tok.reshape(-1)
     dwte = np.array(dwte_in, dtype=np.float32, copy=True)
-    order = np.argsort(ids, kind="stable")
-    i = 0
-    while i < order.size:
-        vtok = ids[order[i]]
-        acc = np.zeros(C, np.float32)
-        j = i
-        while j < order.size and ids[order[j]] == vtok:
-            acc = (acc + flat[order[j]]).astype(np.float32)
-            j += 1
-        dwte[vtok] = (dwte[vtok] + acc).astype(np.float32)
-        i = j
+    for vtok in np.unique(ids):
+        pos = np.nonzero(ids == vtok)[0]  # ascending
+        total = np.zeros(C, np.float32)
+        for r0 in range(0, pos.size, run):
+            acc = np.zeros(C, np.float32)
+            for i in pos[r0:r0 + run]:
+                acc = (acc + flat[i]).astype(np.float32)
+            total = (total + acc).astype(np.float32)
+        dwte[vtok] = (dwte[vtok] + total).astype(np.float32)
     dwpe = np.zeros(dwpe_shape, np.float32)
     acc = np.zeros((T, C), np.float32)
     for b in range(B):

@@ -888,7 +888,7 @@ int gpt2_encoder_fwd(const int32_t* tok, const void* wte, const void* wpe, void*
   return GPT2_OK;
 }
 
-int gpt2_encoder_bwd(const int32_t* tok, const float* dx0, void* dwte, void* dwpe, int B, int T,
+int gpt2_encoder_bwd(const int32_t* tok, float* dx0, void* dwte, void* dwpe, int B, int T,
                      int C, int V, int precision, void* workspace, size_t workspace_bytes,
                      void* stream) {
   if (!tok || !al16(dx0) || !dwte || !dwpe || !workspace) return GPT2_E_INVAL;

@@ -106,10 +106,11 @@ void ce_dlogits(T* z, long long ldz, const float* lse, const int32_t* tgt, int M
 void mean_reduce(float* out, const float* rows, int M, unsigned* status, cudaStream_t s);
 
 // Encoder backward: fixed-order scatter of dx0 (fp32) into dwte, and dwpe.
+// dx0 is consumed: some of its rows are overwritten with partial sums.
 void sort_tokens(uint32_t* order, const int32_t* tok, int M, int V, cudaStream_t s);
 template <typename T>
-void encoder_bwd(T* dwte, T* dwpe, const float* dx0, const uint32_t* order, const int32_t* tok,
-                 int B, int Tn, int C, cudaStream_t s);
+void encoder_bwd(T* dwte, T* dwpe, float* dx0, const uint32_t* order, const int32_t* tok, int B,
+                 int Tn, int C, cudaStream_t s);
 
 // Split-K reduction: out = sum over splits of ws[s][m][n].
 void splitk_reduce(void* out, int out_f32, long long ldo, const float* ws, int splits, int M, int N,

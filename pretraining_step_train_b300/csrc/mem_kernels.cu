@@ -175,11 +175,17 @@ static void reduce_parts(T* o0, T* o1, T* o2, const float* partials, int nparts,
 // ------------------------------------------------------------------ LayerNorm backward
 // dx = rstd * (g - mean(g) - xhat * mean(g * xhat)),  g = dy * w.
 // dres = (accumulate ? dres : 0) + dx in fp32; dres_b (if given) = storage copy.
-// Column sums per block, each warp in its own shared-memory slice (no
-// atomics): dw = sum dy * xhat, db = sum dy and, when dsum is wanted, the
-// column sum of the new dres (the next projection's bias gradient).
+// One warp per row.  All three row inputs (dy, x and the fp32 dres being
+// accumulated into) are loaded together before the row reductions, so a warp
+// keeps 6 KB (C = 768, bf16) in flight.  Column sums per block, each warp in
+// its own shared-memory slice (no atomics): dw = sum dy * xhat, db = sum dy and,
+// when dsum is wanted, the column sum of the new dres (the next projection's
+// bias gradient).  A slice stores element (vector vi, lane e) at
+// ((e / 4) * nv + vi) * 4 + e % 4, so a warp's float4 updates are conflict-free.
 constexpr int kLnbBlocks = 592;
 constexpr int kLnbWarps = 4;
+
+__device__ __forceinline__ int lnb_slot(int vi, int e, int nv) { return (((e >> 2) * nv + vi) << 2) + (e & 3); }
 
 template <typename T, int MAXV>
 __global__ void __launch_bounds__(kLnbWarps * 32)
@@ -194,6 +200,7 @@ __global__ void __launch_bounds__(kLnbWarps * 32)
   const int nv = C / N;
   float* mine = sacc + warp * 3 * C;
   for (int i = lane; i < 3 * C; i += 32) mine[i] = 0.f;
+  __syncwarp();
   float wv[MAXV][N];
 #pragma unroll
   for (int j = 0; j < MAXV; ++j) {
@@ -204,14 +211,31 @@ __global__ void __launch_bounds__(kLnbWarps * 32)
   const int r1 = min(M, r0 + rows_per_block);
   for (int r = r0 + warp; r < r1; r += kLnbWarps) {
     const float mu = mean[r], rs = rstd[r];
-    float dyv[MAXV][N], xh[MAXV][N];
-    float sg = 0.f, sgx = 0.f;
+    float dyv[MAXV][N], xh[MAXV][N], d[MAXV][N];
 #pragma unroll
     for (int j = 0; j < MAXV; ++j) {
       int vi = lane + j * 32;
       if (vi < nv) {
         load16(dy + (long long)r * C + vi * N, dyv[j]);
         load16(x + (long long)r * C + vi * N, xh[j]);
+        if (accumulate) {
+          const float* dp = dres + (long long)r * C + vi * N;
+#pragma unroll
+          for (int e = 0; e < N; e += 4) {
+            float4 o = *reinterpret_cast<const float4*>(dp + e);
+            d[j][e] = o.x; d[j][e + 1] = o.y; d[j][e + 2] = o.z; d[j][e + 3] = o.w;
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < N; ++e) d[j][e] = 0.f;
+        }
+      }
+    }
+    float sg = 0.f, sgx = 0.f;
+#pragma unroll
+    for (int j = 0; j < MAXV; ++j) {
+      int vi = lane + j * 32;
+      if (vi < nv) {
 #pragma unroll
         for (int e = 0; e < N; ++e) {
           xh[j][e] = (xh[j][e] - mu) * rs;
@@ -227,39 +251,41 @@ __global__ void __launch_bounds__(kLnbWarps * 32)
     for (int j = 0; j < MAXV; ++j) {
       int vi = lane + j * 32;
       if (vi < nv) {
-        float d[N];
+#pragma unroll
+        for (int e = 0; e < N; ++e) d[j][e] += rs * (dyv[j][e] * wv[j][e] - sg - xh[j][e] * sgx);
         float* dp = dres + (long long)r * C + vi * N;
-        if (accumulate) {
-#pragma unroll
-          for (int e = 0; e < N; e += 4) {
-            float4 o = *reinterpret_cast<const float4*>(dp + e);
-            d[e] = o.x; d[e + 1] = o.y; d[e + 2] = o.z; d[e + 3] = o.w;
-          }
-        } else {
-#pragma unroll
-          for (int e = 0; e < N; ++e) d[e] = 0.f;
-        }
-        float* m0 = mine + vi * N;
-#pragma unroll
-        for (int e = 0; e < N; ++e) {
-          d[e] += rs * (dyv[j][e] * wv[j][e] - sg - xh[j][e] * sgx);
-          m0[e] += dyv[j][e] * xh[j][e];
-          m0[C + e] += dyv[j][e];
-          if (want_sum) m0[2 * C + e] += d[e];
-        }
 #pragma unroll
         for (int e = 0; e < N; e += 4)
-          *reinterpret_cast<float4*>(dp + e) = make_float4(d[e], d[e + 1], d[e + 2], d[e + 3]);
-        if (dres_b) store16(dres_b + (long long)r * C + vi * N, d);
+          *reinterpret_cast<float4*>(dp + e) = make_float4(d[j][e], d[j][e + 1], d[j][e + 2], d[j][e + 3]);
+        if (dres_b) store16(dres_b + (long long)r * C + vi * N, d[j]);
+#pragma unroll
+        for (int e = 0; e < N; e += 4) {
+          float4* a0 = reinterpret_cast<float4*>(mine + lnb_slot(vi, e, nv));
+          float4* a1 = reinterpret_cast<float4*>(mine + C + lnb_slot(vi, e, nv));
+          float4 u = *a0, b = *a1;
+          u.x += dyv[j][e] * xh[j][e]; u.y += dyv[j][e + 1] * xh[j][e + 1];
+          u.z += dyv[j][e + 2] * xh[j][e + 2]; u.w += dyv[j][e + 3] * xh[j][e + 3];
+          b.x += dyv[j][e]; b.y += dyv[j][e + 1]; b.z += dyv[j][e + 2]; b.w += dyv[j][e + 3];
+          *a0 = u;
+          *a1 = b;
+          if (want_sum) {
+            float4* a2 = reinterpret_cast<float4*>(mine + 2 * C + lnb_slot(vi, e, nv));
+            float4 q = *a2;
+            q.x += d[j][e]; q.y += d[j][e + 1]; q.z += d[j][e + 2]; q.w += d[j][e + 3];
+            *a2 = q;
+          }
+        }
       }
     }
   }
   __syncthreads();
   const int width = (want_sum ? 3 : 2) * C;
   for (int i = threadIdx.x; i < width; i += blockDim.x) {
+    const int kind = i / C, c = i - kind * C;
+    const int slot = kind * C + lnb_slot(c / N, c % N, nv);
     float t = 0.f;
 #pragma unroll
-    for (int ww = 0; ww < kLnbWarps; ++ww) t += sacc[ww * 3 * C + i];
+    for (int ww = 0; ww < kLnbWarps; ++ww) t += sacc[ww * 3 * C + slot];
     partials[(long long)blockIdx.x * width + i] = t;
   }
 }
@@ -589,23 +615,46 @@ void sort_tokens(uint32_t* order, const int32_t* tok, int M, int V, cudaStream_t
   k_sort_tokens<<<1, 1024, sm, s>>>(order, tok, M, V, P);
 }
 
-// One block per segment head p of the sorted list: acc = sum over the
-// segment's positions in ascending order (fp32), then dwte[v] = dwte[v] + acc.
-template <typename T>
-__global__ void __launch_bounds__(256)
-    k_encoder_bwd_wte(T* __restrict__ dwte, const float* __restrict__ dx0,
-                      const uint32_t* __restrict__ order, int M, int C) {
-  const int p = blockIdx.x;
-  const uint32_t* stok = order + M;
+// Fixed summation order of the tied-embedding scatter: the positions holding
+// token v, in ascending order, are cut into runs of kEncRun; each run is summed
+// from zero in ascending order (fp32), the run sums are added in run order from
+// zero, and dwte[v] = dwte[v] + total (one rounding to the storage type).  Runs
+// spread the most frequent tokens over many blocks.
+constexpr int kEncRun = 64;
+
+// [s, e): the segment of the sorted token list holding stok[p] (stok ascending).
+__device__ __forceinline__ void token_segment(const uint32_t* stok, int M, int p, int& s, int& e) {
   const uint32_t v = stok[p];
-  if (p > 0 && stok[p - 1] == v) return;
-  // segment end: first q > p with stok[q] != v (binary search on the sorted ids)
-  int lo = p, hi = M;  // stok[lo] == v; find first index with stok > v
+  int lo = 0, hi = p;  // first index with stok == v lies in [0, p]
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (stok[mid] < v) lo = mid + 1; else hi = mid;
+  }
+  s = lo;
+  lo = p;
+  hi = M;  // stok[lo] == v; find the first index > p with stok != v
   while (hi - lo > 1) {
-    int mid = (lo + hi) >> 1;
+    const int mid = (lo + hi) >> 1;
     if (stok[mid] == v) lo = mid; else hi = mid;
   }
-  const int q = hi;
+  e = hi;
+}
+
+// One block per sorted index p; run heads sum their run.  A token with a single
+// run finishes here (dwte update); otherwise the run sum is parked in the dx0 row
+// of the run's first position, which no other run reads (dx0 is consumed).
+template <typename T>
+__global__ void __launch_bounds__(256)
+    k_encoder_bwd_runs(T* __restrict__ dwte, float* __restrict__ dx0, const uint32_t* __restrict__ order,
+                       int M, int C) {
+  const int p = blockIdx.x;
+  const uint32_t* stok = order + M;
+  int s, e;
+  token_segment(stok, M, p, s, e);
+  if ((p - s) % kEncRun) return;
+  const int q = min(e, p + kEncRun);
+  const bool single = e - s <= kEncRun;
+  const uint32_t v = stok[p];
   for (int c = threadIdx.x * 4; c < C; c += blockDim.x * 4) {
     float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
     int r = p;
@@ -620,6 +669,37 @@ __global__ void __launch_bounds__(256)
     }
     for (; r < q; ++r) {
       float4 u = *reinterpret_cast<const float4*>(dx0 + (long long)order[r] * C + c);
+      a0 = a0 + u.x; a1 = a1 + u.y; a2 = a2 + u.z; a3 = a3 + u.w;
+    }
+    if (single) {
+      T* dst = dwte + (long long)v * C + c;
+      dst[0] = from_f<T>(to_f(dst[0]) + a0);
+      dst[1] = from_f<T>(to_f(dst[1]) + a1);
+      dst[2] = from_f<T>(to_f(dst[2]) + a2);
+      dst[3] = from_f<T>(to_f(dst[3]) + a3);
+    } else {
+      *reinterpret_cast<float4*>(dx0 + (long long)order[p] * C + c) = make_float4(a0, a1, a2, a3);
+    }
+  }
+}
+
+// One block per segment head of a token with more than one run: add the
+// parked run sums in run order, then update dwte once.
+template <typename T>
+__global__ void __launch_bounds__(256)
+    k_encoder_bwd_combine(T* __restrict__ dwte, const float* __restrict__ dx0,
+                          const uint32_t* __restrict__ order, int M, int C) {
+  const int p = blockIdx.x;
+  const uint32_t* stok = order + M;
+  const uint32_t v = stok[p];
+  if (p > 0 && stok[p - 1] == v) return;
+  int s, e;
+  token_segment(stok, M, p, s, e);
+  if (e - s <= kEncRun) return;
+  for (int c = threadIdx.x * 4; c < C; c += blockDim.x * 4) {
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+    for (int r = s; r < e; r += kEncRun) {
+      const float4 u = *reinterpret_cast<const float4*>(dx0 + (long long)order[r] * C + c);
       a0 = a0 + u.x; a1 = a1 + u.y; a2 = a2 + u.z; a3 = a3 + u.w;
     }
     T* dst = dwte + (long long)v * C + c;
@@ -644,14 +724,16 @@ __global__ void k_encoder_bwd_wpe(T* __restrict__ dwpe, const float* __restrict_
 }
 
 template <typename T>
-void encoder_bwd(T* dwte, T* dwpe, const float* dx0, const uint32_t* order, const int32_t* tok,
-                 int B, int Tn, int C, cudaStream_t s) {
+void encoder_bwd(T* dwte, T* dwpe, float* dx0, const uint32_t* order, const int32_t* tok, int B,
+                 int Tn, int C, cudaStream_t s) {
   const int M = B * Tn;
   int threads = C / 4;
   if (threads > 256) threads = 256;
   if (threads < 32) threads = 32;
-  k_encoder_bwd_wte<T><<<M, threads, 0, s>>>(dwte, dx0, order, M, C);
+  // dwpe first: the run kernel overwrites some dx0 rows with run sums
   k_encoder_bwd_wpe<T><<<grid_for((long long)Tn * C, 256), 256, 0, s>>>(dwpe, dx0, B, Tn, C);
+  k_encoder_bwd_runs<T><<<M, threads, 0, s>>>(dwte, dx0, order, M, C);
+  k_encoder_bwd_combine<T><<<M, threads, 0, s>>>(dwte, dx0, order, M, C);
 }
 
 // ------------------------------------------------------------------ split-K reduction
@@ -838,7 +920,7 @@ void adamw(float* master, P* param_copy, const G* grad, float* m, float* v, long
                                cudaStream_t);                                                      \
   template void ce_dlogits<T>(T*, long long, const float*, const int32_t*, int, int, int, float,   \
                               cudaStream_t);                                                       \
-  template void encoder_bwd<T>(T*, T*, const float*, const uint32_t*, const int32_t*, int, int,    \
+  template void encoder_bwd<T>(T*, T*, float*, const uint32_t*, const int32_t*, int, int,    \
                                int, cudaStream_t);                                                 \
   template void grad_sumsq_partials<T>(float*, int, const T*, long long, cudaStream_t);
 INST(float)
