@@ -462,10 +462,9 @@ int attn_bwd_bf16(const AttnArgs& a, cudaStream_t s) {
   if (!strides_ok(a)) return (int)cudaErrorInvalidValue;
   long long rows = (long long)a.B * a.H * a.T;
   k_attn_rowdot64<<<(unsigned)((rows * 8 + 255) / 256), 256, 0, s>>>(a);
-  dim3 grid((a.T + 63) / 64, a.B * a.H);
-  k_attn_bwd_dkdv_bf16<<<grid, 128, 0, s>>>(a);
-  k_attn_bwd_dq_bf16<<<grid, 128, 0, s>>>(a);
-  return (int)cudaGetLastError();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return (int)e;
+  return attn_bwd_tc(a, s);
 }
 
 // ------------------------------------------------------------------ fp32 (CUDA cores)

@@ -1,0 +1,911 @@
+// Causal attention forward on the 5th-generation tensor cores (tcgen05) for
+// sm_103a, d = 64, never materialising the T x T score matrix (online softmax
+// over 128-key tiles, FlashAttention-style: "Let's reproduce GPT-2 (124M)" wiki
+// page, "GPU optimisation ladder").
+//
+// Persistent: one CTA per SM walks a list of work items (128-query tile, batch,
+// head), heaviest causal tiles first, item c, c + grid, c + 2 grid, ...
+//   warp 0      TMA: each item's Q tile, then its K and V tiles of 128 keys into
+//               a 2-stage ring that runs on across items, so the next item's
+//               tiles load while this one finishes (4-D tensor maps over the
+//               strided q / k / v views, 128B swizzle; rows past T arrive as zeros);
+//   warp 1      owns 512 TMEM columns: S double buffer (2 x 128 fp32 columns)
+//               and the O accumulator (64 columns); one thread issues
+//               S_j = Q K_j^T (M=128, N=128, K=64) and O += P_j V_j (M=128, N=64,
+//               K=128, V read MN-major), in the order S_0, S_1, PV_0, S_2, PV_1, ...
+//               so the tensor core computes S_{j+1} while softmax works on S_j;
+//   warps 2-9   softmax, two warps per TMEM lane quadrant (one per 64-key half):
+//               tcgen05.ld of the half row, causal mask on the diagonal tile, row
+//               max exchanged with the partner warp through shared memory,
+//               p = 2^(s*scale*log2e - m), running sum, O rescaled in TMEM only
+//               when the running max has to move by more than 2^8, P (bf16)
+//               written to a 128B-swizzled shared tile (double-buffered) that is
+//               the A operand of the PV MMA.
+// Epilogue: O / l -> bf16 rows, lse = (m + log2 l) ln 2 (natural log).
+// Every wait is bounded; on expiry the CTA latches ST_TIMEOUT (when a status
+// word is given), drains its copies and MMAs, frees TMEM and returns.
+#include "common.cuh"
+#include "internal.h"
+#include "tc_ptx.cuh"
+
+namespace gpt2k {
+
+namespace {
+
+constexpr int AT_B = 128;                       // queries per tile = keys per tile
+constexpr int AT_D = 64;                        // head size
+constexpr int AT_TILE = AT_B * AT_D * 2;        // 16 KB: one [128 x 64] bf16 tile
+constexpr int AT_Q_OFF = 0;
+constexpr int AT_KV_OFF = AT_TILE;              // stage s: K at +s*2*TILE, V at +s*2*TILE+TILE
+constexpr int AT_P_OFF = AT_KV_OFF + 4 * AT_TILE;  // buffer b: +b*2*TILE, key half h at +h*TILE
+constexpr int AT_RED_OFF = AT_P_OFF + 4 * AT_TILE; // row-max exchange [2][2][128] + row-sum [2][128]
+constexpr int AT_BAR_OFF = AT_RED_OFF + 6 * 128 * 4;
+constexpr int AT_NBARS = 27;
+constexpr int AT_SMEM = 1024 + AT_BAR_OFF + 8 * (AT_NBARS + 2);
+constexpr int AT_THREADS = 320;
+constexpr int AT_TMEM_COLS = 512;
+constexpr int AT_O_COL = 256;
+
+struct AtParams {
+  AttnArgs a;
+  int nq;        // query tiles per (batch, head)
+  int swap_ht;   // tensor maps index (d, h, t, b) instead of (d, t, h, b)
+  float c2;      // scale * log2(e)
+  uint32_t idesc_s, idesc_pv;
+  unsigned* status;
+};
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 t = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&t);
+}
+// Bounded mbarrier wait taken by every lane, with a warp-uniform outcome.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          unsigned* status) {
+  const bool ok = mbar_wait(bar, parity, abort_flag, status);
+  return __all_sync(0xffffffffu, ok);
+}
+
+__global__ void __launch_bounds__(AT_THREADS, 1)
+    k_attn_fwd_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const AtParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  float* red = reinterpret_cast<float*>(smem + AT_RED_OFF);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + AT_BAR_OFF);
+  // q_full, kv_full[2], kv_empty[2], s_full[2], s_empty[2], p_full[2], pv_done, done,
+  // xmax[4 quadrants][2], xsum[4 quadrants] (the two warps of a quadrant exchange row
+  // stats), q_empty (the Q tile may be overwritten by the next item)
+  const uint32_t b_q = smem_u32(bars), b_kvf = b_q + 8, b_kve = b_kvf + 16, b_sf = b_kve + 16;
+  const uint32_t b_se = b_sf + 16, b_pf = b_se + 16, b_pv = b_pf + 16, b_done = b_pv + 8;
+  const uint32_t b_xmax = b_done + 8, b_xsum = b_xmax + 64, b_qe = b_xsum + 32;
+  // pv_done[i] (i = tile parity) completes for the PVs of global tiles i, i+2, ...:
+  // b_pv for even tiles, b_pv2 for odd ones
+  const uint32_t b_pv2 = b_qe + 8;
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bars + AT_NBARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + AT_NBARS + 1);
+
+  const AttnArgs& a = p.a;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int BH = a.B * a.H;
+  const int nitems = p.nq * BH;
+  // work item w: query tile nq-1 - w / BH (heaviest first), (batch, head) = w % BH
+
+  if (threadIdx.x == 0) {
+    mbar_init(b_q, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(b_kvf + 8 * i, 1);
+      mbar_init(b_kve + 8 * i, 1);
+      mbar_init(b_sf + 8 * i, 1);
+      mbar_init(b_se + 8 * i, 256);
+      mbar_init(b_pf + 8 * i, 256);
+    }
+    mbar_init(b_pv, 1);
+    mbar_init(b_done, 1);
+    mbar_init(b_qe, 1);
+    mbar_init(b_pv2, 1);
+    for (int i = 0; i < 8; ++i) mbar_init(b_xmax + 8 * i, 64);
+    for (int i = 0; i < 4; ++i) mbar_init(b_xsum + 8 * i, 64);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), AT_TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer
+      int last_par[2] = {-1, -1}, q_par = -1;
+      int g = 0;  // K/V tiles issued so far (ring position)
+      bool ok = true;
+      for (int w = blockIdx.x, it = 0; ok && w < nitems; w += gridDim.x, ++it) {
+        const int qt = p.nq - 1 - w / BH, bh = w % BH, b = bh / a.H, h = bh % a.H;
+        auto load = [&](const CUtensorMap* tm, uint32_t dst, uint32_t bar, int t0) {
+          if (p.swap_ht) tma_load_4d(dst, tm, bar, 0, h, t0, b);
+          else tma_load_4d(dst, tm, bar, 0, t0, h, b);
+        };
+        if (it > 0 && !mbar_wait(b_qe, (uint32_t)(it - 1) & 1u, abort_flag, p.status)) break;
+        mbar_expect_tx(b_q, AT_TILE);
+        load(&tmQ, sbase + AT_Q_OFF, b_q, qt * AT_B);
+        q_par = it & 1;
+        for (int j = 0; j <= qt; ++j, ++g) {
+          const int st = g & 1;
+          const uint32_t ph = (uint32_t)(g >> 1) & 1u;
+          if (!mbar_wait(b_kve + 8 * st, ph ^ 1u, abort_flag, p.status)) { ok = false; break; }
+          const uint32_t kd = sbase + AT_KV_OFF + st * 2 * AT_TILE;
+          mbar_expect_tx(b_kvf + 8 * st, 2 * AT_TILE);
+          load(&tmK, kd, b_kvf + 8 * st, j * AT_B);
+          load(&tmV, kd + AT_TILE, b_kvf + 8 * st, j * AT_B);
+          last_par[st] = (int)ph;
+        }
+      }
+      // never leave with copies still landing in shared memory
+      if (q_par >= 0) mbar_wait_drain(b_q, (uint32_t)q_par);
+      for (int i = 0; i < 2; ++i)
+        if (last_par[i] >= 0) mbar_wait_drain(b_kvf + 8 * i, (uint32_t)last_par[i]);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer
+      const uint32_t qd = sbase + AT_Q_OFF;
+      // O += P_gp V_gp for global tile gp; `first` starts a new item's accumulator
+      auto issue_pv = [&](int gp, bool first) -> bool {
+        const int pb = gp & 1;
+        if (!mbar_wait(b_pf + 8 * pb, (uint32_t)(gp >> 1) & 1u, abort_flag, p.status)) return false;
+        tc_fence_after();
+        const uint32_t pd = sbase + AT_P_OFF + pb * 2 * AT_TILE;
+        const uint32_t vd = sbase + AT_KV_OFF + (gp & 1) * 2 * AT_TILE + AT_TILE;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_bf16(tmem + AT_O_COL, operand_desc(pd + (kk >> 2) * AT_TILE, 0, kk & 3),
+                   operand_desc(vd, 1, kk), p.idesc_pv, (!first || kk > 0) ? 1u : 0u);
+        mma_commit((gp & 1) ? b_pv2 : b_pv);
+        mma_commit(b_kve + 8 * (gp & 1));
+        return true;
+      };
+      bool ok = true;
+      int g = 0;
+      for (int w = blockIdx.x, it = 0; ok && w < nitems; w += gridDim.x, ++it) {
+        const int nk = p.nq - w / BH;
+        if (!mbar_wait(b_q, (uint32_t)it & 1u, abort_flag, p.status)) break;
+        for (int j = 0; j < nk; ++j, ++g) {
+          const int st = g & 1, sb = g & 1;
+          if (!mbar_wait(b_kvf + 8 * st, (uint32_t)(g >> 1) & 1u, abort_flag, p.status)) { ok = false; break; }
+          if (g >= 2 && !mbar_wait(b_se + 8 * sb, ((uint32_t)(g >> 1) & 1u) ^ 1u, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t kd = sbase + AT_KV_OFF + st * 2 * AT_TILE;
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_bf16(tmem + sb * AT_B, operand_desc(qd, 0, k), operand_desc(kd, 0, k), p.idesc_s,
+                     k > 0 ? 1u : 0u);
+          mma_commit(b_sf + 8 * sb);
+          if (j == nk - 1) mma_commit(b_qe);  // Q is free once this item's S MMAs are done
+          if (j >= 1 && !issue_pv(g - 1, j == 1)) { ok = false; break; }
+        }
+        if (ok && !issue_pv(g - 1, nk == 1)) ok = false;
+      }
+      // every MMA issued by this thread has completed once b_done flips
+      mma_commit(b_done);
+      mbar_wait_drain(b_done, 0);
+    }
+  } else {
+    // ---------------- softmax warps 2..9: lane quadrant warp % 4, key half (warp - 2) / 4
+    const int quad = warp & 3, half = (warp - 2) >> 2;
+    const int r = quad * 32 + lane;
+    const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+    bool ok = true;
+    int g = 0;  // global tile counter: S / P buffers, barrier parities
+    for (int w = blockIdx.x, it = 0; ok && w < nitems; w += gridDim.x, ++it) {
+      const int qt = p.nq - 1 - w / BH, bh = w % BH, b = bh / a.H, h = bh % a.H;
+      const int nk = qt + 1;
+      const int qi = qt * AT_B + r;
+      float m = -INFINITY, l = 0.f;
+      for (int j = 0; j < nk; ++j, ++g) {
+        const int sb = g & 1;
+        if (!warp_wait(b_sf + 8 * sb, (uint32_t)(g >> 1) & 1u, abort_flag, p.status)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t s0[32], s1[32];
+        tmem_ld32(lane_base + sb * AT_B + half * 64, s0);
+        tmem_ld32(lane_base + sb * AT_B + half * 64 + 32, s1);
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(b_se + 8 * sb);  // this thread is done reading S
+        float s[64];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          s[c] = __uint_as_float(s0[c]);
+          s[32 + c] = __uint_as_float(s1[c]);
+        }
+        if (j == qt) {  // diagonal tile: keys after the query are masked
+          const int k0 = j * AT_B + half * 64;
+#pragma unroll
+          for (int c = 0; c < 64; ++c)
+            if (k0 + c > qi) s[c] = -INFINITY;
+        }
+        float tmax = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 64; ++c) tmax = fmaxf(tmax, s[c]);
+        // exchange the half-row maxima with the partner warp (double-buffered slots;
+        // the mbarrier arrive releases the slot write, the wait acquires the partner's)
+        float* rx = red + (g & 1) * 256;
+        rx[half * 128 + r] = tmax;
+        const uint32_t xb = b_xmax + 8 * (quad * 2 + (g & 1));
+        mbar_arrive(xb);
+        if (!warp_wait(xb, (uint32_t)(g >> 1) & 1u, abort_flag, p.status)) { ok = false; break; }
+        tmax = fmaxf(tmax, rx[(half ^ 1) * 128 + r]) * p.c2;
+        // Lazy rescaling: the running max m (log2 units) only moves when the tile's
+        // max exceeds it by more than 8, so p <= 2^8 stays exact in fp32 and bf16;
+        // O and l always share the same m, so the result is unchanged.
+        const bool move = j == 0 || tmax > m + 8.0f;
+        const float m_new = move ? fmaxf(m, tmax) : m;
+        const float alpha = j == 0 ? 0.f : ex2(m - m_new);
+        float lsum = 0.f;
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const float p0 = ex2(fmaf(s[2 * c], p.c2, -m_new));
+          const float p1 = ex2(fmaf(s[2 * c + 1], p.c2, -m_new));
+          lsum += p0 + p1;
+          pk[c] = pack_bf16x2(p0, p1);
+        }
+        l = l * alpha + lsum;
+        m = m_new;
+        const bool rescale = j >= 1 && __any_sync(0xffffffffu, move);
+        if (rescale) {
+          // O must be stable: wait for the previous PV (tile g-1), then scale it
+          const uint32_t pb = (g - 1) & 1 ? b_pv2 : b_pv;
+          if (!warp_wait(pb, (uint32_t)((g - 1) >> 1) & 1u, abort_flag, p.status)) { ok = false; break; }
+          tc_fence_after();
+          uint32_t o[32];
+          tmem_ld32(lane_base + AT_O_COL + half * 32, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+          tmem_st32(lane_base + AT_O_COL + half * 32, o);
+          tmem_st_wait();
+        } else if (g >= 2) {
+          // the P buffer of this tile parity was last read by the PV of tile g-2
+          const uint32_t pb = g & 1 ? b_pv2 : b_pv;
+          if (!warp_wait(pb, (uint32_t)((g - 2) >> 1) & 1u, abort_flag, p.status)) { ok = false; break; }
+          tc_fence_after();
+        }
+        // P (bf16) into the 128B-swizzled A tile: row r, keys half*64 .. +64
+        const uint32_t prow = sbase + AT_P_OFF + (g & 1) * 2 * AT_TILE + half * AT_TILE + r * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(prow + ((c ^ (r & 7)) << 4)),
+                       "r"(pk[4 * c]), "r"(pk[4 * c + 1]), "r"(pk[4 * c + 2]), "r"(pk[4 * c + 3])
+                       : "memory");
+        fence_async_smem();
+        tc_fence_before();
+        mbar_arrive(b_pf + 8 * (g & 1));
+      }
+      if (!ok) break;
+      // epilogue of this item: its last PV (global tile g-1) is done
+      if (!warp_wait((g - 1) & 1 ? b_pv2 : b_pv, (uint32_t)((g - 1) >> 1) & 1u, abort_flag, p.status))
+        break;
+      tc_fence_after();
+      float* rl = red + 512;
+      rl[half * 128 + r] = l;
+      mbar_arrive(b_xsum + 8 * quad);
+      if (!warp_wait(b_xsum + 8 * quad, (uint32_t)it & 1u, abort_flag, p.status)) break;
+      const float lt = l + rl[(half ^ 1) * 128 + r];
+      const float inv = 1.0f / lt;
+      uint32_t o[32];
+      tmem_ld32(lane_base + AT_O_COL + half * 32, o);
+      tmem_ld_wait();
+      tc_fence_before();  // the next item's first PV overwrites O after this read
+      if (qi < a.T) {
+        bf16* dst = static_cast<bf16*>(a.o) + (long long)b * a.osb + (long long)h * a.osh +
+                    (long long)qi * a.ost + half * 32;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint4 u;
+          u.x = pack_bf16x2(__uint_as_float(o[8 * q]) * inv, __uint_as_float(o[8 * q + 1]) * inv);
+          u.y = pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv);
+          u.z = pack_bf16x2(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv);
+          u.w = pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv);
+          *reinterpret_cast<uint4*>(dst + 8 * q) = u;
+        }
+        if (half == 0) a.lse[(long long)bh * a.T + qi] = (m + __log2f(lt)) * 0.6931471805599453f;
+      }
+    }
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, AT_TMEM_COLS);
+  }
+}
+
+// ================================================================== backward
+// dS = P o (dP - D) with P = 2^(s*scale*log2e - lse*log2e) (the forward's lse),
+// dP = dO V^T, D = rowsum(dO o O); dQ = scale dS K, dK = scale dS^T Q, dV = P^T dO.
+// Two persistent kernels, both deterministic (no atomics): one owns 128-query
+// tiles and accumulates dQ over their key tiles, the other owns 128-key tiles
+// and accumulates dK and dV over their query tiles.
+
+constexpr int BW_THREADS = 320;
+
+// 64 bf16 of row r into a 128B-swizzled [128 x 64] tile (piece c at (c ^ (r & 7)) * 16).
+__device__ __forceinline__ void tile_row_store(uint32_t tile, int r, const uint32_t* pk) {
+  const uint32_t row = tile + r * 128;
+#pragma unroll
+  for (int c = 0; c < 8; ++c)
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + ((c ^ (r & 7)) << 4)),
+                 "r"(pk[4 * c]), "r"(pk[4 * c + 1]), "r"(pk[4 * c + 2]), "r"(pk[4 * c + 3])
+                 : "memory");
+}
+
+struct BwParams {
+  AttnArgs a;
+  int nq;
+  int swap_q, swap_o;  // index order of the q/k/v and the o/dO tensor maps
+  float c2;            // scale * log2(e)
+  uint32_t idesc_s, idesc_d;  // M128 N128 (K-major B) and M128 N64 (MN-major B)
+  unsigned* status;
+};
+
+__device__ __forceinline__ void bw_load(const CUtensorMap* tm, int swap, uint32_t dst, uint32_t bar,
+                                        int t0, int h, int b) {
+  if (swap) tma_load_4d(dst, tm, bar, 0, h, t0, b);
+  else tma_load_4d(dst, tm, bar, 0, t0, h, b);
+}
+
+// ------------------------------------------------------------------ dQ
+// smem: Q | dO (per item) | K,V ring (2 stages) | dS (two 64-key halves)
+constexpr int DQ_Q = 0, DQ_DO = AT_TILE, DQ_KV = 2 * AT_TILE, DQ_DS = 6 * AT_TILE;
+constexpr int DQ_BAR = 8 * AT_TILE;
+constexpr int DQ_NBARS = 12;
+constexpr int DQ_SMEM = 1024 + DQ_BAR + 8 * (DQ_NBARS + 2);
+
+__global__ void __launch_bounds__(BW_THREADS, 1)
+    k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                     const BwParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + DQ_BAR);
+  // q_full, q_empty, kv_full[2], kv_empty[2], sdp_full, sdp_empty, ds_full, dq_done, done
+  const uint32_t b_qf = smem_u32(bars), b_qe = b_qf + 8, b_kvf = b_qe + 8, b_kve = b_kvf + 16;
+  const uint32_t b_sf = b_kve + 16, b_se = b_sf + 8, b_dsf = b_se + 8, b_dq = b_dsf + 8, b_done = b_dq + 8;
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bars + DQ_NBARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + DQ_NBARS + 1);
+  const AttnArgs& a = p.a;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int BH = a.B * a.H, nitems = p.nq * BH;
+
+  if (threadIdx.x == 0) {
+    mbar_init(b_qf, 1);
+    mbar_init(b_qe, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(b_kvf + 8 * i, 1);
+      mbar_init(b_kve + 8 * i, 1);
+    }
+    mbar_init(b_sf, 1);
+    mbar_init(b_se, 256);
+    mbar_init(b_dsf, 256);
+    mbar_init(b_dq, 1);
+    mbar_init(b_done, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), AT_TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  constexpr uint32_t C_S = 0, C_DP = 128, C_DQ = 256;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int last_par[2] = {-1, -1}, q_par = -1, g = 0;
+      bool ok = true;
+      for (int w = blockIdx.x, it = 0; ok && w < nitems; w += gridDim.x, ++it) {
+        const int qt = p.nq - 1 - w / BH, bh = w % BH, b = bh / a.H, h = bh % a.H;
+        if (it > 0 && !mbar_wait(b_qe, (uint32_t)(it - 1) & 1u, abort_flag, p.status)) break;
+        mbar_expect_tx(b_qf, 2 * AT_TILE);
+        bw_load(&tmQ, p.swap_q, sbase + DQ_Q, b_qf, qt * AT_B, h, b);
+        bw_load(&tmdO, p.swap_o, sbase + DQ_DO, b_qf, qt * AT_B, h, b);
+        q_par = it & 1;
+        for (int j = 0; j <= qt; ++j, ++g) {
+          const int st = g & 1;
+          const uint32_t ph = (uint32_t)(g >> 1) & 1u;
+          if (!mbar_wait(b_kve + 8 * st, ph ^ 1u, abort_flag, p.status)) { ok = false; break; }
+          const uint32_t kd = sbase + DQ_KV + st * 2 * AT_TILE;
+          mbar_expect_tx(b_kvf + 8 * st, 2 * AT_TILE);
+          bw_load(&tmK, p.swap_q, kd, b_kvf + 8 * st, j * AT_B, h, b);
+          bw_load(&tmV, p.swap_q, kd + AT_TILE, b_kvf + 8 * st, j * AT_B, h, b);
+          last_par[st] = (int)ph;
+        }
+      }
+      if (q_par >= 0) mbar_wait_drain(b_qf, (uint32_t)q_par);
+      for (int i = 0; i < 2; ++i)
+        if (last_par[i] >= 0) mbar_wait_drain(b_kvf + 8 * i, (uint32_t)last_par[i]);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      auto issue_dq = [&](int gp, bool first) -> bool {
+        if (!mbar_wait(b_dsf, (uint32_t)gp & 1u, abort_flag, p.status)) return false;
+        tc_fence_after();
+        const uint32_t kd = sbase + DQ_KV + (gp & 1) * 2 * AT_TILE;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_bf16(tmem + C_DQ, operand_desc(sbase + DQ_DS + (kk >> 2) * AT_TILE, 0, kk & 3),
+                   operand_desc(kd, 1, kk), p.idesc_d, (!first || kk > 0) ? 1u : 0u);
+        mma_commit(b_dq);
+        mma_commit(b_kve + 8 * (gp & 1));
+        return true;
+      };
+      bool ok = true;
+      int g = 0;
+      for (int w = blockIdx.x, it = 0; ok && w < nitems; w += gridDim.x, ++it) {
+        const int nk = p.nq - w / BH;
+        if (!mbar_wait(b_qf, (uint32_t)it & 1u, abort_flag, p.status)) break;
+        for (int j = 0; j < nk; ++j, ++g) {
+          const int st = g & 1;
+          if (!mbar_wait(b_kvf + 8 * st, (uint32_t)(g >> 1) & 1u, abort_flag, p.status)) { ok = false; break; }
+          if (g >= 1 && !mbar_wait(b_se, (uint32_t)(g - 1) & 1u, abort_flag, p.status)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t kd = sbase + DQ_KV + st * 2 * AT_TILE;
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_bf16(tmem + C_S, operand_desc(sbase + DQ_Q, 0, k), operand_desc(kd, 0, k), p.idesc_s,
+                     k > 0 ? 1u : 0u);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_bf16(tmem + C_DP, operand_desc(sbase + DQ_DO, 0, k), operand_desc(kd + AT_TILE, 0, k),
+                     p.idesc_s, k > 0 ? 1u : 0u);
+          mma_commit(b_sf);
+          if (j == nk - 1) mma_commit(b_qe);
+          if (j >= 1 && !issue_dq(g - 1, j == 1)) { ok = false; break; }
+        }
+        if (ok && !issue_dq(g - 1, nk == 1)) ok = false;
+      }
+      mma_commit(b_done);
+      mbar_wait_drain(b_done, 0);
+    }
+  } else {
+    const int quad = warp & 3, half = (warp - 2) >> 2;
+    const int r = quad * 32 + lane;
+    const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+    bool ok = true;
+    int g = 0;
+    for (int w = blockIdx.x, it = 0; ok && w < nitems; w += gridDim.x, ++it) {
+      const int qt = p.nq - 1 - w / BH, bh = w % BH, b = bh / a.H, h = bh % a.H;
+      const int nk = qt + 1;
+      const int qi = qt * AT_B + r;
+      const bool valid = qi < a.T;
+      const float lse2 = valid ? a.lse[(long long)bh * a.T + qi] * 1.4426950408889634f : 0.f;
+      const float Dr = valid ? a.Dbuf[(long long)bh * a.T + qi] : 0.f;
+      for (int j = 0; j < nk; ++j, ++g) {
+        if (!warp_wait(b_sf, (uint32_t)g & 1u, abort_flag, p.status)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t sv[64], dv[64];
+        tmem_ld32(lane_base + C_S + half * 64, *reinterpret_cast<uint32_t(*)[32]>(sv));
+        tmem_ld32(lane_base + C_S + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
+        tmem_ld32(lane_base + C_DP + half * 64, *reinterpret_cast<uint32_t(*)[32]>(dv));
+        tmem_ld32(lane_base + C_DP + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(dv + 32));
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(b_se);
+        const bool diag = j == qt;
+        const int k0 = j * AT_B + half * 64;
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          float p0 = ex2(fmaf(__uint_as_float(sv[2 * c]), p.c2, -lse2));
+          float p1 = ex2(fmaf(__uint_as_float(sv[2 * c + 1]), p.c2, -lse2));
+          if (diag && k0 + 2 * c > qi) p0 = 0.f;
+          if (diag && k0 + 2 * c + 1 > qi) p1 = 0.f;
+          pk[c] = pack_bf16x2(p0 * (__uint_as_float(dv[2 * c]) - Dr), p1 * (__uint_as_float(dv[2 * c + 1]) - Dr));
+        }
+        // the dS tile is free once the previous dQ MMA has completed
+        if (g >= 1 && !warp_wait(b_dq, (uint32_t)(g - 1) & 1u, abort_flag, p.status)) { ok = false; break; }
+        tile_row_store(sbase + DQ_DS + half * AT_TILE, r, pk);
+        fence_async_smem();
+        tc_fence_before();
+        mbar_arrive(b_dsf);
+      }
+      if (!ok) break;
+      if (!warp_wait(b_dq, (uint32_t)(g - 1) & 1u, abort_flag, p.status)) break;
+      tc_fence_after();
+      uint32_t o[32];
+      tmem_ld32(lane_base + C_DQ + half * 32, o);
+      tmem_ld_wait();
+      tc_fence_before();
+      if (valid) {
+        bf16* dst = static_cast<bf16*>(a.dq) + (long long)b * a.sb + (long long)h * a.sh +
+                    (long long)qi * a.st + half * 32;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint4 u;
+          u.x = pack_bf16x2(__uint_as_float(o[8 * q]) * a.scale, __uint_as_float(o[8 * q + 1]) * a.scale);
+          u.y = pack_bf16x2(__uint_as_float(o[8 * q + 2]) * a.scale, __uint_as_float(o[8 * q + 3]) * a.scale);
+          u.z = pack_bf16x2(__uint_as_float(o[8 * q + 4]) * a.scale, __uint_as_float(o[8 * q + 5]) * a.scale);
+          u.w = pack_bf16x2(__uint_as_float(o[8 * q + 6]) * a.scale, __uint_as_float(o[8 * q + 7]) * a.scale);
+          *reinterpret_cast<uint4*>(dst + 8 * q) = u;
+        }
+      }
+    }
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, AT_TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ dK, dV
+// smem: K | V (per item) | Q,dO ring (2 stages) | lse2, D ring (2 x 1 KB) | P^T | dS^T
+constexpr int DK_K = 0, DK_V = AT_TILE, DK_QD = 2 * AT_TILE, DK_LD = 6 * AT_TILE;
+constexpr int DK_PT = DK_LD + 2048, DK_DST = DK_PT + 2 * AT_TILE;
+constexpr int DK_BAR = DK_DST + 2 * AT_TILE;
+constexpr int DK_NBARS = 12;
+constexpr int DK_SMEM = 1024 + DK_BAR + 8 * (DK_NBARS + 2);
+
+__global__ void __launch_bounds__(BW_THREADS, 1)
+    k_attn_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                       const BwParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  float* ldbuf = reinterpret_cast<float*>(smem + DK_LD);  // stage s: lse2[128] then D[128]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + DK_BAR);
+  // kv_full, kv_empty, qd_full[2], qd_empty[2], sdp_full, sdp_empty, ds_full, mma_done, done
+  const uint32_t b_kvf = smem_u32(bars), b_kve = b_kvf + 8, b_qdf = b_kve + 8, b_qde = b_qdf + 16;
+  const uint32_t b_sf = b_qde + 16, b_se = b_sf + 8, b_dsf = b_se + 8, b_mm = b_dsf + 8, b_done = b_mm + 8;
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bars + DK_NBARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + DK_NBARS + 1);
+  const AttnArgs& a = p.a;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int BH = a.B * a.H, nitems = p.nq * BH;
+  // work item w: key tile w / BH (tile 0 has the most query tiles), (batch, head) = w % BH
+
+  if (threadIdx.x == 0) {
+    mbar_init(b_kvf, 1);
+    mbar_init(b_kve, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(b_qdf + 8 * i, 33);  // the TMA expect_tx arrive + 32 lanes that stage lse2 / D
+      mbar_init(b_qde + 8 * i, 1);
+    }
+    mbar_init(b_sf, 1);
+    mbar_init(b_se, 256);
+    mbar_init(b_dsf, 256);
+    mbar_init(b_mm, 1);
+    mbar_init(b_done, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), AT_TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  constexpr uint32_t C_S = 0, C_DP = 128, C_DV = 256, C_DK = 320;
+
+  if (warp == 0) {
+    // ---------------- producer warp: TMA by lane 0, lse2 / D staged by all lanes
+    int last_par[2] = {-1, -1}, kv_par = -1, g = 0;
+    bool ok = true;
+    for (int w = blockIdx.x, it = 0; ok && w < nitems; w += gridDim.x, ++it) {
+      const int kt = w / BH, bh = w % BH, b = bh / a.H, h = bh % a.H;
+      if (it > 0 && !warp_wait(b_kve, (uint32_t)(it - 1) & 1u, abort_flag, p.status)) break;
+      if (lane == 0) {
+        mbar_expect_tx(b_kvf, 2 * AT_TILE);
+        bw_load(&tmK, p.swap_q, sbase + DK_K, b_kvf, kt * AT_B, h, b);
+        bw_load(&tmV, p.swap_q, sbase + DK_V, b_kvf, kt * AT_B, h, b);
+      }
+      kv_par = it & 1;
+      for (int i = kt; i < p.nq; ++i, ++g) {
+        const int st = g & 1;
+        const uint32_t ph = (uint32_t)(g >> 1) & 1u;
+        if (!warp_wait(b_qde + 8 * st, ph ^ 1u, abort_flag, p.status)) { ok = false; break; }
+        if (lane == 0) {
+          const uint32_t qd = sbase + DK_QD + st * 2 * AT_TILE;
+          mbar_expect_tx(b_qdf + 8 * st, 2 * AT_TILE);
+          bw_load(&tmQ, p.swap_q, qd, b_qdf + 8 * st, i * AT_B, h, b);
+          bw_load(&tmdO, p.swap_o, qd + AT_TILE, b_qdf + 8 * st, i * AT_B, h, b);
+        }
+        float* lb = ldbuf + st * 256;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int c = lane * 4 + e, q = i * AT_B + c;
+          const bool v = q < a.T;
+          lb[c] = v ? a.lse[(long long)bh * a.T + q] * 1.4426950408889634f : INFINITY;
+          lb[128 + c] = v ? a.Dbuf[(long long)bh * a.T + q] : 0.f;
+        }
+        mbar_arrive(b_qdf + 8 * st);
+        last_par[st] = (int)ph;
+      }
+    }
+    if (lane == 0) {
+      if (kv_par >= 0) mbar_wait_drain(b_kvf, (uint32_t)kv_par);
+      for (int i = 0; i < 2; ++i)
+        if (last_par[i] >= 0) mbar_wait_drain(b_qdf + 8 * i, (uint32_t)last_par[i]);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      auto issue_kv = [&](int gp, bool first) -> bool {
+        if (!mbar_wait(b_dsf, (uint32_t)gp & 1u, abort_flag, p.status)) return false;
+        tc_fence_after();
+        const uint32_t qd = sbase + DK_QD + (gp & 1) * 2 * AT_TILE;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_bf16(tmem + C_DV, operand_desc(sbase + DK_PT + (kk >> 2) * AT_TILE, 0, kk & 3),
+                   operand_desc(qd + AT_TILE, 1, kk), p.idesc_d, (!first || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_bf16(tmem + C_DK, operand_desc(sbase + DK_DST + (kk >> 2) * AT_TILE, 0, kk & 3),
+                   operand_desc(qd, 1, kk), p.idesc_d, (!first || kk > 0) ? 1u : 0u);
+        mma_commit(b_mm);
+        mma_commit(b_qde + 8 * (gp & 1));
+        return true;
+      };
+      bool ok = true;
+      int g = 0;
+      for (int w = blockIdx.x, it = 0; ok && w < nitems; w += gridDim.x, ++it) {
+        const int n = p.nq - w / BH;  // query tiles kt .. nq-1
+        if (!mbar_wait(b_kvf, (uint32_t)it & 1u, abort_flag, p.status)) break;
+        for (int j = 0; j < n; ++j, ++g) {
+          const int st = g & 1;
+          if (!mbar_wait(b_qdf + 8 * st, (uint32_t)(g >> 1) & 1u, abort_flag, p.status)) { ok = false; break; }
+          if (g >= 1 && !mbar_wait(b_se, (uint32_t)(g - 1) & 1u, abort_flag, p.status)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t qd = sbase + DK_QD + st * 2 * AT_TILE;
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_bf16(tmem + C_S, operand_desc(sbase + DK_K, 0, k), operand_desc(qd, 0, k), p.idesc_s,
+                     k > 0 ? 1u : 0u);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_bf16(tmem + C_DP, operand_desc(sbase + DK_V, 0, k), operand_desc(qd + AT_TILE, 0, k),
+                     p.idesc_s, k > 0 ? 1u : 0u);
+          mma_commit(b_sf);
+          if (j >= 1 && !issue_kv(g - 1, j == 1)) { ok = false; break; }
+        }
+        if (ok && !issue_kv(g - 1, n == 1)) ok = false;
+        if (ok) mma_commit(b_kve);  // K, V of this item are no longer read
+      }
+      mma_commit(b_done);
+      mbar_wait_drain(b_done, 0);
+    }
+  } else {
+    const int quad = warp & 3, half = (warp - 2) >> 2;
+    const int r = quad * 32 + lane;
+    const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+    bool ok = true;
+    int g = 0;
+    for (int w = blockIdx.x, it = 0; ok && w < nitems; w += gridDim.x, ++it) {
+      const int kt = w / BH, bh = w % BH, b = bh / a.H, h = bh % a.H;
+      const int kr = kt * AT_B + r;
+      for (int i = kt; i < p.nq; ++i, ++g) {
+        const int st = g & 1;
+        // lse2 / D of this query tile (staged with the Q / dO tiles)
+        if (!warp_wait(b_qdf + 8 * st, (uint32_t)(g >> 1) & 1u, abort_flag, p.status)) { ok = false; break; }
+        if (!warp_wait(b_sf, (uint32_t)g & 1u, abort_flag, p.status)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t sv[64], dv[64];
+        tmem_ld32(lane_base + C_S + half * 64, *reinterpret_cast<uint32_t(*)[32]>(sv));
+        tmem_ld32(lane_base + C_S + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
+        tmem_ld32(lane_base + C_DP + half * 64, *reinterpret_cast<uint32_t(*)[32]>(dv));
+        tmem_ld32(lane_base + C_DP + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(dv + 32));
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(b_se);
+        const float* lb = ldbuf + st * 256 + half * 64;
+        const bool diag = i == kt;
+        const int q0 = i * AT_B + half * 64;
+        uint32_t pp[32], pd[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          float p0 = ex2(fmaf(__uint_as_float(sv[2 * c]), p.c2, -lb[2 * c]));
+          float p1 = ex2(fmaf(__uint_as_float(sv[2 * c + 1]), p.c2, -lb[2 * c + 1]));
+          if (diag && kr > q0 + 2 * c) p0 = 0.f;
+          if (diag && kr > q0 + 2 * c + 1) p1 = 0.f;
+          pp[c] = pack_bf16x2(p0, p1);
+          pd[c] = pack_bf16x2(p0 * (__uint_as_float(dv[2 * c]) - lb[128 + 2 * c]),
+                              p1 * (__uint_as_float(dv[2 * c + 1]) - lb[128 + 2 * c + 1]));
+        }
+        // P^T / dS^T tiles are free once the previous dV / dK MMAs have completed
+        if (g >= 1 && !warp_wait(b_mm, (uint32_t)(g - 1) & 1u, abort_flag, p.status)) { ok = false; break; }
+        tile_row_store(sbase + DK_PT + half * AT_TILE, r, pp);
+        tile_row_store(sbase + DK_DST + half * AT_TILE, r, pd);
+        fence_async_smem();
+        tc_fence_before();
+        mbar_arrive(b_dsf);
+      }
+      if (!ok) break;
+      if (!warp_wait(b_mm, (uint32_t)(g - 1) & 1u, abort_flag, p.status)) break;
+      tc_fence_after();
+      uint32_t ov[32], ok_[32];
+      tmem_ld32(lane_base + C_DV + half * 32, ov);
+      tmem_ld32(lane_base + C_DK + half * 32, ok_);
+      tmem_ld_wait();
+      tc_fence_before();
+      if (kr < a.T) {
+        const long long off = (long long)b * a.sb + (long long)h * a.sh + (long long)kr * a.st + half * 32;
+        bf16* dvd = static_cast<bf16*>(a.dv) + off;
+        bf16* dkd = static_cast<bf16*>(a.dk) + off;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint4 u, k;
+          u.x = pack_bf16x2(__uint_as_float(ov[8 * q]), __uint_as_float(ov[8 * q + 1]));
+          u.y = pack_bf16x2(__uint_as_float(ov[8 * q + 2]), __uint_as_float(ov[8 * q + 3]));
+          u.z = pack_bf16x2(__uint_as_float(ov[8 * q + 4]), __uint_as_float(ov[8 * q + 5]));
+          u.w = pack_bf16x2(__uint_as_float(ov[8 * q + 6]), __uint_as_float(ov[8 * q + 7]));
+          k.x = pack_bf16x2(__uint_as_float(ok_[8 * q]) * a.scale, __uint_as_float(ok_[8 * q + 1]) * a.scale);
+          k.y = pack_bf16x2(__uint_as_float(ok_[8 * q + 2]) * a.scale, __uint_as_float(ok_[8 * q + 3]) * a.scale);
+          k.z = pack_bf16x2(__uint_as_float(ok_[8 * q + 4]) * a.scale, __uint_as_float(ok_[8 * q + 5]) * a.scale);
+          k.w = pack_bf16x2(__uint_as_float(ok_[8 * q + 6]) * a.scale, __uint_as_float(ok_[8 * q + 7]) * a.scale);
+          *reinterpret_cast<uint4*>(dvd + 8 * q) = u;
+          *reinterpret_cast<uint4*>(dkd + 8 * q) = k;
+        }
+      }
+    }
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, AT_TMEM_COLS);
+  }
+}
+
+typedef CUresult (*PFN_encodeTiled_t)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                      const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                      const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                      CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+PFN_encodeTiled_t encode_fn() {
+  static PFN_encodeTiled_t fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_encodeTiled_t>(ptr);
+  }
+  return fn;
+}
+
+// 4-D map over a strided [B, H, T, 64] bf16 view: dims (d, t, h, b), or (d, h, t, b)
+// when the head stride is the smaller one; boxes of 128 rows x 64 bf16, 128B swizzle.
+bool make_head_map(CUtensorMap* tm, const void* base, const AttnArgs& a, int swap) {
+  PFN_encodeTiled_t enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[4], strides[3];
+  cuuint32_t box[4], el[4] = {1, 1, 1, 1};
+  dims[0] = AT_D;
+  box[0] = AT_D;
+  if (swap) {
+    dims[1] = a.H; dims[2] = a.T;
+    strides[0] = a.sh * 2; strides[1] = a.st * 2;
+    box[1] = 1; box[2] = AT_B;
+  } else {
+    dims[1] = a.T; dims[2] = a.H;
+    strides[0] = a.st * 2; strides[1] = a.sh * 2;
+    box[1] = AT_B; box[2] = 1;
+  }
+  dims[3] = a.B;
+  strides[2] = a.sb * 2;
+  box[3] = 1;
+  CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
+                   el, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+uint32_t mma_idesc(int n, int b_mn) {
+  // kind::f16: D fp32, A and B bf16, A K-major, B K- or MN-major, N >> 3, M = 128 >> 4
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)b_mn << 16) | ((uint32_t)(n >> 3) << 17) |
+         ((uint32_t)(AT_B >> 4) << 24);
+}
+
+}  // namespace
+
+static bool tc_args_ok(const AttnArgs& a) {
+  if (a.d != AT_D || a.T <= 0 || a.B <= 0 || a.H <= 0) return false;
+  if (a.st % 8 || a.sh % 8 || a.sb % 8 || a.ost % 8 || a.osh % 8 || a.osb % 8) return false;
+  return true;
+}
+
+int attn_fwd_tc(const AttnArgs& a, cudaStream_t s) {
+  if (!tc_args_ok(a)) return (int)cudaErrorInvalidValue;
+  if ((reinterpret_cast<uintptr_t>(a.q) | reinterpret_cast<uintptr_t>(a.k) |
+       reinterpret_cast<uintptr_t>(a.v) | reinterpret_cast<uintptr_t>(a.o)) & 15)
+    return (int)cudaErrorInvalidValue;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(k_attn_fwd_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, AT_SMEM);
+    if (e != cudaSuccess) return (int)e;
+    attr_set = true;
+  }
+  AtParams p;
+  p.a = a;
+  p.nq = (a.T + AT_B - 1) / AT_B;
+  p.swap_ht = a.sh < a.st ? 1 : 0;
+  p.c2 = a.scale * 1.4426950408889634f;
+  p.idesc_s = mma_idesc(AT_B, 0);
+  p.idesc_pv = mma_idesc(AT_D, 1);
+  p.status = a.status;
+  CUtensorMap tq, tk, tv;
+  if (!make_head_map(&tq, a.q, a, p.swap_ht) || !make_head_map(&tk, a.k, a, p.swap_ht) ||
+      !make_head_map(&tv, a.v, a, p.swap_ht))
+    return (int)cudaErrorInvalidValue;
+  const long long items = (long long)p.nq * a.B * a.H;
+  const int grid = (int)(items < num_sms() ? items : num_sms());
+  k_attn_fwd_tc<<<grid, AT_THREADS, AT_SMEM, s>>>(tq, tk, tv, p);
+  return (int)cudaGetLastError();
+}
+
+int attn_bwd_tc(const AttnArgs& a, cudaStream_t s) {
+  if (!tc_args_ok(a)) return (int)cudaErrorInvalidValue;
+  if ((reinterpret_cast<uintptr_t>(a.q) | reinterpret_cast<uintptr_t>(a.k) |
+       reinterpret_cast<uintptr_t>(a.v) | reinterpret_cast<uintptr_t>(a.dO) |
+       reinterpret_cast<uintptr_t>(a.dq) | reinterpret_cast<uintptr_t>(a.dk) |
+       reinterpret_cast<uintptr_t>(a.dv)) & 15)
+    return (int)cudaErrorInvalidValue;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(k_attn_bwd_dq_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, DQ_SMEM);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(k_attn_bwd_dkdv_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, DK_SMEM);
+    if (e != cudaSuccess) return (int)e;
+    attr_set = true;
+  }
+  BwParams p;
+  p.a = a;
+  p.nq = (a.T + AT_B - 1) / AT_B;
+  p.swap_q = a.sh < a.st ? 1 : 0;
+  p.swap_o = a.osh < a.ost ? 1 : 0;
+  p.c2 = a.scale * 1.4426950408889634f;
+  p.idesc_s = mma_idesc(AT_B, 0);
+  p.idesc_d = mma_idesc(AT_D, 1);
+  p.status = a.status;
+  AttnArgs ao = a;  // dO shares the o strides
+  ao.st = a.ost; ao.sh = a.osh; ao.sb = a.osb;
+  CUtensorMap tq, tk, tv, tdo;
+  if (!make_head_map(&tq, a.q, a, p.swap_q) || !make_head_map(&tk, a.k, a, p.swap_q) ||
+      !make_head_map(&tv, a.v, a, p.swap_q) || !make_head_map(&tdo, a.dO, ao, p.swap_o))
+    return (int)cudaErrorInvalidValue;
+  const long long items = (long long)p.nq * a.B * a.H;
+  const int grid = (int)(items < num_sms() ? items : num_sms());
+  k_attn_bwd_dkdv_tc<<<grid, BW_THREADS, DK_SMEM, s>>>(tq, tk, tv, tdo, p);
+  k_attn_bwd_dq_tc<<<grid, BW_THREADS, DQ_SMEM, s>>>(tq, tk, tv, tdo, p);
+  return (int)cudaGetLastError();
+}
+
+}  // namespace gpt2k

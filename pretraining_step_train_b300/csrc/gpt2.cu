@@ -304,9 +304,10 @@ int forward_impl(gpt2* h) {
     a.sb = (long long)s.T * 3 * C; a.sh = s.d(); a.st = 3 * C;
     a.osb = (long long)s.T * C; a.osh = s.d(); a.ost = C;
     a.scale = 1.0f / sqrtf((float)s.d());
+    a.status = status;
     int e = 0;
     REGION(GPT2_K_ATTN_FWD, attn_flops, 4.0 * MC * E,
-           e = (sizeof(T) == 2 ? attn_fwd_bf16(a, st) : attn_fwd_f32(a, st)));
+           e = (sizeof(T) == 2 ? attn_fwd_tc(a, st) : attn_fwd_f32(a, st)));
     CKI(e);
     g = GemmArgs();
     g.A = P.atty(l); g.lda = C; g.B = P.param(P_APW, l); g.ldb = C;
@@ -440,6 +441,7 @@ int backward_impl(gpt2* h) {
     a.sb = (long long)s.T * 3 * C; a.sh = s.d(); a.st = 3 * C;
     a.osb = (long long)s.T * C; a.osh = s.d(); a.ost = C;
     a.scale = 1.0f / sqrtf((float)s.d());
+    a.status = h->at<unsigned>(h->p.status);
     int e = 0;
     REGION(GPT2_K_ATTN_BWD, attn_flops, 8.0 * MC * E, e = (bf ? attn_bwd_bf16(a, st) : attn_bwd_f32(a, st)));
     CKI(e);
@@ -775,7 +777,7 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   a.B = B; a.H = H; a.T = T; a.d = d;
   a.sb = sb; a.sh = sh; a.st = st; a.osb = osb; a.osh = osh; a.ost = ost;
   a.scale = scale;
-  int e = attn_fwd_bf16(a, static_cast<cudaStream_t>(stream));
+  int e = attn_fwd_tc(a, static_cast<cudaStream_t>(stream));
   if (e == (int)cudaErrorInvalidValue) return GPT2_E_INVAL;
   if (e) return cuda_fail((cudaError_t)e, "attn_fwd");
   return GPT2_OK;
