@@ -6,7 +6,7 @@
 // Persistent: one CTA per SM walks a list of work items (128-query tile, batch,
 // head), heaviest causal tiles first, item c, c + grid, c + 2 grid, ...
 //   warp 0      TMA: each item's Q tile, then its K and V tiles of 128 keys into
-//               a 2-stage ring that runs on across items, so the next item's
+//               a 4-stage ring that runs on across items, so the next item's
 //               tiles load while this one finishes (4-D tensor maps over the
 //               strided q / k / v views, 128B swizzle; rows past T arrive as zeros);
 //   warp 1      owns 512 TMEM columns: S double buffer (2 x 128 fp32 columns)
@@ -36,11 +36,12 @@ constexpr int AT_B = 128;                       // queries per tile = keys per t
 constexpr int AT_D = 64;                        // head size
 constexpr int AT_TILE = AT_B * AT_D * 2;        // 16 KB: one [128 x 64] bf16 tile
 constexpr int AT_Q_OFF = 0;
+constexpr int AT_KV_STAGES = 4;
 constexpr int AT_KV_OFF = AT_TILE;              // stage s: K at +s*2*TILE, V at +s*2*TILE+TILE
-constexpr int AT_P_OFF = AT_KV_OFF + 4 * AT_TILE;  // buffer b: +b*2*TILE, key half h at +h*TILE
+constexpr int AT_P_OFF = AT_KV_OFF + 2 * AT_KV_STAGES * AT_TILE;  // buffer b: +b*2*TILE, half h at +h*TILE
 constexpr int AT_RED_OFF = AT_P_OFF + 4 * AT_TILE; // row-max exchange [2][2][128] + row-sum [2][128]
 constexpr int AT_BAR_OFF = AT_RED_OFF + 6 * 128 * 4;
-constexpr int AT_NBARS = 27;
+constexpr int AT_NBARS = 31;
 constexpr int AT_SMEM = 1024 + AT_BAR_OFF + 8 * (AT_NBARS + 2);
 constexpr int AT_THREADS = 320;
 constexpr int AT_TMEM_COLS = 512;
@@ -70,6 +71,23 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
   const bool ok = mbar_wait(bar, parity, abort_flag, status);
   return __all_sync(0xffffffffu, ok);
 }
+// One arrival for the warp once every lane's prior work is done.
+__device__ __forceinline__ void warp_arrive(uint32_t bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+// Tree reductions over a thread's own values (short dependency chains).
+template <int N>
+__device__ __forceinline__ float tree_max(const float* v) {
+  float t[N / 2];
+#pragma unroll
+  for (int i = 0; i < N / 2; ++i) t[i] = fmaxf(v[2 * i], v[2 * i + 1]);
+#pragma unroll
+  for (int w = N / 4; w >= 1; w >>= 1)
+#pragma unroll
+    for (int i = 0; i < w; ++i) t[i] = fmaxf(t[i], t[i + w]);
+  return t[0];
+}
 
 __global__ void __launch_bounds__(AT_THREADS, 1)
     k_attn_fwd_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -79,10 +97,11 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   const uint32_t sbase = smem_u32(smem);
   float* red = reinterpret_cast<float*>(smem + AT_RED_OFF);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + AT_BAR_OFF);
-  // q_full, kv_full[2], kv_empty[2], s_full[2], s_empty[2], p_full[2], pv_done, done,
+  // q_full, kv_full[4], kv_empty[4], s_full[2], s_empty[2], p_full[2], pv_done, done,
   // xmax[4 quadrants][2], xsum[4 quadrants] (the two warps of a quadrant exchange row
   // stats), q_empty (the Q tile may be overwritten by the next item)
-  const uint32_t b_q = smem_u32(bars), b_kvf = b_q + 8, b_kve = b_kvf + 16, b_sf = b_kve + 16;
+  const uint32_t b_q = smem_u32(bars), b_kvf = b_q + 8, b_kve = b_kvf + 8 * AT_KV_STAGES;
+  const uint32_t b_sf = b_kve + 8 * AT_KV_STAGES;
   const uint32_t b_se = b_sf + 16, b_pf = b_se + 16, b_pv = b_pf + 16, b_done = b_pv + 8;
   const uint32_t b_xmax = b_done + 8, b_xsum = b_xmax + 64, b_qe = b_xsum + 32;
   // pv_done[i] (i = tile parity) completes for the PVs of global tiles i, i+2, ...:
@@ -99,19 +118,21 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(b_q, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < AT_KV_STAGES; ++i) {
       mbar_init(b_kvf + 8 * i, 1);
       mbar_init(b_kve + 8 * i, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(b_sf + 8 * i, 1);
-      mbar_init(b_se + 8 * i, 256);
-      mbar_init(b_pf + 8 * i, 256);
+      mbar_init(b_se + 8 * i, 8);  // one arrival per softmax warp
+      mbar_init(b_pf + 8 * i, 8);
     }
     mbar_init(b_pv, 1);
     mbar_init(b_done, 1);
     mbar_init(b_qe, 1);
     mbar_init(b_pv2, 1);
-    for (int i = 0; i < 8; ++i) mbar_init(b_xmax + 8 * i, 64);
-    for (int i = 0; i < 4; ++i) mbar_init(b_xsum + 8 * i, 64);
+    for (int i = 0; i < 8; ++i) mbar_init(b_xmax + 8 * i, 2);  // the two warps of a quadrant
+    for (int i = 0; i < 4; ++i) mbar_init(b_xsum + 8 * i, 2);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -128,7 +149,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ---------------- TMA producer
-      int last_par[2] = {-1, -1}, q_par = -1;
+      int last_par[AT_KV_STAGES] = {-1, -1, -1, -1}, q_par = -1;
       int g = 0;  // K/V tiles issued so far (ring position)
       bool ok = true;
       for (int w = blockIdx.x, it = 0; ok && w < nitems; w += gridDim.x, ++it) {
@@ -142,8 +163,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         load(&tmQ, sbase + AT_Q_OFF, b_q, qt * AT_B);
         q_par = it & 1;
         for (int j = 0; j <= qt; ++j, ++g) {
-          const int st = g & 1;
-          const uint32_t ph = (uint32_t)(g >> 1) & 1u;
+          const int st = g % AT_KV_STAGES;
+          const uint32_t ph = (uint32_t)(g / AT_KV_STAGES) & 1u;
           if (!mbar_wait(b_kve + 8 * st, ph ^ 1u, abort_flag, p.status)) { ok = false; break; }
           const uint32_t kd = sbase + AT_KV_OFF + st * 2 * AT_TILE;
           mbar_expect_tx(b_kvf + 8 * st, 2 * AT_TILE);
@@ -154,7 +175,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       }
       // never leave with copies still landing in shared memory
       if (q_par >= 0) mbar_wait_drain(b_q, (uint32_t)q_par);
-      for (int i = 0; i < 2; ++i)
+      for (int i = 0; i < AT_KV_STAGES; ++i)
         if (last_par[i] >= 0) mbar_wait_drain(b_kvf + 8 * i, (uint32_t)last_par[i]);
     }
   } else if (warp == 1) {
@@ -167,13 +188,13 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         if (!mbar_wait(b_pf + 8 * pb, (uint32_t)(gp >> 1) & 1u, abort_flag, p.status)) return false;
         tc_fence_after();
         const uint32_t pd = sbase + AT_P_OFF + pb * 2 * AT_TILE;
-        const uint32_t vd = sbase + AT_KV_OFF + (gp & 1) * 2 * AT_TILE + AT_TILE;
+        const uint32_t vd = sbase + AT_KV_OFF + (gp % AT_KV_STAGES) * 2 * AT_TILE + AT_TILE;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           mma_bf16(tmem + AT_O_COL, operand_desc(pd + (kk >> 2) * AT_TILE, 0, kk & 3),
                    operand_desc(vd, 1, kk), p.idesc_pv, (!first || kk > 0) ? 1u : 0u);
         mma_commit((gp & 1) ? b_pv2 : b_pv);
-        mma_commit(b_kve + 8 * (gp & 1));
+        mma_commit(b_kve + 8 * (gp % AT_KV_STAGES));
         return true;
       };
       bool ok = true;
@@ -182,8 +203,11 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         const int nk = p.nq - w / BH;
         if (!mbar_wait(b_q, (uint32_t)it & 1u, abort_flag, p.status)) break;
         for (int j = 0; j < nk; ++j, ++g) {
-          const int st = g & 1, sb = g & 1;
-          if (!mbar_wait(b_kvf + 8 * st, (uint32_t)(g >> 1) & 1u, abort_flag, p.status)) { ok = false; break; }
+          const int st = g % AT_KV_STAGES, sb = g & 1;
+          if (!mbar_wait(b_kvf + 8 * st, (uint32_t)(g / AT_KV_STAGES) & 1u, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
           if (g >= 2 && !mbar_wait(b_se + 8 * sb, ((uint32_t)(g >> 1) & 1u) ^ 1u, abort_flag, p.status)) {
             ok = false;
             break;
@@ -225,7 +249,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         tmem_ld32(lane_base + sb * AT_B + half * 64 + 32, s1);
         tmem_ld_wait();
         tc_fence_before();
-        mbar_arrive(b_se + 8 * sb);  // this thread is done reading S
+        warp_arrive(b_se + 8 * sb);  // this warp is done reading S
         float s[64];
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
@@ -238,15 +262,13 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
           for (int c = 0; c < 64; ++c)
             if (k0 + c > qi) s[c] = -INFINITY;
         }
-        float tmax = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < 64; ++c) tmax = fmaxf(tmax, s[c]);
+        float tmax = tree_max<64>(s);
         // exchange the half-row maxima with the partner warp (double-buffered slots;
         // the mbarrier arrive releases the slot write, the wait acquires the partner's)
         float* rx = red + (g & 1) * 256;
         rx[half * 128 + r] = tmax;
         const uint32_t xb = b_xmax + 8 * (quad * 2 + (g & 1));
-        mbar_arrive(xb);
+        warp_arrive(xb);
         if (!warp_wait(xb, (uint32_t)(g >> 1) & 1u, abort_flag, p.status)) { ok = false; break; }
         tmax = fmaxf(tmax, rx[(half ^ 1) * 128 + r]) * p.c2;
         // Lazy rescaling: the running max m (log2 units) only moves when the tile's
@@ -255,15 +277,16 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         const bool move = j == 0 || tmax > m + 8.0f;
         const float m_new = move ? fmaxf(m, tmax) : m;
         const float alpha = j == 0 ? 0.f : ex2(m - m_new);
-        float lsum = 0.f;
+        float ps[4] = {0.f, 0.f, 0.f, 0.f};
         uint32_t pk[32];
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
           const float p0 = ex2(fmaf(s[2 * c], p.c2, -m_new));
           const float p1 = ex2(fmaf(s[2 * c + 1], p.c2, -m_new));
-          lsum += p0 + p1;
+          ps[c & 3] += p0 + p1;
           pk[c] = pack_bf16x2(p0, p1);
         }
+        const float lsum = (ps[0] + ps[1]) + (ps[2] + ps[3]);
         l = l * alpha + lsum;
         m = m_new;
         const bool rescale = j >= 1 && __any_sync(0xffffffffu, move);
@@ -294,7 +317,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
                        : "memory");
         fence_async_smem();
         tc_fence_before();
-        mbar_arrive(b_pf + 8 * (g & 1));
+        warp_arrive(b_pf + 8 * (g & 1));
       }
       if (!ok) break;
       // epilogue of this item: its last PV (global tile g-1) is done
@@ -303,7 +326,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       tc_fence_after();
       float* rl = red + 512;
       rl[half * 128 + r] = l;
-      mbar_arrive(b_xsum + 8 * quad);
+      warp_arrive(b_xsum + 8 * quad);
       if (!warp_wait(b_xsum + 8 * quad, (uint32_t)it & 1u, abort_flag, p.status)) break;
       const float lt = l + rl[(half ^ 1) * 128 + r];
       const float inv = 1.0f / lt;
@@ -371,10 +394,11 @@ __device__ __forceinline__ void bw_load(const CUtensorMap* tm, int swap, uint32_
 }
 
 // ------------------------------------------------------------------ dQ
-// smem: Q | dO (per item) | K,V ring (2 stages) | dS (two 64-key halves)
-constexpr int DQ_Q = 0, DQ_DO = AT_TILE, DQ_KV = 2 * AT_TILE, DQ_DS = 6 * AT_TILE;
-constexpr int DQ_BAR = 8 * AT_TILE;
-constexpr int DQ_NBARS = 12;
+// smem: Q | dO (per item) | K,V ring (4 stages) | dS (two 64-key halves)
+constexpr int DQ_STAGES = 4;
+constexpr int DQ_Q = 0, DQ_DO = AT_TILE, DQ_KV = 2 * AT_TILE, DQ_DS = DQ_KV + 2 * DQ_STAGES * AT_TILE;
+constexpr int DQ_BAR = DQ_DS + 2 * AT_TILE;
+constexpr int DQ_NBARS = 16;
 constexpr int DQ_SMEM = 1024 + DQ_BAR + 8 * (DQ_NBARS + 2);
 
 __global__ void __launch_bounds__(BW_THREADS, 1)
@@ -385,9 +409,10 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + DQ_BAR);
-  // q_full, q_empty, kv_full[2], kv_empty[2], sdp_full, sdp_empty, ds_full, dq_done, done
-  const uint32_t b_qf = smem_u32(bars), b_qe = b_qf + 8, b_kvf = b_qe + 8, b_kve = b_kvf + 16;
-  const uint32_t b_sf = b_kve + 16, b_se = b_sf + 8, b_dsf = b_se + 8, b_dq = b_dsf + 8, b_done = b_dq + 8;
+  // q_full, q_empty, kv_full[4], kv_empty[4], sdp_full, sdp_empty, ds_full, dq_done, done
+  const uint32_t b_qf = smem_u32(bars), b_qe = b_qf + 8, b_kvf = b_qe + 8, b_kve = b_kvf + 8 * DQ_STAGES;
+  const uint32_t b_sf = b_kve + 8 * DQ_STAGES, b_se = b_sf + 8, b_dsf = b_se + 8, b_dq = b_dsf + 8;
+  const uint32_t b_done = b_dq + 8;
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bars + DQ_NBARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + DQ_NBARS + 1);
   const AttnArgs& a = p.a;
@@ -397,13 +422,13 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
   if (threadIdx.x == 0) {
     mbar_init(b_qf, 1);
     mbar_init(b_qe, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < DQ_STAGES; ++i) {
       mbar_init(b_kvf + 8 * i, 1);
       mbar_init(b_kve + 8 * i, 1);
     }
     mbar_init(b_sf, 1);
-    mbar_init(b_se, 256);
-    mbar_init(b_dsf, 256);
+    mbar_init(b_se, 8);  // one arrival per compute warp
+    mbar_init(b_dsf, 8);
     mbar_init(b_dq, 1);
     mbar_init(b_done, 1);
     *abort_flag = 0;
@@ -422,7 +447,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      int last_par[2] = {-1, -1}, q_par = -1, g = 0;
+      int last_par[DQ_STAGES] = {-1, -1, -1, -1}, q_par = -1, g = 0;
       bool ok = true;
       for (int w = blockIdx.x, it = 0; ok && w < nitems; w += gridDim.x, ++it) {
         const int qt = p.nq - 1 - w / BH, bh = w % BH, b = bh / a.H, h = bh % a.H;
@@ -432,8 +457,8 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
         bw_load(&tmdO, p.swap_o, sbase + DQ_DO, b_qf, qt * AT_B, h, b);
         q_par = it & 1;
         for (int j = 0; j <= qt; ++j, ++g) {
-          const int st = g & 1;
-          const uint32_t ph = (uint32_t)(g >> 1) & 1u;
+          const int st = g % DQ_STAGES;
+          const uint32_t ph = (uint32_t)(g / DQ_STAGES) & 1u;
           if (!mbar_wait(b_kve + 8 * st, ph ^ 1u, abort_flag, p.status)) { ok = false; break; }
           const uint32_t kd = sbase + DQ_KV + st * 2 * AT_TILE;
           mbar_expect_tx(b_kvf + 8 * st, 2 * AT_TILE);
@@ -443,7 +468,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
         }
       }
       if (q_par >= 0) mbar_wait_drain(b_qf, (uint32_t)q_par);
-      for (int i = 0; i < 2; ++i)
+      for (int i = 0; i < DQ_STAGES; ++i)
         if (last_par[i] >= 0) mbar_wait_drain(b_kvf + 8 * i, (uint32_t)last_par[i]);
     }
   } else if (warp == 1) {
@@ -451,13 +476,13 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
       auto issue_dq = [&](int gp, bool first) -> bool {
         if (!mbar_wait(b_dsf, (uint32_t)gp & 1u, abort_flag, p.status)) return false;
         tc_fence_after();
-        const uint32_t kd = sbase + DQ_KV + (gp & 1) * 2 * AT_TILE;
+        const uint32_t kd = sbase + DQ_KV + (gp % DQ_STAGES) * 2 * AT_TILE;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           mma_bf16(tmem + C_DQ, operand_desc(sbase + DQ_DS + (kk >> 2) * AT_TILE, 0, kk & 3),
                    operand_desc(kd, 1, kk), p.idesc_d, (!first || kk > 0) ? 1u : 0u);
         mma_commit(b_dq);
-        mma_commit(b_kve + 8 * (gp & 1));
+        mma_commit(b_kve + 8 * (gp % DQ_STAGES));
         return true;
       };
       bool ok = true;
@@ -466,8 +491,11 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
         const int nk = p.nq - w / BH;
         if (!mbar_wait(b_qf, (uint32_t)it & 1u, abort_flag, p.status)) break;
         for (int j = 0; j < nk; ++j, ++g) {
-          const int st = g & 1;
-          if (!mbar_wait(b_kvf + 8 * st, (uint32_t)(g >> 1) & 1u, abort_flag, p.status)) { ok = false; break; }
+          const int st = g % DQ_STAGES;
+          if (!mbar_wait(b_kvf + 8 * st, (uint32_t)(g / DQ_STAGES) & 1u, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
           if (g >= 1 && !mbar_wait(b_se, (uint32_t)(g - 1) & 1u, abort_flag, p.status)) { ok = false; break; }
           tc_fence_after();
           const uint32_t kd = sbase + DQ_KV + st * 2 * AT_TILE;
@@ -511,7 +539,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
         tmem_ld32(lane_base + C_DP + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(dv + 32));
         tmem_ld_wait();
         tc_fence_before();
-        mbar_arrive(b_se);
+        warp_arrive(b_se);
         const bool diag = j == qt;
         const int k0 = j * AT_B + half * 64;
         uint32_t pk[32];
@@ -528,7 +556,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
         tile_row_store(sbase + DQ_DS + half * AT_TILE, r, pk);
         fence_async_smem();
         tc_fence_before();
-        mbar_arrive(b_dsf);
+        warp_arrive(b_dsf);
       }
       if (!ok) break;
       if (!warp_wait(b_dq, (uint32_t)(g - 1) & 1u, abort_flag, p.status)) break;
@@ -562,11 +590,12 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
 }
 
 // ------------------------------------------------------------------ dK, dV
-// smem: K | V (per item) | Q,dO ring (2 stages) | lse2, D ring (2 x 1 KB) | P^T | dS^T
-constexpr int DK_K = 0, DK_V = AT_TILE, DK_QD = 2 * AT_TILE, DK_LD = 6 * AT_TILE;
-constexpr int DK_PT = DK_LD + 2048, DK_DST = DK_PT + 2 * AT_TILE;
+// smem: K | V (per item) | Q,dO ring (3 stages) | lse2, D ring (3 x 1 KB) | P^T | dS^T
+constexpr int DK_STAGES = 3;
+constexpr int DK_K = 0, DK_V = AT_TILE, DK_QD = 2 * AT_TILE, DK_LD = DK_QD + 2 * DK_STAGES * AT_TILE;
+constexpr int DK_PT = DK_LD + DK_STAGES * 1024, DK_DST = DK_PT + 2 * AT_TILE;
 constexpr int DK_BAR = DK_DST + 2 * AT_TILE;
-constexpr int DK_NBARS = 12;
+constexpr int DK_NBARS = 15;
 constexpr int DK_SMEM = 1024 + DK_BAR + 8 * (DK_NBARS + 2);
 
 __global__ void __launch_bounds__(BW_THREADS, 1)
@@ -578,9 +607,10 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
   const uint32_t sbase = smem_u32(smem);
   float* ldbuf = reinterpret_cast<float*>(smem + DK_LD);  // stage s: lse2[128] then D[128]
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + DK_BAR);
-  // kv_full, kv_empty, qd_full[2], qd_empty[2], sdp_full, sdp_empty, ds_full, mma_done, done
-  const uint32_t b_kvf = smem_u32(bars), b_kve = b_kvf + 8, b_qdf = b_kve + 8, b_qde = b_qdf + 16;
-  const uint32_t b_sf = b_qde + 16, b_se = b_sf + 8, b_dsf = b_se + 8, b_mm = b_dsf + 8, b_done = b_mm + 8;
+  // kv_full, kv_empty, qd_full[3], qd_empty[3], sdp_full, sdp_empty, ds_full, mma_done, done
+  const uint32_t b_kvf = smem_u32(bars), b_kve = b_kvf + 8, b_qdf = b_kve + 8, b_qde = b_qdf + 8 * DK_STAGES;
+  const uint32_t b_sf = b_qde + 8 * DK_STAGES, b_se = b_sf + 8, b_dsf = b_se + 8, b_mm = b_dsf + 8;
+  const uint32_t b_done = b_mm + 8;
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bars + DK_NBARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + DK_NBARS + 1);
   const AttnArgs& a = p.a;
@@ -591,13 +621,13 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
   if (threadIdx.x == 0) {
     mbar_init(b_kvf, 1);
     mbar_init(b_kve, 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(b_qdf + 8 * i, 33);  // the TMA expect_tx arrive + 32 lanes that stage lse2 / D
+    for (int i = 0; i < DK_STAGES; ++i) {
+      mbar_init(b_qdf + 8 * i, 2);  // the TMA expect_tx arrive + the warp that staged lse2 / D
       mbar_init(b_qde + 8 * i, 1);
     }
     mbar_init(b_sf, 1);
-    mbar_init(b_se, 256);
-    mbar_init(b_dsf, 256);
+    mbar_init(b_se, 8);  // one arrival per compute warp
+    mbar_init(b_dsf, 8);
     mbar_init(b_mm, 1);
     mbar_init(b_done, 1);
     *abort_flag = 0;
@@ -616,7 +646,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
 
   if (warp == 0) {
     // ---------------- producer warp: TMA by lane 0, lse2 / D staged by all lanes
-    int last_par[2] = {-1, -1}, kv_par = -1, g = 0;
+    int last_par[DK_STAGES] = {-1, -1, -1}, kv_par = -1, g = 0;
     bool ok = true;
     for (int w = blockIdx.x, it = 0; ok && w < nitems; w += gridDim.x, ++it) {
       const int kt = w / BH, bh = w % BH, b = bh / a.H, h = bh % a.H;
@@ -628,8 +658,8 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
       }
       kv_par = it & 1;
       for (int i = kt; i < p.nq; ++i, ++g) {
-        const int st = g & 1;
-        const uint32_t ph = (uint32_t)(g >> 1) & 1u;
+        const int st = g % DK_STAGES;
+        const uint32_t ph = (uint32_t)(g / DK_STAGES) & 1u;
         if (!warp_wait(b_qde + 8 * st, ph ^ 1u, abort_flag, p.status)) { ok = false; break; }
         if (lane == 0) {
           const uint32_t qd = sbase + DK_QD + st * 2 * AT_TILE;
@@ -645,13 +675,13 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
           lb[c] = v ? a.lse[(long long)bh * a.T + q] * 1.4426950408889634f : INFINITY;
           lb[128 + c] = v ? a.Dbuf[(long long)bh * a.T + q] : 0.f;
         }
-        mbar_arrive(b_qdf + 8 * st);
+        warp_arrive(b_qdf + 8 * st);
         last_par[st] = (int)ph;
       }
     }
     if (lane == 0) {
       if (kv_par >= 0) mbar_wait_drain(b_kvf, (uint32_t)kv_par);
-      for (int i = 0; i < 2; ++i)
+      for (int i = 0; i < DK_STAGES; ++i)
         if (last_par[i] >= 0) mbar_wait_drain(b_qdf + 8 * i, (uint32_t)last_par[i]);
     }
   } else if (warp == 1) {
@@ -659,7 +689,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
       auto issue_kv = [&](int gp, bool first) -> bool {
         if (!mbar_wait(b_dsf, (uint32_t)gp & 1u, abort_flag, p.status)) return false;
         tc_fence_after();
-        const uint32_t qd = sbase + DK_QD + (gp & 1) * 2 * AT_TILE;
+        const uint32_t qd = sbase + DK_QD + (gp % DK_STAGES) * 2 * AT_TILE;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           mma_bf16(tmem + C_DV, operand_desc(sbase + DK_PT + (kk >> 2) * AT_TILE, 0, kk & 3),
@@ -669,7 +699,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
           mma_bf16(tmem + C_DK, operand_desc(sbase + DK_DST + (kk >> 2) * AT_TILE, 0, kk & 3),
                    operand_desc(qd, 1, kk), p.idesc_d, (!first || kk > 0) ? 1u : 0u);
         mma_commit(b_mm);
-        mma_commit(b_qde + 8 * (gp & 1));
+        mma_commit(b_qde + 8 * (gp % DK_STAGES));
         return true;
       };
       bool ok = true;
@@ -678,8 +708,11 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
         const int n = p.nq - w / BH;  // query tiles kt .. nq-1
         if (!mbar_wait(b_kvf, (uint32_t)it & 1u, abort_flag, p.status)) break;
         for (int j = 0; j < n; ++j, ++g) {
-          const int st = g & 1;
-          if (!mbar_wait(b_qdf + 8 * st, (uint32_t)(g >> 1) & 1u, abort_flag, p.status)) { ok = false; break; }
+          const int st = g % DK_STAGES;
+          if (!mbar_wait(b_qdf + 8 * st, (uint32_t)(g / DK_STAGES) & 1u, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
           if (g >= 1 && !mbar_wait(b_se, (uint32_t)(g - 1) & 1u, abort_flag, p.status)) { ok = false; break; }
           tc_fence_after();
           const uint32_t qd = sbase + DK_QD + st * 2 * AT_TILE;
@@ -710,9 +743,12 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
       const int kt = w / BH, bh = w % BH, b = bh / a.H, h = bh % a.H;
       const int kr = kt * AT_B + r;
       for (int i = kt; i < p.nq; ++i, ++g) {
-        const int st = g & 1;
+        const int st = g % DK_STAGES;
         // lse2 / D of this query tile (staged with the Q / dO tiles)
-        if (!warp_wait(b_qdf + 8 * st, (uint32_t)(g >> 1) & 1u, abort_flag, p.status)) { ok = false; break; }
+        if (!warp_wait(b_qdf + 8 * st, (uint32_t)(g / DK_STAGES) & 1u, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
         if (!warp_wait(b_sf, (uint32_t)g & 1u, abort_flag, p.status)) { ok = false; break; }
         tc_fence_after();
         uint32_t sv[64], dv[64];
@@ -722,7 +758,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
         tmem_ld32(lane_base + C_DP + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(dv + 32));
         tmem_ld_wait();
         tc_fence_before();
-        mbar_arrive(b_se);
+        warp_arrive(b_se);
         const float* lb = ldbuf + st * 256 + half * 64;
         const bool diag = i == kt;
         const int q0 = i * AT_B + half * 64;
@@ -743,7 +779,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
         tile_row_store(sbase + DK_DST + half * AT_TILE, r, pd);
         fence_async_smem();
         tc_fence_before();
-        mbar_arrive(b_dsf);
+        warp_arrive(b_dsf);
       }
       if (!ok) break;
       if (!warp_wait(b_mm, (uint32_t)(g - 1) & 1u, abort_flag, p.status)) break;
