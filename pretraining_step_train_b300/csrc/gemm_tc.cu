@@ -126,17 +126,15 @@ __device__ __forceinline__ float tanh_hw(float x) {
   asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-// tanh-form GELU and its derivative with the hardware tanh (bf16 epilogues only).
-__device__ __forceinline__ float gelu_hw(float x) {
-  const float u = x * (GELU_K + GELU_K * GELU_C * x * x);
-  const float hx = 0.5f * x;
-  return fmaf(hx, tanh_hw(u), hx);
-}
-__device__ __forceinline__ float gelu_grad_hw(float x) {
+// tanh-form GELU with the hardware tanh (bf16 epilogues only).
+// gelu(x) and gelu'(x) sharing one hardware tanh.
+__device__ __forceinline__ void gelu_and_grad_hw(float x, float& y, float& dy) {
   const float x2 = x * x;
   const float th = tanh_hw(x * (GELU_K + GELU_K * GELU_C * x2));
+  const float hx = 0.5f * x;
+  y = fmaf(hx, th, hx);
   const float du = GELU_K + 3.0f * GELU_K * GELU_C * x2;
-  return 0.5f * (1.0f + th) + 0.5f * x * (1.0f - th * th) * du;
+  dy = 0.5f * (1.0f + th) + hx * (1.0f - th * th) * du;
 }
 
 __global__ void __launch_bounds__(NUM_THREADS, 1)
@@ -368,7 +366,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int j = 0; j < 32; ++j) v[j] += xv[j];
         } else if (epi == EPI_GELU_BWD) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] *= gelu_grad_hw(xv[j]);
+          for (int j = 0; j < 32; ++j) v[j] *= xv[j];
         } else if (epi == EPI_CE) {
           // logits rounded to bf16 are stored and used for the statistics
 #pragma unroll
@@ -396,12 +394,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
         uint32_t w[16];
-        pack32_bf16(v, w);
         if (epi == EPI_BIAS_GELU) {
-          // h and gelu(h): both staged boxes
+          // gelu'(h) (D, for the backward) and gelu(h) (D2) from one tanh: both staged boxes
           float a[32];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) a[j] = gelu_hw(v[j]);
+          for (int j = 0; j < 32; ++j) gelu_and_grad_hw(v[j], a[j], v[j]);
+          pack32_bf16(v, w);
           uint32_t wa[16];
           pack32_bf16(a, wa);
           if (lane == 0) bulk_wait_read<0>();
@@ -418,6 +416,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           prev_stored = true;
           continue;
         }
+        pack32_bf16(v, w);
         if (!p.load_x) {
           // box b was last read by the store two chunks back (or one, if the last chunk stored nothing)
           if (lane == 0) {

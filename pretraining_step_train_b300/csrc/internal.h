@@ -14,8 +14,8 @@ enum EpiKind {
   EPI_STORE = 0,       // D = acc                          (storage type)
   EPI_BIAS = 1,        // D = acc + bias[n]
   EPI_BIAS_RESID = 2,  // D = acc + bias[n] + resid[m, n]
-  EPI_BIAS_GELU = 3,   // D = h = acc + bias[n];  D2 = gelu(h)
-  EPI_GELU_BWD = 4,    // D = acc * gelu'(aux[m, n])
+  EPI_BIAS_GELU = 3,   // h = acc + bias[n];  D = gelu'(h), D2 = gelu(h)
+  EPI_GELU_BWD = 4,    // D = acc * aux[m, n]  (aux = the gelu'(h) the forward stored)
   EPI_CE = 5,          // D = z = acc; per (row, N tile) max / sum exp over n < V; target logit
   EPI_F32 = 6,         // D (float*) = acc
 };
