@@ -69,26 +69,50 @@ void check_ids(int32_t* ids, int n, int V, unsigned* status, cudaStream_t s) {
 }
 
 // ------------------------------------------------------------------ LayerNorm forward
-// One warp per row; the row stays in registers (two-pass mean / biased variance).
+// One warp per row; the row stays in registers in its storage format (16-byte
+// vectors: packed bf16 or fp32) and is unpacked on each of the three passes
+// (mean, biased variance, output), so a warp holds few registers and many warps
+// keep row loads in flight.
+template <typename T>
+__device__ __forceinline__ void unpack16(const uint4& u, float* out) {
+  if constexpr (sizeof(T) == 4) {
+    out[0] = __uint_as_float(u.x); out[1] = __uint_as_float(u.y);
+    out[2] = __uint_as_float(u.z); out[3] = __uint_as_float(u.w);
+  } else {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      out[2 * i] = __uint_as_float(w[i] << 16);
+      out[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+  }
+}
+
 template <typename T, int MAXV>
-__global__ void k_layernorm_fwd(T* __restrict__ y, float* __restrict__ mean,
-                                float* __restrict__ rstd, const T* __restrict__ x,
-                                const T* __restrict__ w, const T* __restrict__ b, int M, int C) {
+__global__ void __launch_bounds__(256) k_layernorm_fwd(T* __restrict__ y, float* __restrict__ mean,
+                                                       float* __restrict__ rstd, const T* __restrict__ x,
+                                                       const T* __restrict__ w, const T* __restrict__ b,
+                                                       int M, int C) {
   constexpr int N = V16<T>::N;
   const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (row >= M) return;
   const int nv = C / N;
   const T* xr = x + (long long)row * C;
-  float v[MAXV][N];
+  uint4 raw[MAXV];
+#pragma unroll
+  for (int j = 0; j < MAXV; ++j) {
+    const int vi = lane + j * 32;
+    if (vi < nv) raw[j] = *reinterpret_cast<const uint4*>(xr + vi * N);
+  }
   float s = 0.f;
 #pragma unroll
   for (int j = 0; j < MAXV; ++j) {
-    int vi = lane + j * 32;
-    if (vi < nv) {
-      load16(xr + vi * N, v[j]);
+    if (lane + j * 32 < nv) {
+      float v[N];
+      unpack16<T>(raw[j], v);
 #pragma unroll
-      for (int e = 0; e < N; ++e) s += v[j][e];
+      for (int e = 0; e < N; ++e) s += v[e];
     }
   }
   s = warp_sum(s);
@@ -96,11 +120,12 @@ __global__ void k_layernorm_fwd(T* __restrict__ y, float* __restrict__ mean,
   float ss = 0.f;
 #pragma unroll
   for (int j = 0; j < MAXV; ++j) {
-    int vi = lane + j * 32;
-    if (vi < nv) {
+    if (lane + j * 32 < nv) {
+      float v[N];
+      unpack16<T>(raw[j], v);
 #pragma unroll
       for (int e = 0; e < N; ++e) {
-        float d = v[j][e] - mu;
+        const float d = v[e] - mu;
         ss += d * d;
       }
     }
@@ -110,13 +135,14 @@ __global__ void k_layernorm_fwd(T* __restrict__ y, float* __restrict__ mean,
   T* yr = y + (long long)row * C;
 #pragma unroll
   for (int j = 0; j < MAXV; ++j) {
-    int vi = lane + j * 32;
+    const int vi = lane + j * 32;
     if (vi < nv) {
-      float wv[N], bv[N], o[N];
+      float v[N], wv[N], bv[N], o[N];
+      unpack16<T>(raw[j], v);
       load16(w + vi * N, wv);
       load16(b + vi * N, bv);
 #pragma unroll
-      for (int e = 0; e < N; ++e) o[e] = (v[j][e] - mu) * rs * wv[e] + bv[e];
+      for (int e = 0; e < N; ++e) o[e] = (v[e] - mu) * rs * wv[e] + bv[e];
       store16(yr + vi * N, o);
     }
   }
@@ -142,24 +168,34 @@ void layernorm_fwd(T* y, float* mean, float* rstd, const T* x, const T* w, const
 
 // ------------------------------------------------------------------ fixed-order partial sums
 // out_j[c] = sum over parts of partials[p][j * seg + c] for j = 0..2: each
-// block owns 32 columns, warp w sums parts w, w+8, ..., and the 8 warp sums
-// are then added in warp order.  Deterministic.
+// block owns 32 columns with 32 warps; warp w sums parts w, w+32, ... in four
+// interleaved accumulators (p = w + 32(4i + k) goes to accumulator k), combined
+// as (a0 + a1) + (a2 + a3); the 32 warp sums are then added in warp order.
+// Deterministic.
 template <typename T>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(1024)
     k_reduce_parts(T* __restrict__ o0, T* __restrict__ o1, T* __restrict__ o2,
                    const float* __restrict__ partials, int nparts, int width, int seg) {
-  __shared__ float sh[8][33];
+  __shared__ float sh[32][33];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x * 32 + lane;
-  float acc = 0.f;
-  if (c < width)
-    for (int p = warp; p < nparts; p += 8) acc += partials[(long long)p * width + c];
-  sh[warp][lane] = acc;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  if (c < width) {
+    int p = warp;
+    for (; p + 96 < nparts; p += 128) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) acc[k] += partials[(long long)(p + 32 * k) * width + c];
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      if (p + 32 * k < nparts) acc[k] += partials[(long long)(p + 32 * k) * width + c];
+  }
+  sh[warp][lane] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
   __syncthreads();
   if (warp == 0 && c < width) {
     float t = 0.f;
 #pragma unroll
-    for (int w = 0; w < 8; ++w) t += sh[w][lane];
+    for (int w = 0; w < 32; ++w) t += sh[w][lane];
     const int j = c / seg, cc = c % seg;
     T* o = j == 0 ? o0 : (j == 1 ? o1 : o2);
     if (o) o[cc] = from_f<T>(t);
@@ -169,7 +205,7 @@ __global__ void __launch_bounds__(256)
 template <typename T>
 static void reduce_parts(T* o0, T* o1, T* o2, const float* partials, int nparts, int width, int seg,
                          cudaStream_t s) {
-  k_reduce_parts<T><<<(width + 31) / 32, 256, 0, s>>>(o0, o1, o2, partials, nparts, width, seg);
+  k_reduce_parts<T><<<(width + 31) / 32, 1024, 0, s>>>(o0, o1, o2, partials, nparts, width, seg);
 }
 
 // ------------------------------------------------------------------ LayerNorm backward
@@ -338,12 +374,15 @@ __global__ void __launch_bounds__(256)
   const int r0 = blockIdx.y * rows_per_block, r1 = min(M, r0 + rows_per_block);
   if (c < N) {
     int r = r0 + warp;
-    for (; r + 8 < r1; r += 16) {
-      float v[NV], u[NV];
-      load16(x + (long long)r * ld + c, v);
-      load16(x + (long long)(r + 8) * ld + c, u);
+    for (; r + 24 < r1; r += 32) {  // four rows in flight per warp
+      uint4 q[4];
 #pragma unroll
-      for (int e = 0; e < NV; ++e) acc[e] += v[e] + u[e];
+      for (int k = 0; k < 4; ++k) q[k] = *reinterpret_cast<const uint4*>(x + (long long)(r + 8 * k) * ld + c);
+      float v[4][NV];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) unpack16<T>(q[k], v[k]);
+#pragma unroll
+      for (int e = 0; e < NV; ++e) acc[e] += (v[0][e] + v[1][e]) + (v[2][e] + v[3][e]);
     }
     for (; r < r1; r += 8) {
       float v[NV];
