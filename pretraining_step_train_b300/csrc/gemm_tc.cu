@@ -6,19 +6,20 @@
 //   backward  dX = dY W      A = dY (K-major), B = W  (MN-major)
 //             dW = dY^T X    A = dY (MN-major), B = X (MN-major), split over the rows
 //
-// Structure (one persistent CTA per SM, 10 warps):
+// Structure (one persistent CTA per SM, 18 warps):
 //   warp 0      TMA producer: 128B-swizzled A (128 x 64) and B (256 x 64) tiles
 //               into a 4-stage shared-memory ring, completion on mbarriers;
 //   warp 1      owns 512 TMEM columns (two 128 x 256 fp32 accumulators) and one
 //               thread issues tcgen05.mma (M=128, N=256, K=16) per 16-wide k step,
 //               releasing ring stages and finished accumulators with tcgen05.commit;
-//   warps 2-9   epilogue, two warps per TMEM lane quadrant (one per 128-column
-//               half): tcgen05.ld 32 rows x 32 columns at a time, fused bias /
+//   warps 2-17  epilogue, four warps per TMEM lane quadrant (one per 64-column
+//               quarter): tcgen05.ld 32 rows x 16 columns at a time, fused bias /
 //               residual / GELU / GELU' / cross-entropy statistics, then the
-//               32 x 32 result is staged in 64B-swizzled shared memory and
+//               32 x 16 result is staged in 32B-swizzled shared memory and
 //               written by a TMA bulk tensor store (coalesced, asynchronous).
-//               Residual and pre-activation operands arrive the same way, by a
-//               TMA load of the matching 32 x 32 box, one chunk ahead.
+//               Residual and GELU' operands arrive the same way, by a TMA load
+//               of the matching 32 x 16 box, one chunk ahead.  Sixteen warps
+//               (four per SM sub-partition) hide the epilogue's latencies.
 // The accumulator double buffer lets the epilogue of tile i overlap the
 // mainloop of tile i+1.  Every wait is bounded (about 2 s of %globaltimer);
 // on expiry the CTA latches ST_TIMEOUT in the status word, the other roles
@@ -38,9 +39,12 @@ constexpr int B_TILE = BN * BK * 2;  // 32 KB
 constexpr int STAGE_BYTES = A_TILE + B_TILE;
 constexpr int RING_BYTES = STAGES * STAGE_BYTES;
 constexpr int TMEM_COLS = 2 * BN;
-constexpr int EPI_WARPS = 8;
+constexpr int EPI_WARPS = 16;
 constexpr int NUM_THREADS = 64 + 32 * EPI_WARPS;
-constexpr int BOX_BYTES = 2048;                 // one staged box: 32 rows x 64 bytes
+constexpr int CW = 16;                          // chunk width: columns per TMEM load
+constexpr int WCOLS = BN / (EPI_WARPS / 4);     // columns per epilogue warp and tile (64)
+constexpr int NCHUNK = WCOLS / CW;              // chunks per epilogue warp and tile (4)
+constexpr int BOX_BYTES = 1024;                 // one staged box: 32 rows x 32 bytes
 constexpr int STG_BYTES = 2 * BOX_BYTES;        // per epilogue warp
 constexpr int BAR_BYTES = 512;
 constexpr int SMEM_BYTES = 1024 + RING_BYTES + EPI_WARPS * STG_BYTES + BAR_BYTES;
@@ -54,6 +58,7 @@ struct TcParams {
   int out_f32;  // D (or the split-K workspace) holds fp32
   int load_x;   // the epilogue reads a [M, N] bf16 operand (residual or GELU pre-activation)
   int m_fast;   // tile raster: consecutive tiles walk M (sharing a B tile) instead of N
+  int a3d, b3d; // MN-major operand loaded by one 3-D box (all its 64-wide blocks) per stage
 };
 
 int g_poison = 0;
@@ -80,23 +85,23 @@ __device__ __forceinline__ void tma_load_x(uint32_t dst, const CUtensorMap* tm, 
                                            int y) {
   tma_load_2d(dst, tm, bar, x, y);
 }
-// One staged box holds 32 rows of 64 bytes in the TMA 64-byte swizzle: the
-// 16-byte piece p of row r sits at r*64 + ((p ^ ((r >> 1) & 3)) << 4).  A
+// One staged box holds 32 rows of 32 bytes in the TMA 32-byte swizzle: the
+// 16-byte piece p of row r sits at r*32 + ((p ^ ((r >> 2) & 1)) << 4).  A
 // quarter-warp writing the same piece of 8 consecutive rows hits 8 distinct
 // 16-byte bank groups.
 __device__ __forceinline__ uint32_t box_addr(uint32_t box, int r, int p) {
-  return box + (uint32_t)(r * 64 + ((p ^ ((r >> 1) & 3)) << 4));
+  return box + (uint32_t)(r * 32 + ((p ^ ((r >> 2) & 1)) << 4));
 }
 __device__ __forceinline__ void box_store_row(uint32_t box, int r, const uint32_t* w) {
 #pragma unroll
-  for (int p = 0; p < 4; ++p)
+  for (int p = 0; p < 2; ++p)
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(box_addr(box, r, p)), "r"(w[4 * p]),
                  "r"(w[4 * p + 1]), "r"(w[4 * p + 2]), "r"(w[4 * p + 3])
                  : "memory");
 }
 __device__ __forceinline__ void box_load_row_bf16(uint32_t box, int r, float* v) {
 #pragma unroll
-  for (int p = 0; p < 4; ++p) {
+  for (int p = 0; p < 2; ++p) {
     uint32_t w0, w1, w2, w3;
     asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                  : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
@@ -110,13 +115,22 @@ __device__ __forceinline__ void box_load_row_bf16(uint32_t box, int r, float* v)
     }
   }
 }
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
 __device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
   __nv_bfloat162 t = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&t);
 }
-__device__ __forceinline__ void pack32_bf16(const float* v, uint32_t* w) {
+__device__ __forceinline__ void pack16_bf16(const float* v, uint32_t* w) {
 #pragma unroll
-  for (int j = 0; j < 16; ++j) w[j] = pack2_bf16(v[2 * j], v[2 * j + 1]);
+  for (int j = 0; j < 8; ++j) w[j] = pack2_bf16(v[2 * j], v[2 * j + 1]);
 }
 
 // Hardware tanh (MUFU, PTX tanh.approx.f32): relative error about 2^-11, far
@@ -207,12 +221,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_expect_tx(fb, STAGE_BYTES);
             if (!g.a_mn) {
               tma_load_2d(sa, &tmA, fb, kb * BK, m_t * BM);
+            } else if (p.a3d) {
+              tma_load_3d(sa, &tmA, fb, 0, kb * BK, m_t * (BM / 64));
             } else {
               tma_load_2d(sa, &tmA, fb, m_t * BM, kb * BK);
               tma_load_2d(sa + 8192, &tmA, fb, m_t * BM + 64, kb * BK);
             }
             if (!g.b_mn) {
               tma_load_2d(sb, &tmB, fb, kb * BK, n_t * BN);
+            } else if (p.b3d) {
+              tma_load_3d(sb, &tmB, fb, 0, kb * BK, n_t * (BN / 64));
             } else {
 #pragma unroll
               for (int j = 0; j < 4; ++j) tma_load_2d(sb + j * 8192, &tmB, fb, n_t * BN + j * 64, kb * BK);
@@ -264,8 +282,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_wait_drain(b_done, 0);
     }
   } else {
-    // ---------------- epilogue warps 2..9: TMEM lane quadrant warp % 4, column half (warp-2)/4
-    const int ew = warp - 2, quad = warp & 3, hh = ew >> 2;
+    // ---------------- epilogue warps 2..17: TMEM lane quadrant warp % 4, column quarter (warp-2)/4
+    const int ew = warp - 2, quad = warp & 3, qq = ew >> 2;
     const uint32_t stg = s_stg + ew * STG_BYTES;   // two staged boxes
     const uint32_t xbar = b_xload + 16 * ew;       // their load barriers
     uint32_t xpar = 0;                             // bit b: parity of the next completion of xbar b
@@ -274,12 +292,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     bool prev_stored = false;                      // the previous chunk issued a store
     const int epi = g.epi;
     const bool split = p.splits > 1;
-    // chunk (tile, c): rows m_t*BM + quad*32 .. +32, columns n_t*BN + hh*128 + c*32 .. +32
+    // chunk (tile, c): rows m_t*BM + quad*32 .. +32, columns n_t*BN + qq*WCOLS + c*CW .. +CW
     auto chunk_valid = [&](int tile, int c, int& x, int& y) {
       if (tile >= ntiles) return false;
       int m_t, n_t, sp;
       tile_coords(p, tile, m_t, n_t, sp);
-      x = n_t * BN + hh * 128 + c * 32;
+      x = n_t * BN + qq * WCOLS + c * CW;
       y = m_t * BM + quad * 32;
       return x < g.N && y < g.M;
     };
@@ -303,56 +321,64 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!mbar_wait(b_tfull + 8 * abuf, aphase, abort_flag, p.status)) break;
       tc_fence_after();
       const int m = m_t * BM + quad * 32 + lane;
+      const int tgt = (epi == EPI_CE && m < g.M) ? g.targets[m] : -1;
       float ce_m = -INFINITY, ce_s = 0.f, ce_t = 0.f;
       bool stop = false;
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < NCHUNK; ++c) {
         const int b = bx;
-        uint32_t r[32];
-        tmem_ld32(tmem_base + ((uint32_t)(quad * 32) << 16) + abuf * BN + hh * 128 + c * 32, r);
+        uint32_t r[16];
+        tmem_ld16(tmem_base + ((uint32_t)(quad * 32) << 16) + abuf * BN + qq * WCOLS + c * CW, r);
         tmem_ld_wait();
-        if (c == 3) {  // every TMEM read of this accumulator is done: hand it back to the MMA
+        if (c == NCHUNK - 1) {  // every TMEM read of this accumulator is done: hand it back to the MMA
           tc_fence_before();
           mbar_arrive(b_tempty + 8 * abuf);
         }
         // prefetch the next chunk's operand into the other box
-        if (c < 3) x_issue(tile, c + 1, b ^ 1);
+        if (c < NCHUNK - 1) x_issue(tile, c + 1, b ^ 1);
         else x_issue(tile + gridDim.x, 0, b ^ 1);
         bx ^= 1;
         int x0, y0;
         if (!chunk_valid(tile, c, x0, y0)) { prev_stored = false; continue; }
-        float v[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-        float xv[32];
-        if (p.load_x) {
-          if (!mbar_wait(xbar + 8 * b, (xpar >> b) & 1u, abort_flag, p.status)) { stop = true; break; }
-          xpar ^= 1u << b;
-          xpend &= ~(1u << b);
-          box_load_row_bf16(stg + b * BOX_BYTES, lane, xv);
-        }
-        const uint32_t box0 = stg + b * BOX_BYTES;
         if (split || epi == EPI_F32) {
-          // fp32 result: two 16-column boxes (both staged boxes)
+          // fp32 result: two 8-column boxes (both staged boxes)
           if (lane == 0) bulk_wait_read<0>();
           __syncwarp();
           box_store_row(stg, lane, r);
-          box_store_row(stg + BOX_BYTES, lane, r + 16);
+          box_store_row(stg + BOX_BYTES, lane, r + 8);
           fence_async_smem();
           __syncwarp();
           if (lane == 0) {
             const int z = split ? sp : 0;
             tma_store_3d(&tmD, stg, x0, y0, z);
-            if (x0 + 16 < g.N) tma_store_3d(&tmD, stg + BOX_BYTES, x0 + 16, y0, z);
+            if (x0 + 8 < g.N) tma_store_3d(&tmD, stg + BOX_BYTES, x0 + 8, y0, z);
             bulk_commit();
           }
           prev_stored = true;
           continue;
         }
+        float v[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+        const uint32_t box0 = stg + b * BOX_BYTES;
+        if (p.load_x) {
+          if (!mbar_wait(xbar + 8 * b, (xpar >> b) & 1u, abort_flag, p.status)) { stop = true; break; }
+          xpar ^= 1u << b;
+          xpend &= ~(1u << b);
+          float xv[16];
+          box_load_row_bf16(box0, lane, xv);
+          if (epi == EPI_BIAS_RESID) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] += xv[j];
+          } else {  // EPI_GELU_BWD: dh = da * gelu'(h)
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] *= xv[j];
+          }
+        }
         if (epi == EPI_BIAS || epi == EPI_BIAS_RESID || epi == EPI_BIAS_GELU) {
           const bf16* bias = static_cast<const bf16*>(g.bias);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
+          for (int q = 0; q < 2; ++q) {
             if (x0 + q * 8 < g.N) {
               float bb[8];
               load16<bf16>(bias + x0 + q * 8, bb);
@@ -361,47 +387,38 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
           }
         }
-        if (epi == EPI_BIAS_RESID) {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] += xv[j];
-        } else if (epi == EPI_GELU_BWD) {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] *= xv[j];
-        } else if (epi == EPI_CE) {
+        if (epi == EPI_CE) {
           // logits rounded to bf16 are stored and used for the statistics
 #pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = __bfloat162float(__float2bfloat16_rn(v[j]));
+          for (int j = 0; j < 16; ++j) v[j] = __bfloat162float(__float2bfloat16_rn(v[j]));
           float cm = -INFINITY;
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
+          for (int j = 0; j < 16; ++j)
             if (x0 + j < g.V) cm = fmaxf(cm, v[j]);
           if (cm > -INFINITY) {
             const float mn = fmaxf(ce_m, cm);
-            float s = (ce_m > -INFINITY) ? ce_s * __expf(ce_m - mn) : 0.f;
+            float sacc = (ce_m > -INFINITY) ? ce_s * __expf(ce_m - mn) : 0.f;
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (x0 + j < g.V) s += __expf(v[j] - mn);
+            for (int j = 0; j < 16; ++j)
+              if (x0 + j < g.V) sacc += __expf(v[j] - mn);
             ce_m = mn;
-            ce_s = s;
+            ce_s = sacc;
           }
-          if (m < g.M) {
-            const int t = g.targets[m];
-            if (t >= x0 && t < x0 + 32) {
+          if (tgt >= x0 && tgt < x0 + CW) {
 #pragma unroll
-              for (int j = 0; j < 32; ++j)
-                if (x0 + j == t) ce_t = v[j];
-            }
+            for (int j = 0; j < 16; ++j)
+              if (x0 + j == tgt) ce_t = v[j];
           }
         }
-        uint32_t w[16];
+        uint32_t w[8];
         if (epi == EPI_BIAS_GELU) {
           // gelu'(h) (D, for the backward) and gelu(h) (D2) from one tanh: both staged boxes
-          float a[32];
+          float a[16];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) gelu_and_grad_hw(v[j], a[j], v[j]);
-          pack32_bf16(v, w);
-          uint32_t wa[16];
-          pack32_bf16(a, wa);
+          for (int j = 0; j < 16; ++j) gelu_and_grad_hw(v[j], a[j], v[j]);
+          pack16_bf16(v, w);
+          uint32_t wa[8];
+          pack16_bf16(a, wa);
           if (lane == 0) bulk_wait_read<0>();
           __syncwarp();
           box_store_row(stg, lane, w);
@@ -416,7 +433,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           prev_stored = true;
           continue;
         }
-        pack32_bf16(v, w);
+        pack16_bf16(v, w);
         if (!p.load_x) {
           // box b was last read by the store two chunks back (or one, if the last chunk stored nothing)
           if (lane == 0) {
@@ -435,14 +452,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         prev_stored = true;
       }
       if (stop) break;
-      // one statistics partial per row and 128-column half tile that starts inside N
-      if (epi == EPI_CE && !split && m < g.M && n_t * BN + hh * 128 < g.N) {
-        const int part = n_t * 2 + hh;
+      // one statistics partial per row and WCOLS-column quarter tile that starts inside N
+      if (epi == EPI_CE && !split && m < g.M && n_t * BN + qq * WCOLS < g.N) {
+        const int part = n_t * (BN / WCOLS) + qq;
         g.ce_max[(long long)m * g.ce_ld + part] = ce_m;
         g.ce_sum[(long long)m * g.ce_ld + part] = ce_s;
-        const int t = g.targets[m];
-        const int c0 = n_t * BN + hh * 128;
-        if (t >= c0 && t < c0 + 128) g.ce_tgt[m] = ce_t;
+        const int c0 = n_t * BN + qq * WCOLS;
+        if (tgt >= c0 && tgt < c0 + WCOLS) g.ce_tgt[m] = ce_t;
       }
       if (++abuf == 2) { abuf = 0; aphase ^= 1; }
     }
@@ -496,8 +512,25 @@ bool make_tmap(CUtensorMap* tm, const void* base, long long inner, long long out
   return r == CUDA_SUCCESS;
 }
 
+// MN-major operand map over a row-major [K, MN] matrix (leading dimension ld,
+// MN % 64 == 0) seen as 3-D (64 MN elements, K rows, MN / 64 blocks): one box of
+// 64 x 64 x nblk lands as nblk consecutive 8 KB blocks of 64 K rows x 128 bytes,
+// the layout the MMA descriptors expect (128B swizzle).
+bool make_tmap_mn3d(CUtensorMap* tm, const void* base, long long mn, long long k, long long ld, int nblk) {
+  PFN_encodeTiled_t enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {64, (cuuint64_t)k, (cuuint64_t)(mn / 64)};
+  cuuint64_t strides[2] = {(cuuint64_t)ld * 2, 128};
+  cuuint32_t box[3] = {64, 64, (cuuint32_t)nblk};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+                   es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // Epilogue box map: [depth][rows][cols] with leading dimension ld (elements) and
-// depth stride rows*ld, boxes of 64 bytes x 32 rows x 1, 64-byte swizzle.
+// depth stride rows*ld, boxes of 32 bytes x 32 rows x 1, 32-byte swizzle.
 bool make_box_map(CUtensorMap* tm, const void* base, int f32, long long cols, long long rows,
                   long long depth, long long ld) {
   PFN_encodeTiled_t enc = get_encode();
@@ -505,25 +538,25 @@ bool make_box_map(CUtensorMap* tm, const void* base, int f32, long long cols, lo
   const int es = f32 ? 4 : 2;
   cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)depth};
   cuuint64_t strides[2] = {(cuuint64_t)ld * es, (cuuint64_t)ld * es * rows};
-  cuuint32_t box[3] = {(cuuint32_t)(64 / es), 32, 1};
+  cuuint32_t box[3] = {(cuuint32_t)(32 / es), 32, 1};
   cuuint32_t el[3] = {1, 1, 1};
   CUresult r = enc(tm, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
                    const_cast<void*>(base), dims, strides, box, el, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
-// 2-D bf16 epilogue operand map (residual / pre-activation): 32 x 32 boxes, 64-byte swizzle.
+// 2-D bf16 epilogue operand map (residual / gelu'): 32 rows x 16 columns, 32-byte swizzle.
 bool make_x_map(CUtensorMap* tm, const void* base, long long cols, long long rows, long long ld) {
   PFN_encodeTiled_t enc = get_encode();
   if (!enc) return false;
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
-  cuuint32_t box[2] = {32, 32};
+  cuuint32_t box[2] = {16, 32};
   cuuint32_t el[2] = {1, 1};
   CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-                   el, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                   el, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -547,7 +580,7 @@ int gemm_tc_poison(int on) {
   return old;
 }
 
-int gemm_tc_stat_cols() { return BN / 2; }
+int gemm_tc_stat_cols() { return WCOLS; }
 
 size_t gemm_tc_ws_bytes(int M, int N, int splits) {
   return splits > 1 ? (size_t)splits * M * N * sizeof(float) : 0;
@@ -617,10 +650,14 @@ int gemm_tc(const GemmArgs& g, int splits, void* ws, size_t ws_bytes, unsigned* 
   p.load_x = (g.epi == EPI_BIAS_RESID || g.epi == EPI_GELU_BWD) ? 1 : 0;
   p.m_fast = ((double)g.N * g.K > (double)g.M * g.K) ? 1 : 0;
   CUtensorMap tmA, tmB, tmD, tmD2, tmX;
-  bool ok = g.a_mn ? make_tmap(&tmA, g.A, g.M, g.K, g.lda, 64, 64)
-                   : make_tmap(&tmA, g.A, g.K, g.M, g.lda, 64, BM);
-  ok = ok && (g.b_mn ? make_tmap(&tmB, g.B, g.N, g.K, g.ldb, 64, 64)
-                     : make_tmap(&tmB, g.B, g.K, g.N, g.ldb, 64, BN));
+  p.a3d = (g.a_mn && g.M % 64 == 0) ? 1 : 0;
+  p.b3d = (g.b_mn && g.N % 64 == 0) ? 1 : 0;
+  bool ok = p.a3d ? make_tmap_mn3d(&tmA, g.A, g.M, g.K, g.lda, BM / 64)
+                  : g.a_mn ? make_tmap(&tmA, g.A, g.M, g.K, g.lda, 64, 64)
+                           : make_tmap(&tmA, g.A, g.K, g.M, g.lda, 64, BM);
+  ok = ok && (p.b3d ? make_tmap_mn3d(&tmB, g.B, g.N, g.K, g.ldb, BN / 64)
+                    : g.b_mn ? make_tmap(&tmB, g.B, g.N, g.K, g.ldb, 64, 64)
+                             : make_tmap(&tmB, g.B, g.K, g.N, g.ldb, 64, BN));
   if (p.splits > 1)
     ok = ok && make_box_map(&tmD, ws, 1, g.N, g.M, p.splits, g.N);
   else

@@ -132,6 +132,14 @@ __device__ __forceinline__ uint64_t operand_desc(uint32_t tile, int mn_major, in
   return mn_major ? sdesc(tile + kstep * 2048, 8192, 1024) : sdesc(tile + kstep * 32, 16, 1024);
 }
 
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* tm, uint32_t bar, int c0,
+                                            int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+      "%3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      : "memory");
+}
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* tm, uint32_t bar, int c0,
                                             int c1, int c2, int c3) {
   asm volatile(
