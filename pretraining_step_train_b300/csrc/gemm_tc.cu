@@ -133,6 +133,32 @@ __device__ __forceinline__ void pack16_bf16(const float* v, uint32_t* w) {
   for (int j = 0; j < 8; ++j) w[j] = pack2_bf16(v[2 * j], v[2 * j + 1]);
 }
 
+// Packed fp32 pair arithmetic (Blackwell f32x2 FMA pipe: two lanes per instruction).
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n.reg .b64 ra, rb, rc, rd;\nmov.b64 ra, {%2, %3};\nmov.b64 rb, {%4, %5};\n"
+      "mov.b64 rc, {%6, %7};\nfma.rn.f32x2 rd, ra, rb, rc;\nmov.b64 {%0, %1}, rd;\n}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n.reg .b64 ra, rb, rd;\nmov.b64 ra, {%2, %3};\nmov.b64 rb, {%4, %5};\n"
+      "mul.rn.f32x2 rd, ra, rb;\nmov.b64 {%0, %1}, rd;\n}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n.reg .b64 ra, rb, rd;\nmov.b64 ra, {%2, %3};\nmov.b64 rb, {%4, %5};\n"
+      "add.rn.f32x2 rd, ra, rb;\nmov.b64 {%0, %1}, rd;\n}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
 // Hardware tanh (MUFU, PTX tanh.approx.f32): relative error about 2^-11, far
 // below the bf16 rounding of the values it feeds.
 __device__ __forceinline__ float tanh_hw(float x) {
@@ -141,14 +167,19 @@ __device__ __forceinline__ float tanh_hw(float x) {
   return y;
 }
 // tanh-form GELU with the hardware tanh (bf16 epilogues only).
-// gelu(x) and gelu'(x) sharing one hardware tanh.
-__device__ __forceinline__ void gelu_and_grad_hw(float x, float& y, float& dy) {
-  const float x2 = x * x;
-  const float th = tanh_hw(x * (GELU_K + GELU_K * GELU_C * x2));
-  const float hx = 0.5f * x;
-  y = fmaf(hx, th, hx);
-  const float du = GELU_K + 3.0f * GELU_K * GELU_C * x2;
-  dy = 0.5f * (1.0f + th) + hx * (1.0f - th * th) * du;
+// gelu and gelu' of a pair of values sharing one hardware tanh each, in packed
+// fp32 pair arithmetic: y = x/2 (1 + th), dy = (1 + th)/2 + x/2 (1 - th^2) du with
+// th = tanh(x (k + k c x^2)), du = k + 3 k c x^2.
+__device__ __forceinline__ void gelu_and_grad2(float2 x, float2& y, float2& dy) {
+  const float2 x2 = mul2(x, x);
+  const float2 u = mul2(x, fma2(x2, make_float2(GELU_K * GELU_C, GELU_K * GELU_C), make_float2(GELU_K, GELU_K)));
+  const float2 th = make_float2(tanh_hw(u.x), tanh_hw(u.y));
+  const float2 hx = mul2(x, make_float2(0.5f, 0.5f));
+  y = fma2(hx, th, hx);
+  const float2 du = fma2(x2, make_float2(3.0f * GELU_K * GELU_C, 3.0f * GELU_K * GELU_C), make_float2(GELU_K, GELU_K));
+  const float2 om = fma2(th, make_float2(-th.x, -th.y), make_float2(1.0f, 1.0f));  // 1 - th^2
+  const float2 half_p = fma2(th, make_float2(0.5f, 0.5f), make_float2(0.5f, 0.5f));   // (1 + th) / 2
+  dy = fma2(mul2(hx, om), du, half_p);
 }
 
 __global__ void __launch_bounds__(NUM_THREADS, 1)
@@ -292,19 +323,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     bool prev_stored = false;                      // the previous chunk issued a store
     const int epi = g.epi;
     const bool split = p.splits > 1;
-    // chunk (tile, c): rows m_t*BM + quad*32 .. +32, columns n_t*BN + qq*WCOLS + c*CW .. +CW
-    auto chunk_valid = [&](int tile, int c, int& x, int& y) {
-      if (tile >= ntiles) return false;
+    // chunk c of a tile: rows y = m_t*BM + quad*32 .. +32, columns x = xb + c*CW .. +CW with
+    // xb = n_t*BN + qq*WCOLS; this warp's origin of a tile (xb, y), or y = M past the last tile
+    auto warp_origin = [&](int tile, int& xb, int& y) {
+      if (tile >= ntiles) { xb = 0; y = g.M; return; }
       int m_t, n_t, sp;
       tile_coords(p, tile, m_t, n_t, sp);
-      x = n_t * BN + qq * WCOLS + c * CW;
+      xb = n_t * BN + qq * WCOLS;
       y = m_t * BM + quad * 32;
-      return x < g.N && y < g.M;
     };
-    // Prefetch the x operand of chunk (tile, c) into box b (all lanes track the state).
-    auto x_issue = [&](int tile, int c, int b) {
-      int x, y;
-      if (!p.load_x || !chunk_valid(tile, c, x, y)) return;
+    // Prefetch the x operand of the chunk at (x, y) into box b (all lanes track the state).
+    auto x_issue = [&](int x, int y, int b) {
+      if (!p.load_x || x >= g.N || y >= g.M) return;
       if (lane == 0) {
         bulk_wait_read<0>();  // the last store out of this box has finished reading it
         mbar_expect_tx(xbar + 8 * b, BOX_BYTES);
@@ -312,12 +342,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       xpend |= 1u << b;
     };
-    x_issue(blockIdx.x, 0, 0);
+    int nxb, ny;  // origin of the next tile this warp handles
+    warp_origin(blockIdx.x, nxb, ny);
+    x_issue(nxb, ny, 0);
     int abuf = 0;
     uint32_t aphase = 0;
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
       int m_t, n_t, sp;
       tile_coords(p, tile, m_t, n_t, sp);
+      const int xb = nxb, y0 = ny;
+      warp_origin(tile + gridDim.x, nxb, ny);
       if (!mbar_wait(b_tfull + 8 * abuf, aphase, abort_flag, p.status)) break;
       tc_fence_after();
       const int m = m_t * BM + quad * 32 + lane;
@@ -335,11 +369,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           mbar_arrive(b_tempty + 8 * abuf);
         }
         // prefetch the next chunk's operand into the other box
-        if (c < NCHUNK - 1) x_issue(tile, c + 1, b ^ 1);
-        else x_issue(tile + gridDim.x, 0, b ^ 1);
+        if (c < NCHUNK - 1) x_issue(xb + (c + 1) * CW, y0, b ^ 1);
+        else x_issue(nxb, ny, b ^ 1);
         bx ^= 1;
-        int x0, y0;
-        if (!chunk_valid(tile, c, x0, y0)) { prev_stored = false; continue; }
+        const int x0 = xb + c * CW;
+        if (x0 >= g.N || y0 >= g.M) { prev_stored = false; continue; }
         if (split || epi == EPI_F32) {
           // fp32 result: two 8-column boxes (both staged boxes)
           if (lane == 0) bulk_wait_read<0>();
@@ -369,10 +403,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           box_load_row_bf16(box0, lane, xv);
           if (epi == EPI_BIAS_RESID) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) v[j] += xv[j];
+            for (int j = 0; j < 16; j += 2) {
+              const float2 t = add2(make_float2(v[j], v[j + 1]), make_float2(xv[j], xv[j + 1]));
+              v[j] = t.x; v[j + 1] = t.y;
+            }
           } else {  // EPI_GELU_BWD: dh = da * gelu'(h)
 #pragma unroll
-            for (int j = 0; j < 16; ++j) v[j] *= xv[j];
+            for (int j = 0; j < 16; j += 2) {
+              const float2 t = mul2(make_float2(v[j], v[j + 1]), make_float2(xv[j], xv[j + 1]));
+              v[j] = t.x; v[j + 1] = t.y;
+            }
           }
         }
         if (epi == EPI_BIAS || epi == EPI_BIAS_RESID || epi == EPI_BIAS_GELU) {
@@ -383,7 +423,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               float bb[8];
               load16<bf16>(bias + x0 + q * 8, bb);
 #pragma unroll
-              for (int i = 0; i < 8; ++i) v[q * 8 + i] += bb[i];
+              for (int i = 0; i < 8; i += 2) {
+                const float2 t = add2(make_float2(v[q * 8 + i], v[q * 8 + i + 1]), make_float2(bb[i], bb[i + 1]));
+                v[q * 8 + i] = t.x; v[q * 8 + i + 1] = t.y;
+              }
             }
           }
         }
@@ -415,7 +458,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           // gelu'(h) (D, for the backward) and gelu(h) (D2) from one tanh: both staged boxes
           float a[16];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) gelu_and_grad_hw(v[j], a[j], v[j]);
+          for (int j = 0; j < 16; j += 2) {
+            float2 y, dy;
+            gelu_and_grad2(make_float2(v[j], v[j + 1]), y, dy);
+            a[j] = y.x; a[j + 1] = y.y;
+            v[j] = dy.x; v[j + 1] = dy.y;
+          }
           pack16_bf16(v, w);
           uint32_t wa[8];
           pack16_bf16(a, wa);
