@@ -9,8 +9,9 @@
 //               a 4-stage ring that runs on across items, so the next item's
 //               tiles load while this one finishes (4-D tensor maps over the
 //               strided q / k / v views, 128B swizzle; rows past T arrive as zeros);
-//   warp 1      owns 512 TMEM columns: S double buffer (2 x 128 fp32 columns)
-//               and the O accumulator (64 columns); one thread issues
+//   warp 1      owns 512 TMEM columns: S double buffer (2 x 128 fp32 columns),
+//               the O accumulator (64 columns) and a P double buffer (2 x 64
+//               columns of bf16 pairs); one thread issues
 //               S_j = Q K_j^T (M=128, N=128, K=64) and O += P_j V_j (M=128, N=64,
 //               K=128, V read MN-major), in the order S_0, S_1, PV_0, S_2, PV_1, ...
 //               so the tensor core computes S_{j+1} while softmax works on S_j;
@@ -18,9 +19,9 @@
 //               tcgen05.ld of the half row, causal mask on the diagonal tile, row
 //               max exchanged with the partner warp through shared memory,
 //               p = 2^(s*scale*log2e - m), running sum, O rescaled in TMEM only
-//               when the running max has to move by more than 2^8, P (bf16)
-//               written to a 128B-swizzled shared tile (double-buffered) that is
-//               the A operand of the PV MMA.
+//               when the running max has to move by more than 2^8, P (bf16 pairs)
+//               written to tensor memory (double-buffered), where the PV MMA reads
+//               its A operand.
 // Epilogue: O / l -> bf16 rows, lse = (m + log2 l) ln 2 (natural log).
 // Every wait is bounded; on expiry the CTA latches ST_TIMEOUT (when a status
 // word is given), drains its copies and MMAs, frees TMEM and returns.
@@ -38,14 +39,14 @@ constexpr int AT_TILE = AT_B * AT_D * 2;        // 16 KB: one [128 x 64] bf16 ti
 constexpr int AT_Q_OFF = 0;
 constexpr int AT_KV_STAGES = 4;
 constexpr int AT_KV_OFF = AT_TILE;              // stage s: K at +s*2*TILE, V at +s*2*TILE+TILE
-constexpr int AT_P_OFF = AT_KV_OFF + 2 * AT_KV_STAGES * AT_TILE;  // buffer b: +b*2*TILE, half h at +h*TILE
-constexpr int AT_RED_OFF = AT_P_OFF + 4 * AT_TILE; // row-max exchange [2][2][128] + row-sum [2][128]
+constexpr int AT_RED_OFF = AT_KV_OFF + 2 * AT_KV_STAGES * AT_TILE;  // row-max exchange [2][2][128] + row-sum [2][128]
 constexpr int AT_BAR_OFF = AT_RED_OFF + 6 * 128 * 4;
 constexpr int AT_NBARS = 31;
 constexpr int AT_SMEM = 1024 + AT_BAR_OFF + 8 * (AT_NBARS + 2);
 constexpr int AT_THREADS = 320;
 constexpr int AT_TMEM_COLS = 512;
 constexpr int AT_O_COL = 256;
+constexpr int AT_P_COL = 320;  // P buffers (bf16 pairs): 320 + 64 * buffer
 
 struct AtParams {
   AttnArgs a;
@@ -187,12 +188,12 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         const int pb = gp & 1;
         if (!mbar_wait(b_pf + 8 * pb, (uint32_t)(gp >> 1) & 1u, abort_flag, p.status)) return false;
         tc_fence_after();
-        const uint32_t pd = sbase + AT_P_OFF + pb * 2 * AT_TILE;
         const uint32_t vd = sbase + AT_KV_OFF + (gp % AT_KV_STAGES) * 2 * AT_TILE + AT_TILE;
+        // A = P_gp in TMEM: 16 keys per MMA = 8 columns of bf16 pairs
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_bf16(tmem + AT_O_COL, operand_desc(pd + (kk >> 2) * AT_TILE, 0, kk & 3),
-                   operand_desc(vd, 1, kk), p.idesc_pv, (!first || kk > 0) ? 1u : 0u);
+          mma_bf16_tmem_a(tmem + AT_O_COL, tmem + AT_P_COL + pb * 64 + kk * 8, operand_desc(vd, 1, kk),
+                          p.idesc_pv, (!first || kk > 0) ? 1u : 0u);
         mma_commit((gp & 1) ? b_pv2 : b_pv);
         mma_commit(b_kve + 8 * (gp % AT_KV_STAGES));
         return true;
@@ -262,31 +263,51 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
           for (int c = 0; c < 64; ++c)
             if (k0 + c > qi) s[c] = -INFINITY;
         }
-        float tmax = tree_max<64>(s);
-        // exchange the half-row maxima with the partner warp (double-buffered slots;
-        // the mbarrier arrive releases the slot write, the wait acquires the partner's)
+        // Lazy rescaling: the running max m (log2 units) only moves when the row's tile max
+        // exceeds it by more than 8, so p <= 2^8 stays exact in fp32 and bf16; O and l
+        // always share the same m, so the result is unchanged.  The half-row maxima are
+        // exchanged with the partner warp through shared memory (double-buffered slots;
+        // the mbarrier arrive releases the write, the wait acquires the partner's).  The
+        // exponentials are computed speculatively with the current m unless this half
+        // already needs a move, and redone in the rare case the partner's half does.
+        const float hmax = tree_max<64>(s) * p.c2;
         float* rx = red + (g & 1) * 256;
-        rx[half * 128 + r] = tmax;
+        rx[half * 128 + r] = hmax;
         const uint32_t xb = b_xmax + 8 * (quad * 2 + (g & 1));
         warp_arrive(xb);
-        if (!warp_wait(xb, (uint32_t)(g >> 1) & 1u, abort_flag, p.status)) { ok = false; break; }
-        tmax = fmaxf(tmax, rx[(half ^ 1) * 128 + r]) * p.c2;
-        // Lazy rescaling: the running max m (log2 units) only moves when the tile's
-        // max exceeds it by more than 8, so p <= 2^8 stays exact in fp32 and bf16;
-        // O and l always share the same m, so the result is unchanged.
-        const bool move = j == 0 || tmax > m + 8.0f;
-        const float m_new = move ? fmaxf(m, tmax) : m;
-        const float alpha = j == 0 ? 0.f : ex2(m - m_new);
-        float ps[4] = {0.f, 0.f, 0.f, 0.f};
-        uint32_t pk[32];
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const float p0 = ex2(fmaf(s[2 * c], p.c2, -m_new));
-          const float p1 = ex2(fmaf(s[2 * c + 1], p.c2, -m_new));
-          ps[c & 3] += p0 + p1;
-          pk[c] = pack_bf16x2(p0, p1);
+        bool waited = false;
+        float m_new = m;
+        if (j == 0 || __any_sync(0xffffffffu, hmax > m + 8.0f)) {
+          if (!warp_wait(xb, (uint32_t)(g >> 1) & 1u, abort_flag, p.status)) { ok = false; break; }
+          waited = true;
+          const float tmax = fmaxf(hmax, rx[(half ^ 1) * 128 + r]);
+          if (j == 0 || tmax > m + 8.0f) m_new = fmaxf(m, tmax);
         }
-        const float lsum = (ps[0] + ps[1]) + (ps[2] + ps[3]);
+        uint32_t pk[32];
+        float lsum = 0.f;
+        for (int pass = 0; pass < 2; ++pass) {
+          const float2 nm = make_float2(-m_new, -m_new), c2 = make_float2(p.c2, p.c2);
+          float2 ps[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const float2 x = fma2(make_float2(s[2 * c], s[2 * c + 1]), c2, nm);
+            const float2 pr = make_float2(ex2(x.x), ex2(x.y));
+            ps[c & 1] = add2(ps[c & 1], pr);
+            pk[c] = pack_bf16x2(pr.x, pr.y);
+          }
+          lsum = (ps[0].x + ps[0].y) + (ps[1].x + ps[1].y);
+          if (waited) break;
+          // speculation check: does the partner half need the max to move?
+          if (!warp_wait(xb, (uint32_t)(g >> 1) & 1u, abort_flag, p.status)) { ok = false; break; }
+          waited = true;
+          const float tmax = fmaxf(hmax, rx[(half ^ 1) * 128 + r]);
+          const bool mv = tmax > m + 8.0f;
+          if (!__any_sync(0xffffffffu, mv)) break;
+          if (mv) m_new = fmaxf(m, tmax);
+        }
+        if (!ok) break;
+        const bool move = m_new != m;
+        const float alpha = j == 0 ? 0.f : ex2(m - m_new);
         l = l * alpha + lsum;
         m = m_new;
         const bool rescale = j >= 1 && __any_sync(0xffffffffu, move);
@@ -301,21 +322,15 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
 #pragma unroll
           for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
           tmem_st32(lane_base + AT_O_COL + half * 32, o);
-          tmem_st_wait();
         } else if (g >= 2) {
           // the P buffer of this tile parity was last read by the PV of tile g-2
           const uint32_t pb = g & 1 ? b_pv2 : b_pv;
           if (!warp_wait(pb, (uint32_t)((g - 2) >> 1) & 1u, abort_flag, p.status)) { ok = false; break; }
           tc_fence_after();
         }
-        // P (bf16) into the 128B-swizzled A tile: row r, keys half*64 .. +64
-        const uint32_t prow = sbase + AT_P_OFF + (g & 1) * 2 * AT_TILE + half * AT_TILE + r * 128;
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(prow + ((c ^ (r & 7)) << 4)),
-                       "r"(pk[4 * c]), "r"(pk[4 * c + 1]), "r"(pk[4 * c + 2]), "r"(pk[4 * c + 3])
-                       : "memory");
-        fence_async_smem();
+        // P (bf16 pairs) into TMEM: row r, keys half*64 .. +64 = columns half*32 .. +32
+        tmem_st32(lane_base + AT_P_COL + (g & 1) * 64 + half * 32, pk);
+        tmem_st_wait();
         tc_fence_before();
         warp_arrive(b_pf + 8 * (g & 1));
       }
