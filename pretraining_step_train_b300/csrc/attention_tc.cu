@@ -383,16 +383,6 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
 
 constexpr int BW_THREADS = 320;
 
-// 64 bf16 of row r into a 128B-swizzled [128 x 64] tile (piece c at (c ^ (r & 7)) * 16).
-__device__ __forceinline__ void tile_row_store(uint32_t tile, int r, const uint32_t* pk) {
-  const uint32_t row = tile + r * 128;
-#pragma unroll
-  for (int c = 0; c < 8; ++c)
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + ((c ^ (r & 7)) << 4)),
-                 "r"(pk[4 * c]), "r"(pk[4 * c + 1]), "r"(pk[4 * c + 2]), "r"(pk[4 * c + 3])
-                 : "memory");
-}
-
 struct BwParams {
   AttnArgs a;
   int nq;
@@ -409,11 +399,11 @@ __device__ __forceinline__ void bw_load(const CUtensorMap* tm, int swap, uint32_
 }
 
 // ------------------------------------------------------------------ dQ
-// smem: Q | dO (per item) | K,V ring (4 stages) | dS (two 64-key halves)
+// smem: Q | dO (per item) | K,V ring (4 stages); TMEM: S | dP | dQ | dS double buffer
 constexpr int DQ_STAGES = 4;
-constexpr int DQ_Q = 0, DQ_DO = AT_TILE, DQ_KV = 2 * AT_TILE, DQ_DS = DQ_KV + 2 * DQ_STAGES * AT_TILE;
-constexpr int DQ_BAR = DQ_DS + 2 * AT_TILE;
-constexpr int DQ_NBARS = 16;
+constexpr int DQ_Q = 0, DQ_DO = AT_TILE, DQ_KV = 2 * AT_TILE;
+constexpr int DQ_BAR = DQ_KV + 2 * DQ_STAGES * AT_TILE;
+constexpr int DQ_NBARS = 17;
 constexpr int DQ_SMEM = 1024 + DQ_BAR + 8 * (DQ_NBARS + 2);
 
 __global__ void __launch_bounds__(BW_THREADS, 1)
@@ -424,10 +414,11 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + DQ_BAR);
-  // q_full, q_empty, kv_full[4], kv_empty[4], sdp_full, sdp_empty, ds_full, dq_done, done
+  // q_full, q_empty, kv_full[4], kv_empty[4], sdp_full, sdp_empty, ds_full[2], dq_done[2], done
+  // (ds_full / dq_done per dS buffer: tile parity)
   const uint32_t b_qf = smem_u32(bars), b_qe = b_qf + 8, b_kvf = b_qe + 8, b_kve = b_kvf + 8 * DQ_STAGES;
-  const uint32_t b_sf = b_kve + 8 * DQ_STAGES, b_se = b_sf + 8, b_dsf = b_se + 8, b_dq = b_dsf + 8;
-  const uint32_t b_done = b_dq + 8;
+  const uint32_t b_sf = b_kve + 8 * DQ_STAGES, b_se = b_sf + 8, b_dsf = b_se + 8, b_dq = b_dsf + 16;
+  const uint32_t b_done = b_dq + 16;
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bars + DQ_NBARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + DQ_NBARS + 1);
   const AttnArgs& a = p.a;
@@ -443,8 +434,10 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
     }
     mbar_init(b_sf, 1);
     mbar_init(b_se, 8);  // one arrival per compute warp
-    mbar_init(b_dsf, 8);
-    mbar_init(b_dq, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(b_dsf + 8 * i, 8);
+      mbar_init(b_dq + 8 * i, 1);
+    }
     mbar_init(b_done, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -458,7 +451,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  constexpr uint32_t C_S = 0, C_DP = 128, C_DQ = 256;
+  constexpr uint32_t C_S = 0, C_DP = 128, C_DQ = 256, C_DS = 320;  // dS buffer b at C_DS + 64 b
 
   if (warp == 0) {
     if (lane == 0) {
@@ -489,14 +482,16 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       auto issue_dq = [&](int gp, bool first) -> bool {
-        if (!mbar_wait(b_dsf, (uint32_t)gp & 1u, abort_flag, p.status)) return false;
+        const int db = gp & 1;
+        if (!mbar_wait(b_dsf + 8 * db, (uint32_t)(gp >> 1) & 1u, abort_flag, p.status)) return false;
         tc_fence_after();
         const uint32_t kd = sbase + DQ_KV + (gp % DQ_STAGES) * 2 * AT_TILE;
+        // A = dS in TMEM: 16 keys per MMA = 8 columns of bf16 pairs
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_bf16(tmem + C_DQ, operand_desc(sbase + DQ_DS + (kk >> 2) * AT_TILE, 0, kk & 3),
-                   operand_desc(kd, 1, kk), p.idesc_d, (!first || kk > 0) ? 1u : 0u);
-        mma_commit(b_dq);
+          mma_bf16_tmem_a(tmem + C_DQ, tmem + C_DS + db * 64 + kk * 8, operand_desc(kd, 1, kk), p.idesc_d,
+                          (!first || kk > 0) ? 1u : 0u);
+        mma_commit(b_dq + 8 * db);
         mma_commit(b_kve + 8 * (gp % DQ_STAGES));
         return true;
       };
@@ -555,26 +550,32 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
         tmem_ld_wait();
         tc_fence_before();
         warp_arrive(b_se);
-        const bool diag = j == qt;
-        const int k0 = j * AT_B + half * 64;
+        const int kmask = j == qt ? qi - j * AT_B - half * 64 : AT_B;  // key offsets > kmask are masked
+        const float2 c2 = make_float2(p.c2, p.c2), nl = make_float2(-lse2, -lse2);
+        const float2 nd = make_float2(-Dr, -Dr);
         uint32_t pk[32];
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
-          float p0 = ex2(fmaf(__uint_as_float(sv[2 * c]), p.c2, -lse2));
-          float p1 = ex2(fmaf(__uint_as_float(sv[2 * c + 1]), p.c2, -lse2));
-          if (diag && k0 + 2 * c > qi) p0 = 0.f;
-          if (diag && k0 + 2 * c + 1 > qi) p1 = 0.f;
-          pk[c] = pack_bf16x2(p0 * (__uint_as_float(dv[2 * c]) - Dr), p1 * (__uint_as_float(dv[2 * c + 1]) - Dr));
+          const float2 x = fma2(make_float2(__uint_as_float(sv[2 * c]), __uint_as_float(sv[2 * c + 1])), c2, nl);
+          float2 pr = make_float2(ex2(x.x), ex2(x.y));
+          if (2 * c > kmask) pr.x = 0.f;
+          if (2 * c + 1 > kmask) pr.y = 0.f;
+          const float2 t = mul2(pr, add2(make_float2(__uint_as_float(dv[2 * c]), __uint_as_float(dv[2 * c + 1])), nd));
+          pk[c] = pack_bf16x2(t.x, t.y);
         }
-        // the dS tile is free once the previous dQ MMA has completed
-        if (g >= 1 && !warp_wait(b_dq, (uint32_t)(g - 1) & 1u, abort_flag, p.status)) { ok = false; break; }
-        tile_row_store(sbase + DQ_DS + half * AT_TILE, r, pk);
-        fence_async_smem();
+        // this dS buffer is free once the dQ MMA of tile g-2 has completed
+        const int db = g & 1;
+        if (g >= 2 && !warp_wait(b_dq + 8 * db, (uint32_t)((g - 2) >> 1) & 1u, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        tmem_st32(lane_base + C_DS + db * 64 + half * 32, pk);
+        tmem_st_wait();
         tc_fence_before();
-        warp_arrive(b_dsf);
+        warp_arrive(b_dsf + 8 * db);
       }
       if (!ok) break;
-      if (!warp_wait(b_dq, (uint32_t)(g - 1) & 1u, abort_flag, p.status)) break;
+      if (!warp_wait(b_dq + 8 * ((g - 1) & 1), (uint32_t)((g - 1) >> 1) & 1u, abort_flag, p.status)) break;
       tc_fence_after();
       uint32_t o[32];
       tmem_ld32(lane_base + C_DQ + half * 32, o);
@@ -605,12 +606,12 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
 }
 
 // ------------------------------------------------------------------ dK, dV
-// smem: K | V (per item) | Q,dO ring (3 stages) | lse2, D ring (3 x 1 KB) | P^T | dS^T
-constexpr int DK_STAGES = 3;
+// smem: K | V (per item) | Q,dO ring (4 stages) | lse2, D ring (4 x 1 KB);
+// TMEM: S^T | dP^T | dV | dK | P^T | dS^T
+constexpr int DK_STAGES = 4;
 constexpr int DK_K = 0, DK_V = AT_TILE, DK_QD = 2 * AT_TILE, DK_LD = DK_QD + 2 * DK_STAGES * AT_TILE;
-constexpr int DK_PT = DK_LD + DK_STAGES * 1024, DK_DST = DK_PT + 2 * AT_TILE;
-constexpr int DK_BAR = DK_DST + 2 * AT_TILE;
-constexpr int DK_NBARS = 15;
+constexpr int DK_BAR = DK_LD + DK_STAGES * 1024;
+constexpr int DK_NBARS = 17;
 constexpr int DK_SMEM = 1024 + DK_BAR + 8 * (DK_NBARS + 2);
 
 __global__ void __launch_bounds__(BW_THREADS, 1)
@@ -622,7 +623,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
   const uint32_t sbase = smem_u32(smem);
   float* ldbuf = reinterpret_cast<float*>(smem + DK_LD);  // stage s: lse2[128] then D[128]
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + DK_BAR);
-  // kv_full, kv_empty, qd_full[3], qd_empty[3], sdp_full, sdp_empty, ds_full, mma_done, done
+  // kv_full, kv_empty, qd_full[4], qd_empty[4], sdp_full, sdp_empty, ds_full, mma_done, done
   const uint32_t b_kvf = smem_u32(bars), b_kve = b_kvf + 8, b_qdf = b_kve + 8, b_qde = b_qdf + 8 * DK_STAGES;
   const uint32_t b_sf = b_qde + 8 * DK_STAGES, b_se = b_sf + 8, b_dsf = b_se + 8, b_mm = b_dsf + 8;
   const uint32_t b_done = b_mm + 8;
@@ -657,11 +658,11 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  constexpr uint32_t C_S = 0, C_DP = 128, C_DV = 256, C_DK = 320;
+  constexpr uint32_t C_S = 0, C_DP = 128, C_DV = 256, C_DK = 320, C_PT = 384, C_DST = 448;
 
   if (warp == 0) {
     // ---------------- producer warp: TMA by lane 0, lse2 / D staged by all lanes
-    int last_par[DK_STAGES] = {-1, -1, -1}, kv_par = -1, g = 0;
+    int last_par[DK_STAGES] = {-1, -1, -1, -1}, kv_par = -1, g = 0;
     bool ok = true;
     for (int w = blockIdx.x, it = 0; ok && w < nitems; w += gridDim.x, ++it) {
       const int kt = w / BH, bh = w % BH, b = bh / a.H, h = bh % a.H;
@@ -705,14 +706,15 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
         if (!mbar_wait(b_dsf, (uint32_t)gp & 1u, abort_flag, p.status)) return false;
         tc_fence_after();
         const uint32_t qd = sbase + DK_QD + (gp % DK_STAGES) * 2 * AT_TILE;
+        // A = P^T / dS^T in TMEM: 16 queries per MMA = 8 columns of bf16 pairs
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_bf16(tmem + C_DV, operand_desc(sbase + DK_PT + (kk >> 2) * AT_TILE, 0, kk & 3),
-                   operand_desc(qd + AT_TILE, 1, kk), p.idesc_d, (!first || kk > 0) ? 1u : 0u);
+          mma_bf16_tmem_a(tmem + C_DV, tmem + C_PT + kk * 8, operand_desc(qd + AT_TILE, 1, kk), p.idesc_d,
+                          (!first || kk > 0) ? 1u : 0u);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_bf16(tmem + C_DK, operand_desc(sbase + DK_DST + (kk >> 2) * AT_TILE, 0, kk & 3),
-                   operand_desc(qd, 1, kk), p.idesc_d, (!first || kk > 0) ? 1u : 0u);
+          mma_bf16_tmem_a(tmem + C_DK, tmem + C_DST + kk * 8, operand_desc(qd, 1, kk), p.idesc_d,
+                          (!first || kk > 0) ? 1u : 0u);
         mma_commit(b_mm);
         mma_commit(b_qde + 8 * (gp % DK_STAGES));
         return true;
@@ -774,25 +776,30 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
         tmem_ld_wait();
         tc_fence_before();
         warp_arrive(b_se);
-        const float* lb = ldbuf + st * 256 + half * 64;
-        const bool diag = i == kt;
-        const int q0 = i * AT_B + half * 64;
+        const float2* lb = reinterpret_cast<const float2*>(ldbuf + st * 256 + half * 64);
+        const float2* db = reinterpret_cast<const float2*>(ldbuf + st * 256 + 128 + half * 64);
+        // diagonal tile: query offsets below kmask (relative to this half) are masked
+        const int kmask = i == kt ? r - half * 64 : -1;
+        const float2 c2 = make_float2(p.c2, p.c2);
         uint32_t pp[32], pd[32];
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
-          float p0 = ex2(fmaf(__uint_as_float(sv[2 * c]), p.c2, -lb[2 * c]));
-          float p1 = ex2(fmaf(__uint_as_float(sv[2 * c + 1]), p.c2, -lb[2 * c + 1]));
-          if (diag && kr > q0 + 2 * c) p0 = 0.f;
-          if (diag && kr > q0 + 2 * c + 1) p1 = 0.f;
-          pp[c] = pack_bf16x2(p0, p1);
-          pd[c] = pack_bf16x2(p0 * (__uint_as_float(dv[2 * c]) - lb[128 + 2 * c]),
-                              p1 * (__uint_as_float(dv[2 * c + 1]) - lb[128 + 2 * c + 1]));
+          const float2 l2 = lb[c], d2 = db[c];
+          const float2 x = fma2(make_float2(__uint_as_float(sv[2 * c]), __uint_as_float(sv[2 * c + 1])), c2,
+                                make_float2(-l2.x, -l2.y));
+          float2 pr = make_float2(ex2(x.x), ex2(x.y));
+          if (2 * c < kmask) pr.x = 0.f;
+          if (2 * c + 1 < kmask) pr.y = 0.f;
+          pp[c] = pack_bf16x2(pr.x, pr.y);
+          const float2 t = mul2(pr, add2(make_float2(__uint_as_float(dv[2 * c]), __uint_as_float(dv[2 * c + 1])),
+                                         make_float2(-d2.x, -d2.y)));
+          pd[c] = pack_bf16x2(t.x, t.y);
         }
-        // P^T / dS^T tiles are free once the previous dV / dK MMAs have completed
+        // P^T / dS^T are free once the previous dV / dK MMAs have completed
         if (g >= 1 && !warp_wait(b_mm, (uint32_t)(g - 1) & 1u, abort_flag, p.status)) { ok = false; break; }
-        tile_row_store(sbase + DK_PT + half * AT_TILE, r, pp);
-        tile_row_store(sbase + DK_DST + half * AT_TILE, r, pd);
-        fence_async_smem();
+        tmem_st32(lane_base + C_PT + half * 32, pp);
+        tmem_st32(lane_base + C_DST + half * 32, pd);
+        tmem_st_wait();
         tc_fence_before();
         warp_arrive(b_dsf);
       }
