@@ -56,6 +56,29 @@ def measured_peaks():
         return {}
 
 
+GEMM_SOURCES = ["gemm_tc.cu", "tc_ptx.cuh", "common.cuh", "internal.h"]
+TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "gemm_tc_dram_step_124m_b16.md")
+
+
+def gemm_traffic_per_launch():
+    """DRAM bytes per k_gemm_tc launch from the committed ncu summary, or None when the
+    GEMM sources changed since those counters were taken (hash mismatch) or the
+    summary is missing."""
+    import hashlib
+    try:
+        text = open(TRAFFIC_SUMMARY).read()
+        fields = dict(line.split(": ", 1) for line in text.splitlines()
+                      if line.startswith(("traffic_bytes_per_launch:", "source_sha256:")))
+        h = hashlib.sha256()
+        for f in GEMM_SOURCES:
+            h.update(open(os.path.join(ROOT, "pretraining_step_train_b300", "csrc", f), "rb").read())
+        if h.hexdigest() != fields["source_sha256"].strip():
+            return None
+        return int(fields["traffic_bytes_per_launch"])
+    except Exception:
+        return None
+
+
 def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
@@ -385,7 +408,11 @@ def main():
                      "peak": gemm_peak, "unit": "TFLOP/s",
                      "frac": round(gemm_tflops / gemm_peak, 4) if gemm_tflops else None,
                      "peak_source": "MEASURED_PEAKS.json bf16_tflops_sustained (kernel timed inside a long step)",
-                     "traffic": None},
+                     "achieved_source": "sum of 2MNK over the step's GEMM launches / their CUDA-event time, "
+                                        "one instrumented eager step on the bench stream",
+                     "traffic": gemm_traffic_per_launch(),
+                     "traffic_source": "ncu dram__bytes_read+write per k_gemm_tc launch, "
+                                       "profiles/gemm_tc_dram_step_124m_b16.md (null if the kernel changed)"},
         "kernels": kernels,
         "gemm_shapes": gemm_shapes,
         "e2e": {"value": round(world * M / e2e_s, 1), "unit": "tokens/s", "h2d_bytes_per_step": 2 * M * 4,
