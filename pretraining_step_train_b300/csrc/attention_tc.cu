@@ -554,14 +554,21 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
         const float2 c2 = make_float2(p.c2, p.c2), nl = make_float2(-lse2, -lse2);
         const float2 nd = make_float2(-Dr, -Dr);
         uint32_t pk[32];
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
+        // dS = P (dP - D) for a pair of key columns
+        auto pair = [&](int c, bool zero0, bool zero1) {
           const float2 x = fma2(make_float2(__uint_as_float(sv[2 * c]), __uint_as_float(sv[2 * c + 1])), c2, nl);
           float2 pr = make_float2(ex2(x.x), ex2(x.y));
-          if (2 * c > kmask) pr.x = 0.f;
-          if (2 * c + 1 > kmask) pr.y = 0.f;
+          if (zero0) pr.x = 0.f;
+          if (zero1) pr.y = 0.f;
           const float2 t = mul2(pr, add2(make_float2(__uint_as_float(dv[2 * c]), __uint_as_float(dv[2 * c + 1])), nd));
           pk[c] = pack_bf16x2(t.x, t.y);
+        };
+        if (j == qt) {  // diagonal tile: keys after the query are masked
+#pragma unroll
+          for (int c = 0; c < 32; ++c) pair(c, 2 * c > kmask, 2 * c + 1 > kmask);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) pair(c, false, false);
         }
         // this dS buffer is free once the dQ MMA of tile g-2 has completed
         const int db = g & 1;
@@ -621,7 +628,8 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
-  float* ldbuf = reinterpret_cast<float*>(smem + DK_LD);  // stage s: lse2[128] then D[128]
+  // stage s: for each query pair (2i, 2i+1) the float4 {-lse2[2i], -lse2[2i+1], -D[2i], -D[2i+1]}
+  float* ldbuf = reinterpret_cast<float*>(smem + DK_LD);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + DK_BAR);
   // kv_full, kv_empty, qd_full[4], qd_empty[4], sdp_full, sdp_empty, ds_full, mma_done, done
   const uint32_t b_kvf = smem_u32(bars), b_kve = b_kvf + 8, b_qdf = b_kve + 8, b_qde = b_qdf + 8 * DK_STAGES;
@@ -688,8 +696,9 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
         for (int e = 0; e < 4; ++e) {
           const int c = lane * 4 + e, q = i * AT_B + c;
           const bool v = q < a.T;
-          lb[c] = v ? a.lse[(long long)bh * a.T + q] * 1.4426950408889634f : INFINITY;
-          lb[128 + c] = v ? a.Dbuf[(long long)bh * a.T + q] : 0.f;
+          const int slot = (c >> 1) * 4 + (c & 1);
+          lb[slot] = v ? -a.lse[(long long)bh * a.T + q] * 1.4426950408889634f : -INFINITY;
+          lb[slot + 2] = v ? -a.Dbuf[(long long)bh * a.T + q] : 0.f;
         }
         warp_arrive(b_qdf + 8 * st);
         last_par[st] = (int)ph;
@@ -776,24 +785,29 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
         tmem_ld_wait();
         tc_fence_before();
         warp_arrive(b_se);
-        const float2* lb = reinterpret_cast<const float2*>(ldbuf + st * 256 + half * 64);
-        const float2* db = reinterpret_cast<const float2*>(ldbuf + st * 256 + 128 + half * 64);
-        // diagonal tile: query offsets below kmask (relative to this half) are masked
-        const int kmask = i == kt ? r - half * 64 : -1;
+        const float4* ld4 = reinterpret_cast<const float4*>(ldbuf + st * 256) + half * 32;
         const float2 c2 = make_float2(p.c2, p.c2);
         uint32_t pp[32], pd[32];
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const float2 l2 = lb[c], d2 = db[c];
+        // P^T = 2^(s c2 - lse2) and dS^T = P^T (dP^T - D) for a pair of query columns
+        auto pair = [&](int c, bool zero0, bool zero1) {
+          const float4 w = ld4[c];  // -lse2[q], -lse2[q+1], -D[q], -D[q+1]
           const float2 x = fma2(make_float2(__uint_as_float(sv[2 * c]), __uint_as_float(sv[2 * c + 1])), c2,
-                                make_float2(-l2.x, -l2.y));
+                                make_float2(w.x, w.y));
           float2 pr = make_float2(ex2(x.x), ex2(x.y));
-          if (2 * c < kmask) pr.x = 0.f;
-          if (2 * c + 1 < kmask) pr.y = 0.f;
+          if (zero0) pr.x = 0.f;
+          if (zero1) pr.y = 0.f;
           pp[c] = pack_bf16x2(pr.x, pr.y);
           const float2 t = mul2(pr, add2(make_float2(__uint_as_float(dv[2 * c]), __uint_as_float(dv[2 * c + 1])),
-                                         make_float2(-d2.x, -d2.y)));
+                                         make_float2(w.z, w.w)));
           pd[c] = pack_bf16x2(t.x, t.y);
+        };
+        if (i == kt) {  // diagonal tile: queries before this key (offsets below kmask) are masked
+          const int kmask = r - half * 64;
+#pragma unroll
+          for (int c = 0; c < 32; ++c) pair(c, 2 * c < kmask, 2 * c + 1 < kmask);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) pair(c, false, false);
         }
         // P^T / dS^T are free once the previous dV / dK MMAs have completed
         if (g >= 1 && !warp_wait(b_mm, (uint32_t)(g - 1) & 1u, abort_flag, p.status)) { ok = false; break; }
