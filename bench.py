@@ -58,6 +58,7 @@ def measured_peaks():
 
 GEMM_SOURCES = ["gemm_tc.cu", "tc_ptx.cuh", "common.cuh", "internal.h"]
 TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "gemm_tc_dram_step_124m_b16.md")
+PROF_STEPS = 5  # instrumented eager steps behind the per-kernel and per-GEMM-shape breakdown
 
 
 def gemm_traffic_per_launch():
@@ -326,12 +327,14 @@ def main():
     ms_max = float(t_max.item())
     status = step.sync_status()
 
-    # per-kernel-class timing of one instrumented (uncaptured) step on the same stream
+    # per-kernel-class timing of instrumented (uncaptured) steps on the same stream, per-step means
     step.profile(True)
     with torch.cuda.stream(stream):
-        one_step()
-    prof = step.profile_read()
-    regions = step.profile_regions()
+        for _ in range(PROF_STEPS):
+            one_step()
+    prof = {k: (v[0] // PROF_STEPS, v[1] / PROF_STEPS, v[2] / PROF_STEPS, v[3] / PROF_STEPS)
+            for k, v in step.profile_read().items()}
+    regions = [(c, d, ms / PROF_STEPS, fl / PROF_STEPS, by / PROF_STEPS) for c, d, ms, fl, by in step.profile_regions()]
     step.profile(False)
     shapes = {}
     epi_names = ["store", "bias", "bias+resid", "bias+gelu", "gelu'", "ce", "f32"]
@@ -342,7 +345,7 @@ def main():
         key = f"{Mx}x{Nx}x{Kx} {'MN' if amn else 'K'}{'MN' if bmn else 'K'} {epi_names[epi]}"
         e = shapes.setdefault(key, [0, 0.0, 0.0])
         e[0] += 1; e[1] += rms; e[2] += rfl
-    gemm_shapes = {k: {"calls": v[0], "ms": round(v[1], 4), "tflops": round(v[2] / (v[1] / 1e3) / 1e12, 1)}
+    gemm_shapes = {k: {"calls": v[0] // PROF_STEPS, "ms": round(v[1], 4), "tflops": round(v[2] / (v[1] / 1e3) / 1e12, 1)}
                    for k, v in sorted(shapes.items(), key=lambda kv: -kv[1][1])}
 
     # end to end through the C ABI from pinned host buffers
@@ -409,7 +412,7 @@ def main():
                      "frac": round(gemm_tflops / gemm_peak, 4) if gemm_tflops else None,
                      "peak_source": "MEASURED_PEAKS.json bf16_tflops_sustained (kernel timed inside a long step)",
                      "achieved_source": "sum of 2MNK over the step's GEMM launches / their CUDA-event time, "
-                                        "one instrumented eager step on the bench stream",
+                                        "instrumented eager steps on the bench stream (mean of 5)",
                      "traffic": gemm_traffic_per_launch(),
                      "traffic_source": "ncu dram__bytes_read+write per k_gemm_tc launch, "
                                        "profiles/gemm_tc_dram_step_124m_b16.md (null if the kernel changed)"},

@@ -70,7 +70,7 @@ enum gpt2_tensor {
 /* Kernel classes of the per-region timing (gpt2_profile). */
 enum gpt2_kernel_class {
   GPT2_K_GEMM = 0,      /* every Linear incl. the fused classifier logits (tensor cores) */
-  GPT2_K_SPLITK = 1,    /* fp32 split-K partial reduction of the weight-gradient GEMMs */
+  GPT2_K_SPLITK = 1,    /* fp32 split-K reduction of the many-split weight-gradient GEMMs */
   GPT2_K_ATTN_FWD = 2,  /* fused causal attention forward */
   GPT2_K_ATTN_BWD = 3,  /* rowsum(dO*O) + dK/dV + dQ kernels */
   GPT2_K_LN_FWD = 4,
@@ -241,10 +241,21 @@ int gpt2_encoder_bwd(const int32_t* tok, float* dx0, void* dwte, void* dwpe, int
  * D[m, n] = sum_k A(m, k) B(n, k), A(m, k) = A[m*lda + k] (a_mn = 0) or
  * A[k*lda + m] (a_mn = 1), likewise B(n, k) with b_mn; D bf16 (d_f32 = 0) or
  * fp32 (d_f32 = 1) with leading dimension ldd.  N, lda, ldb, ldd multiples of 8.
- * splits > 1 divides K and needs workspace >= splits*M*N*4 bytes (0 = choose). */
+ * splits > 1 divides K and needs workspace >= splits*M*N*4 bytes (0 = choose).
+ * splits = -1 picks a schedule that adds partial sums inside the kernel where
+ * it pays: stream-K (whole waves of output tiles as usual, the leftover tiles
+ * of a part-empty last wave cut evenly along K over all SMs) for tiles deep in
+ * K, or K splits finished by the last split when there are fewer tiles than
+ * SMs; the sums are added in a fixed order (deterministic).  -2 takes stream-K
+ * whenever the tiles do not fill whole waves.  Both need a 16-byte aligned
+ * workspace of >= gemm_bf16_sk_workspace_bytes() bytes whose contents are zero
+ * before its first use; every completed call leaves it reusable.  Calls that
+ * share a workspace must not run concurrently. */
 int gemm_bf16(const void* A, const void* B, void* D, int M, int N, int K, long long lda,
               long long ldb, long long ldd, int a_mn, int b_mn, int d_f32, int splits,
               void* workspace, size_t workspace_bytes, void* stream);
+/* Workspace bytes of the splits = -1 / -2 schedules on the current device. */
+size_t gemm_bf16_sk_workspace_bytes(void);
 
 /* Test hook for the bounded waits: while on, the GEMM's TMA producer skips its
  * first shared-memory stage, so the MMA thread's wait expires (~2 s) and the

@@ -59,7 +59,13 @@ struct TcParams {
   int load_x;   // the epilogue reads a [M, N] bf16 operand (residual or GELU pre-activation)
   int m_fast;   // tile raster: consecutive tiles walk M (sharing a B tile) instead of N
   int a3d, b3d; // MN-major operand loaded by one 3-D box (all its 64-wide blocks) per stage
+  int sk;              // schedule with in-kernel partial sums: SK_STREAM or SK_SPLIT (see cta_unit)
+  int dp_tiles;        // SK_STREAM: tiles [0, dp_tiles) run whole, one per CTA and wave
+  long long sk_iters;  // SK_STREAM: k blocks of tiles [dp_tiles, mt*nt) end to end, cut evenly over the CTAs
+  float* sk_part;      // BM x BN fp32 partial-sum slots
+  unsigned* sk_flags;  // one ready flag per slot and epilogue warp (zero between launches)
 };
+enum { SK_NONE = 0, SK_STREAM = 1, SK_SPLIT = 2, SK_REDUCE = 3 };  // SK_REDUCE: host-side plan only
 
 int g_poison = 0;
 
@@ -77,6 +83,118 @@ __device__ __forceinline__ void tile_coords(const TcParams& p, int tile, int& m_
     n_t = r % p.nt;
     m_t = r / p.nt;
   }
+}
+
+// One CTA's unit of work: k blocks [kb0, kb1) of tile (m_t, n_t), K split sp.
+// A U_PART unit leaves its fp32 sums in partial-sum slot `slot`.
+enum { U_FULL = 0, U_PART = 1, U_FINISH = 2 };
+struct Unit {
+  int tile, m_t, n_t, sp, kb0, kb1, role, slot;
+};
+
+// First stream-K iteration of CTA c: CTA c owns [sk_lo(c), sk_lo(c + 1)).
+__device__ __forceinline__ long long sk_lo(const TcParams& p, int c) {
+  return p.sk_iters * c / gridDim.x;
+}
+
+// The u-th unit of this CTA; false past its last.
+//   Plain schedule: tiles blockIdx.x, + gridDim.x, ... over (split, M tile, N tile).
+//   SK_SPLIT: the same walk; split s-1 of a tile (U_FINISH) adds the partial
+//   sums that splits 0 .. s-2 (U_PART, slot = their walk index) left for it and
+//   runs the epilogue.  The walk is split-major, so one wave of CTAs covers the
+//   same K range of many tiles and the operands' k blocks are shared in L2.
+//   SK_STREAM: the CTA's share of the stream-K iterations, cut at tile
+//   boundaries into fragments, then its whole tiles.  A fragment that reaches
+//   the end of its tile (U_FINISH) adds the partial sums that lower CTAs left
+//   for that tile and runs the epilogue.  One that does not (U_PART) stores its
+//   fp32 sums in the CTA's slot and raises the CTA's flags; only the share's last
+//   fragment can be one, and it is taken first, so no CTA's U_PART work ever
+//   queues behind a wait on another CTA.
+// In both, a U_FINISH unit waits only on U_PART units, which wait on nothing.
+__device__ __forceinline__ bool cta_unit(const TcParams& p, int u, Unit& w) {
+  int tile;
+  w.slot = blockIdx.x;
+  if (p.sk == SK_STREAM) {
+    const int Kb = p.total_kb;
+    const long long s = sk_lo(p, blockIdx.x), e = sk_lo(p, blockIdx.x + 1);
+    const int nfrag = e > s ? (int)((e - 1) / Kb - s / Kb) + 1 : 0;
+    if (u < nfrag) {
+      const int i = (e % Kb) != 0 ? (u == 0 ? nfrag - 1 : u - 1) : u;
+      const long long t = s / Kb + i;
+      const long long lo = t * Kb > s ? t * Kb : s;
+      const long long hi = (t + 1) * Kb < e ? (t + 1) * Kb : e;
+      w.kb0 = (int)(lo - t * Kb);
+      w.kb1 = (int)(hi - t * Kb);
+      w.role = w.kb1 < Kb ? U_PART : (w.kb0 > 0 ? U_FINISH : U_FULL);
+      tile = p.dp_tiles + (int)t;
+    } else {
+      tile = blockIdx.x + (u - nfrag) * gridDim.x;
+      if (tile >= p.dp_tiles) return false;
+      w.kb0 = 0;
+      w.kb1 = Kb;
+      w.role = U_FULL;
+    }
+    tile_coords(p, tile, w.m_t, w.n_t, w.sp);
+  } else {
+    tile = blockIdx.x + u * gridDim.x;
+    if (tile >= p.mt * p.nt * p.splits) return false;
+    tile_coords(p, tile, w.m_t, w.n_t, w.sp);
+    w.kb0 = w.sp * p.kps;
+    w.kb1 = min(p.total_kb, w.kb0 + p.kps);
+    w.role = U_FULL;
+    if (p.sk == SK_SPLIT) {
+      w.role = w.sp < p.splits - 1 ? U_PART : U_FINISH;
+      w.slot = tile;
+    }
+  }
+  w.tile = tile;
+  return true;
+}
+
+// Stream-K flags and partial sums: gpu-scope release / acquire, L2-only data.
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* f) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_gpu(unsigned* f, unsigned v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(f), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_cg4(float* a, const uint32_t* r) {
+  asm volatile("st.global.cg.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(a), "r"(r[0]), "r"(r[1]), "r"(r[2]),
+               "r"(r[3])
+               : "memory");
+}
+__device__ __forceinline__ float4 ld_cg4(const float* a) {
+  float4 v;
+  asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(a)
+               : "memory");
+  return v;
+}
+// Warp-collective bounded wait for a flag raised by another CTA (false on
+// abort or expiry; expiry latches ST_TIMEOUT).
+__device__ __forceinline__ bool flag_wait(const unsigned* f, int lane, volatile int* abort_flag,
+                                          unsigned* status) {
+  int ok = 1;
+  if (lane == 0 && !ld_acquire_gpu(f)) {
+    const unsigned long long t0 = globaltimer_ns();
+    for (;;) {
+      if (ld_acquire_gpu(f)) break;
+      if (*abort_flag) { ok = 0; break; }
+      if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+        if (status) atomicOr(status, ST_TIMEOUT);
+        *abort_flag = 1;
+        ok = 0;
+        break;
+      }
+      __nanosleep(100);
+    }
+  }
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  if (ok) (void)ld_acquire_gpu(f);  // every lane's later reads are ordered after the flag
+  return ok != 0;
 }
 
 
@@ -175,7 +293,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const GemmArgs& g = p.g;
-  const int ntiles = p.mt * p.nt * p.splits;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
@@ -213,12 +330,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
       for (int i = 0; i < STAGES; ++i) last_par[i] = -1;
       bool first = true;
-      for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-        int m_t, n_t, sp;
-        tile_coords(p, tile, m_t, n_t, sp);
-        const int kb0 = sp * p.kps, kb1 = min(p.total_kb, kb0 + p.kps);
+      Unit w;
+      for (int u = 0; cta_unit(p, u, w); ++u) {
+        const int m_t = w.m_t, n_t = w.n_t;
         bool stop = false;
-        for (int kb = kb0; kb < kb1; ++kb) {
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
           if (!mbar_wait(b_empty + 8 * stage, phase ^ 1, abort_flag, p.status)) { stop = true; break; }
           if (!(p.poison && first)) {
             const uint32_t sa = s_tiles + stage * STAGE_BYTES, sb = sa + A_TILE;
@@ -259,9 +375,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t phase = 0;
       int abuf = 0;
       uint32_t aphase = 0;
-      for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-        const int sp = tile / (p.nt * p.mt);
-        const int kb0 = sp * p.kps, kb1 = min(p.total_kb, kb0 + p.kps);
+      Unit w;
+      for (int u = 0; cta_unit(p, u, w); ++u) {
+        const int kb0 = w.kb0, kb1 = w.kb1;
         if (!mbar_wait(b_tempty + 8 * abuf, aphase ^ 1, abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + abuf * BN;
@@ -296,15 +412,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int bx = 0;                                    // box of the current chunk
     bool prev_stored = false;                      // the previous chunk issued a store
     const int epi = g.epi;
-    const bool split = p.splits > 1;
+    const bool split = p.splits > 1 && p.sk == SK_NONE;  // fp32 partials out, reduced by another kernel
     // chunk c of a tile: rows y = m_t*BM + quad*32 .. +32, columns x = xb + c*CW .. +CW with
-    // xb = n_t*BN + qq*WCOLS; this warp's origin of a tile (xb, y), or y = M past the last tile
-    auto warp_origin = [&](int tile, int& xb, int& y) {
-      if (tile >= ntiles) { xb = 0; y = g.M; return; }
-      int m_t, n_t, sp;
-      tile_coords(p, tile, m_t, n_t, sp);
-      xb = n_t * BN + qq * WCOLS;
-      y = m_t * BM + quad * 32;
+    // xb = n_t*BN + qq*WCOLS; this warp's origin of a unit (xb, y), or y = M when the unit
+    // stores no output (none left, or a stream-K partial)
+    auto warp_origin = [&](bool ok, const Unit& w, int& xb, int& y) {
+      if (!ok || w.role == U_PART) { xb = 0; y = g.M; return; }
+      xb = w.n_t * BN + qq * WCOLS;
+      y = w.m_t * BM + quad * 32;
+    };
+    // this warp's region of CTA j's partial-sum slot: chunk c, lane l, 16 floats as
+    // four float4 at ((c * 4 + q) * 32 + l) * 4
+    auto slot_of = [&](int j) {
+      return p.sk_part + (size_t)j * (BM * BN) + (size_t)ew * (NCHUNK * CW * 32);
     };
     // Prefetch the x operand of the chunk at (x, y) into box b (all lanes track the state).
     auto x_issue = [&](int x, int y, int b) {
@@ -316,18 +436,70 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       xpend |= 1u << b;
     };
-    int nxb, ny;  // origin of the next tile this warp handles
-    warp_origin(blockIdx.x, nxb, ny);
+    Unit nw;
+    bool nok = cta_unit(p, 0, nw);
+    int nxb, ny;  // origin of the next unit this warp handles
+    warp_origin(nok, nw, nxb, ny);
     x_issue(nxb, ny, 0);
     int abuf = 0;
     uint32_t aphase = 0;
-    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-      int m_t, n_t, sp;
-      tile_coords(p, tile, m_t, n_t, sp);
+    for (int u = 0; nok; ++u) {
+      const Unit w = nw;
+      const int m_t = w.m_t, n_t = w.n_t, sp = w.sp;
       const int xb = nxb, y0 = ny;
-      warp_origin(tile + gridDim.x, nxb, ny);
+      nok = cta_unit(p, u + 1, nw);
+      warp_origin(nok, nw, nxb, ny);
       if (!mbar_wait(b_tfull + 8 * abuf, aphase, abort_flag, p.status)) break;
       tc_fence_after();
+      const uint32_t tacc = tmem_base + ((uint32_t)(quad * 32) << 16) + abuf * BN + qq * WCOLS;
+      if (w.role == U_PART) {
+        // stream-K partial: fp32 sums to this CTA's slot, then this warp's flag
+        float* slot = slot_of(w.slot);
+#pragma unroll 1
+        for (int c = 0; c < NCHUNK; ++c) {
+          uint32_t r[16];
+          tmem_ld16(tacc + c * CW, r);
+          tmem_ld_wait();
+          if (c == NCHUNK - 1) {
+            tc_fence_before();
+            mbar_arrive(b_tempty + 8 * abuf);
+          }
+#pragma unroll
+          for (int q = 0; q < 4; ++q) st_cg4(slot + ((c * 4 + q) * 32 + lane) * 4, r + 4 * q);
+        }
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) st_release_gpu(p.sk_flags + w.slot * EPI_WARPS + ew, 1u);
+        x_issue(nxb, ny, bx);  // the next unit's first operand chunk
+        prev_stored = false;
+        if (++abuf == 2) { abuf = 0; aphase ^= 1; }
+        continue;
+      }
+      // finish: the partial sums of this tile sit in slots ps0 + i * pst, i < pn
+      // (SK_STREAM: CTAs [j0, blockIdx.x), skipping CTAs with an empty share;
+      // SK_SPLIT: the walk indices of splits 0 .. s-2); wait for each one's flag,
+      // then add them in that order
+      int ps0 = 0, pn = 0, pst = 1;
+      if (w.role == U_FINISH) {
+        if (p.sk == SK_STREAM) {
+          const long long t0 = (long long)(w.tile - p.dp_tiles) * p.total_kb;
+          int j0 = blockIdx.x;
+          while (j0 > 0 && sk_lo(p, j0) > t0) --j0;
+          ps0 = j0;
+          pn = blockIdx.x - j0;
+        } else {
+          pst = p.mt * p.nt;
+          ps0 = w.tile - (p.splits - 1) * pst;
+          pn = p.splits - 1;
+        }
+        bool ok = true;
+        for (int i = 0; i < pn && ok; ++i) {
+          const int j = ps0 + i * pst;
+          if (p.sk == SK_STREAM && sk_lo(p, j) == sk_lo(p, j + 1)) continue;
+          ok = flag_wait(p.sk_flags + j * EPI_WARPS + ew, lane, abort_flag, p.status);
+        }
+        if (!ok) break;
+      }
       const int m = m_t * BM + quad * 32 + lane;
       const int tgt = (epi == EPI_CE && m < g.M) ? g.targets[m] : -1;
       float ce_m = -INFINITY, ce_s = 0.f, ce_t = 0.f;
@@ -336,11 +508,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int c = 0; c < NCHUNK; ++c) {
         const int b = bx;
         uint32_t r[16];
-        tmem_ld16(tmem_base + ((uint32_t)(quad * 32) << 16) + abuf * BN + qq * WCOLS + c * CW, r);
+        tmem_ld16(tacc + c * CW, r);
         tmem_ld_wait();
         if (c == NCHUNK - 1) {  // every TMEM read of this accumulator is done: hand it back to the MMA
           tc_fence_before();
           mbar_arrive(b_tempty + 8 * abuf);
+        }
+        if (pn) {
+          float acc[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) acc[j] = __uint_as_float(r[j]);
+          for (int i = 0; i < pn; ++i) {
+            const int j = ps0 + i * pst;
+            if (p.sk == SK_STREAM && sk_lo(p, j) == sk_lo(p, j + 1)) continue;
+            const float* slot = slot_of(j);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const float4 t = ld_cg4(slot + ((c * 4 + q) * 32 + lane) * 4);
+              const float2 lo = add2(make_float2(acc[4 * q], acc[4 * q + 1]), make_float2(t.x, t.y));
+              const float2 hi = add2(make_float2(acc[4 * q + 2], acc[4 * q + 3]), make_float2(t.z, t.w));
+              acc[4 * q] = lo.x; acc[4 * q + 1] = lo.y; acc[4 * q + 2] = hi.x; acc[4 * q + 3] = hi.y;
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(acc[j]);
         }
         // prefetch the next chunk's operand into the other box
         if (c < NCHUNK - 1) x_issue(xb + (c + 1) * CW, y0, b ^ 1);
@@ -474,6 +665,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         prev_stored = true;
       }
       if (stop) break;
+      if (pn) {  // the partial sums are consumed: lower the flags for the next launch
+        __syncwarp();
+        if (lane == 0)
+          for (int i = 0; i < pn; ++i) p.sk_flags[(ps0 + i * pst) * EPI_WARPS + ew] = 0u;
+      }
       // one statistics partial per row and WCOLS-column quarter tile that starts inside N
       if (epi == EPI_CE && !split && m < g.M && n_t * BN + qq * WCOLS < g.N) {
         const int part = n_t * (BN / WCOLS) + qq;
@@ -608,6 +804,13 @@ size_t gemm_tc_ws_bytes(int M, int N, int splits) {
   return splits > 1 ? (size_t)splits * M * N * sizeof(float) : 0;
 }
 
+// Partial-sum slots of the in-kernel schedules: three per SM.
+static int sk_slots() { return 3 * num_sms(); }
+static size_t sk_flag_bytes() { return ((size_t)sk_slots() * EPI_WARPS * 4 + 1023) / 1024 * 1024; }
+
+size_t gemm_tc_sk_ws_bytes() { return sk_flag_bytes() + (size_t)sk_slots() * BM * BN * sizeof(float); }
+size_t gemm_tc_sk_plane_offset() { return sk_flag_bytes(); }
+
 int gemm_tc_pick_splits(int M, int N, int K, int sms) {
   const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
   const int total_kb = (K + BK - 1) / BK;
@@ -636,8 +839,46 @@ int gemm_tc_effective_splits(int K, int splits) {
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
+// Schedule for T tiles of Kb k blocks on G SMs (GEMM_TC_STREAM_K):
+//  - T >= G, last wave part-empty by more than 3%, tiles at least 32 k blocks
+//    deep: SK_STREAM over the leftover tiles (whole waves stay data-parallel).
+//    Shallower tiles are epilogue-bound; cutting them adds epilogues, not speed.
+//  - T < G: s = the split count of gemm_tc_pick_splits.  Two splits: SK_SPLIT
+//    (the second split adds the first's sums).  More: the finishing CTAs would
+//    each read s - 1 partial tiles while the rest idle, so the splits write fp32
+//    planes into the slot area and a separate kernel reduces them over all SMs
+//    (SK_REDUCE; plain-store epilogues whose planes fit), else SK_SPLIT.
+// `force` (GEMM_TC_STREAM_K_FORCE) takes SK_STREAM whenever T % G != 0.
+static int sk_plan(const GemmArgs& g, int T, int Kb, int G, bool force, int& dp, int& skt, int& splits) {
+  const int M = g.M, N = g.N, K = g.K;
+  const int rem = T % G;
+  if (force) {
+    if (T >= G && rem == 0) return SK_NONE;
+    dp = T >= G ? T - rem : 0;
+    skt = T >= G ? rem : T;
+    return SK_STREAM;
+  }
+  if (T >= G) {
+    if (rem == 0 || Kb < 32) return SK_NONE;
+    const double eff = (double)T / ((double)(T / G + 1) * G);
+    if (eff >= 0.97) return SK_NONE;
+    dp = T - rem;
+    skt = rem;
+    return SK_STREAM;
+  }
+  const int s = gemm_tc_effective_splits(K, gemm_tc_pick_splits(M, N, K, G));
+  if (s < 2) return SK_NONE;
+  splits = s;
+  if (s > 2 && (g.epi == EPI_STORE || g.epi == EPI_F32) &&
+      gemm_tc_ws_bytes(M, N, s) <= (size_t)sk_slots() * BM * BN * sizeof(float))
+    return SK_REDUCE;
+  if ((long long)(s - 1) * T > sk_slots()) return SK_NONE;
+  return SK_SPLIT;
+}
+
 int gemm_tc(const GemmArgs& g, int splits, void* ws, size_t ws_bytes, unsigned* status,
-            cudaStream_t s, int reduce) {
+            cudaStream_t s, int reduce, int* reduce_splits) {
+  if (reduce_splits) *reduce_splits = 0;
   if (g.M <= 0 || g.N <= 0 || g.K <= 0) return (int)cudaErrorInvalidValue;
   if (g.N % 8 || g.lda % 8 || g.ldb % 8 || g.ldd % 8) return (int)cudaErrorInvalidValue;
   if (!aligned16(g.A) || !aligned16(g.B) || !aligned16(g.D)) return (int)cudaErrorInvalidValue;
@@ -657,18 +898,45 @@ int gemm_tc(const GemmArgs& g, int splits, void* ws, size_t ws_bytes, unsigned* 
   p.mt = (g.M + BM - 1) / BM;
   p.nt = (g.N + BN - 1) / BN;
   p.total_kb = (g.K + BK - 1) / BK;
+  p.sk = 0;
+  p.dp_tiles = 0;
+  p.sk_iters = 0;
+  p.sk_part = nullptr;
+  p.sk_flags = nullptr;
+  if (splits == GEMM_TC_STREAM_K || splits == GEMM_TC_STREAM_K_FORCE) {
+    if (!ws || !aligned16(ws) || ws_bytes < gemm_tc_sk_ws_bytes()) return (int)cudaErrorInvalidValue;
+    int dp = 0, skt = 0, ssplit = 1;
+    const int plan = sk_plan(g, p.mt * p.nt, p.total_kb, num_sms(), splits == GEMM_TC_STREAM_K_FORCE, dp, skt,
+                             ssplit);
+    char* slots = static_cast<char*>(ws) + sk_flag_bytes();
+    if (plan == SK_REDUCE) {  // plain split-K into the slot area
+      ws = slots;
+      ws_bytes = (size_t)sk_slots() * BM * BN * sizeof(float);
+      splits = ssplit;
+      if (reduce_splits && !reduce) *reduce_splits = ssplit;
+    } else {
+      p.sk = plan;
+      if (p.sk != SK_NONE) {
+        p.dp_tiles = dp;
+        p.sk_iters = (long long)skt * p.total_kb;
+        p.sk_flags = static_cast<unsigned*>(ws);
+        p.sk_part = reinterpret_cast<float*>(slots);
+      }
+      splits = p.sk == SK_SPLIT ? ssplit : 1;
+    }
+  }
   if (splits < 1) splits = 1;
   if (splits > p.total_kb) splits = p.total_kb;
   p.kps = (p.total_kb + splits - 1) / splits;
   p.splits = (p.total_kb + p.kps - 1) / p.kps;
-  if (p.splits > 1) {
+  if (p.splits > 1 && p.sk == SK_NONE) {
     if (g.epi != EPI_STORE && g.epi != EPI_F32) return (int)cudaErrorInvalidValue;
     if (!ws || !aligned16(ws) || ws_bytes < gemm_tc_ws_bytes(g.M, g.N, p.splits))
       return (int)cudaErrorInvalidValue;
   }
   p.status = status;
   p.poison = g_poison;
-  p.out_f32 = (p.splits > 1 || g.epi == EPI_F32) ? 1 : 0;
+  p.out_f32 = ((p.splits > 1 && p.sk == SK_NONE) || g.epi == EPI_F32) ? 1 : 0;
   p.load_x = (g.epi == EPI_BIAS_RESID || g.epi == EPI_GELU_BWD) ? 1 : 0;
   p.m_fast = ((double)g.N * g.K > (double)g.M * g.K) ? 1 : 0;
   CUtensorMap tmA, tmB, tmD, tmD2, tmX;
@@ -680,7 +948,7 @@ int gemm_tc(const GemmArgs& g, int splits, void* ws, size_t ws_bytes, unsigned* 
   ok = ok && (p.b3d ? make_tmap_mn3d(&tmB, g.B, g.N, g.K, g.ldb, BN / 64)
                     : g.b_mn ? make_tmap(&tmB, g.B, g.N, g.K, g.ldb, 64, 64)
                              : make_tmap(&tmB, g.B, g.K, g.N, g.ldb, 64, BN));
-  if (p.splits > 1)
+  if (p.splits > 1 && p.sk == SK_NONE)
     ok = ok && make_box_map(&tmD, ws, 1, g.N, g.M, p.splits, g.N);
   else
     ok = ok && make_box_map(&tmD, g.D, p.out_f32, g.N, g.M, 1, g.ldd);
@@ -699,12 +967,12 @@ int gemm_tc(const GemmArgs& g, int splits, void* ws, size_t ws_bytes, unsigned* 
   p.idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)g.a_mn << 15) |
             ((uint32_t)g.b_mn << 16) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
   const int ntiles = p.mt * p.nt * p.splits;
-  int grid = num_sms();
-  if (grid > ntiles) grid = ntiles;
+  int grid = num_sms();  // a stream-K launch spreads its iterations over every SM
+  if (p.sk != SK_STREAM && grid > ntiles) grid = ntiles;
   k_gemm_tc<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(tmA, tmB, tmD, tmD2, tmX, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return (int)e;
-  if (p.splits > 1 && reduce) {
+  if (p.splits > 1 && p.sk == SK_NONE && reduce) {
     splitk_reduce(g.D, g.epi == EPI_F32, g.ldd, static_cast<float*>(ws), p.splits, g.M, g.N, s);
     e = cudaGetLastError();
   }

@@ -78,10 +78,9 @@ struct Plan {
   size_t tokens, targets;
   size_t res, x1, ln1, ln2, ln1_mean, ln1_rstd, ln2_mean, ln2_rstd, qkv, atty, att_lse, fch, fca;
   size_t lnf, lnf_mean, lnf_rstd, logits, ce_max, ce_sum, ce_tgt, ce_lse, ce_rows, scalars, status;
-  size_t dres, dres_b, dbig, dqkv, dsmall, attD, order, lnb_part, colsum_part, norm_part, splitk_ws;
-  size_t splitk_bytes = 0;
+  size_t dres, dres_b, dbig, dqkv, dsmall, attD, order, lnb_part, colsum_part, norm_part, sk_ws;
+  size_t sk_bytes = 0;
   int ce_tiles = 0;
-  int splits_fcp = 1, splits_fc = 1, splits_ap = 1, splits_qkv = 1;
 };
 
 constexpr int kNormParts = 1024;
@@ -141,20 +140,9 @@ Plan make_plan(const Shape& s) {
   size_t cs = colsum_partials_floats(4 * s.C);
   p.colsum_part = take(cur, cs * f);
   p.norm_part = take(cur, kNormParts * f);
-  if (bf) {
-    const int sms = num_sms();
-    p.splits_fcp = gemm_tc_pick_splits(s.C, 4 * s.C, s.M(), sms);
-    p.splits_fc = gemm_tc_pick_splits(4 * s.C, s.C, s.M(), sms);
-    p.splits_ap = gemm_tc_pick_splits(s.C, s.C, s.M(), sms);
-    p.splits_qkv = gemm_tc_pick_splits(3 * s.C, s.C, s.M(), sms);
-    size_t w = 0;
-    w = std::max(w, gemm_tc_ws_bytes(s.C, 4 * s.C, p.splits_fcp));
-    w = std::max(w, gemm_tc_ws_bytes(4 * s.C, s.C, p.splits_fc));
-    w = std::max(w, gemm_tc_ws_bytes(s.C, s.C, p.splits_ap));
-    w = std::max(w, gemm_tc_ws_bytes(3 * s.C, s.C, p.splits_qkv));
-    p.splitk_bytes = w;
-  }
-  p.splitk_ws = take(cur, p.splitk_bytes ? p.splitk_bytes : 256);
+  // stream-K flags (zeroed with the arena) and partial-sum slots of the GEMM engine
+  if (bf) p.sk_bytes = gemm_tc_sk_ws_bytes();
+  p.sk_ws = take(cur, p.sk_bytes ? p.sk_bytes : 256);
   p.total = cur;
   return p;
 }
@@ -245,24 +233,25 @@ struct Ptrs {
   }
 };
 
-// One Linear through the precision's GEMM engine (split-K reduction timed apart).
+// One Linear through the precision's GEMM engine (bf16: stream-K schedule where it pays).
 template <typename T>
-int linear(gpt2* h, GemmArgs g, int splits = 1) {
+int linear(gpt2* h, GemmArgs g) {
   unsigned* status = h->at<unsigned>(h->p.status);
   const double flops = 2.0 * g.M * g.N * (double)g.K;
   const double bytes = ((double)g.M * g.K + (double)g.N * g.K + (double)g.M * g.N) * sizeof(T);
   int e = 0;
   const int dims[6] = {g.M, g.N, g.K, g.a_mn, g.b_mn, g.epi};
   if (sizeof(T) == 2) {
-    const int eff = gemm_tc_effective_splits(g.K, splits);
+    int rs = 0;
     const int pi = prof_begin(h);
-    e = gemm_tc(g, eff, h->at<void>(h->p.splitk_ws), h->p.splitk_bytes, status, h->stream, 0);
+    e = gemm_tc(g, GEMM_TC_STREAM_K, h->at<void>(h->p.sk_ws), h->p.sk_bytes, status, h->stream, 0, &rs);
     prof_end(h, pi, GPT2_K_GEMM, flops, bytes, dims);
     if (e) return e;
-    if (eff > 1)
-      REGION(GPT2_K_SPLITK, 0.0, (double)g.M * g.N * (4.0 * eff + 2.0),
-             splitk_reduce(g.D, g.epi == EPI_F32, g.ldd, h->at<float>(h->p.splitk_ws), eff, g.M, g.N,
-                           h->stream));
+    if (rs > 1)
+      REGION(GPT2_K_SPLITK, 0.0, (double)g.M * g.N * (4.0 * rs + 2.0),
+             splitk_reduce(g.D, g.epi == EPI_F32, g.ldd,
+                           reinterpret_cast<float*>(h->at<char>(h->p.sk_ws) + gemm_tc_sk_plane_offset()), rs,
+                           g.M, g.N, h->stream));
     return (int)cudaGetLastError();
   }
   const int pi = prof_begin(h);
@@ -401,7 +390,7 @@ int backward_impl(gpt2* h) {
     g = GemmArgs();
     g.A = dcur; g.lda = C; g.a_mn = 1; g.B = P.fca(l); g.ldb = 4 * C; g.b_mn = 1;
     g.M = C; g.N = 4 * C; g.K = M; g.D = P.grad(P_FCPW, l); g.ldd = 4 * C;
-    CKI(linear<T>(h, g, h->p.splits_fcp));
+    CKI(linear<T>(h, g));
     // the fcproj bias gradient (column sum of dcur) came out of the previous LayerNorm backward
     g = GemmArgs();
     g.A = dcur; g.lda = C; g.B = P.param(P_FCPW, l); g.ldb = 4 * C; g.b_mn = 1;
@@ -412,7 +401,7 @@ int backward_impl(gpt2* h) {
     g = GemmArgs();
     g.A = dbig; g.lda = 4 * C; g.a_mn = 1; g.B = P.ln2(l); g.ldb = C; g.b_mn = 1;
     g.M = 4 * C; g.N = C; g.K = M; g.D = P.grad(P_FCW, l); g.ldd = C;
-    CKI(linear<T>(h, g, h->p.splits_fc));
+    CKI(linear<T>(h, g));
     REGION(GPT2_K_BIAS_GRAD, 0.0, 4.0 * MC * E, colsum<T>(P.grad(P_FCB, l), dbig, M, 4 * C, 4 * C, csp, st));
     g = GemmArgs();
     g.A = dbig; g.lda = 4 * C; g.B = P.param(P_FCW, l); g.ldb = C; g.b_mn = 1;
@@ -426,7 +415,7 @@ int backward_impl(gpt2* h) {
     g = GemmArgs();
     g.A = dcur; g.lda = C; g.a_mn = 1; g.B = P.atty(l); g.ldb = C; g.b_mn = 1;
     g.M = C; g.N = C; g.K = M; g.D = P.grad(P_APW, l); g.ldd = C;
-    CKI(linear<T>(h, g, h->p.splits_ap));
+    CKI(linear<T>(h, g));
     g = GemmArgs();
     g.A = dcur; g.lda = C; g.B = P.param(P_APW, l); g.ldb = C; g.b_mn = 1;
     g.M = M; g.N = C; g.K = C; g.D = dsmall; g.ldd = C;
@@ -449,7 +438,7 @@ int backward_impl(gpt2* h) {
     g = GemmArgs();
     g.A = dqkv; g.lda = 3 * C; g.a_mn = 1; g.B = P.ln1(l); g.ldb = C; g.b_mn = 1;
     g.M = 3 * C; g.N = C; g.K = M; g.D = P.grad(P_QKVW, l); g.ldd = C;
-    CKI(linear<T>(h, g, h->p.splits_qkv));
+    CKI(linear<T>(h, g));
     REGION(GPT2_K_BIAS_GRAD, 0.0, 3.0 * MC * E, colsum<T>(P.grad(P_QKVB, l), dqkv, M, 3 * C, 3 * C, csp, st));
     g = GemmArgs();
     g.A = dqkv; g.lda = 3 * C; g.B = P.param(P_QKVW, l); g.ldb = C; g.b_mn = 1;
@@ -918,13 +907,20 @@ int gemm_bf16(const void* A, const void* B, void* D, int M, int N, int K, long l
   GemmArgs g;
   g.A = A; g.lda = lda; g.a_mn = a_mn ? 1 : 0; g.B = B; g.ldb = ldb; g.b_mn = b_mn ? 1 : 0;
   g.M = M; g.N = N; g.K = K; g.D = D; g.ldd = ldd; g.epi = d_f32 ? EPI_F32 : EPI_STORE;
-  if (splits <= 0) splits = gemm_tc_pick_splits(M, N, K, num_sms());
-  if (splits > 1 && workspace_bytes < gemm_tc_ws_bytes(M, N, splits)) return GPT2_E_INVAL;
+  if (splits < -2) return GPT2_E_INVAL;
+  if (splits < 0) {
+    if (!al16(workspace) || workspace_bytes < gemm_tc_sk_ws_bytes()) return GPT2_E_INVAL;
+  } else {
+    if (splits == 0) splits = gemm_tc_pick_splits(M, N, K, num_sms());
+    if (splits > 1 && workspace_bytes < gemm_tc_ws_bytes(M, N, splits)) return GPT2_E_INVAL;
+  }
   int e = gemm_tc(g, splits, workspace, workspace_bytes, nullptr, static_cast<cudaStream_t>(stream));
   if (e == (int)cudaErrorInvalidValue) return GPT2_E_INVAL;
   if (e) return cuda_fail((cudaError_t)e, "gemm_bf16");
   return GPT2_OK;
 }
+
+size_t gemm_bf16_sk_workspace_bytes(void) { return gemm_tc_sk_ws_bytes(); }
 
 int gpt2_test_set_gemm_poison(int on) { return gemm_tc_poison(on); }
 

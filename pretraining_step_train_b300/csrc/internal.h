@@ -37,9 +37,27 @@ struct GemmArgs {
 // bf16 operands on tcgen05 tensor cores (TMA -> smem ring -> MMA -> TMEM -> epilogue).
 // `splits` > 1 splits K; partials go to `ws` as fp32 [splits][M][N] and a
 // reduction kernel applies EPI_STORE / EPI_F32 (skipped when reduce == 0; the
-// caller then runs splitk_reduce itself).  Returns 0 or a cudaError_t.
+// caller then runs splitk_reduce itself).
+// `splits` == GEMM_TC_STREAM_K picks a schedule that adds partial sums inside
+// the kernel where it pays (any epilogue): stream-K over the leftover tiles of
+// a part-empty last wave when tiles are deep in K, or K splits finished by the
+// last split when there are fewer tiles than SMs.  The partial sums are added
+// in a fixed order (deterministic).  `ws` (>= gemm_tc_sk_ws_bytes(), 16-byte
+// aligned) holds a flag area that must be zero before the first such call and
+// is left zero by each call that completes, then the fp32 tile slots.  Calls
+// sharing a `ws` must not overlap in time.  GEMM_TC_STREAM_K_FORCE takes
+// stream-K whenever the tiles do not fill whole waves.  Returns 0 or a
+// cudaError_t.
+constexpr int GEMM_TC_STREAM_K = -1;
+constexpr int GEMM_TC_STREAM_K_FORCE = -2;
+// Where that schedule runs plain K splits with a separate reduction (more than
+// two splits of a plain-store GEMM with fewer tiles than SMs) and reduce == 0,
+// *reduce_splits receives the split count and the fp32 planes sit at
+// ws + gemm_tc_sk_plane_offset(); the caller then runs splitk_reduce.
 int gemm_tc(const GemmArgs& g, int splits, void* ws, size_t ws_bytes, unsigned* status,
-            cudaStream_t s, int reduce = 1);
+            cudaStream_t s, int reduce = 1, int* reduce_splits = nullptr);
+size_t gemm_tc_sk_plane_offset();
+size_t gemm_tc_sk_ws_bytes();
 // Splits the call above will actually use for this K (every split non-empty).
 int gemm_tc_effective_splits(int K, int splits);
 size_t gemm_tc_ws_bytes(int M, int N, int splits);

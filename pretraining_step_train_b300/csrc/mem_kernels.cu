@@ -646,7 +646,103 @@ __global__ void __launch_bounds__(1024) k_sort_tokens(uint32_t* __restrict__ ord
   }
 }
 
+// The same sort for M <= 16384 positions and V <= 2^18 ids on 32-bit keys
+// (id << 14 | position), bitonic over 16384 keys held 16 per thread: stages
+// with partners inside a thread run in registers, inside a warp by shuffles,
+// and only the 15 stages whose partners sit in another warp go through shared
+// memory.  Keys are unique, so the result equals the 64-bit sort above.
+constexpr int kSortKeys = 16384, kSortPerThread = 16, kSortPosBits = 14;
+
+__device__ __forceinline__ void cmp_swap(uint32_t& a, uint32_t& b, bool up) {
+  const uint32_t lo = min(a, b), hi = max(a, b);
+  a = up ? lo : hi;
+  b = up ? hi : lo;
+}
+
+// One bitonic stage (merge size K, partner distance J) on this thread's keys.
+template <int K, int J>
+__device__ __forceinline__ void sort_stage(uint32_t (&key)[kSortPerThread], int t, uint32_t* sk) {
+  if constexpr (J < kSortPerThread) {
+    // partner in this thread: element t*16 + r pairs with t*16 + (r ^ J)
+#pragma unroll
+    for (int r = 0; r < kSortPerThread; ++r) {
+      if ((r & J) == 0) {
+        const bool up = (((t * kSortPerThread + r) & K) == 0);
+        cmp_swap(key[r], key[r | J], up);
+      }
+    }
+  } else {
+    constexpr int TJ = J / kSortPerThread;  // partner thread t ^ TJ, same r
+    const bool up = (((t * kSortPerThread) & K) == 0);
+    const bool keep_min = ((t & TJ) == 0) == up;
+    if constexpr (TJ < 32) {
+#pragma unroll
+      for (int r = 0; r < kSortPerThread; ++r) {
+        const uint32_t o = __shfl_xor_sync(0xffffffffu, key[r], TJ);
+        key[r] = keep_min ? min(key[r], o) : max(key[r], o);
+      }
+    } else {
+#pragma unroll
+      for (int r = 0; r < kSortPerThread; ++r) sk[r * 1024 + t] = key[r];
+      __syncthreads();
+#pragma unroll
+      for (int r = 0; r < kSortPerThread; ++r) {
+        const uint32_t o = sk[r * 1024 + (t ^ TJ)];
+        key[r] = keep_min ? min(key[r], o) : max(key[r], o);
+      }
+      __syncthreads();
+    }
+  }
+}
+template <int K, int J>
+__device__ __forceinline__ void sort_merge(uint32_t (&key)[kSortPerThread], int t, uint32_t* sk) {
+  if constexpr (J > 0) {
+    sort_stage<K, J>(key, t, sk);
+    sort_merge<K, J / 2>(key, t, sk);
+  }
+}
+template <int K>
+__device__ __forceinline__ void sort_levels(uint32_t (&key)[kSortPerThread], int t, uint32_t* sk) {
+  if constexpr (K <= kSortKeys) {
+    sort_merge<K, K / 2>(key, t, sk);
+    sort_levels<K * 2>(key, t, sk);
+  }
+}
+
+__global__ void __launch_bounds__(1024) k_sort_tokens32(uint32_t* __restrict__ order,
+                                                        const int32_t* __restrict__ tok, int M, int V) {
+  extern __shared__ uint32_t sk32[];
+  const int t = threadIdx.x;
+  uint32_t key[kSortPerThread];
+#pragma unroll
+  for (int r = 0; r < kSortPerThread; ++r) {
+    const int i = t * kSortPerThread + r;
+    uint32_t k = 0xFFFFFFFFu;
+    if (i < M) {
+      int v = tok[i];
+      v = (v < 0 || v >= V) ? 0 : v;
+      k = ((uint32_t)v << kSortPosBits) | (uint32_t)i;
+    }
+    key[r] = k;
+  }
+  sort_levels<2>(key, t, sk32);
+#pragma unroll
+  for (int r = 0; r < kSortPerThread; ++r) {
+    const int i = t * kSortPerThread + r;
+    if (i < M) {
+      order[i] = key[r] & ((1u << kSortPosBits) - 1u);
+      order[M + i] = key[r] >> kSortPosBits;  // sorted token ids
+    }
+  }
+}
+
 void sort_tokens(uint32_t* order, const int32_t* tok, int M, int V, cudaStream_t s) {
+  if (M <= kSortKeys && V <= (1 << (32 - kSortPosBits))) {
+    const size_t sm = (size_t)kSortKeys * 4;
+    cudaFuncSetAttribute(k_sort_tokens32, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    k_sort_tokens32<<<1, 1024, sm, s>>>(order, tok, M, V);
+    return;
+  }
   int P = 1;
   while (P < M) P <<= 1;
   size_t sm = (size_t)P * 8;

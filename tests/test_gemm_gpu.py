@@ -78,3 +78,64 @@ def test_gemm_deterministic():
                                               1, 1, 1, 0, ws.data_ptr(), ws.numel(), None))
         outs.append(to_np(D))
     np.testing.assert_array_equal(outs[0], outs[1])
+
+
+def _sk_workspace():
+    import torch
+    n = binding.lib().gemm_bf16_sk_workspace_bytes()
+    assert n > 0
+    return torch.zeros(n, dtype=torch.uint8, device="cuda")
+
+
+@pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 1)])
+@pytest.mark.parametrize("M,N,K", [(300, 520, 200), (1024, 768, 768), (640, 264, 4160), (64, 8, 16)])
+def test_gemm_in_kernel_partials(a_mn, b_mn, M, N, K):
+    """The schedules that add partial sums inside the kernel.  -2 forces stream-K
+    whenever the tiles leave a wave partly empty: with fewer tiles than SMs every
+    tile is cut along K over many CTAs (down to one 64-wide k block each, several
+    partial sums per tile, CTAs with no work).  -1 takes K splits with an
+    in-kernel finish on these few-tile shapes (13 splits for K = 4160, 3 for
+    K = 768, none where K is too short to split)."""
+    import torch
+    a, b, As, Bs, lda, ldb = _operands(M * 3 + N + K, M, N, K, a_mn, b_mn)
+    A, B = to_dev(As), to_dev(Bs)
+    ref = a.astype(np.float64) @ b.astype(np.float64).T
+    ws = _sk_workspace()
+    # the workspace is reused: each call leaves its flags lowered
+    for mode, f32 in ((-2, 1), (-2, 0), (-1, 1), (-1, 0), (-2, 1)):
+        D = torch.full((M, N), float("nan"), dtype=torch.float32 if f32 else torch.bfloat16, device="cuda")
+        binding.check(binding.lib().gemm_bf16(A.data_ptr(), B.data_ptr(), D.data_ptr(), M, N, K, lda, ldb, N,
+                                              a_mn, b_mn, f32, mode, ws.data_ptr(), ws.numel(), None))
+        torch.cuda.synchronize()
+        got = to_np(D)
+        assert np.isfinite(got).all()
+        if f32:
+            np.testing.assert_allclose(got, ref, rtol=0, atol=2e-5 * np.sqrt(K) * 4)
+        else:
+            assert rel_l2(got, ref) < 4e-3
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    flags = to_np(ws[:3 * sms * 16 * 4].view(torch.int32))
+    assert not flags.any()
+
+
+@pytest.mark.parametrize("M,N,K,a_mn,b_mn", [
+    (16384, 768, 3072, 0, 1),   # 384 output tiles: two whole waves + 88 tiles cut along K
+    (768, 3072, 16384, 1, 1),   # 72 tiles, two K splits finished in-kernel
+])
+def test_gemm_stream_k_step_shapes(M, N, K, a_mn, b_mn):
+    """The schedule the training step takes (-1) on two of its GEMM shapes: equal to
+    the float64 product within fp32 rounding, and bitwise repeatable."""
+    import torch
+    a, b, As, Bs, lda, ldb = _operands(11, M, N, K, a_mn, b_mn)
+    A, B = to_dev(As), to_dev(Bs)
+    ws = _sk_workspace()
+    outs = []
+    for _ in range(2):
+        D = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        binding.check(binding.lib().gemm_bf16(A.data_ptr(), B.data_ptr(), D.data_ptr(), M, N, K, lda, ldb, N,
+                                              a_mn, b_mn, 1, -1, ws.data_ptr(), ws.numel(), None))
+        outs.append(to_np(D))
+    np.testing.assert_array_equal(outs[0], outs[1])
+    rows = np.random.default_rng(0).choice(M, 256, replace=False)
+    ref = a[rows].astype(np.float64) @ b.astype(np.float64).T
+    np.testing.assert_allclose(outs[0][rows], ref, rtol=0, atol=2e-5 * np.sqrt(K) * 4)
