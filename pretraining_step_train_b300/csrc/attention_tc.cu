@@ -138,6 +138,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
+  pdl_wait();  // the predecessor kernel is complete: global memory and TMEM are ours
   if (warp == 1) {
     tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), AT_TMEM_COLS);
     tmem_relinquish();
@@ -443,6 +444,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
+  pdl_wait();  // the predecessor kernel is complete: global memory and TMEM are ours
   if (warp == 1) {
     tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), AT_TMEM_COLS);
     tmem_relinquish();
@@ -658,6 +660,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
+  pdl_wait();  // the predecessor kernel is complete: global memory and TMEM are ours
   if (warp == 1) {
     tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), AT_TMEM_COLS);
     tmem_relinquish();
@@ -939,7 +942,7 @@ int attn_fwd_tc(const AttnArgs& a, cudaStream_t s) {
     return (int)cudaErrorInvalidValue;
   const long long items = (long long)p.nq * a.B * a.H;
   const int grid = (int)(items < num_sms() ? items : num_sms());
-  k_attn_fwd_tc<<<grid, AT_THREADS, AT_SMEM, s>>>(tq, tk, tv, p);
+  launch_k(k_attn_fwd_tc, grid, AT_THREADS, AT_SMEM, s, tq, tk, tv, p);
   return (int)cudaGetLastError();
 }
 
@@ -975,8 +978,8 @@ int attn_bwd_tc(const AttnArgs& a, cudaStream_t s) {
     return (int)cudaErrorInvalidValue;
   const long long items = (long long)p.nq * a.B * a.H;
   const int grid = (int)(items < num_sms() ? items : num_sms());
-  k_attn_bwd_dkdv_tc<<<grid, BW_THREADS, DK_SMEM, s>>>(tq, tk, tv, tdo, p);
-  k_attn_bwd_dq_tc<<<grid, BW_THREADS, DQ_SMEM, s>>>(tq, tk, tv, tdo, p);
+  launch_k(k_attn_bwd_dkdv_tc, grid, BW_THREADS, DK_SMEM, s, tq, tk, tv, tdo, p);
+  launch_k(k_attn_bwd_dq_tc, grid, BW_THREADS, DQ_SMEM, s, tq, tk, tv, tdo, p);
   return (int)cudaGetLastError();
 }
 

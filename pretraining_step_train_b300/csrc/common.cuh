@@ -1,5 +1,6 @@
 // Device-side helpers shared by the GPT-2 step kernels (sm_103a).
 #pragma once
+#include <utility>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -89,4 +90,31 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// Programmatic dependent launch.  Every kernel of this library is launched by
+// launch_k with programmatic stream serialization allowed: once all CTAs of
+// the previous kernel on the stream have exited, this kernel's CTAs may be
+// scheduled before that grid's completion is processed.  Each kernel waits
+// until its predecessor has completed and its writes are visible (pdl_wait)
+// before it reads or writes global memory or allocates tensor memory.  No
+// kernel triggers its successor early (CTAs that wait while a predecessor
+// still runs took issue slots from it), so only the launch latency overlaps.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_begin() { pdl_wait(); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                            Args&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }

@@ -11,6 +11,7 @@ namespace gpt2k {
 constexpr int SB_M = 64, SB_N = 64, SB_K = 16;
 
 __global__ void __launch_bounds__(256) k_gemm_simt(GemmArgs g) {
+  pdl_begin();
   __shared__ float As[SB_K][SB_M + 4];
   __shared__ float Bs[SB_K][SB_N + 4];
   const float* A = static_cast<const float*>(g.A);
@@ -84,7 +85,7 @@ __global__ void __launch_bounds__(256) k_gemm_simt(GemmArgs g) {
 int gemm_simt(const GemmArgs& g, cudaStream_t s) {
   if (g.epi == EPI_CE) return (int)cudaErrorInvalidValue;
   dim3 grid((g.N + SB_N - 1) / SB_N, (g.M + SB_M - 1) / SB_M);
-  k_gemm_simt<<<grid, 256, 0, s>>>(g);
+  launch_k(k_gemm_simt, grid, 256, 0, s, g);
   return (int)cudaGetLastError();
 }
 

@@ -312,6 +312,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmD)) : "memory");
   }
+  pdl_wait();  // the predecessor kernel is complete: global memory and TMEM are ours
   if (warp == 1) {
     tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), TMEM_COLS);
     tmem_relinquish();
@@ -969,7 +970,7 @@ int gemm_tc(const GemmArgs& g, int splits, void* ws, size_t ws_bytes, unsigned* 
   const int ntiles = p.mt * p.nt * p.splits;
   int grid = num_sms();  // a stream-K launch spreads its iterations over every SM
   if (p.sk != SK_STREAM && grid > ntiles) grid = ntiles;
-  k_gemm_tc<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(tmA, tmB, tmD, tmD2, tmX, p);
+  launch_k(k_gemm_tc, grid, NUM_THREADS, SMEM_BYTES, s, tmA, tmB, tmD, tmD2, tmX, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return (int)e;
   if (p.splits > 1 && p.sk == SK_NONE && reduce) {

@@ -26,6 +26,7 @@ template <typename T>
 __global__ void k_encoder_fwd(T* __restrict__ x0, const int32_t* __restrict__ tok,
                               const T* __restrict__ wte, const T* __restrict__ wpe, int M, int Tn,
                               int C, int V, unsigned* status) {
+  pdl_begin();
   constexpr int N = V16<T>::N;
   const int cv = C / N;
   const long long nvec = (long long)M * cv;
@@ -51,11 +52,12 @@ template <typename T>
 void encoder_fwd(T* x0, const int32_t* tok, const T* wte, const T* wpe, int B, int Tn, int C, int V,
                  unsigned* status, cudaStream_t s) {
   long long nvec = (long long)B * Tn * C / V16<T>::N;
-  k_encoder_fwd<T><<<grid_for(nvec, 256), 256, 0, s>>>(x0, tok, wte, wpe, B * Tn, Tn, C, V, status);
+  launch_k(k_encoder_fwd<T>, grid_for(nvec, 256), 256, 0, s, x0, tok, wte, wpe, B * Tn, Tn, C, V, status);
 }
 
 // Clamp ids outside [0, V) to 0 in place and latch ST_TOKEN.
 __global__ void k_check_ids(int32_t* __restrict__ ids, int n, int V, unsigned* status) {
+  pdl_begin();
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
     int t = ids[i];
     if (t < 0 || t >= V) {
@@ -65,7 +67,7 @@ __global__ void k_check_ids(int32_t* __restrict__ ids, int n, int V, unsigned* s
   }
 }
 void check_ids(int32_t* ids, int n, int V, unsigned* status, cudaStream_t s) {
-  k_check_ids<<<grid_for(n, 256, 148), 256, 0, s>>>(ids, n, V, status);
+  launch_k(k_check_ids, grid_for(n, 256, 148), 256, 0, s, ids, n, V, status);
 }
 
 // ------------------------------------------------------------------ LayerNorm forward
@@ -93,6 +95,7 @@ __global__ void __launch_bounds__(256) k_layernorm_fwd(T* __restrict__ y, float*
                                                        float* __restrict__ rstd, const T* __restrict__ x,
                                                        const T* __restrict__ w, const T* __restrict__ b,
                                                        int M, int C) {
+  pdl_begin();
   constexpr int N = V16<T>::N;
   const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
@@ -159,11 +162,11 @@ void layernorm_fwd(T* y, float* mean, float* rstd, const T* x, const T* w, const
   const int per = (nv + 31) / 32;
   const int block = 256;
   const int grid = (M * 32 + block - 1) / block;
-  if (per <= 1) k_layernorm_fwd<T, 1><<<grid, block, 0, s>>>(y, mean, rstd, x, w, b, M, C);
-  else if (per <= 2) k_layernorm_fwd<T, 2><<<grid, block, 0, s>>>(y, mean, rstd, x, w, b, M, C);
-  else if (per <= 3) k_layernorm_fwd<T, 3><<<grid, block, 0, s>>>(y, mean, rstd, x, w, b, M, C);
-  else if (per <= 4) k_layernorm_fwd<T, 4><<<grid, block, 0, s>>>(y, mean, rstd, x, w, b, M, C);
-  else k_layernorm_fwd<T, 8><<<grid, block, 0, s>>>(y, mean, rstd, x, w, b, M, C);
+  if (per <= 1) launch_k(k_layernorm_fwd<T, 1>, grid, block, 0, s, y, mean, rstd, x, w, b, M, C);
+  else if (per <= 2) launch_k(k_layernorm_fwd<T, 2>, grid, block, 0, s, y, mean, rstd, x, w, b, M, C);
+  else if (per <= 3) launch_k(k_layernorm_fwd<T, 3>, grid, block, 0, s, y, mean, rstd, x, w, b, M, C);
+  else if (per <= 4) launch_k(k_layernorm_fwd<T, 4>, grid, block, 0, s, y, mean, rstd, x, w, b, M, C);
+  else launch_k(k_layernorm_fwd<T, 8>, grid, block, 0, s, y, mean, rstd, x, w, b, M, C);
 }
 
 // ------------------------------------------------------------------ fixed-order partial sums
@@ -176,6 +179,7 @@ template <typename T>
 __global__ void __launch_bounds__(1024)
     k_reduce_parts(T* __restrict__ o0, T* __restrict__ o1, T* __restrict__ o2,
                    const float* __restrict__ partials, int nparts, int width, int seg) {
+  pdl_begin();
   __shared__ float sh[32][33];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x * 32 + lane;
@@ -205,7 +209,7 @@ __global__ void __launch_bounds__(1024)
 template <typename T>
 static void reduce_parts(T* o0, T* o1, T* o2, const float* partials, int nparts, int width, int seg,
                          cudaStream_t s) {
-  k_reduce_parts<T><<<(width + 31) / 32, 1024, 0, s>>>(o0, o1, o2, partials, nparts, width, seg);
+  launch_k(k_reduce_parts<T>, (width + 31) / 32, 1024, 0, s, o0, o1, o2, partials, nparts, width, seg);
 }
 
 // ------------------------------------------------------------------ LayerNorm backward
@@ -230,6 +234,7 @@ __global__ void __launch_bounds__(kLnbWarps * 32)
                     const float* __restrict__ rstd, const T* __restrict__ w,
                     float* __restrict__ partials, int M, int C, int accumulate, int want_sum,
                     int rows_per_block) {
+  pdl_begin();
   constexpr int N = V16<T>::N;
   extern __shared__ float sacc[];  // [kLnbWarps][3][C]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -344,7 +349,7 @@ void layernorm_bwd(float* dres, T* dres_b, const T* dy, const T* x, const float*
     if (sm > 48 * 1024)                                                                           \
       cudaFuncSetAttribute(k_layernorm_bwd<T, P>, cudaFuncAttributeMaxDynamicSharedMemorySize,    \
                            (int)sm);                                                              \
-    k_layernorm_bwd<T, P><<<nblocks, kLnbWarps * 32, sm, s>>>(dres, dres_b, dy, x, mean, rstd, w, \
+    launch_k(k_layernorm_bwd<T, P>, nblocks, kLnbWarps * 32, sm, s, dres, dres_b, dy, x, mean, rstd, w, \
                                                               partials, M, C, accumulate,         \
                                                               want_sum, rpb);                     \
   } while (0)
@@ -364,6 +369,7 @@ template <typename T>
 __global__ void __launch_bounds__(256)
     k_colsum_partial(float* __restrict__ partials, const T* __restrict__ x, int M, int N,
                      long long ld, int rows_per_block) {
+  pdl_begin();
   constexpr int NV = V16<T>::N;
   __shared__ float sred[8][32 * NV];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -412,13 +418,14 @@ void colsum(T* out, const T* x, int M, int N, long long ld, float* partials, cud
   if (nrb > kColsumRowBlocks) nrb = kColsumRowBlocks;
   const int rpb = (M + nrb - 1) / nrb;
   dim3 grid((N + 32 * NV - 1) / (32 * NV), nrb);
-  k_colsum_partial<T><<<grid, 256, 0, s>>>(partials, x, M, N, ld, rpb);
+  launch_k(k_colsum_partial<T>, grid, 256, 0, s, partials, x, M, N, ld, rpb);
   reduce_parts<T>(out, (T*)nullptr, (T*)nullptr, partials, nrb, N, N, s);
 }
 
 // ------------------------------------------------------------------ elementwise
 template <typename T>
 __global__ void k_gelu_fwd(T* __restrict__ y, const T* __restrict__ x, long long n) {
+  pdl_begin();
   constexpr int N = V16<T>::N;
   for (long long i = (blockIdx.x * (long long)blockDim.x + threadIdx.x) * N; i < n;
        i += (long long)gridDim.x * blockDim.x * N) {
@@ -432,6 +439,7 @@ __global__ void k_gelu_fwd(T* __restrict__ y, const T* __restrict__ x, long long
 template <typename T>
 __global__ void k_gelu_bwd(T* __restrict__ dx, const T* __restrict__ dy, const T* __restrict__ x,
                            long long n) {
+  pdl_begin();
   constexpr int N = V16<T>::N;
   for (long long i = (blockIdx.x * (long long)blockDim.x + threadIdx.x) * N; i < n;
        i += (long long)gridDim.x * blockDim.x * N) {
@@ -446,6 +454,7 @@ __global__ void k_gelu_bwd(T* __restrict__ dx, const T* __restrict__ dy, const T
 template <typename T>
 __global__ void k_residual(T* __restrict__ y, const T* __restrict__ a, const T* __restrict__ b,
                            long long n) {
+  pdl_begin();
   constexpr int N = V16<T>::N;
   for (long long i = (blockIdx.x * (long long)blockDim.x + threadIdx.x) * N; i < n;
        i += (long long)gridDim.x * blockDim.x * N) {
@@ -459,31 +468,33 @@ __global__ void k_residual(T* __restrict__ y, const T* __restrict__ a, const T* 
 }
 template <typename T>
 __global__ void k_to_storage(T* __restrict__ dst, const float* __restrict__ src, long long n) {
+  pdl_begin();
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
        i += (long long)gridDim.x * blockDim.x)
     dst[i] = from_f<T>(src[i]);
 }
 template <typename T>
 __global__ void k_to_f32(float* __restrict__ dst, const T* __restrict__ src, long long n) {
+  pdl_begin();
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
        i += (long long)gridDim.x * blockDim.x)
     dst[i] = to_f(src[i]);
 }
 
 template <typename T> void gelu_fwd(T* y, const T* x, long long n, cudaStream_t s) {
-  k_gelu_fwd<T><<<grid_for(n / V16<T>::N, 256), 256, 0, s>>>(y, x, n);
+  launch_k(k_gelu_fwd<T>, grid_for(n / V16<T>::N, 256), 256, 0, s, y, x, n);
 }
 template <typename T> void gelu_bwd(T* dx, const T* dy, const T* x, long long n, cudaStream_t s) {
-  k_gelu_bwd<T><<<grid_for(n / V16<T>::N, 256), 256, 0, s>>>(dx, dy, x, n);
+  launch_k(k_gelu_bwd<T>, grid_for(n / V16<T>::N, 256), 256, 0, s, dx, dy, x, n);
 }
 template <typename T> void residual_add(T* y, const T* a, const T* b, long long n, cudaStream_t s) {
-  k_residual<T><<<grid_for(n / V16<T>::N, 256), 256, 0, s>>>(y, a, b, n);
+  launch_k(k_residual<T>, grid_for(n / V16<T>::N, 256), 256, 0, s, y, a, b, n);
 }
 template <typename T> void to_storage(T* dst, const float* src, long long n, cudaStream_t s) {
-  k_to_storage<T><<<grid_for(n, 256), 256, 0, s>>>(dst, src, n);
+  launch_k(k_to_storage<T>, grid_for(n, 256), 256, 0, s, dst, src, n);
 }
 template <typename T> void to_f32(float* dst, const T* src, long long n, cudaStream_t s) {
-  k_to_f32<T><<<grid_for(n, 256), 256, 0, s>>>(dst, src, n);
+  launch_k(k_to_f32<T>, grid_for(n, 256), 256, 0, s, dst, src, n);
 }
 
 // ------------------------------------------------------------------ cross-entropy
@@ -502,6 +513,7 @@ __device__ __forceinline__ float block_reduce(float v, float* sh, bool is_max) {
 template <typename T>
 __global__ void k_ce_rowstats(const T* __restrict__ z, long long ldz, const int32_t* __restrict__ tgt,
                               int V, float* __restrict__ lse, float* __restrict__ loss_rows) {
+  pdl_begin();
   __shared__ float sh[32];
   const int r = blockIdx.x;
   const T* zr = z + (long long)r * ldz;
@@ -522,13 +534,14 @@ __global__ void k_ce_rowstats(const T* __restrict__ z, long long ldz, const int3
 template <typename T>
 void ce_rowstats(const T* z, long long ldz, const int32_t* tgt, int M, int V, float* lse,
                  float* loss_rows, cudaStream_t s) {
-  k_ce_rowstats<T><<<M, 256, 0, s>>>(z, ldz, tgt, V, lse, loss_rows);
+  launch_k(k_ce_rowstats<T>, M, 256, 0, s, z, ldz, tgt, V, lse, loss_rows);
 }
 
 // One warp per row: combine per-tile (max, sum exp) partials into lse.
 __global__ void k_ce_reduce_partials(const float* __restrict__ pmax, const float* __restrict__ psum,
                                      int ntiles, int ld, const float* __restrict__ ztgt, int M,
                                      float* __restrict__ lse, float* __restrict__ loss_rows) {
+  pdl_begin();
   const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (row >= M) return;
   const float* pm = pmax + (long long)row * ld;
@@ -550,7 +563,7 @@ __global__ void k_ce_reduce_partials(const float* __restrict__ pmax, const float
 }
 void ce_reduce_partials(const float* pmax, const float* psum, int ntiles, int ld, const float* ztgt,
                         int M, float* lse, float* loss_rows, cudaStream_t s) {
-  k_ce_reduce_partials<<<(M * 32 + 255) / 256, 256, 0, s>>>(pmax, psum, ntiles, ld, ztgt, M, lse,
+  launch_k(k_ce_reduce_partials, (M * 32 + 255) / 256, 256, 0, s, pmax, psum, ntiles, ld, ztgt, M, lse,
                                                            loss_rows);
 }
 
@@ -559,6 +572,7 @@ template <typename T>
 __global__ void __launch_bounds__(256)
     k_ce_dlogits(T* __restrict__ z, long long ldz, const float* __restrict__ lse,
                  const int32_t* __restrict__ tgt, int V, int Vpad, float inv_scale) {
+  pdl_begin();
   constexpr int N = V16<T>::N;
   const int r = blockIdx.x;
   T* zr = z + (long long)r * ldz;
@@ -581,11 +595,12 @@ __global__ void __launch_bounds__(256)
 template <typename T>
 void ce_dlogits(T* z, long long ldz, const float* lse, const int32_t* tgt, int M, int V, int Vpad,
                 float inv_scale, cudaStream_t s) {
-  k_ce_dlogits<T><<<M, 256, 0, s>>>(z, ldz, lse, tgt, V, Vpad, inv_scale);
+  launch_k(k_ce_dlogits<T>, M, 256, 0, s, z, ldz, lse, tgt, V, Vpad, inv_scale);
 }
 
 // Mean of M per-row values in a fixed order; flags a non-finite result.
 __global__ void k_mean_reduce(float* out, const float* __restrict__ rows, int M, unsigned* status) {
+  pdl_begin();
   __shared__ double sh[32];
   double s = 0.0;
   for (int i = threadIdx.x; i < M; i += blockDim.x) s += (double)rows[i];
@@ -603,7 +618,7 @@ __global__ void k_mean_reduce(float* out, const float* __restrict__ rows, int M,
   }
 }
 void mean_reduce(float* out, const float* rows, int M, unsigned* status, cudaStream_t s) {
-  k_mean_reduce<<<1, 1024, 0, s>>>(out, rows, M, status);
+  launch_k(k_mean_reduce, 1, 1024, 0, s, out, rows, M, status);
 }
 
 // ------------------------------------------------------------------ encoder backward
@@ -613,6 +628,7 @@ void mean_reduce(float* out, const float* rows, int M, unsigned* status, cudaStr
 __global__ void __launch_bounds__(1024) k_sort_tokens(uint32_t* __restrict__ order,
                                                       const int32_t* __restrict__ tok, int M, int V,
                                                       int P) {
+  pdl_begin();
   extern __shared__ unsigned long long keys[];
   for (int i = threadIdx.x; i < P; i += blockDim.x) {
     unsigned long long k = ~0ull;
@@ -711,6 +727,7 @@ __device__ __forceinline__ void sort_levels(uint32_t (&key)[kSortPerThread], int
 
 __global__ void __launch_bounds__(1024) k_sort_tokens32(uint32_t* __restrict__ order,
                                                         const int32_t* __restrict__ tok, int M, int V) {
+  pdl_begin();
   extern __shared__ uint32_t sk32[];
   const int t = threadIdx.x;
   uint32_t key[kSortPerThread];
@@ -740,14 +757,14 @@ void sort_tokens(uint32_t* order, const int32_t* tok, int M, int V, cudaStream_t
   if (M <= kSortKeys && V <= (1 << (32 - kSortPosBits))) {
     const size_t sm = (size_t)kSortKeys * 4;
     cudaFuncSetAttribute(k_sort_tokens32, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    k_sort_tokens32<<<1, 1024, sm, s>>>(order, tok, M, V);
+    launch_k(k_sort_tokens32, 1, 1024, sm, s, order, tok, M, V);
     return;
   }
   int P = 1;
   while (P < M) P <<= 1;
   size_t sm = (size_t)P * 8;
   cudaFuncSetAttribute(k_sort_tokens, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-  k_sort_tokens<<<1, 1024, sm, s>>>(order, tok, M, V, P);
+  launch_k(k_sort_tokens, 1, 1024, sm, s, order, tok, M, V, P);
 }
 
 // Fixed summation order of the tied-embedding scatter: the positions holding
@@ -782,6 +799,7 @@ template <typename T>
 __global__ void __launch_bounds__(256)
     k_encoder_bwd_runs(T* __restrict__ dwte, float* __restrict__ dx0, const uint32_t* __restrict__ order,
                        int M, int C) {
+  pdl_begin();
   const int p = blockIdx.x;
   const uint32_t* stok = order + M;
   int s, e;
@@ -824,6 +842,7 @@ template <typename T>
 __global__ void __launch_bounds__(256)
     k_encoder_bwd_combine(T* __restrict__ dwte, const float* __restrict__ dx0,
                           const uint32_t* __restrict__ order, int M, int C) {
+  pdl_begin();
   const int p = blockIdx.x;
   const uint32_t* stok = order + M;
   const uint32_t v = stok[p];
@@ -849,6 +868,7 @@ __global__ void __launch_bounds__(256)
 template <typename T>
 __global__ void k_encoder_bwd_wpe(T* __restrict__ dwpe, const float* __restrict__ dx0, int B, int Tn,
                                   int C) {
+  pdl_begin();
   long long n = (long long)Tn * C;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
        i += (long long)gridDim.x * blockDim.x) {
@@ -866,14 +886,15 @@ void encoder_bwd(T* dwte, T* dwpe, float* dx0, const uint32_t* order, const int3
   if (threads > 256) threads = 256;
   if (threads < 32) threads = 32;
   // dwpe first: the run kernel overwrites some dx0 rows with run sums
-  k_encoder_bwd_wpe<T><<<grid_for((long long)Tn * C, 256), 256, 0, s>>>(dwpe, dx0, B, Tn, C);
-  k_encoder_bwd_runs<T><<<M, threads, 0, s>>>(dwte, dx0, order, M, C);
-  k_encoder_bwd_combine<T><<<M, threads, 0, s>>>(dwte, dx0, order, M, C);
+  launch_k(k_encoder_bwd_wpe<T>, grid_for((long long)Tn * C, 256), 256, 0, s, dwpe, dx0, B, Tn, C);
+  launch_k(k_encoder_bwd_runs<T>, M, threads, 0, s, dwte, dx0, order, M, C);
+  launch_k(k_encoder_bwd_combine<T>, M, threads, 0, s, dwte, dx0, order, M, C);
 }
 
 // ------------------------------------------------------------------ split-K reduction
 __global__ void k_splitk_reduce(void* __restrict__ out, int out_f32, long long ldo,
                                 const float* __restrict__ ws, int splits, int M, int N) {
+  pdl_begin();
   const long long nq = (long long)M * N / 4;
   const long long plane = (long long)M * N;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < nq;
@@ -899,7 +920,7 @@ __global__ void k_splitk_reduce(void* __restrict__ out, int out_f32, long long l
 }
 void splitk_reduce(void* out, int out_f32, long long ldo, const float* ws, int splits, int M, int N,
                    cudaStream_t s) {
-  k_splitk_reduce<<<grid_for((long long)M * N / 4, 256), 256, 0, s>>>(out, out_f32, ldo, ws, splits,
+  launch_k(k_splitk_reduce, grid_for((long long)M * N / 4, 256), 256, 0, s, out, out_f32, ldo, ws, splits,
                                                                      M, N);
 }
 
@@ -907,6 +928,7 @@ void splitk_reduce(void* out, int out_f32, long long ldo, const float* ws, int s
 template <typename G>
 __global__ void __launch_bounds__(512)
     k_sumsq(float* __restrict__ partials, const G* __restrict__ g, long long n, long long chunk) {
+  pdl_begin();
   constexpr int N = V16<G>::N;
   __shared__ float sh[32];
   const long long b0 = blockIdx.x * chunk;
@@ -926,7 +948,7 @@ void grad_sumsq_partials(float* partials, int nparts, const G* g, long long n, c
   constexpr int N = V16<G>::N;
   long long chunk = (n + nparts - 1) / nparts;
   chunk = (chunk + N - 1) / N * N;
-  k_sumsq<G><<<nparts, 512, 0, s>>>(partials, g, n, chunk);
+  launch_k(k_sumsq<G>, nparts, 512, 0, s, partials, g, n, chunk);
 }
 
 // norm_scale[0] = ||g||, [1] = clip scale, [2] = 1 - b1^t, [3] = 1 - b2^t where
@@ -934,6 +956,7 @@ void grad_sumsq_partials(float* partials, int nparts, const G* g, long long n, c
 __global__ void k_norm_finalize(float* norm_scale, const float* __restrict__ partials, int nparts,
                                 float max_norm, unsigned* status, int* counter, int host_t,
                                 float b1, float b2) {
+  pdl_begin();
   __shared__ double sh[32];
   double s = 0.0;
   for (int i = threadIdx.x; i < nparts; i += blockDim.x) s += (double)partials[i];
@@ -957,7 +980,7 @@ __global__ void k_norm_finalize(float* norm_scale, const float* __restrict__ par
 void grad_norm_finalize(float* norm_scale, const float* partials, int nparts, float max_norm,
                         unsigned* status, int* counter, int host_t, float b1, float b2,
                         cudaStream_t s) {
-  k_norm_finalize<<<1, 1024, 0, s>>>(norm_scale, partials, nparts, max_norm, status, counter,
+  launch_k(k_norm_finalize, 1, 1024, 0, s, norm_scale, partials, nparts, max_norm, status, counter,
                                      host_t, b1, b2);
 }
 
@@ -997,6 +1020,7 @@ __global__ void __launch_bounds__(256)
             float* __restrict__ m, float* __restrict__ v, long long n, SegTable segs,
             const float* __restrict__ norm_scale, float lr, float b1, float b2, float eps,
             float wd) {
+  pdl_begin();
   const float sc = norm_scale[1], bc1 = norm_scale[2], bc2 = norm_scale[3];
   const long long n4 = n / 4;
   for (long long q = blockIdx.x * (long long)blockDim.x + threadIdx.x; q < n4;
@@ -1033,7 +1057,7 @@ void adamw(float* master, P* param_copy, const G* grad, float* m, float* v, long
   SegTable t;
   t.n = nsegs;
   for (int i = 0; i < nsegs && i < kMaxSegments; ++i) t.s[i] = segs[i];
-  k_adamw<G, P><<<grid_for(n / 4, 256, 148 * 8), 256, 0, s>>>(master, param_copy, grad, m, v, n, t,
+  launch_k(k_adamw<G, P>, grid_for(n / 4, 256, 148 * 8), 256, 0, s, master, param_copy, grad, m, v, n, t,
                                                              norm_scale, lr, beta1, beta2, eps, wd);
 }
 
