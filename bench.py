@@ -418,8 +418,11 @@ def main():
                                        "profiles/gemm_tc_dram_step_124m_b16.md (null if the kernel changed)"},
         "kernels": kernels,
         "gemm_shapes": gemm_shapes,
-        "e2e": {"value": round(world * M / e2e_s, 1), "unit": "tokens/s", "h2d_bytes_per_step": 2 * M * 4,
-                "d2h_bytes_per_step": 8, "path": "gpt2_train_step_host, pinned host tokens, eager launches"},
+        "e2e": {"value": round(world * M / e2e_s, 1), "unit": "tokens/s", "h2d_bytes_per_step": 2 * M * 4 + 32,
+                "d2h_bytes_per_step": 12,
+                "path": "gpt2_train_step_host from pinned host tokens: the library copies them into its pinned "
+                        "staging and replays its CUDA graph of the step (tokens, targets, hyperparameters in; "
+                        "loss, norm, status out)"},
         "gpu_launches": (n_kernels * args.steps) if n_kernels else None,
         "kernels_per_step": n_kernels,
         "clocks": clk,

@@ -132,10 +132,15 @@ int gpt2_backward(gpt2_t* h);
 int gpt2_clip_adamw(gpt2_t* h, float lr, float beta1, float beta2, float eps, float weight_decay,
                     float max_norm, int step_t, float* h_norm);
 
-/* One whole step from host buffers: copies h_tokens / h_targets (int32 [B, T],
- * preferably pinned) to the device, runs forward, backward, clip + AdamW, and
- * copies the loss and gradient norm back (h_loss / h_norm may be NULL).
- * Synchronises the stream. */
+/* One whole step from host buffers: copies h_tokens / h_targets (int32 [B, T])
+ * to the device, runs forward, backward, clip + AdamW, and copies the loss and
+ * gradient norm back (h_loss / h_norm may be NULL).  Synchronises the stream.
+ * The first call captures the step as one CUDA graph (on a private stream, with
+ * pinned staging buffers for tokens, targets, hyperparameters and the results)
+ * and every call replays it on the handle's stream, so the arguments may change
+ * from call to call; while gpt2_profile is on the step runs eagerly instead.
+ * Returns GPT2_E_TOKEN / GPT2_E_TIMEOUT / GPT2_E_NONFINITE for this step's
+ * status bits (which it clears). */
 int gpt2_train_step_host(gpt2_t* h, const int32_t* h_tokens, const int32_t* h_targets, float lr,
                          float beta1, float beta2, float eps, float weight_decay, float max_norm,
                          int step_t, float* h_loss, float* h_norm);

@@ -11,6 +11,7 @@
 
 #include <algorithm>
 #include <string>
+#include <cstring>
 #include <vector>
 
 #include "common.cuh"
@@ -77,7 +78,7 @@ struct Plan {
   size_t params, grads, master, adam_m, adam_v;
   size_t tokens, targets;
   size_t res, x1, ln1, ln2, ln1_mean, ln1_rstd, ln2_mean, ln2_rstd, qkv, atty, att_lse, fch, fca;
-  size_t lnf, lnf_mean, lnf_rstd, logits, ce_max, ce_sum, ce_tgt, ce_lse, ce_rows, scalars, status;
+  size_t lnf, lnf_mean, lnf_rstd, logits, ce_max, ce_sum, ce_tgt, ce_lse, ce_rows, scalars, status, hyper;
   size_t dres, dres_b, dbig, dqkv, dsmall, attD, order, lnb_part, colsum_part, norm_part, sk_ws;
   size_t sk_bytes = 0;
   int ce_tiles = 0;
@@ -129,6 +130,7 @@ Plan make_plan(const Shape& s) {
   p.ce_rows = take(cur, M * f);
   p.scalars = take(cur, 16 * f);  // [0] loss, [1] norm, [2] clip scale
   p.status = take(cur, 16);
+  p.hyper = take(cur, sizeof(OptHyper));
   p.dres = take(cur, M * C * f);
   p.dres_b = bf ? take(cur, M * C * e) : p.dres;
   p.dbig = take(cur, M * 4 * C * e);
@@ -179,6 +181,15 @@ struct gpt2 {
   std::vector<cudaEvent_t> evpool;
   int evnext = 0;
   std::vector<ProfRec> recs;
+  // gpt2_train_step_host: the whole step as one CUDA graph, captured on the first
+  // call, fed from pinned staging buffers (tokens, targets, hyperparameters) and
+  // writing loss, norm and status bits back to pinned memory
+  cudaGraphExec_t host_exec = nullptr;
+  cudaStream_t cap_stream = nullptr;
+  int32_t* pin_tok = nullptr;
+  int32_t* pin_tgt = nullptr;
+  OptHyper* pin_hyp = nullptr;
+  float* pin_out = nullptr;  // [0] loss, [1] norm, [2] status bits
   template <typename T> T* at(size_t off) const { return reinterpret_cast<T*>(base + off); }
 };
 
@@ -463,7 +474,7 @@ int backward_impl(gpt2* h) {
 
 template <typename T>
 int clip_adamw_impl(gpt2* h, float lr, float b1, float b2, float eps, float wd, float max_norm,
-                    int t) {
+                    int t, const OptHyper* hp = nullptr) {
   cudaStream_t st = h->stream;
   float* ns = h->at<float>(h->p.scalars) + 1;
   int* counter = reinterpret_cast<int*>(h->at<float>(h->p.scalars) + 8);
@@ -472,7 +483,7 @@ int clip_adamw_impl(gpt2* h, float lr, float b1, float b2, float eps, float wd, 
   const double N = (double)h->N, E = sizeof(T);
   REGION(GPT2_K_NORM, 0.0, N * E, {
     grad_sumsq_partials<T>(np_, kNormParts, h->at<T>(h->p.grads), (long long)h->N, st);
-    grad_norm_finalize(ns, np_, kNormParts, max_norm, status, counter, t, b1, b2, st);
+    grad_norm_finalize(ns, np_, kNormParts, max_norm, status, counter, t, b1, b2, hp, st);
   });
   Segment segs[P_COUNT];
   for (int i = 0; i < P_COUNT; ++i) segs[i] = Segment{h->pl.off[i], h->pl.off[i + 1], is_decayed(i) ? 1 : 0};
@@ -482,7 +493,7 @@ int clip_adamw_impl(gpt2* h, float lr, float b1, float b2, float eps, float wd, 
   REGION(GPT2_K_ADAMW, 0.0, bytes,
          adamw<T, T>(h->at<float>(h->p.master), pcopy, h->at<T>(h->p.grads), h->at<float>(h->p.adam_m),
                      h->at<float>(h->p.adam_v), (long long)h->N, segs, P_COUNT, ns, lr, b1, b2, eps, wd,
-                     st));
+                     hp, st));
   CK(cudaGetLastError());
   return GPT2_OK;
 }
@@ -544,6 +555,12 @@ int gpt2_create(int L, int H, int C, int V, int Vpad, int T, int B, int precisio
 void gpt2_destroy(gpt2_t* h) {
   if (!h) return;
   for (cudaEvent_t e : h->evpool) cudaEventDestroy(e);
+  if (h->host_exec) cudaGraphExecDestroy(h->host_exec);
+  if (h->cap_stream) cudaStreamDestroy(h->cap_stream);
+  if (h->pin_tok) cudaFreeHost(h->pin_tok);
+  if (h->pin_tgt) cudaFreeHost(h->pin_tgt);
+  if (h->pin_hyp) cudaFreeHost(h->pin_hyp);
+  if (h->pin_out) cudaFreeHost(h->pin_out);
   delete h;
 }
 
@@ -704,28 +721,103 @@ int gpt2_clip_adamw(gpt2_t* h, float lr, float beta1, float beta2, float eps, fl
   return GPT2_OK;
 }
 
+}  // extern "C"
+
+namespace {
+
+// Captures the host-buffer step (staging copies in, forward, backward, clip +
+// AdamW with device hyperparameters, loss / norm / status out, status cleared)
+// into h->host_exec.  Capture runs on a private stream; h->stream is restored.
+int build_host_graph(gpt2* h) {
+  const size_t bytes = (size_t)h->s.M() * 4;
+  if (!h->pin_tok) CK(cudaHostAlloc(reinterpret_cast<void**>(&h->pin_tok), bytes, cudaHostAllocDefault));
+  if (!h->pin_tgt) CK(cudaHostAlloc(reinterpret_cast<void**>(&h->pin_tgt), bytes, cudaHostAllocDefault));
+  if (!h->pin_hyp) CK(cudaHostAlloc(reinterpret_cast<void**>(&h->pin_hyp), sizeof(OptHyper), cudaHostAllocDefault));
+  if (!h->pin_out) CK(cudaHostAlloc(reinterpret_cast<void**>(&h->pin_out), 16, cudaHostAllocDefault));
+  if (!h->cap_stream) CK(cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking));
+  CK(cudaStreamSynchronize(h->stream));
+  const cudaStream_t user = h->stream;
+  h->stream = h->cap_stream;
+  cudaGraph_t graph = nullptr;
+  int r = GPT2_OK;
+  cudaError_t e = cudaStreamBeginCapture(h->cap_stream, cudaStreamCaptureModeThreadLocal);
+  if (e == cudaSuccess) {
+    OptHyper* dh = h->at<OptHyper>(h->p.hyper);
+    unsigned* status = h->at<unsigned>(h->p.status);
+    cudaMemcpyAsync(h->at<int32_t>(h->p.tokens), h->pin_tok, bytes, cudaMemcpyHostToDevice, h->stream);
+    cudaMemcpyAsync(h->at<int32_t>(h->p.targets), h->pin_tgt, bytes, cudaMemcpyHostToDevice, h->stream);
+    cudaMemcpyAsync(dh, h->pin_hyp, sizeof(OptHyper), cudaMemcpyHostToDevice, h->stream);
+    r = h->s.prec == GPT2_BF16 ? forward_impl<bf16>(h) : forward_impl<float>(h);
+    if (r == GPT2_OK) r = h->s.prec == GPT2_BF16 ? backward_impl<bf16>(h) : backward_impl<float>(h);
+    if (r == GPT2_OK)
+      r = h->s.prec == GPT2_BF16 ? clip_adamw_impl<bf16>(h, 0.f, 0.f, 0.f, 0.f, 0.f, 1.f, 1, dh)
+                                 : clip_adamw_impl<float>(h, 0.f, 0.f, 0.f, 0.f, 0.f, 1.f, 1, dh);
+    cudaMemcpyAsync(h->pin_out, h->at<float>(h->p.scalars), 8, cudaMemcpyDeviceToHost, h->stream);
+    cudaMemcpyAsync(h->pin_out + 2, status, 4, cudaMemcpyDeviceToHost, h->stream);
+    cudaMemsetAsync(status, 0, 4, h->stream);
+    e = cudaStreamEndCapture(h->cap_stream, &graph);
+  }
+  h->stream = user;
+  if (r == GPT2_OK && e == cudaSuccess) e = cudaGraphInstantiate(&h->host_exec, graph, 0);
+  if (graph) cudaGraphDestroy(graph);
+  if (r != GPT2_OK) {
+    h->host_exec = nullptr;
+    return r;
+  }
+  if (e != cudaSuccess) {
+    h->host_exec = nullptr;
+    return cuda_fail(e, "gpt2_train_step_host graph");
+  }
+  return GPT2_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
 int gpt2_train_step_host(gpt2_t* h, const int32_t* h_tokens, const int32_t* h_targets, float lr,
                          float beta1, float beta2, float eps, float weight_decay, float max_norm,
                          int step_t, float* h_loss, float* h_norm) {
   if (!h || !h_tokens || !h_targets) return GPT2_E_INVAL;
+  if (step_t < 0 || !(max_norm > 0.f)) return GPT2_E_INVAL;
   const size_t bytes = (size_t)h->s.M() * 4;
-  int32_t* dt = h->at<int32_t>(h->p.tokens);
-  int32_t* dg = h->at<int32_t>(h->p.targets);
-  CK(cudaMemcpyAsync(dt, h_tokens, bytes, cudaMemcpyHostToDevice, h->stream));
-  CK(cudaMemcpyAsync(dg, h_targets, bytes, cudaMemcpyHostToDevice, h->stream));
-  int r = h->s.prec == GPT2_BF16 ? forward_impl<bf16>(h) : forward_impl<float>(h);
-  if (r != GPT2_OK) return r;
-  h->state = ST_FWD;
-  r = gpt2_backward(h);
-  if (r != GPT2_OK) return r;
-  r = gpt2_clip_adamw(h, lr, beta1, beta2, eps, weight_decay, max_norm, step_t, nullptr);
-  if (r != GPT2_OK) return r;
-  float sc[2];
-  CK(cudaMemcpyAsync(sc, h->at<float>(h->p.scalars), 8, cudaMemcpyDeviceToHost, h->stream));
-  int st = read_status(h);
-  if (h_loss) *h_loss = sc[0];
-  if (h_norm) *h_norm = sc[1];
-  return st;
+  if (h->prof_on) {  // per-region events: run the step eagerly
+    int32_t* dt = h->at<int32_t>(h->p.tokens);
+    int32_t* dg = h->at<int32_t>(h->p.targets);
+    CK(cudaMemcpyAsync(dt, h_tokens, bytes, cudaMemcpyHostToDevice, h->stream));
+    CK(cudaMemcpyAsync(dg, h_targets, bytes, cudaMemcpyHostToDevice, h->stream));
+    int r = h->s.prec == GPT2_BF16 ? forward_impl<bf16>(h) : forward_impl<float>(h);
+    if (r != GPT2_OK) return r;
+    h->state = ST_FWD;
+    r = gpt2_backward(h);
+    if (r != GPT2_OK) return r;
+    r = gpt2_clip_adamw(h, lr, beta1, beta2, eps, weight_decay, max_norm, step_t, nullptr);
+    if (r != GPT2_OK) return r;
+    float sc[2];
+    CK(cudaMemcpyAsync(sc, h->at<float>(h->p.scalars), 8, cudaMemcpyDeviceToHost, h->stream));
+    int st = read_status(h);
+    if (h_loss) *h_loss = sc[0];
+    if (h_norm) *h_norm = sc[1];
+    return st;
+  }
+  if (!h->host_exec) {
+    int r = build_host_graph(h);
+    if (r != GPT2_OK) return r;
+  }
+  std::memcpy(h->pin_tok, h_tokens, bytes);
+  std::memcpy(h->pin_tgt, h_targets, bytes);
+  *h->pin_hyp = OptHyper{lr, beta1, beta2, eps, weight_decay, max_norm, step_t, 0};
+  CK(cudaGraphLaunch(h->host_exec, h->stream));
+  CK(cudaStreamSynchronize(h->stream));
+  h->state = ST_IDLE;
+  if (h_loss) *h_loss = h->pin_out[0];
+  if (h_norm) *h_norm = h->pin_out[1];
+  unsigned st;
+  std::memcpy(&st, h->pin_out + 2, 4);
+  if (st & ST_TIMEOUT) return GPT2_E_TIMEOUT;
+  if (st & ST_TOKEN) return GPT2_E_TOKEN;
+  if (st & ST_NONFINITE) return GPT2_E_NONFINITE;
+  return GPT2_OK;
 }
 
 const float* gpt2_device_loss(gpt2_t* h) { return h ? h->at<float>(h->p.scalars) : nullptr; }

@@ -144,13 +144,21 @@ struct Segment { long long begin, end; int decay; };
 constexpr int kMaxSegments = 16;
 template <typename G>
 void grad_sumsq_partials(float* partials, int nparts, const G* g, long long n, cudaStream_t s);
+// Optimizer hyperparameters in device memory.  When the kernels below get a
+// non-null `hp` they take lr, betas, eps, weight decay, max_norm and t from it
+// instead of their value arguments (a captured CUDA graph then picks up new
+// values from a host-to-device copy inside the graph).
+struct OptHyper {
+  float lr, b1, b2, eps, wd, max_norm;
+  int t, pad;
+};
 void grad_norm_finalize(float* norm_scale, const float* partials, int nparts, float max_norm,
                         unsigned* status, int* counter, int host_t, float b1, float b2,
-                        cudaStream_t s);
+                        const OptHyper* hp, cudaStream_t s);
 // bf16 mode: master/m/v fp32 with a bf16 copy of the parameters; fp32 mode: param_copy null.
 template <typename G, typename P>
 void adamw(float* master, P* param_copy, const G* grad, float* m, float* v, long long n,
            const Segment* segs, int nsegs, const float* norm_scale, float lr, float beta1,
-           float beta2, float eps, float wd, cudaStream_t s);
+           float beta2, float eps, float wd, const OptHyper* hp, cudaStream_t s);
 
 }  // namespace gpt2k

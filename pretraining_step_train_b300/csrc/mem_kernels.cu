@@ -955,8 +955,14 @@ void grad_sumsq_partials(float* partials, int nparts, const G* g, long long n, c
 // t = host_t when > 0, else the device step counter + 1 (the counter is stored).
 __global__ void k_norm_finalize(float* norm_scale, const float* __restrict__ partials, int nparts,
                                 float max_norm, unsigned* status, int* counter, int host_t,
-                                float b1, float b2) {
+                                float b1, float b2, const OptHyper* __restrict__ hp) {
   pdl_begin();
+  if (hp) {
+    max_norm = hp->max_norm;
+    host_t = hp->t;
+    b1 = hp->b1;
+    b2 = hp->b2;
+  }
   __shared__ double sh[32];
   double s = 0.0;
   for (int i = threadIdx.x; i < nparts; i += blockDim.x) s += (double)partials[i];
@@ -979,9 +985,9 @@ __global__ void k_norm_finalize(float* norm_scale, const float* __restrict__ par
 }
 void grad_norm_finalize(float* norm_scale, const float* partials, int nparts, float max_norm,
                         unsigned* status, int* counter, int host_t, float b1, float b2,
-                        cudaStream_t s) {
+                        const OptHyper* hp, cudaStream_t s) {
   launch_k(k_norm_finalize, 1, 1024, 0, s, norm_scale, partials, nparts, max_norm, status, counter,
-                                     host_t, b1, b2);
+           host_t, b1, b2, hp);
 }
 
 struct SegTable { Segment s[kMaxSegments]; int n; };
@@ -1019,8 +1025,15 @@ __global__ void __launch_bounds__(256)
     k_adamw(float* __restrict__ master, P* __restrict__ pcopy, const G* __restrict__ grad,
             float* __restrict__ m, float* __restrict__ v, long long n, SegTable segs,
             const float* __restrict__ norm_scale, float lr, float b1, float b2, float eps,
-            float wd) {
+            float wd, const OptHyper* __restrict__ hp) {
   pdl_begin();
+  if (hp) {
+    lr = hp->lr;
+    b1 = hp->b1;
+    b2 = hp->b2;
+    eps = hp->eps;
+    wd = hp->wd;
+  }
   const float sc = norm_scale[1], bc1 = norm_scale[2], bc2 = norm_scale[3];
   const long long n4 = n / 4;
   for (long long q = blockIdx.x * (long long)blockDim.x + threadIdx.x; q < n4;
@@ -1053,12 +1066,12 @@ __global__ void __launch_bounds__(256)
 template <typename G, typename P>
 void adamw(float* master, P* param_copy, const G* grad, float* m, float* v, long long n,
            const Segment* segs, int nsegs, const float* norm_scale, float lr, float beta1,
-           float beta2, float eps, float wd, cudaStream_t s) {
+           float beta2, float eps, float wd, const OptHyper* hp, cudaStream_t s) {
   SegTable t;
   t.n = nsegs;
   for (int i = 0; i < nsegs && i < kMaxSegments; ++i) t.s[i] = segs[i];
   launch_k(k_adamw<G, P>, grid_for(n / 4, 256, 148 * 8), 256, 0, s, master, param_copy, grad, m, v, n, t,
-                                                             norm_scale, lr, beta1, beta2, eps, wd);
+           norm_scale, lr, beta1, beta2, eps, wd, hp);
 }
 
 // ------------------------------------------------------------------ instantiations
@@ -1087,9 +1100,9 @@ INST(bf16)
 #undef INST
 template void adamw<float, float>(float*, float*, const float*, float*, float*, long long,
                                   const Segment*, int, const float*, float, float, float, float,
-                                  float, cudaStream_t);
+                                  float, const OptHyper*, cudaStream_t);
 template void adamw<bf16, bf16>(float*, bf16*, const bf16*, float*, float*, long long,
                                 const Segment*, int, const float*, float, float, float, float,
-                                float, cudaStream_t);
+                                float, const OptHyper*, cudaStream_t);
 
 }  // namespace gpt2k

@@ -155,3 +155,38 @@ def test_call_order_and_host_step():
     assert r == binding.GPT2_E_TOKEN
     assert s.sync_status() == binding.GPT2_OK  # the status word was read and cleared
     s.close()
+
+
+def test_host_step_graph_matches_device_steps():
+    """gpt2_train_step_host replays one CUDA graph captured on its first call; its
+    hyperparameters and tokens arrive through pinned staging copies inside the
+    graph.  Three steps with a different learning rate, step index and batch each
+    must equal, bit for bit, the same steps issued through forward / backward /
+    clip_adamw; a clamped target is reported by the step that saw it and the
+    status is clear again on the next."""
+    L, H, C, V, Vpad, T, B = 2, 2, 128, 1000, 1024, 128, 2
+    P = synth.init_params(21, L, C, V, Vpad, T, bf16_representable=True)
+    flat = synth.flatten_params(P, L, C, Vpad, T)
+    a = binding.Step(L, H, C, V, Vpad, T, B, precision=binding.GPT2_BF16)
+    b = binding.Step(L, H, C, V, Vpad, T, B, precision=binding.GPT2_BF16)
+    a.set_params(flat)
+    b.set_params(flat)
+    for i, lr in enumerate((LR, 0.5 * LR, 2.0 * LR)):
+        tok, tgt = synth.token_batch(30 + i, B, T, V)
+        la, na = a.train_step_host(tok, tgt, lr=lr, beta1=B1, beta2=B2, eps=EPS, weight_decay=WD,
+                                   max_norm=CLIP, t=i + 1)
+        lb = b.forward(to_dev(tok, "i32"), to_dev(tgt, "i32"))
+        b.backward()
+        nb = b.clip_adamw(lr=lr, beta1=B1, beta2=B2, eps=EPS, weight_decay=WD, max_norm=CLIP, t=i + 1)
+        assert la == lb and na == nb, (i, la, lb, na, nb)
+    for which in (0, 2, 3, 4):  # working and master parameters, AdamW m and v
+        np.testing.assert_array_equal(a.get(which), b.get(which))
+    tok, tgt = synth.token_batch(40, B, T, V)
+    bad = tgt.copy()
+    bad[1, 3] = V + 7
+    with pytest.raises(binding.GPT2Error) as ei:
+        a.train_step_host(tok, bad, t=4)
+    assert ei.value.status == binding.GPT2_E_TOKEN
+    a.train_step_host(tok, tgt, t=5)
+    a.close()
+    b.close()
