@@ -251,6 +251,31 @@ __device__ __forceinline__ void pack16_bf16(const float* v, uint32_t* w) {
   for (int j = 0; j < 8; ++j) w[j] = pack2_bf16(v[2 * j], v[2 * j + 1]);
 }
 
+// Column sums of a 32-row x 16-column chunk held one row per lane (v[0..15]):
+// four exchange-and-halve shuffle stages leave lane l with column (l >> 1) & 15
+// summed over 16 lanes, and a last shuffle adds lane l ^ 1.  Fixed order.
+__device__ __forceinline__ float colsum_32x16(const float* v, int lane) {
+  float a[8], b[4], c[2];
+  const bool h16 = lane & 16, h8 = lane & 8, h4 = lane & 4, h2 = lane & 2;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float send = h16 ? v[j] : v[j + 8];
+    a[j] = (h16 ? v[j + 8] : v[j]) + __shfl_xor_sync(0xffffffffu, send, 16);
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float send = h8 ? a[j] : a[j + 4];
+    b[j] = (h8 ? a[j + 4] : a[j]) + __shfl_xor_sync(0xffffffffu, send, 8);
+  }
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const float send = h4 ? b[j] : b[j + 2];
+    c[j] = (h4 ? b[j + 2] : b[j]) + __shfl_xor_sync(0xffffffffu, send, 4);
+  }
+  float d = (h2 ? c[1] : c[0]) + __shfl_xor_sync(0xffffffffu, h2 ? c[0] : c[1], 2);
+  return d + __shfl_xor_sync(0xffffffffu, d, 1);
+}
+
 // Hardware tanh (MUFU, PTX tanh.approx.f32): relative error about 2^-11, far
 // below the bf16 rounding of the values it feeds.
 __device__ __forceinline__ float tanh_hw(float x) {
@@ -437,6 +462,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       xpend |= 1u << b;
     };
+    const bool has_bias = epi == EPI_BIAS || epi == EPI_BIAS_RESID || epi == EPI_BIAS_GELU;
     Unit nw;
     bool nok = cta_unit(p, 0, nw);
     int nxb, ny;  // origin of the next unit this warp handles
@@ -579,9 +605,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               const float2 t = mul2(make_float2(v[j], v[j + 1]), make_float2(xv[j], xv[j + 1]));
               v[j] = t.x; v[j + 1] = t.y;
             }
+            if (g.colpart) {  // the bias gradient's partial: this chunk's column sums over 32 rows
+              const float cs = colsum_32x16(v, lane);
+              const int col = x0 + (lane >> 1);
+              if (!(lane & 1) && col < g.N) g.colpart[(size_t)(y0 >> 5) * g.N + col] = cs;
+            }
           }
         }
-        if (epi == EPI_BIAS || epi == EPI_BIAS_RESID || epi == EPI_BIAS_GELU) {
+        if (has_bias) {
           const bf16* bias = static_cast<const bf16*>(g.bias);
 #pragma unroll
           for (int q = 0; q < 2; ++q) {

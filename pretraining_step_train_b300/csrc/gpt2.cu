@@ -139,7 +139,8 @@ Plan make_plan(const Shape& s) {
   p.attD = take(cur, (size_t)s.B * s.H * s.T * f);
   p.order = take(cur, 2 * M * 4);
   p.lnb_part = take(cur, layernorm_bwd_partials_floats(s.C) * f);
-  size_t cs = colsum_partials_floats(4 * s.C);
+  // column-sum partials: the colsum kernel's, or the GELU' GEMM's one row per 32 rows
+  size_t cs = std::max(colsum_partials_floats(4 * s.C), (size_t)((s.M() + 31) / 32) * 4 * s.C);
   p.colsum_part = take(cur, cs * f);
   p.norm_part = take(cur, kNormParts * f);
   // stream-K flags (zeroed with the arena) and partial-sum slots of the GEMM engine
@@ -407,13 +408,18 @@ int backward_impl(gpt2* h) {
     g.A = dcur; g.lda = C; g.B = P.param(P_FCPW, l); g.ldb = 4 * C; g.b_mn = 1;
     g.M = M; g.N = 4 * C; g.K = C; g.epi = EPI_GELU_BWD; g.aux = P.fch(l); g.ldaux = 4 * C;
     g.D = dbig; g.ldd = 4 * C;
+    if (bf) g.colpart = csp;  // the fc bias gradient's partial column sums come out of this epilogue
     CKI(linear<T>(h, g));
     // MLP up-projection: h = ln2 Wfc^T + b
     g = GemmArgs();
     g.A = dbig; g.lda = 4 * C; g.a_mn = 1; g.B = P.ln2(l); g.ldb = C; g.b_mn = 1;
     g.M = 4 * C; g.N = C; g.K = M; g.D = P.grad(P_FCW, l); g.ldd = C;
     CKI(linear<T>(h, g));
-    REGION(GPT2_K_BIAS_GRAD, 0.0, 4.0 * MC * E, colsum<T>(P.grad(P_FCB, l), dbig, M, 4 * C, 4 * C, csp, st));
+    if (bf)
+      REGION(GPT2_K_BIAS_GRAD, 0.0, 4.0 * ((M + 31) / 32) * 4.0 * C,
+             colsum_reduce<T>(P.grad(P_FCB, l), csp, (M + 31) / 32, 4 * C, st));
+    else
+      REGION(GPT2_K_BIAS_GRAD, 0.0, 4.0 * MC * E, colsum<T>(P.grad(P_FCB, l), dbig, M, 4 * C, 4 * C, csp, st));
     g = GemmArgs();
     g.A = dbig; g.lda = 4 * C; g.B = P.param(P_FCW, l); g.ldb = C; g.b_mn = 1;
     g.M = M; g.N = C; g.K = 4 * C; g.D = dsmall; g.ldd = C;

@@ -32,6 +32,9 @@ struct GemmArgs {
   const void* aux = nullptr; long long ldaux = 0;
   float* ce_max = nullptr; float* ce_sum = nullptr; int ce_ld = 0;
   float* ce_tgt = nullptr; const int32_t* targets = nullptr; int V = 0;
+  // EPI_GELU_BWD, tcgen05 engine only: when set, colpart[(m / 32) * N + n] receives
+  // the fp32 sum of D over rows m .. m + 31 (before rounding), ceil(M / 32) x N floats
+  float* colpart = nullptr;
 };
 
 // bf16 operands on tcgen05 tensor cores (TMA -> smem ring -> MMA -> TMEM -> epilogue).
@@ -110,6 +113,9 @@ void layernorm_bwd(float* dres, T* dres_b, const T* dy, const T* x, const float*
 size_t layernorm_bwd_partials_floats(int C);
 template <typename T>
 void colsum(T* out, const T* x, int M, int N, long long ld, float* partials, cudaStream_t s);
+// out[n] = sum over p < nparts of partials[p * N + n], fixed order (deterministic).
+template <typename T>
+void colsum_reduce(T* out, const float* partials, int nparts, int N, cudaStream_t s);
 size_t colsum_partials_floats(int N);
 template <typename T> void gelu_fwd(T* y, const T* x, long long n, cudaStream_t s);
 template <typename T> void gelu_bwd(T* dx, const T* dy, const T* x, long long n, cudaStream_t s);

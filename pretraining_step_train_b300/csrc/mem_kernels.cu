@@ -412,6 +412,11 @@ __global__ void __launch_bounds__(256)
 size_t colsum_partials_floats(int N) { return (size_t)kColsumRowBlocks * N; }
 
 template <typename T>
+void colsum_reduce(T* out, const float* partials, int nparts, int N, cudaStream_t s) {
+  reduce_parts<T>(out, (T*)nullptr, (T*)nullptr, partials, nparts, N, N, s);
+}
+
+template <typename T>
 void colsum(T* out, const T* x, int M, int N, long long ld, float* partials, cudaStream_t s) {
   constexpr int NV = V16<T>::N;
   int nrb = (M + 127) / 128;
@@ -1083,6 +1088,7 @@ void adamw(float* master, P* param_copy, const G* grad, float* m, float* v, long
   template void layernorm_bwd<T>(float*, T*, const T*, const T*, const float*, const float*,       \
                                  const T*, T*, T*, T*, float*, int, int, int, cudaStream_t);       \
   template void colsum<T>(T*, const T*, int, int, long long, float*, cudaStream_t);                \
+  template void colsum_reduce<T>(T*, const float*, int, int, cudaStream_t);                        \
   template void gelu_fwd<T>(T*, const T*, long long, cudaStream_t);                                \
   template void gelu_bwd<T>(T*, const T*, const T*, long long, cudaStream_t);                      \
   template void residual_add<T>(T*, const T*, const T*, long long, cudaStream_t);                  \
