@@ -396,7 +396,7 @@ int backward_impl(gpt2* h) {
          layernorm_bwd<T>(dres, dres_b, dsmall, P.res(L), h->at<float>(h->p.lnf_mean),
                           h->at<float>(h->p.lnf_rstd), P.param(P_LNFW), P.grad(P_LNFW),
                           P.grad(P_LNFB), L > 0 ? P.grad(P_FCPB, L - 1) : nullptr, lnbp, M, C, 0,
-                          st));
+                          st, h->at<unsigned>(h->p.status)));
   for (int l = L - 1; l >= 0; --l) {
     // MLP projection: x2 = x1 + fca Wfcp^T + b
     g = GemmArgs();
@@ -427,7 +427,7 @@ int backward_impl(gpt2* h) {
     REGION(GPT2_K_LN_BWD, 0.0, lnb_acc,
            layernorm_bwd<T>(dres, dres_b, dsmall, P.x1(l), P.stat(h->p.ln2_mean, l),
                             P.stat(h->p.ln2_rstd, l), P.param(P_LN2W, l), P.grad(P_LN2W, l),
-                            P.grad(P_LN2B, l), P.grad(P_APB, l), lnbp, M, C, 1, st));
+                            P.grad(P_LN2B, l), P.grad(P_APB, l), lnbp, M, C, 1, st, h->at<unsigned>(h->p.status)));
     // attention projection: x1 = x + atty Wap^T + b
     g = GemmArgs();
     g.A = dcur; g.lda = C; g.a_mn = 1; g.B = P.atty(l); g.ldb = C; g.b_mn = 1;
@@ -465,7 +465,7 @@ int backward_impl(gpt2* h) {
            layernorm_bwd<T>(dres, dres_b, dsmall, P.res(l), P.stat(h->p.ln1_mean, l),
                             P.stat(h->p.ln1_rstd, l), P.param(P_LN1W, l), P.grad(P_LN1W, l),
                             P.grad(P_LN1B, l), l > 0 ? P.grad(P_FCPB, l - 1) : nullptr, lnbp, M, C,
-                            1, st));
+                            1, st, h->at<unsigned>(h->p.status)));
   }
   // encoder: dwte[tok] += dx0 in a fixed order, dwpe = sum over the batch
   uint32_t* order = h->at<uint32_t>(h->p.order);

@@ -106,10 +106,11 @@ void layernorm_fwd(T* y, float* mean, float* rstd, const T* x, const T* w, const
                    cudaStream_t s);
 // dres (+)= LNbwd(dy); dres_b (optional) = storage copy of dres; dw, db = the LayerNorm's
 // weight / bias gradients; dsum (optional) = column sum of the new dres.
+// `status` (may be null) receives ST_TIMEOUT if a bounded wait of the streaming kernel expires.
 template <typename T>
 void layernorm_bwd(float* dres, T* dres_b, const T* dy, const T* x, const float* mean,
                    const float* rstd, const T* w, T* dw, T* db, T* dsum, float* partials, int M,
-                   int C, int accumulate, cudaStream_t s);
+                   int C, int accumulate, cudaStream_t s, unsigned* status = nullptr);
 size_t layernorm_bwd_partials_floats(int C);
 template <typename T>
 void colsum(T* out, const T* x, int M, int N, long long ld, float* partials, cudaStream_t s);

@@ -331,12 +331,237 @@ __global__ void __launch_bounds__(kLnbWarps * 32)
   }
 }
 
+// Streaming variant for bf16 storage (C <= 2048): one persistent block of 8
+// warps per SM.  Warp w of block b takes rows b*8 + w, + 8*gridDim.x, ...; lane
+// 0 keeps the warp's next rows in flight with bulk copies (cp.async.bulk, one
+// mbarrier per stage) into a ring of nbuf row stages [dy | x | dres] in shared
+// memory, so a warp's memory stays busy while it computes.  Each row is read
+// twice from shared memory (row sums, then the update).  The column sums for
+// dw, db and dsum live in registers across all of the warp's rows; at the end
+// the 8 warps add theirs in warp order and the block writes one partial row
+// (the same fixed-order reduction follows).
+constexpr int kLnsWarps = 8;
+constexpr int kLnsBarBytes = 1024;
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ bool lns_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Warp-collective bounded wait (about 2 s of %globaltimer): lane 0 spins, every
+// lane then observes the completed phase itself.
+__device__ __forceinline__ bool lns_wait(uint32_t bar, uint32_t parity, int lane) {
+  int ok = 1;
+  if (lane == 0 && !lns_try_wait(bar, parity)) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!lns_try_wait(bar, parity))
+      if (globaltimer_ns() - t0 > 2000000000ull) { ok = 0; break; }
+  }
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  if (ok) (void)lns_try_wait(bar, parity);
+  return ok != 0;
+}
+__device__ __forceinline__ void bf16x8_to_f(const uint4& q, float* v) {
+  const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = __uint_as_float(u[i] << 16);
+    v[2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
+  }
+}
+
+template <int MAXV>
+__global__ void __launch_bounds__(kLnsWarps * 32, 1)
+    k_layernorm_bwd_stream(float* __restrict__ dres, bf16* __restrict__ dres_b, const bf16* __restrict__ dy,
+                           const bf16* __restrict__ x, const float* __restrict__ mean,
+                           const float* __restrict__ rstd, const bf16* __restrict__ w,
+                           float* __restrict__ partials, int M, int C, int accumulate, int want_sum, int nbuf,
+                           unsigned* status) {
+  pdl_begin();
+  extern __shared__ __align__(128) uint8_t lsm[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nv = C / 8;
+  const uint32_t SB = 8u * (uint32_t)C;  // one row stage: dy, x (bf16), dres (fp32)
+  uint8_t* mine = lsm + kLnsBarBytes + (size_t)warp * nbuf * SB;
+  const uint32_t bar0 = smem_u32(lsm) + 8u * warp * nbuf;
+  if (lane == 0) {
+    for (int i = 0; i < nbuf; ++i)
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar0 + 8u * i) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncwarp();
+  float wv[MAXV][8];
+#pragma unroll
+  for (int j = 0; j < MAXV; ++j) {
+    const int vi = lane + j * 32;
+    if (vi < nv) bf16x8_to_f(*reinterpret_cast<const uint4*>(w + vi * 8), wv[j]);
+  }
+  const int gw = blockIdx.x * kLnsWarps + warp, nw = gridDim.x * kLnsWarps;
+  const int nrows = gw < M ? (M - 1 - gw) / nw + 1 : 0;
+  const uint32_t tx = (accumulate ? 8u : 4u) * (uint32_t)C;
+  auto issue = [&](int k) {  // lane 0: row k of this warp into stage k % nbuf
+    const long long r = gw + (long long)k * nw;
+    const int st = k % nbuf;
+    const uint32_t dst = smem_u32(mine + (size_t)st * SB), bar = bar0 + 8u * st;
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(tx) : "memory");
+    bulk_g2s(dst, dy + r * C, 2u * C, bar);
+    bulk_g2s(dst + 2u * C, x + r * C, 2u * C, bar);
+    if (accumulate) bulk_g2s(dst + 4u * C, dres + r * C, 4u * C, bar);
+  };
+  int issued = 0;
+  if (lane == 0)
+    for (; issued < nbuf - 1 && issued < nrows; ++issued) issue(issued);
+  issued = __shfl_sync(0xffffffffu, issued, 0);
+  float aw[MAXV][8], ab[MAXV][8], as[MAXV][8];
+#pragma unroll
+  for (int j = 0; j < MAXV; ++j)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) aw[j][e] = ab[j][e] = as[j][e] = 0.f;
+  const float invC = 1.0f / (float)C;
+  float mu_n = 0.f, rs_n = 0.f;
+  if (nrows > 0) { mu_n = mean[gw]; rs_n = rstd[gw]; }
+  bool ok = true;
+  int k = 0;
+  for (; k < nrows; ++k) {
+    if (issued < nrows) {  // refill the stage that row k - 1 used
+      if (lane == 0) issue(issued);
+      ++issued;
+    }
+    const long long r = gw + (long long)k * nw;
+    const float mu = mu_n, rs = rs_n;
+    if (k + 1 < nrows) { mu_n = mean[r + nw]; rs_n = rstd[r + nw]; }
+    const int st = k % nbuf;
+    if (!lns_wait(bar0 + 8u * st, (uint32_t)((k / nbuf) & 1), lane)) { ok = false; break; }
+    const uint8_t* sp = mine + (size_t)st * SB;
+    const bf16* sdy = reinterpret_cast<const bf16*>(sp);
+    const bf16* sx = sdy + C;
+    const float* sd = reinterpret_cast<const float*>(sp + 4u * C);
+    float sg = 0.f, sgx = 0.f;
+#pragma unroll
+    for (int j = 0; j < MAXV; ++j) {
+      const int vi = lane + j * 32;
+      if (vi < nv) {
+        float a[8], b[8];
+        bf16x8_to_f(*reinterpret_cast<const uint4*>(sdy + vi * 8), a);
+        bf16x8_to_f(*reinterpret_cast<const uint4*>(sx + vi * 8), b);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float g = a[e] * wv[j][e];
+          sg += g;
+          sgx += g * ((b[e] - mu) * rs);
+        }
+      }
+    }
+    sg = warp_sum(sg) * invC;
+    sgx = warp_sum(sgx) * invC;
+#pragma unroll
+    for (int j = 0; j < MAXV; ++j) {
+      const int vi = lane + j * 32;
+      if (vi < nv) {
+        float a[8], b[8], d[8];
+        bf16x8_to_f(*reinterpret_cast<const uint4*>(sdy + vi * 8), a);
+        bf16x8_to_f(*reinterpret_cast<const uint4*>(sx + vi * 8), b);
+        if (accumulate) {
+          const float4 d0 = *reinterpret_cast<const float4*>(sd + vi * 8);
+          const float4 d1 = *reinterpret_cast<const float4*>(sd + vi * 8 + 4);
+          d[0] = d0.x; d[1] = d0.y; d[2] = d0.z; d[3] = d0.w;
+          d[4] = d1.x; d[5] = d1.y; d[6] = d1.z; d[7] = d1.w;
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) d[e] = 0.f;
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float xh = (b[e] - mu) * rs;
+          d[e] += rs * (a[e] * wv[j][e] - sg - xh * sgx);
+          aw[j][e] += a[e] * xh;
+          ab[j][e] += a[e];
+          as[j][e] += d[e];
+        }
+        float* dp = dres + r * C + vi * 8;
+        *reinterpret_cast<float4*>(dp) = make_float4(d[0], d[1], d[2], d[3]);
+        *reinterpret_cast<float4*>(dp + 4) = make_float4(d[4], d[5], d[6], d[7]);
+        if (dres_b) store16(dres_b + r * C + vi * 8, d);
+      }
+    }
+    __syncwarp();  // every lane is done with this stage before lane 0 refills it
+  }
+  if (!ok) {
+    if (status && lane == 0) atomicOr(status, ST_TIMEOUT);
+    // never leave with bulk copies still landing in this warp's stages
+    for (int kk = k; kk < issued; ++kk) (void)lns_wait(bar0 + 8u * (kk % nbuf), (uint32_t)((kk / nbuf) & 1), lane);
+  }
+  __syncthreads();
+  // block partial: the 8 warps' column sums added in warp order
+  float* red = reinterpret_cast<float*>(lsm + kLnsBarBytes);  // [warps][3][C]
+  float* my = red + (size_t)warp * 3 * C;
+#pragma unroll
+  for (int j = 0; j < MAXV; ++j) {
+    const int vi = lane + j * 32;
+    if (vi < nv) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        my[vi * 8 + e] = aw[j][e];
+        my[C + vi * 8 + e] = ab[j][e];
+        my[2 * C + vi * 8 + e] = as[j][e];
+      }
+    }
+  }
+  __syncthreads();
+  const int width = (want_sum ? 3 : 2) * C;
+  for (int i = threadIdx.x; i < width; i += blockDim.x) {
+    float t = 0.f;
+#pragma unroll
+    for (int ww = 0; ww < kLnsWarps; ++ww) t += red[(size_t)ww * 3 * C + i];
+    partials[(long long)blockIdx.x * width + i] = t;
+  }
+}
+
 size_t layernorm_bwd_partials_floats(int C) { return (size_t)kLnbBlocks * 3 * C; }
 
 template <typename T>
 void layernorm_bwd(float* dres, T* dres_b, const T* dy, const T* x, const float* mean,
                    const float* rstd, const T* w, T* dw, T* db, T* dsum, float* partials, int M,
-                   int C, int accumulate, cudaStream_t s) {
+                   int C, int accumulate, cudaStream_t s, unsigned* status) {
+  if constexpr (sizeof(T) == 2) {
+    // streaming kernel when at least two row stages per warp fit in shared memory
+    const size_t budget = 227 * 1024 - kLnsBarBytes;
+    int nbuf = (int)(budget / ((size_t)kLnsWarps * 8 * C));
+    if (nbuf > 4) nbuf = 4;
+    const int nv = C / 8, per = (nv + 31) / 32;
+    if (nbuf >= 2 && per <= 8 && C % 8 == 0) {
+      int nblocks = num_sms();
+      const int want_rows = (M + kLnsWarps - 1) / kLnsWarps;
+      if (nblocks > want_rows) nblocks = want_rows;
+      if (nblocks > kLnbBlocks) nblocks = kLnbBlocks;
+      const size_t sm = kLnsBarBytes + (size_t)kLnsWarps * nbuf * 8 * C;
+      const int want_sum = dsum != nullptr;
+#define LNS(P)                                                                                         \
+  do {                                                                                                 \
+    cudaFuncSetAttribute(k_layernorm_bwd_stream<P>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm); \
+    launch_k(k_layernorm_bwd_stream<P>, nblocks, kLnsWarps * 32, sm, s, dres, (bf16*)dres_b, (const bf16*)dy, \
+             (const bf16*)x, mean, rstd, (const bf16*)w, partials, M, C, accumulate, want_sum, nbuf, status); \
+  } while (0)
+      if (per <= 1) LNS(1);
+      else if (per <= 2) LNS(2);
+      else if (per <= 3) LNS(3);
+      else if (per <= 4) LNS(4);
+      else LNS(8);
+#undef LNS
+      reduce_parts<T>(dw, db, dsum, partials, nblocks, (want_sum ? 3 : 2) * C, C, s);
+      return;
+    }
+  }
   const int nv = C / V16<T>::N;
   const int per = (nv + 31) / 32;
   int nblocks = (M + kLnbWarps - 1) / kLnbWarps;
@@ -1086,7 +1311,8 @@ void adamw(float* master, P* param_copy, const G* grad, float* m, float* v, long
   template void layernorm_fwd<T>(T*, float*, float*, const T*, const T*, const T*, int, int,       \
                                  cudaStream_t);                                                    \
   template void layernorm_bwd<T>(float*, T*, const T*, const T*, const float*, const float*,       \
-                                 const T*, T*, T*, T*, float*, int, int, int, cudaStream_t);       \
+                                 const T*, T*, T*, T*, float*, int, int, int, cudaStream_t,        \
+                                 unsigned*);                                                        \
   template void colsum<T>(T*, const T*, int, int, long long, float*, cudaStream_t);                \
   template void colsum_reduce<T>(T*, const float*, int, int, cudaStream_t);                        \
   template void gelu_fwd<T>(T*, const T*, long long, cudaStream_t);                                \
