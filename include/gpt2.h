@@ -262,6 +262,18 @@ int gemm_bf16(const void* A, const void* B, void* D, int M, int N, int K, long l
 /* Workspace bytes of the splits = -1 / -2 schedules on the current device. */
 size_t gemm_bf16_sk_workspace_bytes(void);
 
+/* The GEMM engine with one of its fused epilogues, for tests.  As gemm_bf16
+ * (bf16 D, same splits / workspace rules, no split > 1 with a fused epilogue)
+ * with epi: 1 D = acc + bias[n]; 2 D = acc + bias[n] + X[m, n]; 3 h = acc +
+ * bias[n], D = gelu'(h), D2 = gelu(h) (tanh form); 4 D = acc * X[m, n] and, if
+ * colpart is not NULL, colpart[(m / 32) * N + n] = the fp32 sum of D over rows
+ * m .. m + 31 before rounding.  bias: bf16 [N]; X, D2: bf16 [M, N] with leading
+ * dimension ldd; colpart: fp32, ceil(M / 32) * N. */
+int gemm_bf16_epilogue(const void* A, const void* B, void* D, void* D2, const void* bias, const void* X,
+                       float* colpart, int M, int N, int K, long long lda, long long ldb, long long ldd,
+                       int a_mn, int b_mn, int epi, int splits, void* workspace, size_t workspace_bytes,
+                       void* stream);
+
 /* Test hook for the bounded waits: while on, the GEMM's TMA producer skips its
  * first shared-memory stage, so the MMA thread's wait expires (~2 s) and the
  * call's status word reports GPT2_E_TIMEOUT.  gemm_bf16_status runs one GEMM

@@ -1020,6 +1020,31 @@ int gemm_bf16(const void* A, const void* B, void* D, int M, int N, int K, long l
 
 size_t gemm_bf16_sk_workspace_bytes(void) { return gemm_tc_sk_ws_bytes(); }
 
+int gemm_bf16_epilogue(const void* A, const void* B, void* D, void* D2, const void* bias, const void* X,
+                       float* colpart, int M, int N, int K, long long lda, long long ldb, long long ldd,
+                       int a_mn, int b_mn, int epi, int splits, void* workspace, size_t workspace_bytes,
+                       void* stream) {
+  if (epi < 1 || epi > 4) return GPT2_E_INVAL;
+  if (!al16(A) || !al16(B) || !al16(D)) return GPT2_E_INVAL;
+  if (M <= 0 || N <= 0 || K <= 0 || N % 8 || lda % 8 || ldb % 8 || ldd % 8) return GPT2_E_INVAL;
+  if (epi != 4 && !al16(bias)) return GPT2_E_INVAL;
+  if ((epi == 2 || epi == 4) && !al16(X)) return GPT2_E_INVAL;
+  if (epi == 3 && !al16(D2)) return GPT2_E_INVAL;
+  if (splits < -2 || splits > 1) return GPT2_E_INVAL;
+  if (splits < 0 && (!al16(workspace) || workspace_bytes < gemm_tc_sk_ws_bytes())) return GPT2_E_INVAL;
+  GemmArgs g;
+  g.A = A; g.lda = lda; g.a_mn = a_mn ? 1 : 0; g.B = B; g.ldb = ldb; g.b_mn = b_mn ? 1 : 0;
+  g.M = M; g.N = N; g.K = K; g.D = D; g.ldd = ldd;
+  g.epi = epi == 1 ? EPI_BIAS : epi == 2 ? EPI_BIAS_RESID : epi == 3 ? EPI_BIAS_GELU : EPI_GELU_BWD;
+  g.bias = bias; g.D2 = D2; g.resid = X; g.ldr = ldd; g.aux = X; g.ldaux = ldd;
+  if (epi == 4) g.colpart = colpart;
+  int e = gemm_tc(g, splits == 0 ? 1 : splits, workspace, workspace_bytes, nullptr,
+                  static_cast<cudaStream_t>(stream));
+  if (e == (int)cudaErrorInvalidValue) return GPT2_E_INVAL;
+  if (e) return cuda_fail((cudaError_t)e, "gemm_bf16_epilogue");
+  return GPT2_OK;
+}
+
 int gpt2_test_set_gemm_poison(int on) { return gemm_tc_poison(on); }
 
 int gemm_bf16_status(const void* A, const void* B, void* D, int M, int N, int K, long long lda,

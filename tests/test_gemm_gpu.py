@@ -139,3 +139,88 @@ def test_gemm_stream_k_step_shapes(M, N, K, a_mn, b_mn):
     rows = np.random.default_rng(0).choice(M, 256, replace=False)
     ref = a[rows].astype(np.float64) @ b.astype(np.float64).T
     np.testing.assert_allclose(outs[0][rows], ref, rtol=0, atol=2e-5 * np.sqrt(K) * 4)
+
+
+def _epilogue_case(seed, M, N, K, a_mn, b_mn, epi, splits):
+    """Run gemm_bf16_epilogue and its float64 reference on the same bf16 inputs."""
+    import torch
+    from oracle import gpt2_oracle as O
+    a, b, As, Bs, lda, ldb = _operands(seed, M, N, K, a_mn, b_mn)
+    A, B = to_dev(As), to_dev(Bs)
+    bias = synth.round_to_bf16(synth.normal(seed + 2, N) * 0.5)
+    X = synth.round_to_bf16(synth.normal(seed + 3, M * N).reshape(M, N))
+    bias_d, X_d = to_dev(bias, "bf16"), to_dev(X, "bf16")
+    D = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    D2 = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    G = (M + 31) // 32
+    colpart = torch.full((G, N), float("nan"), dtype=torch.float32, device="cuda")
+    ws = _sk_workspace()
+    binding.check(binding.lib().gemm_bf16_epilogue(
+        A.data_ptr(), B.data_ptr(), D.data_ptr(), D2.data_ptr(), bias_d.data_ptr(), X_d.data_ptr(),
+        colpart.data_ptr() if epi == 4 else None, M, N, K, lda, ldb, N, a_mn, b_mn, epi, splits,
+        ws.data_ptr(), ws.numel(), None))
+    torch.cuda.synchronize()
+    acc = a.astype(np.float64) @ b.astype(np.float64).T
+    x = X.astype(np.float64)
+    if epi == 1:
+        ref = {"D": acc + bias}
+    elif epi == 2:
+        ref = {"D": acc + bias + x}
+    elif epi == 3:
+        h = acc + bias
+        ref = {"D": O.gelu_grad(h), "D2": O.gelu(h)}
+    else:
+        dh = acc * x
+        pad = np.zeros((G * 32, N)); pad[:M] = dh
+        ref = {"D": dh, "colpart": pad.reshape(G, 32, N).sum(axis=1)}
+    got = {"D": to_np(D), "D2": to_np(D2), "colpart": to_np(colpart)}
+    return got, ref
+
+
+@pytest.mark.parametrize("M,N,K,a_mn,b_mn,splits", [
+    (640, 264, 2112, 0, 0, -2),     # 10 tiles cut along K over all SMs: 2-3 k blocks per CTA, ragged N
+    (640, 264, 2112, 0, 1, -1),     # fewer tiles than SMs: K splits finished in-kernel
+    (4160, 1280, 2048, 0, 1, -1),   # 165 tiles: one whole wave + a stream-K tail of 17 tiles
+    (300, 520, 200, 0, 0, 1),       # plain schedule, ragged M and K
+])
+@pytest.mark.parametrize("epi", [1, 2, 3, 4])
+def test_gemm_fused_epilogues_under_each_schedule(M, N, K, a_mn, b_mn, splits, epi):
+    """Bias, bias + residual, bias + GELU (gelu' and gelu from one tanh) and the
+    GELU' backward with its per-32-row column sums, under the plain, in-kernel
+    split and stream-K schedules: a partial-sum finish runs the same epilogue,
+    and the epilogue's operand prefetch skips the partial-only fragments."""
+    got, ref = _epilogue_case(M + N + K + epi, M, N, K, a_mn, b_mn, epi, splits)
+    for k, r in ref.items():
+        g = got[k]
+        assert np.isfinite(g).all(), k
+        if k == "colpart":
+            # fp32 sums of fp32 products: rounding of K-long dot products and 32-row sums
+            assert rel_l2(g, r) < 1e-5, (k, rel_l2(g, r))
+        else:
+            # bf16 output (2^-9) plus the hardware tanh (about 2^-11 relative)
+            assert rel_l2(g, r) < 4e-3, (k, rel_l2(g, r))
+
+
+def test_gemm_bounded_wait_expires_and_context_survives():
+    """With the producer told to skip its first stage, the MMA thread's bounded
+    wait runs out (about 2 s): the call reports GPT2_E_TIMEOUT, the kernel drains
+    and returns, and the next GEMM on the same context is correct."""
+    import torch
+    M, N, K = 256, 512, 1024
+    a, b, As, Bs, lda, ldb = _operands(17, M, N, K, 0, 0)
+    A, B = to_dev(As), to_dev(Bs)
+    D = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lib = binding.lib()
+    old = lib.gpt2_test_set_gemm_poison(1)
+    try:
+        r = lib.gemm_bf16_status(A.data_ptr(), B.data_ptr(), D.data_ptr(), M, N, K, lda, ldb, N, 0, 0,
+                                 st.data_ptr(), None)
+    finally:
+        lib.gpt2_test_set_gemm_poison(old)
+    assert r == binding.GPT2_E_TIMEOUT
+    r = lib.gemm_bf16_status(A.data_ptr(), B.data_ptr(), D.data_ptr(), M, N, K, lda, ldb, N, 0, 0,
+                             st.data_ptr(), None)
+    assert r == binding.GPT2_OK
+    ref = a.astype(np.float64) @ b.astype(np.float64).T
+    assert rel_l2(to_np(D), ref) < 4e-3
