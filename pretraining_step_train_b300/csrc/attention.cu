@@ -44,37 +44,9 @@ static bool strides_ok(const AttnArgs& a) {
          a.osh % 8 == 0 && a.osb % 8 == 0;
 }
 
-// D[b, h, i] = sum_c dO[i, c] O[i, c] for d = 64: 8 threads per row, 16 B each.
-__global__ void __launch_bounds__(256) k_attn_rowdot64(AttnArgs a) {
-  pdl_begin();
-  const long long gid = blockIdx.x * (long long)blockDim.x + threadIdx.x;
-  const long long row = gid >> 3;
-  const int part = (int)(gid & 7);
-  const long long rows = (long long)a.B * a.H * a.T;
-  float s = 0.f;
-  if (row < rows) {
-    const int i = (int)(row % a.T);
-    const int bh = (int)(row / a.T);
-    const int b = bh / a.H, h = bh % a.H;
-    const long long off = b * a.osb + h * a.osh + (long long)i * a.ost + part * 8;
-    float o[8], g[8];
-    load16(static_cast<const bf16*>(a.o) + off, o);
-    load16(static_cast<const bf16*>(a.dO) + off, g);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) s += o[e] * g[e];
-  }
-  s += __shfl_xor_sync(0xffffffffu, s, 1);
-  s += __shfl_xor_sync(0xffffffffu, s, 2);
-  s += __shfl_xor_sync(0xffffffffu, s, 4);
-  if (row < rows && part == 0) a.Dbuf[row] = s;
-}
-
+// bf16: the tcgen05 kernels, which form D = rowsum(dO * O) themselves (into a.Dbuf).
 int attn_bwd_bf16(const AttnArgs& a, cudaStream_t s) {
   if (!strides_ok(a)) return (int)cudaErrorInvalidValue;
-  long long rows = (long long)a.B * a.H * a.T;
-  launch_k(k_attn_rowdot64, (unsigned)((rows * 8 + 255) / 256), 256, 0, s, a);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return (int)e;
   return attn_bwd_tc(a, s);
 }
 

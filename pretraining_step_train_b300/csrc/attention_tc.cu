@@ -400,9 +400,11 @@ __device__ __forceinline__ void bw_load(const CUtensorMap* tm, int swap, uint32_
 }
 
 // ------------------------------------------------------------------ dQ
-// smem: Q | dO (per item) | K,V ring (4 stages); TMEM: S | dP | dQ | dS double buffer
+// smem: Q | dO | O (per item) | K,V ring (4 stages); TMEM: S | dP | dQ | dS double buffer.
+// The compute warps also form D = rowsum(dO * O) for their query rows from the
+// dO and O tiles and store it for the dK/dV kernel, which runs after this one.
 constexpr int DQ_STAGES = 4;
-constexpr int DQ_Q = 0, DQ_DO = AT_TILE, DQ_KV = 2 * AT_TILE;
+constexpr int DQ_Q = 0, DQ_DO = AT_TILE, DQ_O = 2 * AT_TILE, DQ_KV = 3 * AT_TILE;
 constexpr int DQ_BAR = DQ_KV + 2 * DQ_STAGES * AT_TILE;
 constexpr int DQ_NBARS = 17;
 constexpr int DQ_SMEM = 1024 + DQ_BAR + 8 * (DQ_NBARS + 2);
@@ -410,7 +412,7 @@ constexpr int DQ_SMEM = 1024 + DQ_BAR + 8 * (DQ_NBARS + 2);
 __global__ void __launch_bounds__(BW_THREADS, 1)
     k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                     const BwParams p) {
+                     const __grid_constant__ CUtensorMap tmO, const BwParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -428,7 +430,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(b_qf, 1);
-    mbar_init(b_qe, 1);
+    mbar_init(b_qe, 9);  // the MMA thread's commit after the item's last S / dP + the 8 compute warps (D formed)
     for (int i = 0; i < DQ_STAGES; ++i) {
       mbar_init(b_kvf + 8 * i, 1);
       mbar_init(b_kve + 8 * i, 1);
@@ -462,9 +464,10 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
       for (int w = blockIdx.x, it = 0; ok && w < nitems; w += gridDim.x, ++it) {
         const int qt = p.nq - 1 - w / BH, bh = w % BH, b = bh / a.H, h = bh % a.H;
         if (it > 0 && !mbar_wait(b_qe, (uint32_t)(it - 1) & 1u, abort_flag, p.status)) break;
-        mbar_expect_tx(b_qf, 2 * AT_TILE);
+        mbar_expect_tx(b_qf, 3 * AT_TILE);
         bw_load(&tmQ, p.swap_q, sbase + DQ_Q, b_qf, qt * AT_B, h, b);
         bw_load(&tmdO, p.swap_o, sbase + DQ_DO, b_qf, qt * AT_B, h, b);
+        bw_load(&tmO, p.swap_o, sbase + DQ_O, b_qf, qt * AT_B, h, b);
         q_par = it & 1;
         for (int j = 0; j <= qt; ++j, ++g) {
           const int st = g % DQ_STAGES;
@@ -540,7 +543,29 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
       const int qi = qt * AT_B + r;
       const bool valid = qi < a.T;
       const float lse2 = valid ? a.lse[(long long)bh * a.T + qi] * 1.4426950408889634f : 0.f;
-      const float Dr = valid ? a.Dbuf[(long long)bh * a.T + qi] : 0.f;
+      // D = sum over d of dO[q, d] O[q, d] from the staged tiles (row r: 128 B, 16-byte
+      // piece c at ((c ^ (r & 7)) << 4), the 128B swizzle), pieces in order
+      if (!warp_wait(b_qf, (uint32_t)it & 1u, abort_flag, p.status)) break;
+      float Dr = 0.f;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint32_t off = (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
+        uint32_t x[4], y[4];
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3])
+                     : "r"(sbase + DQ_DO + off));
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(y[0]), "=r"(y[1]), "=r"(y[2]), "=r"(y[3])
+                     : "r"(sbase + DQ_O + off));
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          Dr = fmaf(__uint_as_float(x[e] << 16), __uint_as_float(y[e] << 16), Dr);
+          Dr = fmaf(__uint_as_float(x[e] & 0xFFFF0000u), __uint_as_float(y[e] & 0xFFFF0000u), Dr);
+        }
+      }
+      if (!valid) Dr = 0.f;
+      if (valid && half == 0) a.Dbuf[(long long)bh * a.T + qi] = Dr;
+      warp_arrive(b_qe);  // this warp is done with the item's dO and O tiles
       for (int j = 0; j < nk; ++j, ++g) {
         if (!warp_wait(b_sf, (uint32_t)g & 1u, abort_flag, p.status)) { ok = false; break; }
         tc_fence_after();
@@ -950,8 +975,8 @@ int attn_bwd_tc(const AttnArgs& a, cudaStream_t s) {
   if (!tc_args_ok(a)) return (int)cudaErrorInvalidValue;
   if ((reinterpret_cast<uintptr_t>(a.q) | reinterpret_cast<uintptr_t>(a.k) |
        reinterpret_cast<uintptr_t>(a.v) | reinterpret_cast<uintptr_t>(a.dO) |
-       reinterpret_cast<uintptr_t>(a.dq) | reinterpret_cast<uintptr_t>(a.dk) |
-       reinterpret_cast<uintptr_t>(a.dv)) & 15)
+       reinterpret_cast<uintptr_t>(a.o) | reinterpret_cast<uintptr_t>(a.dq) |
+       reinterpret_cast<uintptr_t>(a.dk) | reinterpret_cast<uintptr_t>(a.dv)) & 15 || !a.Dbuf)
     return (int)cudaErrorInvalidValue;
   static bool attr_set = false;
   if (!attr_set) {
@@ -972,14 +997,16 @@ int attn_bwd_tc(const AttnArgs& a, cudaStream_t s) {
   p.status = a.status;
   AttnArgs ao = a;  // dO shares the o strides
   ao.st = a.ost; ao.sh = a.osh; ao.sb = a.osb;
-  CUtensorMap tq, tk, tv, tdo;
+  CUtensorMap tq, tk, tv, tdo, to;
   if (!make_head_map(&tq, a.q, a, p.swap_q) || !make_head_map(&tk, a.k, a, p.swap_q) ||
-      !make_head_map(&tv, a.v, a, p.swap_q) || !make_head_map(&tdo, a.dO, ao, p.swap_o))
+      !make_head_map(&tv, a.v, a, p.swap_q) || !make_head_map(&tdo, a.dO, ao, p.swap_o) ||
+      !make_head_map(&to, a.o, ao, p.swap_o))
     return (int)cudaErrorInvalidValue;
   const long long items = (long long)p.nq * a.B * a.H;
   const int grid = (int)(items < num_sms() ? items : num_sms());
+  // dQ first: it also writes D = rowsum(dO * O), which the dK/dV kernel reads
+  launch_k(k_attn_bwd_dq_tc, grid, BW_THREADS, DQ_SMEM, s, tq, tk, tv, tdo, to, p);
   launch_k(k_attn_bwd_dkdv_tc, grid, BW_THREADS, DK_SMEM, s, tq, tk, tv, tdo, p);
-  launch_k(k_attn_bwd_dq_tc, grid, BW_THREADS, DQ_SMEM, s, tq, tk, tv, tdo, p);
   return (int)cudaGetLastError();
 }
 

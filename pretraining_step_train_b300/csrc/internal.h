@@ -88,10 +88,10 @@ struct AttnArgs {
   unsigned* status = nullptr;  // device status word for bounded-wait expiry (may be null)
 };
 // tcgen05 kernels (d = 64); a.status (may be null) receives ST_TIMEOUT on a bounded-wait expiry.
-// attn_bwd_tc expects a.Dbuf = rowsum(dO * O) already computed.
+// attn_bwd_tc writes D = rowsum(dO * O) to a.Dbuf ([B, H, T] fp32 scratch) and uses it.
 int attn_fwd_tc(const AttnArgs& a, cudaStream_t s);
 int attn_bwd_tc(const AttnArgs& a, cudaStream_t s);
-// bf16: the rowsum(dO * O) pre-pass into a.Dbuf, then attn_bwd_tc.
+// bf16: attn_bwd_tc (stride checks first).
 int attn_bwd_bf16(const AttnArgs& a, cudaStream_t s);
 int attn_fwd_f32(const AttnArgs& a, cudaStream_t s);
 int attn_bwd_f32(const AttnArgs& a, cudaStream_t s);
