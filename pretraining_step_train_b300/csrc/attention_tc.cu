@@ -393,6 +393,23 @@ struct BwParams {
   unsigned* status;
 };
 
+// Column sums of a 32-row x 32-column block held one row per lane: five
+// exchange-and-halve shuffle stages leave lane l with column l summed over the
+// 32 rows, in a fixed order.
+__device__ __forceinline__ float colsum_32x32(const float* v, int lane) {
+  float a[16], b[8], c[4], d[2];
+  const bool h16 = lane & 16, h8 = lane & 8, h4 = lane & 4, h2 = lane & 2, h1 = lane & 1;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) a[j] = (h16 ? v[j + 16] : v[j]) + __shfl_xor_sync(0xffffffffu, h16 ? v[j] : v[j + 16], 16);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) b[j] = (h8 ? a[j + 8] : a[j]) + __shfl_xor_sync(0xffffffffu, h8 ? a[j] : a[j + 8], 8);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) c[j] = (h4 ? b[j + 4] : b[j]) + __shfl_xor_sync(0xffffffffu, h4 ? b[j] : b[j + 4], 4);
+#pragma unroll
+  for (int j = 0; j < 2; ++j) d[j] = (h2 ? c[j + 2] : c[j]) + __shfl_xor_sync(0xffffffffu, h2 ? c[j] : c[j + 2], 2);
+  return (h1 ? d[1] : d[0]) + __shfl_xor_sync(0xffffffffu, h1 ? d[0] : d[1], 1);
+}
+
 __device__ __forceinline__ void bw_load(const CUtensorMap* tm, int swap, uint32_t dst, uint32_t bar,
                                         int t0, int h, int b) {
   if (swap) tma_load_4d(dst, tm, bar, 0, h, t0, b);
@@ -615,6 +632,14 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
       tmem_ld32(lane_base + C_DQ + half * 32, o);
       tmem_ld_wait();
       tc_fence_before();
+      if (a.bias_part) {  // this warp's 32 rows x 32 dq columns, summed per column
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = valid ? __uint_as_float(o[i]) * a.scale : 0.f;
+        const float cs = colsum_32x32(v, lane);
+        const long long prow = ((long long)b * p.nq + qt) * 4 + quad;
+        a.bias_part[prow * 3 * a.H * AT_D + h * AT_D + half * 32 + lane] = cs;
+      }
       if (valid) {
         bf16* dst = static_cast<bf16*>(a.dq) + (long long)b * a.sb + (long long)h * a.sh +
                     (long long)qi * a.st + half * 32;
@@ -853,6 +878,19 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
       tmem_ld32(lane_base + C_DK + half * 32, ok_);
       tmem_ld_wait();
       tc_fence_before();
+      if (a.bias_part) {  // this warp's 32 key rows x 32 columns of dk and of dv, summed per column
+        const int C = a.H * AT_D;
+        const long long prow = ((long long)b * p.nq + kt) * 4 + quad;
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = kr < a.T ? __uint_as_float(ok_[i]) * a.scale : 0.f;
+        float cs = colsum_32x32(v, lane);
+        a.bias_part[prow * 3 * C + C + h * AT_D + half * 32 + lane] = cs;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = kr < a.T ? __uint_as_float(ov[i]) : 0.f;
+        cs = colsum_32x32(v, lane);
+        a.bias_part[prow * 3 * C + 2 * C + h * AT_D + half * 32 + lane] = cs;
+      }
       if (kr < a.T) {
         const long long off = (long long)b * a.sb + (long long)h * a.sh + (long long)kr * a.st + half * 32;
         bf16* dvd = static_cast<bf16*>(a.dv) + off;

@@ -141,6 +141,7 @@ Plan make_plan(const Shape& s) {
   p.lnb_part = take(cur, layernorm_bwd_partials_floats(s.C) * f);
   // column-sum partials: the colsum kernel's, or the GELU' GEMM's one row per 32 rows
   size_t cs = std::max(colsum_partials_floats(4 * s.C), (size_t)((s.M() + 31) / 32) * 4 * s.C);
+  cs = std::max(cs, (size_t)attn_bias_part_rows(s.B, s.T) * 3 * s.C);  // QKV bias partials of the attention backward
   p.colsum_part = take(cur, cs * f);
   p.norm_part = take(cur, kNormParts * f);
   // stream-K flags (zeroed with the arena) and partial-sum slots of the GEMM engine
@@ -448,6 +449,7 @@ int backward_impl(gpt2* h) {
     a.osb = (long long)s.T * C; a.osh = s.d(); a.ost = C;
     a.scale = 1.0f / sqrtf((float)s.d());
     a.status = h->at<unsigned>(h->p.status);
+    if (bf) a.bias_part = csp;  // the QKV bias gradient's partial column sums
     int e = 0;
     REGION(GPT2_K_ATTN_BWD, attn_flops, 8.0 * MC * E, e = (bf ? attn_bwd_bf16(a, st) : attn_bwd_f32(a, st)));
     CKI(e);
@@ -456,7 +458,11 @@ int backward_impl(gpt2* h) {
     g.A = dqkv; g.lda = 3 * C; g.a_mn = 1; g.B = P.ln1(l); g.ldb = C; g.b_mn = 1;
     g.M = 3 * C; g.N = C; g.K = M; g.D = P.grad(P_QKVW, l); g.ldd = C;
     CKI(linear<T>(h, g));
-    REGION(GPT2_K_BIAS_GRAD, 0.0, 3.0 * MC * E, colsum<T>(P.grad(P_QKVB, l), dqkv, M, 3 * C, 3 * C, csp, st));
+    if (bf)
+      REGION(GPT2_K_BIAS_GRAD, 0.0, 4.0 * attn_bias_part_rows(s.B, s.T) * 3.0 * C,
+             colsum_reduce<T>(P.grad(P_QKVB, l), csp, attn_bias_part_rows(s.B, s.T), 3 * C, st));
+    else
+      REGION(GPT2_K_BIAS_GRAD, 0.0, 3.0 * MC * E, colsum<T>(P.grad(P_QKVB, l), dqkv, M, 3 * C, 3 * C, csp, st));
     g = GemmArgs();
     g.A = dqkv; g.lda = 3 * C; g.B = P.param(P_QKVW, l); g.ldb = C; g.b_mn = 1;
     g.M = M; g.N = C; g.K = 3 * C; g.D = dsmall; g.ldd = C;

@@ -86,7 +86,13 @@ struct AttnArgs {
   long long osb = 0, osh = 0, ost = 0;  // o, dO
   float scale = 0.f;
   unsigned* status = nullptr;  // device status word for bounded-wait expiry (may be null)
+  // tcgen05 backward only, may be null: bias_part[((b * nq + t / 128) * 4 + (t % 128) / 32) * 3C + c]
+  // receives the fp32 sum over those 32 positions t of column c of [dq | dk | dv] (C = H * d,
+  // nq = ceil(T / 128)), the partials of the QKV bias gradient
+  float* bias_part = nullptr;
 };
+// Rows of AttnArgs::bias_part for batch B and sequence length T.
+inline int attn_bias_part_rows(int B, int T) { return B * ((T + 127) / 128) * 4; }
 // tcgen05 kernels (d = 64); a.status (may be null) receives ST_TIMEOUT on a bounded-wait expiry.
 // attn_bwd_tc writes D = rowsum(dO * O) to a.Dbuf ([B, H, T] fp32 scratch) and uses it.
 int attn_fwd_tc(const AttnArgs& a, cudaStream_t s);
