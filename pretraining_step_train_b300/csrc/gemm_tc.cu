@@ -276,6 +276,13 @@ __device__ __forceinline__ float colsum_32x16(const float* v, int lane) {
   return d + __shfl_xor_sync(0xffffffffu, d, 1);
 }
 
+// 2^x by the hardware approximation (PTX ex2.approx.ftz.f32; relative error about 2^-22).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Hardware tanh (MUFU, PTX tanh.approx.f32): relative error about 2^-11, far
 // below the bf16 rounding of the values it feeds.
 __device__ __forceinline__ float tanh_hw(float x) {
@@ -628,21 +635,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
         if (epi == EPI_CE) {
-          // logits rounded to bf16 are stored and used for the statistics
+          // the logits are rounded to bf16 (pairwise); the stored values feed the statistics
 #pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] = __bfloat162float(__float2bfloat16_rn(v[j]));
+          for (int j = 0; j < 8; ++j) {
+            const uint32_t t = pack2_bf16(v[2 * j], v[2 * j + 1]);
+            v[2 * j] = __uint_as_float(t << 16);
+            v[2 * j + 1] = __uint_as_float(t & 0xFFFF0000u);
+          }
+          const bool full = x0 + CW <= g.V;  // only the last tile of the vocabulary has padding
           float cm = -INFINITY;
 #pragma unroll
           for (int j = 0; j < 16; ++j)
-            if (x0 + j < g.V) cm = fmaxf(cm, v[j]);
+            if (full || x0 + j < g.V) cm = fmaxf(cm, v[j]);
           if (cm > -INFINITY) {
-            const float mn = fmaxf(ce_m, cm);
-            float sacc = (ce_m > -INFINITY) ? ce_s * __expf(ce_m - mn) : 0.f;
+            // e^(z - m) as 2^(z log2(e) - m log2(e)): one fma and one ex2.approx per logit
+            constexpr float L2E = 1.4426950408889634f;
+            const float mn = fmaxf(ce_m, cm), nml = -mn * L2E;
+            float s0 = (ce_m > -INFINITY) ? ce_s * ex2_approx(fmaf(ce_m, L2E, nml)) : 0.f, s1 = 0.f;
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-              if (x0 + j < g.V) sacc += __expf(v[j] - mn);
+            for (int j = 0; j < 16; j += 2) {
+              if (full || x0 + j < g.V) s0 += ex2_approx(fmaf(v[j], L2E, nml));
+              if (full || x0 + j + 1 < g.V) s1 += ex2_approx(fmaf(v[j + 1], L2E, nml));
+            }
             ce_m = mn;
-            ce_s = sacc;
+            ce_s = s0 + s1;
           }
           if (tgt >= x0 && tgt < x0 + CW) {
 #pragma unroll
