@@ -798,28 +798,43 @@ void ce_reduce_partials(const float* pmax, const float* psum, int ntiles, int ld
 }
 
 // dz = (softmax(z) - onehot(target)) * inv_scale on n < V, 0 on the pad columns; in place.
+// e^(z - lse) is formed as 2^(z log2 e - lse log2 e) (one fma, one ex2.approx:
+// relative error about 2^-22, far below the bf16 rounding of dz); each thread
+// keeps two 16-byte vectors in flight.
 template <typename T>
 __global__ void __launch_bounds__(256)
     k_ce_dlogits(T* __restrict__ z, long long ldz, const float* __restrict__ lse,
                  const int32_t* __restrict__ tgt, int V, int Vpad, float inv_scale) {
   pdl_begin();
   constexpr int N = V16<T>::N;
+  constexpr float L2E = 1.4426950408889634f;
   const int r = blockIdx.x;
   T* zr = z + (long long)r * ldz;
-  const float l = lse[r];
+  const float nl = -lse[r] * L2E;
   int t = tgt[r];
   t = (t < 0 || t >= V) ? 0 : t;
-  for (int c0 = threadIdx.x * N; c0 < Vpad; c0 += blockDim.x * N) {
-    float v[N];
-    load16(zr + c0, v);
+  const int step = blockDim.x * N;
+  auto dz = [&](int c0, float* v) {
 #pragma unroll
     for (int e = 0; e < N; ++e) {
-      int c = c0 + e;
-      float p = (c < V) ? expf(v[e] - l) : 0.f;
+      const int c = c0 + e;
+      float p = 0.f;
+      if (c < V) asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(p) : "f"(fmaf(v[e], L2E, nl)));
       if (c == t) p -= 1.0f;
       v[e] = p * inv_scale;
     }
-    store16(zr + c0, v);
+  };
+  for (int c0 = threadIdx.x * N; c0 < Vpad; c0 += 2 * step) {
+    const int c1 = c0 + step;
+    float v0[N], v1[N];
+    load16(zr + c0, v0);
+    if (c1 < Vpad) load16(zr + c1, v1);
+    dz(c0, v0);
+    store16(zr + c0, v0);
+    if (c1 < Vpad) {
+      dz(c1, v1);
+      store16(zr + c1, v1);
+    }
   }
 }
 template <typename T>
@@ -1122,18 +1137,29 @@ void encoder_bwd(T* dwte, T* dwpe, float* dx0, const uint32_t* order, const int3
 }
 
 // ------------------------------------------------------------------ split-K reduction
+// Rows blockIdx.y, + gridDim.y, ... of the output, a float4 of columns per
+// thread; the splits are added in split order (four loads in flight at a time).
 __global__ void k_splitk_reduce(void* __restrict__ out, int out_f32, long long ldo,
                                 const float* __restrict__ ws, int splits, int M, int N) {
   pdl_begin();
-  const long long nq = (long long)M * N / 4;
+  const int n = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
+  if (n >= N) return;
   const long long plane = (long long)M * N;
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < nq;
-       i += (long long)gridDim.x * blockDim.x) {
-    long long e = i * 4;
-    int m = (int)(e / N), n = (int)(e % N);
-    float4 a = *reinterpret_cast<const float4*>(ws + e);
-    for (int sp = 1; sp < splits; ++sp) {
-      float4 b = *reinterpret_cast<const float4*>(ws + sp * plane + e);
+  for (int m = blockIdx.y; m < M; m += gridDim.y) {
+    const float* src = ws + (long long)m * N + n;
+    float4 a = *reinterpret_cast<const float4*>(src);
+    int sp = 1;
+    for (; sp + 3 < splits; sp += 4) {
+      float4 b[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) b[k] = *reinterpret_cast<const float4*>(src + (sp + k) * plane);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        a.x += b[k].x; a.y += b[k].y; a.z += b[k].z; a.w += b[k].w;
+      }
+    }
+    for (; sp < splits; ++sp) {
+      const float4 b = *reinterpret_cast<const float4*>(src + sp * plane);
       a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
     }
     if (out_f32) {
@@ -1150,8 +1176,8 @@ __global__ void k_splitk_reduce(void* __restrict__ out, int out_f32, long long l
 }
 void splitk_reduce(void* out, int out_f32, long long ldo, const float* ws, int splits, int M, int N,
                    cudaStream_t s) {
-  launch_k(k_splitk_reduce, grid_for((long long)M * N / 4, 256), 256, 0, s, out, out_f32, ldo, ws, splits,
-                                                                     M, N);
+  const dim3 grid((unsigned)((N / 4 + 255) / 256), (unsigned)(M < 65535 ? M : 65535));
+  launch_k(k_splitk_reduce, grid, 256, 0, s, out, out_f32, ldo, ws, splits, M, N);
 }
 
 // ------------------------------------------------------------------ global norm + AdamW
