@@ -1292,13 +1292,14 @@ __global__ void __launch_bounds__(256)
   }
   const float sc = norm_scale[1], bc1 = norm_scale[2], bc2 = norm_scale[3];
   const long long n4 = n / 4;
+  // the segments tile [0, n) in ascending order and each thread's i only grows,
+  // so its current segment is found by stepping forward from the last one
+  int seg = 0;
   for (long long q = blockIdx.x * (long long)blockDim.x + threadIdx.x; q < n4;
        q += (long long)gridDim.x * blockDim.x) {
     const long long i = q * 4;
-    float lam = 0.f;
-#pragma unroll 1
-    for (int k = 0; k < segs.n; ++k)
-      if (i >= segs.s[k].begin && i < segs.s[k].end) lam = segs.s[k].decay ? wd : 0.f;
+    while (seg < segs.n && i >= segs.s[seg].end) ++seg;
+    const float lam = (seg < segs.n && i >= segs.s[seg].begin && segs.s[seg].decay) ? wd : 0.f;
     float w[4], g[4], mm[4], vv[4];
     G4<float>::ld(master + i, w);
     G4<G>::ld(grad + i, g);
