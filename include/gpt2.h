@@ -132,6 +132,16 @@ int gpt2_backward(gpt2_t* h);
 int gpt2_clip_adamw(gpt2_t* h, float lr, float beta1, float beta2, float eps, float weight_decay,
                     float max_norm, int step_t, float* h_norm);
 
+/* Learning rate of step step_t (1-based, like step_t above) under linear warmup
+ * then cosine decay (llm.c GPT-2 1558M article, "Parameter guide": -k cosine,
+ * -u warmup, -q final fraction, -x total steps; the run log prints the warmup
+ * values): max_lr * t / warmup_steps for t <= warmup_steps; then
+ * max_lr * (f + (1 - f) * (1 + cos(pi * r)) / 2) with f = final_frac and
+ * r = (t - 1 - warmup_steps) / (total_steps - warmup_steps) clamped to [0, 1].
+ * Host only (no device work).  Returns a negative value for invalid arguments
+ * (t < 1, warmup_steps < 0, total_steps <= warmup_steps, max_lr < 0). */
+float gpt2_lr_schedule(int step_t, float max_lr, int warmup_steps, int total_steps, float final_frac);
+
 /* One whole step from host buffers: copies h_tokens / h_targets (int32 [B, T])
  * to the device, runs forward, backward, clip + AdamW, and copies the loss and
  * gradient norm back (h_loss / h_norm may be NULL).  Synchronises the stream.

@@ -60,6 +60,7 @@ SIGNATURES = {
     "gpt2_encoder_bwd": (_i, [_p, _p, _p, _p, _i, _i, _i, _i, _i, _p, _sz, _p]),
     "gemm_bf16": (_i, [_p, _p, _p, _i, _i, _i, _ll, _ll, _ll, _i, _i, _i, _i, _p, _sz, _p]),
     "gemm_bf16_sk_workspace_bytes": (_sz, []),
+    "gpt2_lr_schedule": (_f, [_i, _f, _i, _i, _f]),
     "gemm_bf16_epilogue": (_i, [_p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _ll, _ll, _ll, _i, _i, _i, _i, _p, _sz,
                                 _p]),
     "gpt2_test_set_gemm_poison": (_i, [_i]),

@@ -8,6 +8,7 @@
 #include <stdio.h>
 #include <stdlib.h>
 #include <string.h>
+#include <math.h>
 
 #include <algorithm>
 #include <string>
@@ -830,6 +831,15 @@ int gpt2_train_step_host(gpt2_t* h, const int32_t* h_tokens, const int32_t* h_ta
   if (st & ST_TOKEN) return GPT2_E_TOKEN;
   if (st & ST_NONFINITE) return GPT2_E_NONFINITE;
   return GPT2_OK;
+}
+
+float gpt2_lr_schedule(int step_t, float max_lr, int warmup_steps, int total_steps, float final_frac) {
+  if (step_t < 1 || warmup_steps < 0 || total_steps <= warmup_steps || !(max_lr >= 0.f)) return -1.f;
+  if (step_t <= warmup_steps) return (float)((double)max_lr * step_t / warmup_steps);
+  double r = (double)(step_t - 1 - warmup_steps) / (double)(total_steps - warmup_steps);
+  r = r < 0.0 ? 0.0 : (r > 1.0 ? 1.0 : r);
+  const double f = final_frac;
+  return (float)((double)max_lr * (f + (1.0 - f) * 0.5 * (1.0 + cos(3.14159265358979323846 * r))));
 }
 
 const float* gpt2_device_loss(gpt2_t* h) { return h ? h->at<float>(h->p.scalars) : nullptr; }
