@@ -64,7 +64,8 @@ enum gpt2_tensor {
   GPT2_GRADS = 1,  /* parameter gradients of the last backward */
   GPT2_ADAM_M = 2, /* AdamW first moment (fp32) */
   GPT2_ADAM_V = 3, /* AdamW second moment (fp32) */
-  GPT2_MASTER = 4  /* fp32 master weights (same as PARAMS in GPT2_FP32 mode) */
+  GPT2_MASTER = 4, /* fp32 master weights (same as PARAMS in GPT2_FP32 mode) */
+  GPT2_GRAD_ACC = 5 /* fp32 gradient accumulator of gpt2_grad_accumulate */
 };
 
 /* Kernel classes of the per-region timing (gpt2_profile). */
@@ -131,6 +132,18 @@ int gpt2_backward(gpt2_t* h);
  * stays on the device; h_norm, if not NULL, receives it after a stream sync. */
 int gpt2_clip_adamw(gpt2_t* h, float lr, float beta1, float beta2, float eps, float weight_decay,
                     float max_norm, int step_t, float* h_norm);
+
+/* Gradient accumulation over micro-batches (llm.c GPT-2 1558M article: the
+ * total batch of -d tokens is reached in micro-steps of B*T; its run log sets
+ * grad_accum_steps=8).  Call after gpt2_backward: acc = (first ? 0 : acc) +
+ * scale * grads, in fp32 (scale = 1/k for k micro-batches of B*T positions, so
+ * acc is the gradient of the mean loss over all of them).  gpt2_forward and
+ * gpt2_backward may then run on the next micro-batch.  gpt2_clip_adamw_accumulated
+ * is gpt2_clip_adamw with acc as the gradient (norm, clip and AdamW over it).
+ * Call order is checked (GPT2_E_STATE). */
+int gpt2_grad_accumulate(gpt2_t* h, int first, float scale);
+int gpt2_clip_adamw_accumulated(gpt2_t* h, float lr, float beta1, float beta2, float eps,
+                                float weight_decay, float max_norm, int step_t, float* h_norm);
 
 /* Learning rate of step step_t (1-based, like step_t above) under linear warmup
  * then cosine decay (llm.c GPT-2 1558M article, "Parameter guide": -k cosine,

@@ -17,7 +17,7 @@ LIB_PATH = os.path.join(HERE, "libgpt2.so")
 GPT2_OK, GPT2_E_INVAL, GPT2_E_STATE, GPT2_E_TOKEN = 0, -1, -2, -3
 GPT2_E_CUDA, GPT2_E_TIMEOUT, GPT2_E_NONFINITE, GPT2_E_UNSUPPORTED = -4, -5, -6, -7
 GPT2_FP32, GPT2_BF16 = 0, 1
-GPT2_PARAMS, GPT2_GRADS, GPT2_ADAM_M, GPT2_ADAM_V, GPT2_MASTER = 0, 1, 2, 3, 4
+GPT2_PARAMS, GPT2_GRADS, GPT2_ADAM_M, GPT2_ADAM_V, GPT2_MASTER, GPT2_GRAD_ACC = 0, 1, 2, 3, 4, 5
 KERNEL_CLASSES = ["gemm", "splitk_reduce", "attn_fwd", "attn_bwd", "layernorm_fwd", "layernorm_bwd",
                   "cross_entropy", "encoder", "bias_grad", "grad_norm", "adamw"]
 
@@ -61,6 +61,8 @@ SIGNATURES = {
     "gemm_bf16": (_i, [_p, _p, _p, _i, _i, _i, _ll, _ll, _ll, _i, _i, _i, _i, _p, _sz, _p]),
     "gemm_bf16_sk_workspace_bytes": (_sz, []),
     "gpt2_lr_schedule": (_f, [_i, _f, _i, _i, _f]),
+    "gpt2_grad_accumulate": (_i, [_p, _i, _f]),
+    "gpt2_clip_adamw_accumulated": (_i, [_p, _f, _f, _f, _f, _f, _f, _i, _p]),
     "gemm_bf16_epilogue": (_i, [_p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _ll, _ll, _ll, _i, _i, _i, _i, _p, _sz,
                                 _p]),
     "gpt2_test_set_gemm_poison": (_i, [_i]),
@@ -178,6 +180,17 @@ class Step:
         norm = ct.c_float(0.0)
         check(lib().gpt2_clip_adamw(self.h, lr, beta1, beta2, eps, weight_decay, max_norm, t,
                                     ct.byref(norm) if want_norm else None), "gpt2_clip_adamw")
+        return norm.value if want_norm else None
+
+    def grad_accumulate(self, first, scale):
+        check(lib().gpt2_grad_accumulate(self.h, 1 if first else 0, scale), "gpt2_grad_accumulate")
+
+    def clip_adamw_accumulated(self, lr=6e-4, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1,
+                               max_norm=1.0, t=1, want_norm=True):
+        norm = ct.c_float(0.0)
+        check(lib().gpt2_clip_adamw_accumulated(self.h, lr, beta1, beta2, eps, weight_decay, max_norm, t,
+                                                ct.byref(norm) if want_norm else None),
+              "gpt2_clip_adamw_accumulated")
         return norm.value if want_norm else None
 
     def train_step_host(self, tokens_np, targets_np, lr=6e-4, beta1=0.9, beta2=0.95, eps=1e-8,

@@ -76,7 +76,7 @@ bool is_decayed(int i) {
 // Arena plan: byte offsets of every region, 256-byte aligned.
 struct Plan {
   size_t total = 0;
-  size_t params, grads, master, adam_m, adam_v;
+  size_t params, grads, master, adam_m, adam_v, grad_acc;
   size_t tokens, targets;
   size_t res, x1, ln1, ln2, ln1_mean, ln1_rstd, ln2_mean, ln2_rstd, qkv, atty, att_lse, fch, fca;
   size_t lnf, lnf_mean, lnf_rstd, logits, ce_max, ce_sum, ce_tgt, ce_lse, ce_rows, scalars, status, hyper;
@@ -104,6 +104,7 @@ Plan make_plan(const Shape& s) {
   p.master = bf ? take(cur, N * f) : p.params;
   p.adam_m = take(cur, N * f);
   p.adam_v = take(cur, N * f);
+  p.grad_acc = take(cur, N * f);
   p.tokens = take(cur, M * 4);
   p.targets = take(cur, M * 4);
   p.res = take(cur, (L + 1) * M * C * e);
@@ -198,7 +199,7 @@ struct gpt2 {
 
 namespace {
 
-enum { ST_IDLE = 0, ST_FWD = 1, ST_BWD = 2 };
+enum { ST_IDLE = 0, ST_FWD = 1, ST_BWD = 2, ST_ACC = 3 };
 
 int prof_begin(gpt2* h) {
   if (!h->prof_on || h->evnext + 2 > (int)h->evpool.size()) return -1;
@@ -485,30 +486,37 @@ int backward_impl(gpt2* h) {
   return GPT2_OK;
 }
 
-template <typename T>
-int clip_adamw_impl(gpt2* h, float lr, float b1, float b2, float eps, float wd, float max_norm,
-                    int t, const OptHyper* hp = nullptr) {
+// Clip + AdamW with gradients g of type G: the step's storage-type gradients, or
+// the fp32 accumulator of gpt2_grad_accumulate.
+template <typename T, typename G>
+int clip_adamw_grads(gpt2* h, const G* g, float lr, float b1, float b2, float eps, float wd, float max_norm,
+                     int t, const OptHyper* hp) {
   cudaStream_t st = h->stream;
   float* ns = h->at<float>(h->p.scalars) + 1;
   int* counter = reinterpret_cast<int*>(h->at<float>(h->p.scalars) + 8);
   float* np_ = h->at<float>(h->p.norm_part);
   unsigned* status = h->at<unsigned>(h->p.status);
-  const double N = (double)h->N, E = sizeof(T);
-  REGION(GPT2_K_NORM, 0.0, N * E, {
-    grad_sumsq_partials<T>(np_, kNormParts, h->at<T>(h->p.grads), (long long)h->N, st);
+  const double N = (double)h->N, E = sizeof(T), EG = sizeof(G);
+  REGION(GPT2_K_NORM, 0.0, N * EG, {
+    grad_sumsq_partials<G>(np_, kNormParts, g, (long long)h->N, st);
     grad_norm_finalize(ns, np_, kNormParts, max_norm, status, counter, t, b1, b2, hp, st);
   });
   Segment segs[P_COUNT];
   for (int i = 0; i < P_COUNT; ++i) segs[i] = Segment{h->pl.off[i], h->pl.off[i + 1], is_decayed(i) ? 1 : 0};
   T* pcopy = sizeof(T) == 2 ? h->at<T>(h->p.params) : nullptr;
-  // master, m, v read + written (fp32), grad read, bf16 copy written
-  const double bytes = N * (24.0 + E + (sizeof(T) == 2 ? 2.0 : 0.0));
+  // master, m, v read + written (fp32), gradient read, bf16 copy written
+  const double bytes = N * (24.0 + EG + (sizeof(T) == 2 ? E : 0.0));
   REGION(GPT2_K_ADAMW, 0.0, bytes,
-         adamw<T, T>(h->at<float>(h->p.master), pcopy, h->at<T>(h->p.grads), h->at<float>(h->p.adam_m),
-                     h->at<float>(h->p.adam_v), (long long)h->N, segs, P_COUNT, ns, lr, b1, b2, eps, wd,
-                     hp, st));
+         adamw<G, T>(h->at<float>(h->p.master), pcopy, g, h->at<float>(h->p.adam_m), h->at<float>(h->p.adam_v),
+                     (long long)h->N, segs, P_COUNT, ns, lr, b1, b2, eps, wd, hp, st));
   CK(cudaGetLastError());
   return GPT2_OK;
+}
+
+template <typename T>
+int clip_adamw_impl(gpt2* h, float lr, float b1, float b2, float eps, float wd, float max_norm,
+                    int t, const OptHyper* hp = nullptr) {
+  return clip_adamw_grads<T, T>(h, h->at<T>(h->p.grads), lr, b1, b2, eps, wd, max_norm, t, hp);
 }
 
 int read_status(gpt2* h) {
@@ -667,6 +675,7 @@ int gpt2_get_tensor(gpt2_t* h, int which, float* dst, int dst_on_device) {
     case GPT2_ADAM_M: off = h->p.adam_m; break;
     case GPT2_ADAM_V: off = h->p.adam_v; break;
     case GPT2_MASTER: off = h->p.master; break;
+    case GPT2_GRAD_ACC: off = h->p.grad_acc; break;
     default: return GPT2_E_INVAL;
   }
   const size_t n = h->N;
@@ -787,6 +796,38 @@ int build_host_graph(gpt2* h) {
 }  // namespace
 
 extern "C" {
+
+int gpt2_grad_accumulate(gpt2_t* h, int first, float scale) {
+  if (!h) return GPT2_E_INVAL;
+  if (h->state != ST_BWD) return GPT2_E_STATE;
+  float* acc = h->at<float>(h->p.grad_acc);
+  if (h->s.prec == GPT2_BF16)
+    grad_accumulate<bf16>(acc, h->at<bf16>(h->p.grads), (long long)h->N, scale, first ? 1 : 0, h->stream);
+  else
+    grad_accumulate<float>(acc, h->at<float>(h->p.grads), (long long)h->N, scale, first ? 1 : 0, h->stream);
+  CK(cudaGetLastError());
+  h->state = ST_ACC;
+  return GPT2_OK;
+}
+
+int gpt2_clip_adamw_accumulated(gpt2_t* h, float lr, float beta1, float beta2, float eps, float weight_decay,
+                                float max_norm, int step_t, float* h_norm) {
+  if (!h) return GPT2_E_INVAL;
+  if (step_t < 0 || !(max_norm > 0.f)) return GPT2_E_INVAL;
+  if (h->state != ST_ACC) return GPT2_E_STATE;
+  const float* acc = h->at<float>(h->p.grad_acc);
+  int r = h->s.prec == GPT2_BF16
+              ? clip_adamw_grads<bf16, float>(h, acc, lr, beta1, beta2, eps, weight_decay, max_norm, step_t, nullptr)
+              : clip_adamw_grads<float, float>(h, acc, lr, beta1, beta2, eps, weight_decay, max_norm, step_t, nullptr);
+  if (r != GPT2_OK) return r;
+  h->state = ST_IDLE;
+  if (h_norm) {
+    int st = read_status(h);
+    CK(cudaMemcpy(h_norm, h->at<float>(h->p.scalars) + 1, 4, cudaMemcpyDeviceToHost));
+    if (st != GPT2_OK) return st;
+  }
+  return GPT2_OK;
+}
 
 int gpt2_train_step_host(gpt2_t* h, const int32_t* h_tokens, const int32_t* h_targets, float lr,
                          float beta1, float beta2, float eps, float weight_decay, float max_norm,

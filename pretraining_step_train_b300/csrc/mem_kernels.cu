@@ -1273,6 +1273,34 @@ template <> struct G4<bf16> {
   }
 };
 
+// acc = (first ? 0 : acc) + scale * g, four values per thread and step.
+template <typename G>
+__global__ void __launch_bounds__(256)
+    k_grad_acc(float* __restrict__ acc, const G* __restrict__ g, long long n, float scale, int first) {
+  pdl_begin();
+  const long long n4 = n / 4;
+  for (long long q = blockIdx.x * (long long)blockDim.x + threadIdx.x; q < n4;
+       q += (long long)gridDim.x * blockDim.x) {
+    const long long i = q * 4;
+    float a[4] = {0.f, 0.f, 0.f, 0.f}, b[4];
+    G4<G>::ld(g + i, b);
+    if (!first) G4<float>::ld(acc + i, a);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) a[e] = fmaf(scale, b[e], a[e]);
+    G4<float>::st(acc + i, a);
+  }
+  if (blockIdx.x == 0 && threadIdx.x < (int)(n - n4 * 4)) {
+    const long long i = n4 * 4 + threadIdx.x;
+    acc[i] = fmaf(scale, to_f(g[i]), first ? 0.f : acc[i]);
+  }
+}
+template <typename G>
+void grad_accumulate(float* acc, const G* g, long long n, float scale, int first, cudaStream_t s) {
+  launch_k(k_grad_acc<G>, grid_for(n / 4 + 1, 256, 148 * 8), 256, 0, s, acc, g, n, scale, first);
+}
+template void grad_accumulate<float>(float*, const float*, long long, float, int, cudaStream_t);
+template void grad_accumulate<bf16>(float*, const bf16*, long long, float, int, cudaStream_t);
+
 // m = b1 m + (1-b1) g; v = b2 v + (1-b2) g^2; w -= lr (m/bc1 / (sqrt(v/bc2) + eps) + wd_seg w)
 // with g = grad * clip_scale; clip scale and bias corrections come from
 // norm_scale[1..3] on the device; one pass over 4-element vectors.
@@ -1363,5 +1391,8 @@ template void adamw<float, float>(float*, float*, const float*, float*, float*, 
 template void adamw<bf16, bf16>(float*, bf16*, const bf16*, float*, float*, long long,
                                 const Segment*, int, const float*, float, float, float, float,
                                 float, const OptHyper*, cudaStream_t);
+template void adamw<float, bf16>(float*, bf16*, const float*, float*, float*, long long,
+                                 const Segment*, int, const float*, float, float, float, float,
+                                 float, const OptHyper*, cudaStream_t);
 
 }  // namespace gpt2k

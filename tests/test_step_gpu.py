@@ -190,3 +190,32 @@ def test_host_step_graph_matches_device_steps():
     a.train_step_host(tok, tgt, t=5)
     a.close()
     b.close()
+
+
+@pytest.mark.parametrize("prec,grad_tol,w_tol", [(binding.GPT2_BF16, 3e-2, 1e-2), (binding.GPT2_FP32, 1e-4, 1e-4)])
+def test_grad_accumulation_equals_the_large_batch(prec, grad_tol, w_tol):
+    """Two micro-batches of B sequences, each gradient accumulated with scale 1/2,
+    then one clip + AdamW, against the oracle's step on the 2B sequences at once:
+    the gradient of the mean loss over 2B rows is the mean of the two
+    micro-batch gradients."""
+    L, H, C, V, Vpad, T, B = (2, 2, 128, 1000, 1024, 128, 2) if prec == binding.GPT2_BF16 else (2, 2, 64, 256, 256, 64, 2)
+    cfg = O.Config(L, H, C, V, Vpad, T)
+    P = synth.init_params(51, L, C, V, Vpad, T, bf16_representable=prec == binding.GPT2_BF16)
+    tok, tgt = synth.token_batch(52, 2 * B, T, V)
+    flat = synth.flatten_params(P, L, C, Vpad, T)
+    s = binding.Step(L, H, C, V, Vpad, T, B, precision=prec)
+    s.set_params(flat)
+    # the accumulated step must follow backward; AdamW on the accumulator must follow an accumulate
+    assert binding.lib().gpt2_grad_accumulate(s.h, 1, 0.5) == binding.GPT2_E_STATE
+    losses = []
+    for i in range(2):
+        losses.append(s.forward(to_dev(tok[i * B:(i + 1) * B], "i32"), to_dev(tgt[i * B:(i + 1) * B], "i32")))
+        s.backward()
+        s.grad_accumulate(i == 0, 0.5)
+    acc = s.get(binding.GPT2_GRAD_ACC)
+    norm = s.clip_adamw_accumulated(LR, B1, B2, EPS, WD, CLIP, 1)
+    assert binding.lib().gpt2_clip_adamw_accumulated(s.h, LR, B1, B2, EPS, WD, CLIP, 1, None) == binding.GPT2_E_STATE
+    res = dict(loss=0.5 * (losses[0] + losses[1]), grads=acc, norm=norm, master=s.get(binding.GPT2_MASTER))
+    s.close()
+    ref = O.train_step(P, tok, tgt, cfg, lr=LR, t=1, beta1=B1, beta2=B2, eps=EPS, wd=WD, max_norm=CLIP)
+    _compare(cfg, P, res, ref, 1e-2 if prec == binding.GPT2_BF16 else 1e-4, grad_tol, w_tol, flat)
