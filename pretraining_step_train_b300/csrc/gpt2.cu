@@ -197,6 +197,12 @@ struct gpt2 {
   template <typename T> T* at(size_t off) const { return reinterpret_cast<T*>(base + off); }
 };
 
+// acc = (first ? 0 : acc) + scale * g over n values (fp32 accumulator; mem_kernels.cu).
+namespace gpt2k {
+template <typename G>
+void grad_accumulate(float* acc, const G* g, long long n, float scale, int first, cudaStream_t s);
+}  // namespace gpt2k
+
 namespace {
 
 enum { ST_IDLE = 0, ST_FWD = 1, ST_BWD = 2, ST_ACC = 3 };

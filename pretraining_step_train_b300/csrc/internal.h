@@ -154,9 +154,6 @@ void splitk_reduce(void* out, int out_f32, long long ldo, const float* ws, int s
 
 // Optimizer.
 struct Segment { long long begin, end; int decay; };
-// acc = (first ? 0 : acc) + scale * g over n values (fp32 accumulator).
-template <typename G>
-void grad_accumulate(float* acc, const G* g, long long n, float scale, int first, cudaStream_t s);
 constexpr int kMaxSegments = 16;
 template <typename G>
 void grad_sumsq_partials(float* partials, int nparts, const G* g, long long n, cudaStream_t s);
