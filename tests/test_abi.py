@@ -88,3 +88,29 @@ def test_strerror(lib):
     for s in range(-7, 1):
         assert lib.gpt2_strerror(s)
     assert binding.GPT2Error(binding.GPT2_E_STATE, "x").status == binding.GPT2_E_STATE
+
+
+def test_gemm_and_step_extensions_validate_on_host(lib):
+    """The stream-K / epilogue GEMM entry points and the accumulation calls refuse
+    bad arguments before any device work."""
+    # splits -1 / -2 need a 16-byte aligned workspace of the stated size
+    need = lib.gemm_bf16_sk_workspace_bytes()
+    assert need > 0
+    assert lib.gemm_bf16(16, 16, 16, 64, 64, 64, 64, 64, 64, 0, 0, 0, -1, None, need, None) == binding.GPT2_E_INVAL
+    assert lib.gemm_bf16(16, 16, 16, 64, 64, 64, 64, 64, 64, 0, 0, 0, -1, 4096, need - 1, None) == binding.GPT2_E_INVAL
+    assert lib.gemm_bf16(16, 16, 16, 64, 64, 64, 64, 64, 64, 0, 0, 0, -3, 4096, need, None) == binding.GPT2_E_INVAL
+    # fused-epilogue entry: epilogue code, operands of the epilogue, splits range
+    args = dict(A=16, B=16, D=16, D2=16, bias=16, X=16, col=None, M=64, N=64, K=64, lda=64, ldb=64, ldd=64)
+    def epi(e, splits=1, **kw):
+        a = dict(args, **kw)
+        return lib.gemm_bf16_epilogue(a["A"], a["B"], a["D"], a["D2"], a["bias"], a["X"], a["col"], a["M"], a["N"],
+                                      a["K"], a["lda"], a["ldb"], a["ldd"], 0, 0, e, splits, None, 0, None)
+    assert epi(0) == binding.GPT2_E_INVAL      # 0 is not a fused epilogue
+    assert epi(5) == binding.GPT2_E_INVAL
+    assert epi(1, bias=None) == binding.GPT2_E_INVAL
+    assert epi(2, X=None) == binding.GPT2_E_INVAL
+    assert epi(3, D2=None) == binding.GPT2_E_INVAL
+    assert epi(1, splits=2) == binding.GPT2_E_INVAL   # no K splits with a fused epilogue
+    assert epi(1, splits=-1) == binding.GPT2_E_INVAL  # stream-K without a workspace
+    assert lib.gpt2_grad_accumulate(None, 1, 0.5) == binding.GPT2_E_INVAL
+    assert lib.gpt2_clip_adamw_accumulated(None, 6e-4, 0.9, 0.95, 1e-8, 0.1, 1.0, 1, None) == binding.GPT2_E_INVAL
