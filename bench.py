@@ -400,7 +400,7 @@ def main():
         "config": {"workload": f"GPT-2 {args.config} train step (fwd+CE+bwd+clip+AdamW)", "B": B, "T": T, "L": L,
                    "H": H, "C": C, "V": V, "Vpad": Vpad, "global_batch_tokens": world * M,
                    "parallelism": f"{world} independent replica(s)", "graph": graph is not None,
-                   "l2": "working set (params+activations ~8 GB) exceeds L2; no flush",
+                   "l2": "working set (params, optimizer state, activations: ~9 GB) exceeds L2; no flush",
                    "tokens": "Zipf(1.1) streams over the vocab, targets shifted by one"},
         "mfu": {"flops_per_token": fpt, "convention": "6N+6LCT, N padded incl. wpe",
                 "vs_nominal_2250": round(achieved_tflops / NOMINAL_BF16_TFLOPS, 4),
