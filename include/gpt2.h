@@ -277,8 +277,10 @@ int gpt2_encoder_bwd(const int32_t* tok, float* dx0, void* dwte, void* dwpe, int
  * SMs; the sums are added in a fixed order (deterministic).  -2 takes stream-K
  * whenever the tiles do not fill whole waves.  Both need a 16-byte aligned
  * workspace of >= gemm_bf16_sk_workspace_bytes() bytes whose contents are zero
- * before its first use; every completed call leaves it reusable.  Calls that
- * share a workspace must not run concurrently. */
+ * before its first use; every completed call leaves it reusable (a call whose
+ * bounded waits expired may not: zero it again).  Calls that share a workspace
+ * must not run concurrently.  The step driver lowers its own workspace's flags
+ * whenever it reports GPT2_E_TIMEOUT. */
 int gemm_bf16(const void* A, const void* B, void* D, int M, int N, int K, long long lda,
               long long ldb, long long ldd, int a_mn, int b_mn, int d_f32, int splits,
               void* workspace, size_t workspace_bytes, void* stream);

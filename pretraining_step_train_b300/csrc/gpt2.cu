@@ -525,12 +525,22 @@ int clip_adamw_impl(gpt2* h, float lr, float b1, float b2, float eps, float wd, 
   return clip_adamw_grads<T, T>(h, h->at<T>(h->p.grads), lr, b1, b2, eps, wd, max_norm, t, hp);
 }
 
+// After an expired bounded wait a GEMM may have left stream-K flags raised;
+// lower them all so the next launch starts from a clean workspace.
+int clear_sk_flags(gpt2* h) {
+  if (h->p.sk_bytes) CK(cudaMemsetAsync(h->at<char>(h->p.sk_ws), 0, gemm_tc_sk_plane_offset(), h->stream));
+  return GPT2_OK;
+}
+
 int read_status(gpt2* h) {
   unsigned st = 0;
   CK(cudaStreamSynchronize(h->stream));
   CK(cudaMemcpy(&st, h->at<unsigned>(h->p.status), 4, cudaMemcpyDeviceToHost));
   if (st) CK(cudaMemsetAsync(h->at<unsigned>(h->p.status), 0, 4, h->stream));
-  if (st & ST_TIMEOUT) return GPT2_E_TIMEOUT;
+  if (st & ST_TIMEOUT) {
+    clear_sk_flags(h);
+    return GPT2_E_TIMEOUT;
+  }
   if (st & ST_TOKEN) return GPT2_E_TOKEN;
   if (st & ST_NONFINITE) return GPT2_E_NONFINITE;
   return GPT2_OK;
@@ -874,7 +884,10 @@ int gpt2_train_step_host(gpt2_t* h, const int32_t* h_tokens, const int32_t* h_ta
   if (h_norm) *h_norm = h->pin_out[1];
   unsigned st;
   std::memcpy(&st, h->pin_out + 2, 4);
-  if (st & ST_TIMEOUT) return GPT2_E_TIMEOUT;
+  if (st & ST_TIMEOUT) {
+    clear_sk_flags(h);
+    return GPT2_E_TIMEOUT;
+  }
   if (st & ST_TOKEN) return GPT2_E_TOKEN;
   if (st & ST_NONFINITE) return GPT2_E_NONFINITE;
   return GPT2_OK;
