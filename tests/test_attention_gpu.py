@@ -71,7 +71,7 @@ def test_attention_parity(B, H, T, layout):
 
 @pytest.mark.parametrize("T", [1024, 2048])
 def test_attention_microbench_shape_sampled_heads(T):
-    """BASELINE microbench layout [16, 12, T, 64]; oracle on a few sampled (b, h)."""
+    """The attention microbench layout [16, 12, T, 64]; oracle on a few sampled (b, h)."""
     import torch
     B, H = 16, 12
     q, k, v, do = synth.attention_inputs(T, B, H, T, D)

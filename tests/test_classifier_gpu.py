@@ -38,7 +38,7 @@ def test_classifier_parity(M, C, V, Vpad):
 
 
 def test_classifier_full_size_loss_and_sampled_rows():
-    """BASELINE classifier microbench size: M=16384, C=768, V=50257 -> 50304.
+    """The classifier microbench size: M=16384, C=768, V=50257 -> 50304.
     The loss matches the closed form ln V + C sigma^2 / 2 at init-like inputs and
     the oracle on sampled rows; dX rows are checked against the oracle row by row."""
     M, C, V, Vpad = 16384, 768, 50257, 50304
