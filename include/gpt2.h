@@ -191,13 +191,42 @@ int gpt2_profile_region(gpt2_t* h, int i, int* kernel_class, int* dims, double* 
  * GPT2_OK, GPT2_E_TOKEN, GPT2_E_TIMEOUT or GPT2_E_NONFINITE. */
 int gpt2_sync_status(gpt2_t* h);
 
+/* Update guard (llm.c GPT-2 1558M article, "400B token run": once instabilities
+ * appeared, the run skipped the parameter update whenever it detected a
+ * momentary spike, flags -sl 5.0 -sg 5.0; its run log prints a z-score beside
+ * the loss and the norm, shown as "+nan" until enough steps have passed).
+ * Every gpt2_clip_adamw / gpt2_clip_adamw_accumulated, on the device:
+ *   - scores the step's mean loss (for the accumulated call: the scale-weighted
+ *     sum of the micro-batch losses) and its gradient norm against the last
+ *     `window` finite values of each: z = (x - mean) / std with the population
+ *     mean and standard deviation; z is NaN while fewer than `window` values are
+ *     held, and 0 (or +-inf) when the deviation is 0;
+ *   - skips the update, leaving master weights, working weights, m and v
+ *     untouched and the device step counter where it was, when the loss or the
+ *     norm is not finite (always; the call reports GPT2_E_NONFINITE as before),
+ *     or when loss_z > 0 and the loss's z exceeds it, or norm_z > 0 and the
+ *     norm's z exceeds it (a spike: the call returns GPT2_OK);
+ *   - then adds the step's loss and norm to the window if both are finite.
+ * gpt2_set_guard sets the thresholds (<= 0 turns a check off) and the window
+ * (2 .. 256) and empties the window and the counters; it synchronises the
+ * stream.  A new handle starts with both checks off and a window of 128.
+ * gpt2_set_params does not touch the guard.  gpt2_guard_read synchronises and
+ * returns the last step's z-scores, the numbers of updates skipped for a spike
+ * and for a non-finite value, and whether the last update was skipped (any
+ * pointer may be NULL). */
+int gpt2_set_guard(gpt2_t* h, float loss_z, float norm_z, int window);
+int gpt2_guard_read(gpt2_t* h, float* z_loss, float* z_norm, int* skipped_spike, int* skipped_nonfinite,
+                    int* last_skipped);
+
 const char* gpt2_strerror(int status);
 /* Text of the last CUDA error seen by any call in this process. */
 const char* gpt2_last_cuda_error(void);
 
 /* ---------------------------------------------------------------- standalone kernels
  * Causal attention over bf16 tensors, head size d = 64, fp32 accumulation,
- * softmax scale `scale`.  Element (b, h, t, i) of q, k, v, dq, dk, dv is at
+ * softmax scale `scale` ("Let's reproduce GPT-2 (124M)" wiki page, "GPU
+ * optimisation ladder": FlashAttention computes the exact causal softmax
+ * attention without materialising the T x T matrix, 7.6x faster).  Element (b, h, t, i) of q, k, v, dq, dk, dv is at
  * b*sb + h*sh + t*st + i; of o and dO at b*osb + h*osh + t*ost + i (elements;
  * all strides multiples of 8, pointers 16-byte aligned).  lse: fp32 [B, H, T],
  * natural-log sum of exp of the scaled, masked scores (keys j <= query t).
@@ -205,7 +234,12 @@ const char* gpt2_last_cuda_error(void);
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int T,
              int d, long long sb, long long sh, long long st, long long osb, long long osh,
              long long ost, float scale, void* stream);
-/* Gradients of attn_fwd; workspace >= attn_workspace_bytes(B, H, T) device bytes. */
+/* Gradients of attn_fwd (same page and section: the backward of the exact
+ * attention, dV = P^T dO, dP = dO V^T, dS = P o (dP - rowsum(dO o O)),
+ * dQ = scale dS K, dK = scale dS^T Q, recomputing P from lse).  Tensor layouts
+ * as attn_fwd; dq, dk, dv are written (not accumulated).  workspace: device,
+ * >= attn_workspace_bytes(B, H, T) bytes, 16-byte aligned, owned by the caller
+ * and free again when the call's kernels have run. */
 int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
              const void* dO, void* dq, void* dk, void* dv, int B, int H, int T, int d, long long sb,
              long long sh, long long st, long long osb, long long osh, long long ost, float scale,
@@ -225,8 +259,10 @@ size_t attn_workspace_bytes(int B, int H, int T);
  *   - B * H * T > ATTN_BWD_NOALLOC_MAX_ROWS returns GPT2_E_UNSUPPORTED before
  *     anything is enqueued; other argument errors are those of attn_bwd.
  *   - The first call on a device, made with that device current, looks up the
- *     array's device address (cudaGetSymbolAddress) and caches it; make that
- *     first call before any stream capture.  A failed lookup returns GPT2_E_CUDA.
+ *     array's device address (cudaGetSymbolAddress) and caches it with the id
+ *     of the current context; make that first call before any stream capture.
+ *     After a device reset the first call in the new context looks it up again.
+ *     A failed lookup returns GPT2_E_CUDA (text in gpt2_last_cuda_error).
  *   - Every call on a device shares the one array.  Calls whose kernels may
  *     overlap on the GPU (different streams with no ordering) race on it.  The
  *     array keeps the last call's contents; nothing needs clearing, since
@@ -237,7 +273,10 @@ int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
                      long long sb, long long sh, long long st, long long osb, long long osh,
                      long long ost, float scale, void* stream);
 
-/* Tied lm_head + mean cross-entropy, fused: logits = x w^T (x bf16 [M, C],
+/* Tied lm_head + mean cross-entropy, fused ("Let's reproduce GPT-2 (124M)"
+ * wiki page, "Training recipe details": lm_head shares wte; "GPU optimisation
+ * ladder": the vocabulary padded 50257 -> 50304; qntz.me nanoGPT page: the
+ * loss is the mean cross-entropy, ln V at a uniform init): logits = x w^T (x bf16 [M, C],
  * w bf16 [Vpad, C]; columns >= V excluded from the softmax), loss = mean over
  * rows of lse - logit[target]; then dlogits = (softmax - onehot) / M,
  * dx = dlogits w (bf16 [M, C]) and dw = dlogits^T x (bf16 [Vpad, C], pad rows 0).
@@ -299,14 +338,32 @@ int gemm_bf16_epilogue(const void* A, const void* B, void* D, void* D2, const vo
                        int a_mn, int b_mn, int epi, int splits, void* workspace, size_t workspace_bytes,
                        void* stream);
 
-/* Test hook for the bounded waits: while on, the GEMM's TMA producer skips its
- * first shared-memory stage, so the MMA thread's wait expires (~2 s) and the
- * call's status word reports GPT2_E_TIMEOUT.  gemm_bf16_status runs one GEMM
- * like gemm_bf16 and returns that status after a stream sync. */
+/* Test hooks for the bounded waits (the pages have no counterpart).  Every
+ * spin-wait in the pipelined kernels gives up after about 2 s, latches
+ * GPT2_E_TIMEOUT in the call's status word and lets the kernel drain its copies,
+ * free its tensor memory and return, so the context stays usable.  While a bit
+ * of the mask is set, the launches that read it make one producer skip one
+ * transfer, so the matching consumer's wait runs out:
+ *   1  GEMM: the TMA producer skips its first shared-memory stage;
+ *   2  GEMM stream-K / in-kernel split schedules: partial units never raise their
+ *      ready flags, so the finishing CTAs' flag waits run out;
+ *   4  attention forward: the producer skips its first K/V stage;
+ *   8  attention backward, dQ kernel: the producer skips its first K/V stage;
+ *  16  attention backward, dK/dV kernel: the producer skips its first Q/dO stage;
+ *  32  streaming LayerNorm backward (bf16): one warp's first row copy is skipped.
+ * gpt2_test_set_poison sets the whole mask and returns the previous one;
+ * gpt2_test_set_gemm_poison(on) sets or clears bit 1 alone and returns its old
+ * value.  The mask is process-wide and read at launch time: use it from one
+ * thread with no other launches in flight. */
+int gpt2_test_set_poison(int mask);
 int gpt2_test_set_gemm_poison(int on);
+/* One GEMM like gemm_bf16 (bf16 D, no fused epilogue) with a caller-owned
+ * device status word (uint32, zeroed by the call), returning its status after a
+ * stream sync: GPT2_OK or GPT2_E_TIMEOUT.  splits: 1 (plain) or -1 / -2 (the
+ * in-kernel partial-sum schedules of gemm_bf16, with their workspace rules). */
 int gemm_bf16_status(const void* A, const void* B, void* D, int M, int N, int K, long long lda,
-                     long long ldb, long long ldd, int a_mn, int b_mn, void* d_status_word,
-                     void* stream);
+                     long long ldb, long long ldd, int a_mn, int b_mn, int splits, void* workspace,
+                     size_t workspace_bytes, void* d_status_word, void* stream);
 
 #ifdef __cplusplus
 }

@@ -65,8 +65,11 @@ SIGNATURES = {
     "gpt2_clip_adamw_accumulated": (_i, [_p, _f, _f, _f, _f, _f, _f, _i, _p]),
     "gemm_bf16_epilogue": (_i, [_p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _ll, _ll, _ll, _i, _i, _i, _i, _p, _sz,
                                 _p]),
+    "gpt2_test_set_poison": (_i, [_i]),
     "gpt2_test_set_gemm_poison": (_i, [_i]),
-    "gemm_bf16_status": (_i, [_p, _p, _p, _i, _i, _i, _ll, _ll, _ll, _i, _i, _p, _p]),
+    "gemm_bf16_status": (_i, [_p, _p, _p, _i, _i, _i, _ll, _ll, _ll, _i, _i, _i, _p, _sz, _p, _p]),
+    "gpt2_set_guard": (_i, [_p, _f, _f, _i]),
+    "gpt2_guard_read": (_i, [_p, _fp, _fp, ct.POINTER(_i), ct.POINTER(_i), ct.POINTER(_i)]),
 }
 
 _lib = None
@@ -242,3 +245,15 @@ class Step:
 
     def sync_status(self) -> int:
         return lib().gpt2_sync_status(self.h)
+
+    def set_guard(self, loss_z=0.0, norm_z=0.0, window=128):
+        check(lib().gpt2_set_guard(self.h, loss_z, norm_z, window), "gpt2_set_guard")
+
+    def guard_read(self):
+        """{z_loss, z_norm, skipped_spike, skipped_nonfinite, last_skipped} of the update guard."""
+        zl, zn = ct.c_float(), ct.c_float()
+        sp, nf, last = ct.c_int(), ct.c_int(), ct.c_int()
+        check(lib().gpt2_guard_read(self.h, ct.byref(zl), ct.byref(zn), ct.byref(sp), ct.byref(nf),
+                                    ct.byref(last)), "gpt2_guard_read")
+        return dict(z_loss=zl.value, z_norm=zn.value, skipped_spike=sp.value, skipped_nonfinite=nf.value,
+                    last_skipped=last.value)

@@ -55,6 +55,7 @@ struct AtParams {
   float c2;      // scale * log2(e)
   uint32_t idesc_s, idesc_pv;
   unsigned* status;
+  int poison;  // test hook (POISON_ATTN_FWD): the producer skips its first K/V stage
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -168,6 +169,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
           const int st = g % AT_KV_STAGES;
           const uint32_t ph = (uint32_t)(g / AT_KV_STAGES) & 1u;
           if (!mbar_wait(b_kve + 8 * st, ph ^ 1u, abort_flag, p.status)) { ok = false; break; }
+          if ((p.poison & POISON_ATTN_FWD) && g == 0) continue;
           const uint32_t kd = sbase + AT_KV_OFF + st * 2 * AT_TILE;
           mbar_expect_tx(b_kvf + 8 * st, 2 * AT_TILE);
           load(&tmK, kd, b_kvf + 8 * st, j * AT_B);
@@ -391,6 +393,7 @@ struct BwParams {
   float c2;            // scale * log2(e)
   uint32_t idesc_s, idesc_d;  // M128 N128 (K-major B) and M128 N64 (MN-major B)
   unsigned* status;
+  int poison;  // test hook (POISON_ATTN_DQ / POISON_ATTN_DKDV): a producer skips its first stage
 };
 
 // Column sums of a 32-row x 32-column block held one row per lane: five
@@ -490,6 +493,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
           const int st = g % DQ_STAGES;
           const uint32_t ph = (uint32_t)(g / DQ_STAGES) & 1u;
           if (!mbar_wait(b_kve + 8 * st, ph ^ 1u, abort_flag, p.status)) { ok = false; break; }
+          if ((p.poison & POISON_ATTN_DQ) && g == 0) continue;
           const uint32_t kd = sbase + DQ_KV + st * 2 * AT_TILE;
           mbar_expect_tx(b_kvf + 8 * st, 2 * AT_TILE);
           bw_load(&tmK, p.swap_q, kd, b_kvf + 8 * st, j * AT_B, h, b);
@@ -738,7 +742,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
         const int st = g % DK_STAGES;
         const uint32_t ph = (uint32_t)(g / DK_STAGES) & 1u;
         if (!warp_wait(b_qde + 8 * st, ph ^ 1u, abort_flag, p.status)) { ok = false; break; }
-        if (lane == 0) {
+        if (lane == 0 && !((p.poison & POISON_ATTN_DKDV) && g == 0)) {
           const uint32_t qd = sbase + DK_QD + st * 2 * AT_TILE;
           mbar_expect_tx(b_qdf + 8 * st, 2 * AT_TILE);
           bw_load(&tmQ, p.swap_q, qd, b_qdf + 8 * st, i * AT_B, h, b);
@@ -754,7 +758,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
           lb[slot + 2] = v ? -a.Dbuf[(long long)bh * a.T + q] : 0.f;
         }
         warp_arrive(b_qdf + 8 * st);
-        last_par[st] = (int)ph;
+        if (!((p.poison & POISON_ATTN_DKDV) && g == 0)) last_par[st] = (int)ph;
       }
     }
     if (lane == 0) {
@@ -985,12 +989,9 @@ int attn_fwd_tc(const AttnArgs& a, cudaStream_t s) {
   if ((reinterpret_cast<uintptr_t>(a.q) | reinterpret_cast<uintptr_t>(a.k) |
        reinterpret_cast<uintptr_t>(a.v) | reinterpret_cast<uintptr_t>(a.o)) & 15)
     return (int)cudaErrorInvalidValue;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k_attn_fwd_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, AT_SMEM);
-    if (e != cudaSuccess) return (int)e;
-    attr_set = true;
-  }
+  static PerDeviceOnce attr;
+  cudaError_t e = smem_limit_once(reinterpret_cast<const void*>(k_attn_fwd_tc), AT_SMEM, &attr);
+  if (e != cudaSuccess) return (int)e;
   AtParams p;
   p.a = a;
   p.nq = (a.T + AT_B - 1) / AT_B;
@@ -999,6 +1000,7 @@ int attn_fwd_tc(const AttnArgs& a, cudaStream_t s) {
   p.idesc_s = mma_idesc(AT_B, 0);
   p.idesc_pv = mma_idesc(AT_D, 1);
   p.status = a.status;
+  p.poison = test_poison();
   CUtensorMap tq, tk, tv;
   if (!make_head_map(&tq, a.q, a, p.swap_ht) || !make_head_map(&tk, a.k, a, p.swap_ht) ||
       !make_head_map(&tv, a.v, a, p.swap_ht))
@@ -1016,14 +1018,11 @@ int attn_bwd_tc(const AttnArgs& a, cudaStream_t s) {
        reinterpret_cast<uintptr_t>(a.o) | reinterpret_cast<uintptr_t>(a.dq) |
        reinterpret_cast<uintptr_t>(a.dk) | reinterpret_cast<uintptr_t>(a.dv)) & 15 || !a.Dbuf)
     return (int)cudaErrorInvalidValue;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k_attn_bwd_dq_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, DQ_SMEM);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(k_attn_bwd_dkdv_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, DK_SMEM);
-    if (e != cudaSuccess) return (int)e;
-    attr_set = true;
-  }
+  static PerDeviceOnce attr_dq, attr_dkdv;
+  cudaError_t e = smem_limit_once(reinterpret_cast<const void*>(k_attn_bwd_dq_tc), DQ_SMEM, &attr_dq);
+  if (e == cudaSuccess)
+    e = smem_limit_once(reinterpret_cast<const void*>(k_attn_bwd_dkdv_tc), DK_SMEM, &attr_dkdv);
+  if (e != cudaSuccess) return (int)e;
   BwParams p;
   p.a = a;
   p.nq = (a.T + AT_B - 1) / AT_B;
@@ -1033,6 +1032,7 @@ int attn_bwd_tc(const AttnArgs& a, cudaStream_t s) {
   p.idesc_s = mma_idesc(AT_B, 0);
   p.idesc_d = mma_idesc(AT_D, 1);
   p.status = a.status;
+  p.poison = test_poison();
   AttnArgs ao = a;  // dO shares the o strides
   ao.st = a.ost; ao.sh = a.osh; ao.sb = a.osb;
   CUtensorMap tq, tk, tv, tdo, to;

@@ -10,13 +10,14 @@
 //
 // The array is static device memory of this library: every GPU that loads the
 // library holds it (4 MiB) until the process exits.  Its address is looked up
-// once per device, on the first call made with that device current, and
-// cached.  That first call should therefore be made before any stream capture.
-// Every call on a device uses the same array: calls whose kernels may overlap
-// on the GPU (different streams, no ordering between them) race on it.  The
-// array keeps whatever the last call left in it; nothing needs clearing,
-// because the pre-pass writes every row of D before the dK/dV and dQ kernels
-// read it.
+// on the first call made on a device, with that device current, and cached
+// together with the id of the context it belongs to; a call in a new context
+// (after a device reset) looks it up again.  The first call on a device should
+// therefore be made before any stream capture.  Every call on a device uses
+// the same array: calls whose kernels may overlap on the GPU (different
+// streams, no ordering between them) race on it.  The array keeps whatever the
+// last call left in it; nothing needs clearing, because the dQ kernel, which
+// runs first, writes every row of D before the dK/dV kernel reads it.
 #include <mutex>
 
 #include "common.cuh"
@@ -29,22 +30,28 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
-float* g_scratch_ptr[kMaxDevices] = {};
+struct CachedAddress {
+  unsigned long long ctx = 0;  // id of the context the address belongs to (0: none cached)
+  float* ptr = nullptr;
+};
+CachedAddress g_scratch[kMaxDevices];
 
-// Device address of g_attn_bwd_scratch on the current device (looked up once).
+// Device address of g_attn_bwd_scratch in the current device's current context.
 cudaError_t scratch_for_current_device(float** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
+  const unsigned long long id = gpt2k::current_context_id();
+  if (id == 0 || g_scratch[dev].ctx != id) {
     void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_attn_bwd_scratch);
+    e = cudaGetSymbolAddress(&p, g_attn_bwd_scratch);  // makes the device's context current if it was not
     if (e != cudaSuccess) return e;
-    g_scratch_ptr[dev] = static_cast<float*>(p);
+    g_scratch[dev].ptr = static_cast<float*>(p);
+    g_scratch[dev].ctx = gpt2k::current_context_id();
   }
-  *out = g_scratch_ptr[dev];
+  *out = g_scratch[dev].ptr;
   return cudaSuccess;
 }
 
@@ -64,7 +71,8 @@ extern "C" int attn_bwd_noalloc(const void* q, const void* k, const void* v, con
   if (d != 64) return GPT2_E_UNSUPPORTED;
   if ((long long)B * H * T > ATTN_BWD_NOALLOC_MAX_ROWS) return GPT2_E_UNSUPPORTED;
   float* scratch = nullptr;
-  if (scratch_for_current_device(&scratch) != cudaSuccess) return GPT2_E_CUDA;
+  cudaError_t ce = scratch_for_current_device(&scratch);
+  if (ce != cudaSuccess) return gpt2k::cuda_fail(ce, "attn_bwd_noalloc: scratch address");
   gpt2k::AttnArgs a;
   a.q = q; a.k = k; a.v = v; a.o = const_cast<void*>(o); a.lse = const_cast<float*>(lse); a.dO = dO;
   a.dq = dq; a.dk = dk; a.dv = dv; a.Dbuf = scratch;
@@ -73,6 +81,6 @@ extern "C" int attn_bwd_noalloc(const void* q, const void* k, const void* v, con
   a.scale = scale;
   int e = gpt2k::attn_bwd_bf16(a, static_cast<cudaStream_t>(stream));
   if (e == (int)cudaErrorInvalidValue) return GPT2_E_INVAL;
-  if (e) return GPT2_E_CUDA;
+  if (e) return gpt2k::cuda_fail((cudaError_t)e, "attn_bwd_noalloc");
   return GPT2_OK;
 }

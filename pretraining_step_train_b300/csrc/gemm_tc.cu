@@ -67,8 +67,6 @@ struct TcParams {
 };
 enum { SK_NONE = 0, SK_STREAM = 1, SK_SPLIT = 2, SK_REDUCE = 3 };  // SK_REDUCE: host-side plan only
 
-int g_poison = 0;
-
 // Tile index -> (M tile, N tile, K split).  Consecutive tiles (one wave of
 // CTAs) share the tile of the larger operand, so it is read from DRAM about
 // once while the smaller operand is re-read from L2.
@@ -369,7 +367,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         bool stop = false;
         for (int kb = w.kb0; kb < w.kb1; ++kb) {
           if (!mbar_wait(b_empty + 8 * stage, phase ^ 1, abort_flag, p.status)) { stop = true; break; }
-          if (!(p.poison && first)) {
+          if (!((p.poison & POISON_GEMM_TMA) && first)) {
             const uint32_t sa = s_tiles + stage * STAGE_BYTES, sb = sa + A_TILE;
             const uint32_t fb = b_full + 8 * stage;
             mbar_expect_tx(fb, STAGE_BYTES);
@@ -503,7 +501,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         __threadfence();
         __syncwarp();
-        if (lane == 0) st_release_gpu(p.sk_flags + w.slot * EPI_WARPS + ew, 1u);
+        if (lane == 0 && !(p.poison & POISON_GEMM_FLAG)) st_release_gpu(p.sk_flags + w.slot * EPI_WARPS + ew, 1u);
         x_issue(nxb, ny, bx);  // the next unit's first operand chunk
         prev_stored = false;
         if (++abuf == 2) { abuf = 0; aphase ^= 1; }
@@ -840,12 +838,6 @@ int num_sms() {
   return n;
 }
 
-int gemm_tc_poison(int on) {
-  int old = g_poison;
-  g_poison = on;
-  return old;
-}
-
 int gemm_tc_stat_cols() { return WCOLS; }
 
 size_t gemm_tc_ws_bytes(int M, int N, int splits) {
@@ -935,12 +927,9 @@ int gemm_tc(const GemmArgs& g, int splits, void* ws, size_t ws_bytes, unsigned* 
   if (g.epi == EPI_BIAS_GELU && !aligned16(g.D2)) return (int)cudaErrorInvalidValue;
   if ((g.epi == EPI_BIAS || g.epi == EPI_BIAS_RESID || g.epi == EPI_BIAS_GELU) && !aligned16(g.bias))
     return (int)cudaErrorInvalidValue;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e != cudaSuccess) return (int)e;
-    attr_set = true;
-  }
+  static PerDeviceOnce attr;
+  cudaError_t ae = smem_limit_once(reinterpret_cast<const void*>(k_gemm_tc), SMEM_BYTES, &attr);
+  if (ae != cudaSuccess) return (int)ae;
   TcParams p;
   p.g = g;
   p.mt = (g.M + BM - 1) / BM;
@@ -983,7 +972,7 @@ int gemm_tc(const GemmArgs& g, int splits, void* ws, size_t ws_bytes, unsigned* 
       return (int)cudaErrorInvalidValue;
   }
   p.status = status;
-  p.poison = g_poison;
+  p.poison = test_poison();
   p.out_f32 = ((p.splits > 1 && p.sk == SK_NONE) || g.epi == EPI_F32) ? 1 : 0;
   p.load_x = (g.epi == EPI_BIAS_RESID || g.epi == EPI_GELU_BWD) ? 1 : 0;
   p.m_fast = ((double)g.N * g.K > (double)g.M * g.K) ? 1 : 0;

@@ -11,9 +11,12 @@
 #include <math.h>
 
 #include <algorithm>
-#include <string>
 #include <cstring>
+#include <mutex>
+#include <string>
 #include <vector>
+
+#include <cuda.h>
 
 #include "common.cuh"
 #include "internal.h"
@@ -22,13 +25,61 @@
 using namespace gpt2k;
 
 namespace {
-
 thread_local std::string g_last_cuda_error = "no error";
+std::mutex g_once_mu;
+int g_test_poison = 0;
+}  // namespace
+
+namespace gpt2k {
+
+int test_poison() { return g_test_poison; }
 
 int cuda_fail(cudaError_t e, const char* where) {
   g_last_cuda_error = std::string(where) + ": " + cudaGetErrorString(e);
   return GPT2_E_CUDA;
 }
+
+unsigned long long current_context_id() {
+  typedef CUresult (*GetCurrent)(CUcontext*);
+  typedef CUresult (*GetId)(CUcontext, unsigned long long*);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  static std::once_flag looked_up;
+  std::call_once(looked_up, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrent>(p);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetId>(p);
+  });
+  if (!get_current || !get_id) return 0;
+  CUcontext c = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&c) != CUDA_SUCCESS || !c) return 0;
+  if (get_id(c, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+cudaError_t smem_limit_once(const void* kernel, int bytes, PerDeviceOnce* once) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_once_mu);
+  const unsigned long long id = current_context_id();
+  if (id != 0 && once->ctx[dev] == id) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  once->ctx[dev] = current_context_id();  // the call above made the context current if it was not
+  return cudaSuccess;
+}
+
+}  // namespace gpt2k
+
+namespace {
 #define CK(call)                                        \
   do {                                                  \
     cudaError_t e_ = (call);                            \
@@ -79,7 +130,7 @@ struct Plan {
   size_t params, grads, master, adam_m, adam_v, grad_acc;
   size_t tokens, targets;
   size_t res, x1, ln1, ln2, ln1_mean, ln1_rstd, ln2_mean, ln2_rstd, qkv, atty, att_lse, fch, fca;
-  size_t lnf, lnf_mean, lnf_rstd, logits, ce_max, ce_sum, ce_tgt, ce_lse, ce_rows, scalars, status, hyper;
+  size_t lnf, lnf_mean, lnf_rstd, logits, ce_max, ce_sum, ce_tgt, ce_lse, ce_rows, scalars, status, hyper, guard;
   size_t dres, dres_b, dbig, dqkv, dsmall, attD, order, lnb_part, colsum_part, norm_part, sk_ws;
   size_t sk_bytes = 0;
   int ce_tiles = 0;
@@ -130,9 +181,12 @@ Plan make_plan(const Shape& s) {
   p.ce_tgt = take(cur, M * f);
   p.ce_lse = take(cur, M * f);
   p.ce_rows = take(cur, M * f);
-  p.scalars = take(cur, 16 * f);  // [0] loss, [1] norm, [2] clip scale
+  // [0] loss, [1] norm, [2] clip scale, [3..4] bias corrections, [5] update skipped,
+  // [6] accumulated loss of gpt2_grad_accumulate, [8] step counter (int)
+  p.scalars = take(cur, 16 * f);
   p.status = take(cur, 16);
   p.hyper = take(cur, sizeof(OptHyper));
+  p.guard = take(cur, sizeof(GuardState));
   p.dres = take(cur, M * C * f);
   p.dres_b = bf ? take(cur, M * C * e) : p.dres;
   p.dbig = take(cur, M * 4 * C * e);
@@ -194,13 +248,17 @@ struct gpt2 {
   int32_t* pin_tgt = nullptr;
   OptHyper* pin_hyp = nullptr;
   float* pin_out = nullptr;  // [0] loss, [1] norm, [2] status bits
+  // update guard settings (thresholds <= 0: off; the device state lives in the arena)
+  float guard_loss_z = 0.f, guard_norm_z = 0.f;
+  int guard_window = 0;
   template <typename T> T* at(size_t off) const { return reinterpret_cast<T*>(base + off); }
 };
 
 // acc = (first ? 0 : acc) + scale * g over n values (fp32 accumulator; mem_kernels.cu).
 namespace gpt2k {
 template <typename G>
-void grad_accumulate(float* acc, const G* g, long long n, float scale, int first, cudaStream_t s);
+void grad_accumulate(float* acc, const G* g, long long n, float scale, int first, const float* loss,
+                     float* acc_loss, cudaStream_t s);
 }  // namespace gpt2k
 
 namespace {
@@ -495,8 +553,8 @@ int backward_impl(gpt2* h) {
 // Clip + AdamW with gradients g of type G: the step's storage-type gradients, or
 // the fp32 accumulator of gpt2_grad_accumulate.
 template <typename T, typename G>
-int clip_adamw_grads(gpt2* h, const G* g, float lr, float b1, float b2, float eps, float wd, float max_norm,
-                     int t, const OptHyper* hp) {
+int clip_adamw_grads(gpt2* h, const G* g, const float* loss, float lr, float b1, float b2, float eps, float wd,
+                     float max_norm, int t, const OptHyper* hp) {
   cudaStream_t st = h->stream;
   float* ns = h->at<float>(h->p.scalars) + 1;
   int* counter = reinterpret_cast<int*>(h->at<float>(h->p.scalars) + 8);
@@ -505,7 +563,8 @@ int clip_adamw_grads(gpt2* h, const G* g, float lr, float b1, float b2, float ep
   const double N = (double)h->N, E = sizeof(T), EG = sizeof(G);
   REGION(GPT2_K_NORM, 0.0, N * EG, {
     grad_sumsq_partials<G>(np_, kNormParts, g, (long long)h->N, st);
-    grad_norm_finalize(ns, np_, kNormParts, max_norm, status, counter, t, b1, b2, hp, st);
+    grad_norm_finalize(ns, np_, kNormParts, max_norm, status, counter, t, b1, b2, hp, loss,
+                       h->at<GuardState>(h->p.guard), st);
   });
   Segment segs[P_COUNT];
   for (int i = 0; i < P_COUNT; ++i) segs[i] = Segment{h->pl.off[i], h->pl.off[i + 1], is_decayed(i) ? 1 : 0};
@@ -522,13 +581,35 @@ int clip_adamw_grads(gpt2* h, const G* g, float lr, float b1, float b2, float ep
 template <typename T>
 int clip_adamw_impl(gpt2* h, float lr, float b1, float b2, float eps, float wd, float max_norm,
                     int t, const OptHyper* hp = nullptr) {
-  return clip_adamw_grads<T, T>(h, h->at<T>(h->p.grads), lr, b1, b2, eps, wd, max_norm, t, hp);
+  return clip_adamw_grads<T, T>(h, h->at<T>(h->p.grads), h->at<float>(h->p.scalars), lr, b1, b2, eps, wd,
+                                max_norm, t, hp);
 }
 
 // After an expired bounded wait a GEMM may have left stream-K flags raised;
 // lower them all so the next launch starts from a clean workspace.
 int clear_sk_flags(gpt2* h) {
   if (h->p.sk_bytes) CK(cudaMemsetAsync(h->at<char>(h->p.sk_ws), 0, gemm_tc_sk_plane_offset(), h->stream));
+  return GPT2_OK;
+}
+
+constexpr int kGuardDefaultWindow = 128;
+
+// Uploads a fresh update-guard state (empty window, zero counters) with these settings.
+int reset_guard(gpt2* h, float loss_z, float norm_z, int window) {
+  GuardState g;
+  memset(&g, 0, sizeof(g));
+  g.loss_z_max = loss_z;
+  g.norm_z_max = norm_z;
+  g.window = window;
+  const float nan = __builtin_nanf("");
+  g.z_loss = nan;
+  g.z_norm = nan;
+  h->guard_loss_z = loss_z;
+  h->guard_norm_z = norm_z;
+  h->guard_window = window;
+  CK(cudaMemcpyAsync(h->at<GuardState>(h->p.guard), &g, sizeof(g), cudaMemcpyHostToDevice, h->stream));
+  // the source is a stack object: finish the copy before it goes out of scope
+  CK(cudaStreamSynchronize(h->stream));
   return GPT2_OK;
 }
 
@@ -584,6 +665,11 @@ int gpt2_create(int L, int H, int C, int V, int Vpad, int T, int B, int precisio
   if (e != cudaSuccess) {
     delete h;
     return cuda_fail(e, "gpt2_create memset");
+  }
+  int r = reset_guard(h, 0.f, 0.f, kGuardDefaultWindow);
+  if (r != GPT2_OK) {
+    delete h;
+    return r;
   }
   *out = h;
   return GPT2_OK;
@@ -817,10 +903,14 @@ int gpt2_grad_accumulate(gpt2_t* h, int first, float scale) {
   if (!h) return GPT2_E_INVAL;
   if (h->state != ST_BWD) return GPT2_E_STATE;
   float* acc = h->at<float>(h->p.grad_acc);
+  const float* loss = h->at<float>(h->p.scalars);
+  float* acc_loss = h->at<float>(h->p.scalars) + 6;
   if (h->s.prec == GPT2_BF16)
-    grad_accumulate<bf16>(acc, h->at<bf16>(h->p.grads), (long long)h->N, scale, first ? 1 : 0, h->stream);
+    grad_accumulate<bf16>(acc, h->at<bf16>(h->p.grads), (long long)h->N, scale, first ? 1 : 0, loss, acc_loss,
+                          h->stream);
   else
-    grad_accumulate<float>(acc, h->at<float>(h->p.grads), (long long)h->N, scale, first ? 1 : 0, h->stream);
+    grad_accumulate<float>(acc, h->at<float>(h->p.grads), (long long)h->N, scale, first ? 1 : 0, loss, acc_loss,
+                           h->stream);
   CK(cudaGetLastError());
   h->state = ST_ACC;
   return GPT2_OK;
@@ -833,8 +923,10 @@ int gpt2_clip_adamw_accumulated(gpt2_t* h, float lr, float beta1, float beta2, f
   if (h->state != ST_ACC) return GPT2_E_STATE;
   const float* acc = h->at<float>(h->p.grad_acc);
   int r = h->s.prec == GPT2_BF16
-              ? clip_adamw_grads<bf16, float>(h, acc, lr, beta1, beta2, eps, weight_decay, max_norm, step_t, nullptr)
-              : clip_adamw_grads<float, float>(h, acc, lr, beta1, beta2, eps, weight_decay, max_norm, step_t, nullptr);
+              ? clip_adamw_grads<bf16, float>(h, acc, h->at<float>(h->p.scalars) + 6, lr, beta1, beta2, eps,
+                                              weight_decay, max_norm, step_t, nullptr)
+              : clip_adamw_grads<float, float>(h, acc, h->at<float>(h->p.scalars) + 6, lr, beta1, beta2, eps,
+                                               weight_decay, max_norm, step_t, nullptr);
   if (r != GPT2_OK) return r;
   h->state = ST_IDLE;
   if (h_norm) {
@@ -908,6 +1000,26 @@ const float* gpt2_device_norm(gpt2_t* h) { return h ? h->at<float>(h->p.scalars)
 int gpt2_sync_status(gpt2_t* h) {
   if (!h) return GPT2_E_INVAL;
   return read_status(h);
+}
+
+int gpt2_set_guard(gpt2_t* h, float loss_z, float norm_z, int window) {
+  if (!h) return GPT2_E_INVAL;
+  if (window < 2 || window > kGuardMaxWindow || !(loss_z == loss_z) || !(norm_z == norm_z)) return GPT2_E_INVAL;
+  return reset_guard(h, loss_z, norm_z, window);
+}
+
+int gpt2_guard_read(gpt2_t* h, float* z_loss, float* z_norm, int* skipped_spike, int* skipped_nonfinite,
+                    int* last_skipped) {
+  if (!h) return GPT2_E_INVAL;
+  GuardState g;
+  CK(cudaStreamSynchronize(h->stream));
+  CK(cudaMemcpy(&g, h->at<GuardState>(h->p.guard), offsetof(GuardState, pad), cudaMemcpyDeviceToHost));
+  if (z_loss) *z_loss = g.z_loss;
+  if (z_norm) *z_norm = g.z_norm;
+  if (skipped_spike) *skipped_spike = g.skipped_spike;
+  if (skipped_nonfinite) *skipped_nonfinite = g.skipped_nonfinite;
+  if (last_skipped) *last_skipped = g.last_skipped;
+  return GPT2_OK;
 }
 
 const char* gpt2_strerror(int status) {
@@ -1121,19 +1233,31 @@ int gemm_bf16_epilogue(const void* A, const void* B, void* D, void* D2, const vo
   return GPT2_OK;
 }
 
-int gpt2_test_set_gemm_poison(int on) { return gemm_tc_poison(on); }
+int gpt2_test_set_gemm_poison(int on) {
+  const int old = g_test_poison;
+  g_test_poison = on ? (old | POISON_GEMM_TMA) : (old & ~POISON_GEMM_TMA);
+  return (old & POISON_GEMM_TMA) ? 1 : 0;
+}
+
+int gpt2_test_set_poison(int mask) {
+  const int old = g_test_poison;
+  g_test_poison = mask;
+  return old;
+}
 
 int gemm_bf16_status(const void* A, const void* B, void* D, int M, int N, int K, long long lda,
-                     long long ldb, long long ldd, int a_mn, int b_mn, void* d_status_word,
-                     void* stream) {
+                     long long ldb, long long ldd, int a_mn, int b_mn, int splits, void* workspace,
+                     size_t workspace_bytes, void* d_status_word, void* stream) {
   if (!al16(A) || !al16(B) || !al16(D) || !d_status_word) return GPT2_E_INVAL;
+  if (splits != 1 && splits != -1 && splits != -2) return GPT2_E_INVAL;
+  if (splits < 0 && (!al16(workspace) || workspace_bytes < gemm_tc_sk_ws_bytes())) return GPT2_E_INVAL;
   GemmArgs g;
   g.A = A; g.lda = lda; g.a_mn = a_mn ? 1 : 0; g.B = B; g.ldb = ldb; g.b_mn = b_mn ? 1 : 0;
   g.M = M; g.N = N; g.K = K; g.D = D; g.ldd = ldd; g.epi = EPI_STORE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   unsigned* status = static_cast<unsigned*>(d_status_word);
   CK(cudaMemsetAsync(status, 0, 4, st));
-  int e = gemm_tc(g, 1, nullptr, 0, status, st);
+  int e = gemm_tc(g, splits, splits < 0 ? workspace : nullptr, splits < 0 ? workspace_bytes : 0, status, st);
   if (e == (int)cudaErrorInvalidValue) return GPT2_E_INVAL;
   if (e) return cuda_fail((cudaError_t)e, "gemm_bf16_status");
   unsigned hs = 0;

@@ -6,6 +6,37 @@
 
 namespace gpt2k {
 
+// ------------------------------------------------------------------ host helpers (gpt2.cu)
+// Records "where: <CUDA error text>" as this thread's last CUDA error (see
+// gpt2_last_cuda_error) and returns GPT2_E_CUDA.
+int cuda_fail(cudaError_t e, const char* where);
+// Unique id of the CUDA context current on this thread, 0 when there is none.
+// A device reset gives the device a new primary context with a new id, and
+// with it new kernel attributes and new addresses of static device memory.
+unsigned long long current_context_id();
+// Per-device record of a one-time setting: the id of the context it was made in.
+struct PerDeviceOnce {
+  unsigned long long ctx[64] = {};
+};
+// Raises `kernel`'s dynamic shared-memory limit to `bytes` in the current
+// context, once per device and context: the attribute belongs to the context,
+// so a process that drives several GPUs (or resets one) sets it again there.
+// Thread-safe.
+cudaError_t smem_limit_once(const void* kernel, int bytes, PerDeviceOnce* once);
+
+// Test hooks for the bounded waits (gpt2_test_set_poison): while a bit is set,
+// the launches that read it make one producer skip one transfer, so that the
+// matching consumer's bounded wait runs out.
+enum PoisonBits {
+  POISON_GEMM_TMA = 1,    // GEMM producer skips its first shared-memory stage
+  POISON_GEMM_FLAG = 2,   // stream-K / split partial units never raise their ready flags
+  POISON_ATTN_FWD = 4,    // attention forward producer skips its first K/V stage
+  POISON_ATTN_DQ = 8,     // attention dQ kernel producer skips its first K/V stage
+  POISON_ATTN_DKDV = 16,  // attention dK/dV kernel producer skips its first Q/dO stage
+  POISON_LN_BWD = 32,     // streaming LayerNorm backward skips the first row copy of one warp
+};
+int test_poison();
+
 // ------------------------------------------------------------------ GEMM
 // D[m, n] = sum_k A(m, k) * B(n, k), fp32 accumulation, then an epilogue.
 // A(m, k) = A[m * lda + k] when a_mn == 0 (K-major), A[k * lda + m] when 1.
@@ -65,7 +96,6 @@ size_t gemm_tc_sk_ws_bytes();
 int gemm_tc_effective_splits(int K, int splits);
 size_t gemm_tc_ws_bytes(int M, int N, int splits);
 int gemm_tc_pick_splits(int M, int N, int K, int num_sms);
-int gemm_tc_poison(int on);  // test hook: the TMA producer skips its first stage when on
 // Columns covered by one EPI_CE statistics partial (row m's partial j covers
 // columns [j*cols, (j+1)*cols)).
 int gemm_tc_stat_cols();
@@ -124,9 +154,6 @@ void colsum(T* out, const T* x, int M, int N, long long ld, float* partials, cud
 template <typename T>
 void colsum_reduce(T* out, const float* partials, int nparts, int N, cudaStream_t s);
 size_t colsum_partials_floats(int N);
-template <typename T> void gelu_fwd(T* y, const T* x, long long n, cudaStream_t s);
-template <typename T> void gelu_bwd(T* dx, const T* dy, const T* x, long long n, cudaStream_t s);
-template <typename T> void residual_add(T* y, const T* a, const T* b, long long n, cudaStream_t s);
 template <typename T> void to_storage(T* dst, const float* src, long long n, cudaStream_t s);
 template <typename T> void to_f32(float* dst, const T* src, long long n, cudaStream_t s);
 
@@ -165,9 +192,34 @@ struct OptHyper {
   float lr, b1, b2, eps, wd, max_norm;
   int t, pad;
 };
+// Update guard, device resident (llm.c GPT-2 1558M article: the long run skipped
+// the parameter update when it saw a momentary spike, flags -sl / -sg; the run
+// log prints a z-score beside the loss and the norm, "+nan" until it is defined).
+// Each step's loss and gradient norm get a z-score against the previous `window`
+// finite values of the same quantity (population mean and standard deviation;
+// NaN while fewer than `window` values are held; 0 when the deviation is 0).
+// The update is skipped when the loss or the norm is not finite, or when a
+// threshold > 0 is set and that z-score exceeds it.
+constexpr int kGuardMaxWindow = 256;
+struct GuardState {
+  float loss_z_max, norm_z_max;  // thresholds (<= 0: that check is off)
+  int window;                    // values held for the statistics (2 .. kGuardMaxWindow)
+  int count;                     // finite values held so far (<= window)
+  int head;                      // next ring slot
+  int skipped_spike;             // updates skipped for a z-score over its threshold
+  int skipped_nonfinite;         // updates skipped for a non-finite loss or norm
+  int last_skipped;              // 1 when the last update was skipped
+  float z_loss, z_norm;          // z-scores of the last step
+  float pad[6];
+  float loss_hist[kGuardMaxWindow];
+  float norm_hist[kGuardMaxWindow];
+};
+// norm_scale[0] = ||g||, [1] = clip scale, [2] = 1 - b1^t, [3] = 1 - b2^t, [4] = 1 when the
+// update is skipped (then the step counter does not advance).  `loss`: the step's
+// mean loss on the device; `guard` may be null (then only non-finite values skip).
 void grad_norm_finalize(float* norm_scale, const float* partials, int nparts, float max_norm,
                         unsigned* status, int* counter, int host_t, float b1, float b2,
-                        const OptHyper* hp, cudaStream_t s);
+                        const OptHyper* hp, const float* loss, GuardState* guard, cudaStream_t s);
 // bf16 mode: master/m/v fp32 with a bf16 copy of the parameters; fp32 mode: param_copy null.
 template <typename G, typename P>
 void adamw(float* master, P* param_copy, const G* grad, float* m, float* v, long long n,

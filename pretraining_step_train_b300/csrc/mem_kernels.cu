@@ -385,7 +385,7 @@ __global__ void __launch_bounds__(kLnsWarps * 32, 1)
                            const bf16* __restrict__ x, const float* __restrict__ mean,
                            const float* __restrict__ rstd, const bf16* __restrict__ w,
                            float* __restrict__ partials, int M, int C, int accumulate, int want_sum, int nbuf,
-                           unsigned* status) {
+                           unsigned* status, int poison) {
   pdl_begin();
   extern __shared__ __align__(128) uint8_t lsm[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -409,6 +409,7 @@ __global__ void __launch_bounds__(kLnsWarps * 32, 1)
   const int nrows = gw < M ? (M - 1 - gw) / nw + 1 : 0;
   const uint32_t tx = (accumulate ? 8u : 4u) * (uint32_t)C;
   auto issue = [&](int k) {  // lane 0: row k of this warp into stage k % nbuf
+    if (poison && k == 0 && gw == 0) return;  // test hook: this row's copy never arrives
     const long long r = gw + (long long)k * nw;
     const int st = k % nbuf;
     const uint32_t dst = smem_u32(mine + (size_t)st * SB), bar = bar0 + 8u * st;
@@ -550,7 +551,8 @@ void layernorm_bwd(float* dres, T* dres_b, const T* dy, const T* x, const float*
   do {                                                                                                 \
     cudaFuncSetAttribute(k_layernorm_bwd_stream<P>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm); \
     launch_k(k_layernorm_bwd_stream<P>, nblocks, kLnsWarps * 32, sm, s, dres, (bf16*)dres_b, (const bf16*)dy, \
-             (const bf16*)x, mean, rstd, (const bf16*)w, partials, M, C, accumulate, want_sum, nbuf, status); \
+             (const bf16*)x, mean, rstd, (const bf16*)w, partials, M, C, accumulate, want_sum, nbuf, status, \
+             (test_poison() & POISON_LN_BWD) ? 1 : 0);                                                 \
   } while (0)
       if (per <= 1) LNS(1);
       else if (per <= 2) LNS(2);
@@ -654,49 +656,6 @@ void colsum(T* out, const T* x, int M, int N, long long ld, float* partials, cud
 
 // ------------------------------------------------------------------ elementwise
 template <typename T>
-__global__ void k_gelu_fwd(T* __restrict__ y, const T* __restrict__ x, long long n) {
-  pdl_begin();
-  constexpr int N = V16<T>::N;
-  for (long long i = (blockIdx.x * (long long)blockDim.x + threadIdx.x) * N; i < n;
-       i += (long long)gridDim.x * blockDim.x * N) {
-    float v[N];
-    load16(x + i, v);
-#pragma unroll
-    for (int e = 0; e < N; ++e) v[e] = gelu_f(v[e]);
-    store16(y + i, v);
-  }
-}
-template <typename T>
-__global__ void k_gelu_bwd(T* __restrict__ dx, const T* __restrict__ dy, const T* __restrict__ x,
-                           long long n) {
-  pdl_begin();
-  constexpr int N = V16<T>::N;
-  for (long long i = (blockIdx.x * (long long)blockDim.x + threadIdx.x) * N; i < n;
-       i += (long long)gridDim.x * blockDim.x * N) {
-    float a[N], b[N];
-    load16(dy + i, a);
-    load16(x + i, b);
-#pragma unroll
-    for (int e = 0; e < N; ++e) a[e] = a[e] * gelu_grad_f(b[e]);
-    store16(dx + i, a);
-  }
-}
-template <typename T>
-__global__ void k_residual(T* __restrict__ y, const T* __restrict__ a, const T* __restrict__ b,
-                           long long n) {
-  pdl_begin();
-  constexpr int N = V16<T>::N;
-  for (long long i = (blockIdx.x * (long long)blockDim.x + threadIdx.x) * N; i < n;
-       i += (long long)gridDim.x * blockDim.x * N) {
-    float u[N], v[N];
-    load16(a + i, u);
-    load16(b + i, v);
-#pragma unroll
-    for (int e = 0; e < N; ++e) u[e] = u[e] + v[e];
-    store16(y + i, u);
-  }
-}
-template <typename T>
 __global__ void k_to_storage(T* __restrict__ dst, const float* __restrict__ src, long long n) {
   pdl_begin();
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
@@ -711,15 +670,6 @@ __global__ void k_to_f32(float* __restrict__ dst, const T* __restrict__ src, lon
     dst[i] = to_f(src[i]);
 }
 
-template <typename T> void gelu_fwd(T* y, const T* x, long long n, cudaStream_t s) {
-  launch_k(k_gelu_fwd<T>, grid_for(n / V16<T>::N, 256), 256, 0, s, y, x, n);
-}
-template <typename T> void gelu_bwd(T* dx, const T* dy, const T* x, long long n, cudaStream_t s) {
-  launch_k(k_gelu_bwd<T>, grid_for(n / V16<T>::N, 256), 256, 0, s, dx, dy, x, n);
-}
-template <typename T> void residual_add(T* y, const T* a, const T* b, long long n, cudaStream_t s) {
-  launch_k(k_residual<T>, grid_for(n / V16<T>::N, 256), 256, 0, s, y, a, b, n);
-}
 template <typename T> void to_storage(T* dst, const float* src, long long n, cudaStream_t s) {
   launch_k(k_to_storage<T>, grid_for(n, 256), 256, 0, s, dst, src, n);
 }
@@ -1207,11 +1157,13 @@ void grad_sumsq_partials(float* partials, int nparts, const G* g, long long n, c
   launch_k(k_sumsq<G>, nparts, 512, 0, s, partials, g, n, chunk);
 }
 
-// norm_scale[0] = ||g||, [1] = clip scale, [2] = 1 - b1^t, [3] = 1 - b2^t where
-// t = host_t when > 0, else the device step counter + 1 (the counter is stored).
-__global__ void k_norm_finalize(float* norm_scale, const float* __restrict__ partials, int nparts,
-                                float max_norm, unsigned* status, int* counter, int host_t,
-                                float b1, float b2, const OptHyper* __restrict__ hp) {
+// Norm, clip scale, bias corrections and the update guard (see GuardState).
+// t = host_t when > 0, else the device step counter + 1 (stored unless the
+// update is skipped).
+__global__ void __launch_bounds__(1024)
+    k_norm_finalize(float* norm_scale, const float* __restrict__ partials, int nparts, float max_norm,
+                    unsigned* status, int* counter, int host_t, float b1, float b2,
+                    const OptHyper* __restrict__ hp, const float* __restrict__ loss, GuardState* guard) {
   pdl_begin();
   if (hp) {
     max_norm = hp->max_norm;
@@ -1219,31 +1171,75 @@ __global__ void k_norm_finalize(float* norm_scale, const float* __restrict__ par
     b1 = hp->b1;
     b2 = hp->b2;
   }
-  __shared__ double sh[32];
-  double s = 0.0;
-  for (int i = threadIdx.x; i < nparts; i += blockDim.x) s += (double)partials[i];
+  __shared__ double sh[5][32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+  // [0]: the squared-gradient partials; [1..4]: the guard's window sums of the held
+  // losses, their squares, the held norms and their squares
+  double q[5] = {0.0, 0.0, 0.0, 0.0, 0.0};
+  for (int i = threadIdx.x; i < nparts; i += blockDim.x) q[0] += (double)partials[i];
+  const int held = guard ? guard->count : 0;
+  if (guard && threadIdx.x < held) {
+    const double lv = guard->loss_hist[threadIdx.x], nv = guard->norm_hist[threadIdx.x];
+    q[1] = lv; q[2] = lv * lv; q[3] = nv; q[4] = nv * nv;
+  }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-  if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = s;
+  for (int k = 0; k < 5; ++k)
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) q[k] += __shfl_xor_sync(0xffffffffu, q[k], o);
+  if (lane == 0)
+#pragma unroll
+    for (int k = 0; k < 5; ++k) sh[k][warp] = q[k];
   __syncthreads();
   if (threadIdx.x == 0) {
-    double t = 0.0;
-    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += sh[w];
-    float norm = (float)sqrt(t);
+    double t[5] = {0.0, 0.0, 0.0, 0.0, 0.0};
+    for (int w = 0; w < nwarps; ++w)
+#pragma unroll
+      for (int k = 0; k < 5; ++k) t[k] += sh[k][w];
+    const float norm = (float)sqrt(t[0]);
+    const float lv = loss ? *loss : 0.f;
     norm_scale[0] = norm;
     norm_scale[1] = (norm > max_norm) ? max_norm / norm : 1.0f;
-    if (!isfinite(norm) && status) atomicOr(status, ST_NONFINITE);
+    const bool finite = isfinite(norm) && isfinite(lv);
+    if (!finite && status) atomicOr(status, ST_NONFINITE);
+    bool skip = !finite;
+    if (guard) {
+      float zl = __int_as_float(0x7fc00000), zn = zl;  // NaN until the window is full
+      if (held >= guard->window) {
+        const double sl = t[1], sl2 = t[2], sn = t[3], sn2 = t[4];
+        const double n = (double)held;
+        const double ml = sl / n, mn = sn / n;
+        const double vl = fmax(sl2 / n - ml * ml, 0.0), vn = fmax(sn2 / n - mn * mn, 0.0);
+        zl = vl > 0.0 ? (float)(((double)lv - ml) / sqrt(vl)) : ((double)lv == ml ? 0.f : (float)copysign(INFINITY, (double)lv - ml));
+        zn = vn > 0.0 ? (float)(((double)norm - mn) / sqrt(vn)) : ((double)norm == mn ? 0.f : (float)copysign(INFINITY, (double)norm - mn));
+      }
+      guard->z_loss = zl;
+      guard->z_norm = zn;
+      const bool spike = finite && ((guard->loss_z_max > 0.f && zl > guard->loss_z_max) ||
+                                    (guard->norm_z_max > 0.f && zn > guard->norm_z_max));
+      if (!finite) guard->skipped_nonfinite += 1;
+      if (spike) guard->skipped_spike += 1;
+      skip = skip || spike;
+      guard->last_skipped = skip ? 1 : 0;
+      if (finite) {  // every finite observation enters the window, skipped or not
+        const int hd = guard->head;
+        guard->loss_hist[hd] = lv;
+        guard->norm_hist[hd] = norm;
+        guard->head = hd + 1 == guard->window ? 0 : hd + 1;
+        if (guard->count < guard->window) guard->count += 1;
+      }
+    }
+    norm_scale[4] = skip ? 1.f : 0.f;
     const int step = host_t > 0 ? host_t : counter[0] + 1;
-    counter[0] = step;
+    if (!skip) counter[0] = step;
     norm_scale[2] = 1.0f - powf(b1, (float)step);
     norm_scale[3] = 1.0f - powf(b2, (float)step);
   }
 }
 void grad_norm_finalize(float* norm_scale, const float* partials, int nparts, float max_norm,
                         unsigned* status, int* counter, int host_t, float b1, float b2,
-                        const OptHyper* hp, cudaStream_t s) {
+                        const OptHyper* hp, const float* loss, GuardState* guard, cudaStream_t s) {
   launch_k(k_norm_finalize, 1, 1024, 0, s, norm_scale, partials, nparts, max_norm, status, counter,
-           host_t, b1, b2, hp);
+           host_t, b1, b2, hp, loss, guard);
 }
 
 struct SegTable { Segment s[kMaxSegments]; int n; };
@@ -1274,10 +1270,14 @@ template <> struct G4<bf16> {
 };
 
 // acc = (first ? 0 : acc) + scale * g, four values per thread and step.
+// The loss is accumulated the same way (acc_loss = (first ? 0 : acc_loss) + scale * loss),
+// so the update guard sees the mean loss of the accumulated micro-batches.
 template <typename G>
 __global__ void __launch_bounds__(256)
-    k_grad_acc(float* __restrict__ acc, const G* __restrict__ g, long long n, float scale, int first) {
+    k_grad_acc(float* __restrict__ acc, const G* __restrict__ g, long long n, float scale, int first,
+               const float* __restrict__ loss, float* __restrict__ acc_loss) {
   pdl_begin();
+  if (blockIdx.x == 0 && threadIdx.x == 0 && loss) *acc_loss = fmaf(scale, *loss, first ? 0.f : *acc_loss);
   const long long n4 = n / 4;
   for (long long q = blockIdx.x * (long long)blockDim.x + threadIdx.x; q < n4;
        q += (long long)gridDim.x * blockDim.x) {
@@ -1295,11 +1295,14 @@ __global__ void __launch_bounds__(256)
   }
 }
 template <typename G>
-void grad_accumulate(float* acc, const G* g, long long n, float scale, int first, cudaStream_t s) {
-  launch_k(k_grad_acc<G>, grid_for(n / 4 + 1, 256, 148 * 8), 256, 0, s, acc, g, n, scale, first);
+void grad_accumulate(float* acc, const G* g, long long n, float scale, int first, const float* loss,
+                     float* acc_loss, cudaStream_t s) {
+  launch_k(k_grad_acc<G>, grid_for(n / 4 + 1, 256, 148 * 8), 256, 0, s, acc, g, n, scale, first, loss, acc_loss);
 }
-template void grad_accumulate<float>(float*, const float*, long long, float, int, cudaStream_t);
-template void grad_accumulate<bf16>(float*, const bf16*, long long, float, int, cudaStream_t);
+template void grad_accumulate<float>(float*, const float*, long long, float, int, const float*, float*,
+                                     cudaStream_t);
+template void grad_accumulate<bf16>(float*, const bf16*, long long, float, int, const float*, float*,
+                                    cudaStream_t);
 
 // m = b1 m + (1-b1) g; v = b2 v + (1-b2) g^2; w -= lr (m/bc1 / (sqrt(v/bc2) + eps) + wd_seg w)
 // with g = grad * clip_scale; clip scale and bias corrections come from
@@ -1318,6 +1321,7 @@ __global__ void __launch_bounds__(256)
     eps = hp->eps;
     wd = hp->wd;
   }
+  if (norm_scale[4] != 0.f) return;  // the guard skipped this update: master, m, v stay as they are
   const float sc = norm_scale[1], bc1 = norm_scale[2], bc2 = norm_scale[3];
   const long long n4 = n / 4;
   // the segments tile [0, n) in ascending order and each thread's i only grows,
@@ -1370,9 +1374,6 @@ void adamw(float* master, P* param_copy, const G* grad, float* m, float* v, long
                                  unsigned*);                                                        \
   template void colsum<T>(T*, const T*, int, int, long long, float*, cudaStream_t);                \
   template void colsum_reduce<T>(T*, const float*, int, int, cudaStream_t);                        \
-  template void gelu_fwd<T>(T*, const T*, long long, cudaStream_t);                                \
-  template void gelu_bwd<T>(T*, const T*, const T*, long long, cudaStream_t);                      \
-  template void residual_add<T>(T*, const T*, const T*, long long, cudaStream_t);                  \
   template void to_storage<T>(T*, const float*, long long, cudaStream_t);                          \
   template void to_f32<T>(float*, const T*, long long, cudaStream_t);                              \
   template void ce_rowstats<T>(const T*, long long, const int32_t*, int, int, float*, float*,      \

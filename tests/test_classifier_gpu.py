@@ -62,3 +62,16 @@ def test_classifier_full_size_loss_and_sampled_rows():
     assert rel_l2(dx[rows], dz @ w64) < 3e-2
     assert np.all(dw[V:] == 0)
     assert np.isfinite(dw).all()
+    # sampled dW rows: dW[v] = sum over all rows m of dz[m, v] x[m], which needs every
+    # row's lse; the oracle's cross-entropy gives them chunk by chunk
+    lse = np.empty(M)
+    for r0 in range(0, M, 2048):
+        zc = (x[r0:r0 + 2048] @ w.T).astype(np.float64)
+        _, lse[r0:r0 + 2048], _ = O.cross_entropy_forward(zc, tgt[r0:r0 + 2048], V)
+    vocab = np.concatenate([rng.choice(V, 24, replace=False), np.unique(tgt)[:8], [V - 1]])
+    zv = x64 @ w64[vocab].T                        # [M, len(vocab)] logits of the sampled columns
+    dzv = (np.exp(zv - lse[:, None]) - (tgt[:, None] == vocab[None, :])) / M
+    dw_ref = dzv.T @ x64
+    assert rel_l2(dw[vocab], dw_ref) < 3e-2, rel_l2(dw[vocab], dw_ref)
+    for i in range(len(vocab)):  # row by row, each at the same bound
+        assert rel_l2(dw[vocab[i]], dw_ref[i]) < 3e-2, (int(vocab[i]), rel_l2(dw[vocab[i]], dw_ref[i]))

@@ -215,12 +215,12 @@ def test_gemm_bounded_wait_expires_and_context_survives():
     old = lib.gpt2_test_set_gemm_poison(1)
     try:
         r = lib.gemm_bf16_status(A.data_ptr(), B.data_ptr(), D.data_ptr(), M, N, K, lda, ldb, N, 0, 0,
-                                 st.data_ptr(), None)
+                                 1, None, 0, st.data_ptr(), None)
     finally:
         lib.gpt2_test_set_gemm_poison(old)
     assert r == binding.GPT2_E_TIMEOUT
     r = lib.gemm_bf16_status(A.data_ptr(), B.data_ptr(), D.data_ptr(), M, N, K, lda, ldb, N, 0, 0,
-                             st.data_ptr(), None)
+                             1, None, 0, st.data_ptr(), None)
     assert r == binding.GPT2_OK
     ref = a.astype(np.float64) @ b.astype(np.float64).T
     assert rel_l2(to_np(D), ref) < 4e-3

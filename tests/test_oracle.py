@@ -366,6 +366,37 @@ def test_encoder_fp32_references():
     np.testing.assert_array_equal(dwpe, dx0.sum(axis=0))
 
 
+def test_encoder_backward_f32_real_data_within_rounding_bound():
+    """The fixed-order float32 scatter (runs of 64 positions per id) on real
+    values with heavy duplication, against the exact sum (float64 add.at, which
+    fixes no order): n float32 additions of any order and grouping stay within
+    n * 2^-24 * (|dwte_in| + sum |dx0|) of the exact result, per element, so a
+    dropped, doubled or misplaced row fails while the grouping itself is free."""
+    B, T, C, V, Vpad = 8, 128, 24, 50, 56
+    tok = synth.token_batch(31, B, T, V)[0]
+    counts = np.bincount(tok.reshape(-1), minlength=Vpad)
+    assert counts.max() > 3 * 64  # the most frequent ids span several runs
+    dx0 = synth.normal(32, B * T * C, 1e-3).astype(np.float32).reshape(B, T, C)
+    din = synth.normal(33, Vpad * C, 1e-3).astype(np.float32).reshape(Vpad, C)
+    dwte, dwpe = O.encoder_backward_f32(tok, dx0, din, (T, C))
+    exact = din.astype(np.float64).copy()
+    np.add.at(exact, tok.reshape(-1), dx0.reshape(-1, C).astype(np.float64))
+    mag = np.abs(din).astype(np.float64)
+    np.add.at(mag, tok.reshape(-1), np.abs(dx0).reshape(-1, C).astype(np.float64))
+    n = (counts + 1)[:, None]
+    err = np.abs(dwte.astype(np.float64) - exact)
+    assert np.all(err <= n * 2.0 ** -24 * mag), float((err / (n * 2.0 ** -24 * mag + 1e-300)).max())
+    assert np.all(dwte[counts == 0] == din[counts == 0])  # rows of absent ids are untouched
+    exact_pe = dx0.astype(np.float64).sum(axis=0)
+    err_pe = np.abs(dwpe.astype(np.float64) - exact_pe)
+    assert np.all(err_pe <= B * 2.0 ** -24 * np.abs(dx0).astype(np.float64).sum(axis=0))
+    # a row scattered to the wrong id is far outside the bound
+    wrong = tok.copy()
+    wrong[0, 0] = (wrong[0, 0] + 1) % V
+    bad, _ = O.encoder_backward_f32(wrong, dx0, din, (T, C))
+    assert np.any(np.abs(bad.astype(np.float64) - exact) > n * 2.0 ** -24 * mag)
+
+
 def test_key_bias_gradient_vanishes():
     """Softmax is invariant to a per-query shift of the scores, so the key part
     of the QKV bias receives exactly zero gradient (up to rounding)."""

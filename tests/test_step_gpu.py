@@ -119,6 +119,114 @@ def test_bf16_step_parity_124m_shapes():
     print("worst grad rel L2:", max(worst.items(), key=lambda kv: kv[1]))
 
 
+def _oracle_sequence_grads(args):
+    """Oracle forward + backward of one sequence (float32), run in a worker."""
+    shape, seed, b, tok, tgt = args
+    L, H, C, V, Vpad, T = shape
+    P = _worker_params(shape, seed)
+    loss, cache = O.forward(P, tok, tgt, O.Config(L, H, C, V, Vpad, T), dtype=np.float32)
+    return b, loss, O.backward(cache, O.Config(L, H, C, V, Vpad, T))
+
+
+_WORKER_P = {}
+
+
+def _worker_params(shape, seed):
+    key = (shape, seed)
+    if key not in _WORKER_P:
+        L, H, C, V, Vpad, T = shape
+        _WORKER_P.clear()
+        _WORKER_P[key] = synth.init_params(seed, L, C, V, Vpad, T, bf16_representable=True)
+    return _WORKER_P[key]
+
+
+def _oracle_batch_step(shape, seed, tok, tgt, workers=8):
+    """The oracle's step on B sequences, evaluated one sequence at a time.
+
+    The loss is the mean over all B*T positions and every sequence has T of
+    them, so the batch loss is the mean of the per-sequence losses and the batch
+    gradient the mean of the per-sequence gradients (linearity of the mean); the
+    clip and AdamW then run once on that gradient, as in the oracle's own step.
+    The sequences run in a spawn-started process pool (no fork after CUDA)."""
+    import multiprocessing as mp
+    L, H, C, V, Vpad, T = shape
+    B = tok.shape[0]
+    jobs = [(shape, seed, b, tok[b:b + 1], tgt[b:b + 1]) for b in range(B)]
+    G, losses = None, [0.0] * B
+    with mp.get_context("spawn").Pool(min(workers, B)) as pool:
+        for b, loss, g in pool.imap_unordered(_oracle_sequence_grads, jobs):
+            losses[b] = loss
+            if G is None:
+                G = {k: np.zeros(v.shape, np.float64) for k, v in g.items()}
+            for k in G:
+                G[k] += g[k]
+    G = {k: v / B for k, v in G.items()}
+    P = synth.init_params(seed, L, C, V, Vpad, T, bf16_representable=True)
+    zeros = {k: np.zeros(v.shape, np.float64) for k, v in G.items()}
+    norm, nP, _, _ = O.clip_adamw({k: v.astype(np.float64) for k, v in P.items()}, G, zeros, zeros, 1, LR,
+                                  beta1=B1, beta2=B2, eps=EPS, wd=WD, max_norm=CLIP)
+    return dict(loss=float(np.mean(losses)), grads=G, norm=norm, params=nP), P
+
+
+@pytest.mark.slow
+def test_bf16_step_parity_124m_bench_batch():
+    """The step the benchmark times: GPT-2 124M shapes at B=16, T=1024 (M = 16384,
+    so every GEMM takes its production schedule: stream-K tails, in-kernel split
+    finishes, 8-split weight gradients with the separate reduction, the
+    persistent LayerNorm backward over 16384 rows, the CE merge over 786 column
+    groups).  Loss, every gradient tensor, the norm and the post-AdamW master
+    weights against the oracle (float32, per sequence, combined exactly)."""
+    L, H, C, V, Vpad, T, B = 12, 12, 768, 50257, 50304, 1024, 16
+    cfg = O.Config(L, H, C, V, Vpad, T)
+    tok, tgt = synth.token_batch(42, B, T, V)
+    ref, P = _oracle_batch_step((L, H, C, V, Vpad, T), 43, tok, tgt)
+    flat = synth.flatten_params(P, L, C, Vpad, T)
+    res = _gpu_step(cfg, B, binding.GPT2_BF16, flat, tok, tgt)[0]
+    worst = _compare(cfg, P, res, ref, 1e-2, 3e-2, 1e-2, flat)
+    print("worst grad rel L2:", max(worst.items(), key=lambda kv: kv[1]))
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("L,H,C,B", [(24, 16, 1024, 1), (2, 25, 1600, 1)])
+def test_bf16_step_parity_350m_and_d48_shapes(L, H, C, B):
+    """GPT-2 350M shapes (L=24, H=16, C=1024) and the d48 model's width (C=1600,
+    H=25 heads of 64: N not a multiple of the 256-wide GEMM tile, 25 k blocks,
+    LayerNorm rows of 200 vectors) at T=1024, against the oracle."""
+    V, Vpad, T = 50257, 50304, 1024
+    cfg = O.Config(L, H, C, V, Vpad, T)
+    P = synth.init_params(71 + L, L, C, V, Vpad, T, bf16_representable=True)
+    tok, tgt = synth.token_batch(72 + L, B, T, V)
+    flat = synth.flatten_params(P, L, C, Vpad, T)
+    res = _gpu_step(cfg, B, binding.GPT2_BF16, flat, tok, tgt)[0]
+    ref = O.train_step(P, tok, tgt, cfg, lr=LR, t=1, beta1=B1, beta2=B2, eps=EPS, wd=WD, max_norm=CLIP,
+                       dtype=np.float32)
+    worst = _compare(cfg, P, res, ref, 1e-2, 3e-2, 1e-2, flat)
+    print("worst grad rel L2:", max(worst.items(), key=lambda kv: kv[1]))
+
+
+@pytest.mark.parametrize("prec,tol", [(binding.GPT2_BF16, (1e-2, 3e-2, 1e-2)), (binding.GPT2_FP32, (1e-4, 1e-4, 1e-4))])
+def test_step_parity_without_clipping(prec, tol):
+    """max_norm far above the gradient norm: the clip scale is exactly 1 and the
+    update is AdamW on the raw gradient."""
+    L, H, C, V, Vpad, T, B = (2, 2, 128, 1000, 1024, 128, 2) if prec == binding.GPT2_BF16 else (2, 2, 64, 256, 256, 64, 2)
+    cfg = O.Config(L, H, C, V, Vpad, T)
+    P = synth.init_params(81, L, C, V, Vpad, T, bf16_representable=prec == binding.GPT2_BF16)
+    tok, tgt = synth.token_batch(82, B, T, V)
+    flat = synth.flatten_params(P, L, C, Vpad, T)
+    big = 1e4
+    s = binding.Step(L, H, C, V, Vpad, T, B, precision=prec)
+    s.set_params(flat)
+    loss = s.forward(to_dev(tok, "i32"), to_dev(tgt, "i32"))
+    s.backward()
+    grads = s.get(binding.GPT2_GRADS)
+    norm = s.clip_adamw(LR, B1, B2, EPS, WD, big, 1)
+    res = dict(loss=loss, grads=grads, norm=norm, master=s.get(binding.GPT2_MASTER))
+    s.close()
+    ref = O.train_step(P, tok, tgt, cfg, lr=LR, t=1, beta1=B1, beta2=B2, eps=EPS, wd=WD, max_norm=big)
+    assert O.clip_scale(ref["norm"], big) == 1.0 and ref["norm"] > CLIP
+    _compare(cfg, P, res, ref, *tol, flat)
+
+
 def test_bf16_step_deterministic():
     L, H, C, V, Vpad, T, B = 2, 2, 128, 1000, 1024, 128, 2
     cfg = O.Config(L, H, C, V, Vpad, T)
