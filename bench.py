@@ -91,6 +91,34 @@ def traffic_per_launch(kernel):
         return None
 
 
+def device_init_params(c, seed=43, std=0.02):
+    """The init recipe (every weight matrix, wte and wpe ~ N(0, std), the two residual
+    projections scaled by 1/sqrt(2L), biases 0, LayerNorm gamma 1 / beta 0, padded wte
+    rows 0) drawn on the device with torch's seeded generator: the same distribution as
+    synth.init_params without generating billions of values on the host.  Returns the
+    flat fp32 CUDA tensor in the canonical order."""
+    import torch
+    from pretraining_step_train_b300 import synth
+    L, C, V, Vpad, T = c["L"], c["C"], c["V"], c["Vpad"], c["T"]
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    parts = []
+    for name, shape in synth.param_shapes(L, C, Vpad, T):
+        n = 1
+        for d in shape:
+            n *= d
+        if name.startswith("ln") and name.endswith("w"):
+            t = torch.ones(n, device="cuda")
+        elif name in ("wte", "wpe", "qkvw", "attprojw", "fcw", "fcprojw"):
+            sd = std / (2.0 * L) ** 0.5 if name in ("attprojw", "fcprojw") else std
+            t = torch.randn(n, generator=g, device="cuda") * sd
+            if name == "wte":
+                t.view(Vpad, C)[V:] = 0.0
+        else:
+            t = torch.zeros(n, device="cuda")
+        parts.append(t)
+    return torch.cat(parts)
+
+
 def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
@@ -554,9 +582,12 @@ def main():
         pg.barrier()
     L, H, C, V, Vpad, T, B = (c[k] for k in ("L", "H", "C", "V", "Vpad", "T", "B"))
     M = B * T
-    P = synth.init_params(43, L, C, V, Vpad, T, bf16_representable=True)
-    flat = synth.flatten_params(P, L, C, Vpad, T)
-    del P
+    if args.config == "124m":
+        P = synth.init_params(43, L, C, V, Vpad, T, bf16_representable=True)
+        flat = synth.flatten_params(P, L, C, Vpad, T)
+        del P
+    else:
+        flat = device_init_params(c)
     NB = 4
     host_batches = [synth.token_batch(42 + 1000 * rank + i, B, T, V) for i in range(NB)]
     dev_tok = torch.stack([torch.from_numpy(b[0]) for b in host_batches]).cuda()
@@ -727,6 +758,7 @@ def main():
                         "loss, norm, status out)"},
         "gpu_launches": (n_kernels * args.steps) if n_kernels else None,
         "kernels_per_step": n_kernels,
+        "gemm_cta_pairs": binding.lib().gemm_bf16_pairs(),
         "clocks": clk,
         "loss_last_e2e": last[0] if last else None,
         "status": status,

@@ -81,7 +81,8 @@ enum gpt2_kernel_class {
   GPT2_K_BIAS_GRAD = 8, /* bias gradients (column sums) */
   GPT2_K_NORM = 9,      /* global gradient norm */
   GPT2_K_ADAMW = 10,    /* fused clip + AdamW + bf16 copy */
-  GPT2_K_COUNT = 11
+  GPT2_K_RECOMPUTE = 11, /* activation recompute in the backward (gelu(h), LayerNorm outputs) */
+  GPT2_K_COUNT = 12
 };
 
 typedef struct gpt2 gpt2_t;
@@ -103,6 +104,24 @@ int gpt2_create(int L, int H, int C, int V, int Vpad, int T, int B, int precisio
                 size_t arena_bytes, void* stream, gpt2_t** out);
 void gpt2_destroy(gpt2_t* h);
 int gpt2_set_stream(gpt2_t* h, void* stream);
+
+/* Activation recompute (llm.c GPT-2 1558M article, "Parameter guide" and
+ * "Memory guide": -r 1 recomputes GELU in the backward pass instead of keeping
+ * it, -r 2 also recomputes LayerNorm; compute traded for memory).  gpt2_create
+ * and gpt2_arena_bytes are these calls with recompute = 0 (everything kept):
+ *   1  the forward keeps h = x W_fc^T + b per layer and gelu(h) only until the
+ *      projection GEMM has read it; the backward recomputes gelu(h) (for the
+ *      projection's weight gradient) and gelu'(h) (in the GELU' epilogue) from
+ *      h.  Saves (L - 1) * B*T * 4C storage elements.
+ *   2  as 1, and the LayerNorm outputs ln1 / ln2 are not kept either: the
+ *      backward recomputes each from the stored residual (the same kernel, so
+ *      the same bits) right before the weight-gradient GEMM that reads it.
+ *      Saves another (2L - 1) * B*T * C elements.
+ * Results agree with recompute = 0 within the bf16 tolerances (the recomputed
+ * GELU uses the rounded h); other values are GPT2_E_INVAL. */
+size_t gpt2_arena_bytes_r(int L, int H, int C, int V, int Vpad, int T, int B, int precision, int recompute);
+int gpt2_create_r(int L, int H, int C, int V, int Vpad, int T, int B, int precision, int recompute, void* d_arena,
+                  size_t arena_bytes, void* stream, gpt2_t** out);
 
 /* Load N fp32 parameters (canonical order) from host (on_device = 0) or device
  * memory; in GPT2_BF16 mode they become the fp32 master copy and the working
@@ -325,6 +344,9 @@ int gemm_bf16(const void* A, const void* B, void* D, int M, int N, int K, long l
               void* workspace, size_t workspace_bytes, void* stream);
 /* Workspace bytes of the splits = -1 / -2 schedules on the current device. */
 size_t gemm_bf16_sk_workspace_bytes(void);
+/* Number of CTA pairs (clusters of two CTAs on two SMs) the GEMM engine keeps
+ * resident on the current device: its persistent grid is twice this. */
+int gemm_bf16_pairs(void);
 
 /* The GEMM engine with one of its fused epilogues, for tests.  As gemm_bf16
  * (bf16 D, same splits / workspace rules, no split > 1 with a fused epilogue)

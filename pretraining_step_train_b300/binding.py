@@ -19,7 +19,7 @@ GPT2_E_CUDA, GPT2_E_TIMEOUT, GPT2_E_NONFINITE, GPT2_E_UNSUPPORTED = -4, -5, -6, 
 GPT2_FP32, GPT2_BF16 = 0, 1
 GPT2_PARAMS, GPT2_GRADS, GPT2_ADAM_M, GPT2_ADAM_V, GPT2_MASTER, GPT2_GRAD_ACC = 0, 1, 2, 3, 4, 5
 KERNEL_CLASSES = ["gemm", "splitk_reduce", "attn_fwd", "attn_bwd", "layernorm_fwd", "layernorm_bwd",
-                  "cross_entropy", "encoder", "bias_grad", "grad_norm", "adamw"]
+                  "cross_entropy", "encoder", "bias_grad", "grad_norm", "adamw", "recompute"]
 
 _i, _ll, _sz, _f, _p = ct.c_int, ct.c_longlong, ct.c_size_t, ct.c_float, ct.c_void_p
 _fp = ct.POINTER(ct.c_float)
@@ -30,6 +30,8 @@ SIGNATURES = {
     "gpt2_arena_bytes": (_sz, [_i, _i, _i, _i, _i, _i, _i, _i]),
     "gpt2_create": (_i, [_i, _i, _i, _i, _i, _i, _i, _i, _p, _sz, _p, ct.POINTER(_p)]),
     "gpt2_destroy": (None, [_p]),
+    "gpt2_arena_bytes_r": (_sz, [_i, _i, _i, _i, _i, _i, _i, _i, _i]),
+    "gpt2_create_r": (_i, [_i, _i, _i, _i, _i, _i, _i, _i, _i, _p, _sz, _p, ct.POINTER(_p)]),
     "gpt2_set_stream": (_i, [_p, _p]),
     "gpt2_set_params": (_i, [_p, _p, _i]),
     "gpt2_get_tensor": (_i, [_p, _i, _p, _i]),
@@ -60,6 +62,7 @@ SIGNATURES = {
     "gpt2_encoder_bwd": (_i, [_p, _p, _p, _p, _i, _i, _i, _i, _i, _p, _sz, _p]),
     "gemm_bf16": (_i, [_p, _p, _p, _i, _i, _i, _ll, _ll, _ll, _i, _i, _i, _i, _p, _sz, _p]),
     "gemm_bf16_sk_workspace_bytes": (_sz, []),
+    "gemm_bf16_pairs": (_i, []),
     "gpt2_lr_schedule": (_f, [_i, _f, _i, _i, _f]),
     "gpt2_grad_accumulate": (_i, [_p, _i, _f]),
     "gpt2_clip_adamw_accumulated": (_i, [_p, _f, _f, _f, _f, _f, _f, _i, _p]),
@@ -124,19 +127,20 @@ def __getattr__(name):
 class Step:
     """One GPT-2 step driver over a torch-allocated device arena."""
 
-    def __init__(self, L, H, C, V, Vpad, T, B, precision=GPT2_BF16, stream=None, device="cuda"):
+    def __init__(self, L, H, C, V, Vpad, T, B, precision=GPT2_BF16, stream=None, device="cuda", recompute=0):
         import torch
 
         self.shape = dict(L=L, H=H, C=C, V=V, Vpad=Vpad, T=T, B=B)
         self.precision = precision
-        nbytes = lib().gpt2_arena_bytes(L, H, C, V, Vpad, T, B, precision)
+        self.recompute = recompute
+        nbytes = lib().gpt2_arena_bytes_r(L, H, C, V, Vpad, T, B, precision, recompute)
         if nbytes == 0:
-            raise GPT2Error(GPT2_E_INVAL, "gpt2_arena_bytes")
+            raise GPT2Error(GPT2_E_INVAL, "gpt2_arena_bytes_r")
         self.arena = torch.empty(nbytes, dtype=torch.uint8, device=device)
         self.stream = stream
         h = _p()
-        check(lib().gpt2_create(L, H, C, V, Vpad, T, B, precision, _ptr(self.arena), nbytes,
-                                _stream_ptr(stream), ct.byref(h)), "gpt2_create")
+        check(lib().gpt2_create_r(L, H, C, V, Vpad, T, B, precision, recompute, _ptr(self.arena), nbytes,
+                                  _stream_ptr(stream), ct.byref(h)), "gpt2_create_r")
         self.h = h
         self.N = lib().gpt2_num_params(L, C, Vpad, T)
 

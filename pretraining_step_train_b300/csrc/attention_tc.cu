@@ -1,27 +1,26 @@
-// Causal attention forward on the 5th-generation tensor cores (tcgen05) for
-// sm_103a, d = 64, never materialising the T x T score matrix (online softmax
-// over 128-key tiles, FlashAttention-style: "Let's reproduce GPT-2 (124M)" wiki
+// Causal attention on the 5th-generation tensor cores (tcgen05) for sm_103a,
+// d = 64, never materialising the T x T score matrix (online softmax over
+// 128-key tiles, FlashAttention-style: "Let's reproduce GPT-2 (124M)" wiki
 // page, "GPU optimisation ladder").
 //
-// Persistent: one CTA per SM walks a list of work items (128-query tile, batch,
-// head), heaviest causal tiles first, item c, c + grid, c + 2 grid, ...
-//   warp 0      TMA: each item's Q tile, then its K and V tiles of 128 keys into
-//               a 4-stage ring that runs on across items, so the next item's
-//               tiles load while this one finishes (4-D tensor maps over the
-//               strided q / k / v views, 128B swizzle; rows past T arrive as zeros);
-//   warp 1      owns 512 TMEM columns: S double buffer (2 x 128 fp32 columns),
-//               the O accumulator (64 columns) and a P double buffer (2 x 64
-//               columns of bf16 pairs); one thread issues
-//               S_j = Q K_j^T (M=128, N=128, K=64) and O += P_j V_j (M=128, N=64,
-//               K=128, V read MN-major), in the order S_0, S_1, PV_0, S_2, PV_1, ...
-//               so the tensor core computes S_{j+1} while softmax works on S_j;
-//   warps 2-9   softmax, two warps per TMEM lane quadrant (one per 64-key half):
-//               tcgen05.ld of the half row, causal mask on the diagonal tile, row
-//               max exchanged with the partner warp through shared memory,
-//               p = 2^(s*scale*log2e - m), running sum, O rescaled in TMEM only
-//               when the running max has to move by more than 2^8, P (bf16 pairs)
-//               written to tensor memory (double-buffered), where the PV MMA reads
-//               its A operand.
+// Forward: persistent, one CTA per SM walks work items (a pair of adjacent
+// 128-query tiles of one (batch, head)), heaviest first, item c, c + grid, ...
+//   warp 0      TMA: the item's two Q tiles, then K and V tiles of 128 keys into
+//               a 4-stage ring that runs on across items (4-D tensor maps over
+//               the strided q / k / v views, 128B swizzle; rows past T are zeros);
+//   warp 1      owns 512 TMEM columns: per query tile t an S buffer (128 fp32
+//               columns), the O accumulator (64) and a P buffer (64 columns of
+//               bf16 pairs); one thread issues S_t = Q_t K_j^T (M=128, N=128,
+//               K=64) and O_t += P_t V_j (M=128, N=64, K=128, A from TMEM), in
+//               the order S_0(j), S_1(j), PV_0(j-1), PV_1(j-1), ..., so the tensor
+//               core works on one tile while the softmax warps work on the other;
+//   warps 2-5   softmax of query tile 0, warps 6-9 of tile 1: each thread owns
+//               one query row (lane quadrant = warp % 4) and all 128 keys of a
+//               tile, so the row max and sum stay in the thread; p =
+//               2^(s*scale*log2e - m) (ex2.approx: 32 per cycle per SM, so the
+//               32K exponentials of a key tile take fewer cycles than its MMAs);
+//               O is rescaled in TMEM only when the running max has to move by
+//               more than 2^8; P (bf16 pairs) goes to TMEM for the PV MMA.
 // Epilogue: O / l -> bf16 rows, lse = (m + log2 l) ln 2 (natural log).
 // Every wait is bounded; on expiry the CTA latches ST_TIMEOUT (when a status
 // word is given), drains its copies and MMAs, frees TMEM and returns.
@@ -36,21 +35,21 @@ namespace {
 constexpr int AT_B = 128;                       // queries per tile = keys per tile
 constexpr int AT_D = 64;                        // head size
 constexpr int AT_TILE = AT_B * AT_D * 2;        // 16 KB: one [128 x 64] bf16 tile
-constexpr int AT_Q_OFF = 0;
-constexpr int AT_KV_STAGES = 4;
-constexpr int AT_KV_OFF = AT_TILE;              // stage s: K at +s*2*TILE, V at +s*2*TILE+TILE
-constexpr int AT_RED_OFF = AT_KV_OFF + 2 * AT_KV_STAGES * AT_TILE;  // row-max exchange [2][2][128] + row-sum [2][128]
-constexpr int AT_BAR_OFF = AT_RED_OFF + 6 * 128 * 4;
-constexpr int AT_NBARS = 31;
-constexpr int AT_SMEM = 1024 + AT_BAR_OFF + 8 * (AT_NBARS + 2);
 constexpr int AT_THREADS = 320;
 constexpr int AT_TMEM_COLS = 512;
-constexpr int AT_O_COL = 256;
-constexpr int AT_P_COL = 320;  // P buffers (bf16 pairs): 320 + 64 * buffer
+// forward: smem two sets of (Q_0 | Q_1) | K,V ring; TMEM S_t at 128 t, O_t at 256 + 64 t,
+// P_t at 384 + 64 t
+constexpr int FW_STAGES = 4;
+constexpr int FW_Q = 0, FW_KV = 4 * AT_TILE;  // Q set q: tile t at FW_Q + (2 q + t) TILE; stage s: K at FW_KV + 2 s TILE, V after
+constexpr int FW_BAR = FW_KV + 2 * FW_STAGES * AT_TILE;
+constexpr int FW_NBARS = 4 + 2 * FW_STAGES + 8 + 1;
+constexpr int AT_SMEM = 1024 + FW_BAR + 8 * (FW_NBARS + 2);
+constexpr uint32_t FW_S_COL = 0, FW_O_COL = 256, FW_P_COL = 384;
 
 struct AtParams {
   AttnArgs a;
   int nq;        // query tiles per (batch, head)
+  int nqp;       // query-tile pairs per (batch, head): ceil(nq / 2)
   int swap_ht;   // tensor maps index (d, h, t, b) instead of (d, t, h, b)
   float c2;      // scale * log2(e)
   uint32_t idesc_s, idesc_pv;
@@ -78,17 +77,23 @@ __device__ __forceinline__ void warp_arrive(uint32_t bar) {
   __syncwarp();
   if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
 }
-// Tree reductions over a thread's own values (short dependency chains).
-template <int N>
-__device__ __forceinline__ float tree_max(const float* v) {
-  float t[N / 2];
+// Three-input fp32 max (one instruction on sm_100+).
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+// Max of 128 values in four independent chains (short dependency depth).
+__device__ __forceinline__ float row_max128(const float* v) {
+  float m[4] = {v[0], v[1], v[2], v[3]};
 #pragma unroll
-  for (int i = 0; i < N / 2; ++i) t[i] = fmaxf(v[2 * i], v[2 * i + 1]);
-#pragma unroll
-  for (int w = N / 4; w >= 1; w >>= 1)
-#pragma unroll
-    for (int i = 0; i < w; ++i) t[i] = fmaxf(t[i], t[i + w]);
-  return t[0];
+  for (int i = 4; i < 128; i += 8) {
+    m[0] = max3(m[0], v[i], v[i + 1]);
+    m[1] = max3(m[1], v[i + 2], v[i + 3]);
+    m[2] = max3(m[2], v[i + 4], v[i + 5]);
+    m[3] = max3(m[3], v[i + 6], v[i + 7]);
+  }
+  return max3(m[0], m[1], fmaxf(m[2], m[3]));
 }
 
 __global__ void __launch_bounds__(AT_THREADS, 1)
@@ -97,44 +102,39 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
-  float* red = reinterpret_cast<float*>(smem + AT_RED_OFF);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + AT_BAR_OFF);
-  // q_full, kv_full[4], kv_empty[4], s_full[2], s_empty[2], p_full[2], pv_done, done,
-  // xmax[4 quadrants][2], xsum[4 quadrants] (the two warps of a quadrant exchange row
-  // stats), q_empty (the Q tile may be overwritten by the next item)
-  const uint32_t b_q = smem_u32(bars), b_kvf = b_q + 8, b_kve = b_kvf + 8 * AT_KV_STAGES;
-  const uint32_t b_sf = b_kve + 8 * AT_KV_STAGES;
-  const uint32_t b_se = b_sf + 16, b_pf = b_se + 16, b_pv = b_pf + 16, b_done = b_pv + 8;
-  const uint32_t b_xmax = b_done + 8, b_xsum = b_xmax + 64, b_qe = b_xsum + 32;
-  // pv_done[i] (i = tile parity) completes for the PVs of global tiles i, i+2, ...:
-  // b_pv for even tiles, b_pv2 for odd ones
-  const uint32_t b_pv2 = b_qe + 8;
-  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bars + AT_NBARS);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + AT_NBARS + 1);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + FW_BAR);
+  // q_full[2], q_empty[2] (per Q set), kv_full[4], kv_empty[4], s_full[2], s_empty[2], p_full[2],
+  // pv_done[2] (per query tile), done
+  const uint32_t b_qf = smem_u32(bars), b_qe = b_qf + 16, b_kvf = b_qe + 16, b_kve = b_kvf + 8 * FW_STAGES;
+  const uint32_t b_sf = b_kve + 8 * FW_STAGES, b_se = b_sf + 16, b_pf = b_se + 16, b_pv = b_pf + 16;
+  const uint32_t b_done = b_pv + 16;
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bars + FW_NBARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + FW_NBARS + 1);
 
   const AttnArgs& a = p.a;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int BH = a.B * a.H;
-  const int nitems = p.nq * BH;
-  // work item w: query tile nq-1 - w / BH (heaviest first), (batch, head) = w % BH
+  const int nitems = p.nqp * BH;
+  // work item w: query tiles 2 qp and 2 qp + 1 with qp = nqp-1 - w / BH (heaviest first),
+  // (batch, head) = w % BH; the second tile is absent when 2 qp + 1 = nq.  Tile 0 uses
+  // key tiles 0 .. 2 qp, tile 1 key tiles 0 .. 2 qp + 1.
 
   if (threadIdx.x == 0) {
-    mbar_init(b_q, 1);
-    for (int i = 0; i < AT_KV_STAGES; ++i) {
+    for (int q = 0; q < 2; ++q) {
+      mbar_init(b_qf + 8 * q, 1);
+      mbar_init(b_qe + 8 * q, 1);
+    }
+    for (int i = 0; i < FW_STAGES; ++i) {
       mbar_init(b_kvf + 8 * i, 1);
       mbar_init(b_kve + 8 * i, 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(b_sf + 8 * i, 1);
-      mbar_init(b_se + 8 * i, 8);  // one arrival per softmax warp
-      mbar_init(b_pf + 8 * i, 8);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(b_sf + 8 * t, 1);
+      mbar_init(b_se + 8 * t, 4);  // one arrival per softmax warp of the tile
+      mbar_init(b_pf + 8 * t, 4);
+      mbar_init(b_pv + 8 * t, 1);
     }
-    mbar_init(b_pv, 1);
     mbar_init(b_done, 1);
-    mbar_init(b_qe, 1);
-    mbar_init(b_pv2, 1);
-    for (int i = 0; i < 8; ++i) mbar_init(b_xmax + 8 * i, 2);  // the two warps of a quadrant
-    for (int i = 0; i < 4; ++i) mbar_init(b_xsum + 8 * i, 2);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -152,25 +152,30 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ---------------- TMA producer
-      int last_par[AT_KV_STAGES] = {-1, -1, -1, -1}, q_par = -1;
+      int last_par[FW_STAGES] = {-1, -1, -1, -1}, q_par[2] = {-1, -1};
       int g = 0;  // K/V tiles issued so far (ring position)
       bool ok = true;
       for (int w = blockIdx.x, it = 0; ok && w < nitems; w += gridDim.x, ++it) {
-        const int qt = p.nq - 1 - w / BH, bh = w % BH, b = bh / a.H, h = bh % a.H;
+        const int qp = p.nqp - 1 - w / BH, bh = w % BH, b = bh / a.H, h = bh % a.H;
+        const bool has1 = 2 * qp + 1 < p.nq;
+        const int nk = 2 * qp + (has1 ? 2 : 1);
         auto load = [&](const CUtensorMap* tm, uint32_t dst, uint32_t bar, int t0) {
           if (p.swap_ht) tma_load_4d(dst, tm, bar, 0, h, t0, b);
           else tma_load_4d(dst, tm, bar, 0, t0, h, b);
         };
-        if (it > 0 && !mbar_wait(b_qe, (uint32_t)(it - 1) & 1u, abort_flag, p.status)) break;
-        mbar_expect_tx(b_q, AT_TILE);
-        load(&tmQ, sbase + AT_Q_OFF, b_q, qt * AT_B);
-        q_par = it & 1;
-        for (int j = 0; j <= qt; ++j, ++g) {
-          const int st = g % AT_KV_STAGES;
-          const uint32_t ph = (uint32_t)(g / AT_KV_STAGES) & 1u;
+        // Q set it % 2 was last read by the S MMAs of item it - 2
+        const int qs = it & 1;
+        if (it >= 2 && !mbar_wait(b_qe + 8 * qs, (uint32_t)((it - 2) >> 1) & 1u, abort_flag, p.status)) break;
+        mbar_expect_tx(b_qf + 8 * qs, (has1 ? 2 : 1) * AT_TILE);
+        load(&tmQ, sbase + FW_Q + 2 * qs * AT_TILE, b_qf + 8 * qs, 2 * qp * AT_B);
+        if (has1) load(&tmQ, sbase + FW_Q + (2 * qs + 1) * AT_TILE, b_qf + 8 * qs, (2 * qp + 1) * AT_B);
+        q_par[qs] = (it >> 1) & 1;
+        for (int j = 0; j < nk; ++j, ++g) {
+          const int st = g % FW_STAGES;
+          const uint32_t ph = (uint32_t)(g / FW_STAGES) & 1u;
           if (!mbar_wait(b_kve + 8 * st, ph ^ 1u, abort_flag, p.status)) { ok = false; break; }
           if ((p.poison & POISON_ATTN_FWD) && g == 0) continue;
-          const uint32_t kd = sbase + AT_KV_OFF + st * 2 * AT_TILE;
+          const uint32_t kd = sbase + FW_KV + st * 2 * AT_TILE;
           mbar_expect_tx(b_kvf + 8 * st, 2 * AT_TILE);
           load(&tmK, kd, b_kvf + 8 * st, j * AT_B);
           load(&tmV, kd + AT_TILE, b_kvf + 8 * st, j * AT_B);
@@ -178,185 +183,198 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         }
       }
       // never leave with copies still landing in shared memory
-      if (q_par >= 0) mbar_wait_drain(b_q, (uint32_t)q_par);
-      for (int i = 0; i < AT_KV_STAGES; ++i)
+      for (int q = 0; q < 2; ++q)
+        if (q_par[q] >= 0) mbar_wait_drain(b_qf + 8 * q, (uint32_t)q_par[q]);
+      for (int i = 0; i < FW_STAGES; ++i)
         if (last_par[i] >= 0) mbar_wait_drain(b_kvf + 8 * i, (uint32_t)last_par[i]);
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer
-      const uint32_t qd = sbase + AT_Q_OFF;
-      // O += P_gp V_gp for global tile gp; `first` starts a new item's accumulator
-      auto issue_pv = [&](int gp, bool first) -> bool {
-        const int pb = gp & 1;
-        if (!mbar_wait(b_pf + 8 * pb, (uint32_t)(gp >> 1) & 1u, abort_flag, p.status)) return false;
-        tc_fence_after();
-        const uint32_t vd = sbase + AT_KV_OFF + (gp % AT_KV_STAGES) * 2 * AT_TILE + AT_TILE;
-        // A = P_gp in TMEM: 16 keys per MMA = 8 columns of bf16 pairs
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_bf16_tmem_a(tmem + AT_O_COL, tmem + AT_P_COL + pb * 64 + kk * 8, operand_desc(vd, 1, kk),
-                          p.idesc_pv, (!first || kk > 0) ? 1u : 0u);
-        mma_commit((gp & 1) ? b_pv2 : b_pv);
-        mma_commit(b_kve + 8 * (gp % AT_KV_STAGES));
-        return true;
-      };
+      // It issues whichever product is ready, so each softmax group starts its next tile as
+      // soon as it finishes one and the two groups drift half a period apart (a fixed order
+      // kept them in step, contending for the exponential unit, each waiting on the other):
+      //   S_t(j)  once K_j has landed and group t has read S_t(j-1) out of TMEM;
+      //   PV_t(j) once group t has written P_t(j);
+      // K_j / V_j's ring stage is released once both tiles' PV(j) are issued.
+      int cnt_s[2] = {0, 0}, cnt_pv[2] = {0, 0};  // S and PV MMAs issued per query tile, all items
       bool ok = true;
-      int g = 0;
+      int g = 0;  // ring position of the item's key tile 0
       for (int w = blockIdx.x, it = 0; ok && w < nitems; w += gridDim.x, ++it) {
-        const int nk = p.nq - w / BH;
-        if (!mbar_wait(b_q, (uint32_t)it & 1u, abort_flag, p.status)) break;
-        for (int j = 0; j < nk; ++j, ++g) {
-          const int st = g % AT_KV_STAGES, sb = g & 1;
-          if (!mbar_wait(b_kvf + 8 * st, (uint32_t)(g / AT_KV_STAGES) & 1u, abort_flag, p.status)) {
-            ok = false;
-            break;
-          }
-          if (g >= 2 && !mbar_wait(b_se + 8 * sb, ((uint32_t)(g >> 1) & 1u) ^ 1u, abort_flag, p.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t kd = sbase + AT_KV_OFF + st * 2 * AT_TILE;
+        const int qp = p.nqp - 1 - w / BH;
+        const int qt0 = 2 * qp;
+        const bool has1 = qt0 + 1 < p.nq;
+        const int nk = qt0 + (has1 ? 2 : 1);
+        const int nkt[2] = {qt0 + 1, has1 ? qt0 + 2 : 0};  // key tiles per query tile
+        const int qs = it & 1;
+        if (!mbar_wait(b_qf + 8 * qs, (uint32_t)(it >> 1) & 1u, abort_flag, p.status)) break;
+        int ns[2] = {0, 0}, np[2] = {0, 0}, rel = 0;  // this item: S issued, PV issued, stages released
+        bool q_released = false;
+        unsigned long long t_idle = 0;
+        while (ok && (np[0] < nkt[0] || np[1] < nkt[1] || rel < nk)) {
+          bool progress = false;
+          for (int t = 0; t < 2; ++t) {
+            const int j = ns[t];
+            if (j < nkt[t] && ns[t] <= np[t] + 1) {  // at most one S ahead of its PV (one P buffer)
+              const int st = (g + j) % FW_STAGES;
+              if (mbar_test(b_kvf + 8 * st, (uint32_t)((g + j) / FW_STAGES) & 1u) &&
+                  (cnt_s[t] == 0 || mbar_test(b_se + 8 * t, (uint32_t)(cnt_s[t] - 1) & 1u))) {
+                tc_fence_after();
+                const uint32_t kd = sbase + FW_KV + st * 2 * AT_TILE;
+                const uint32_t qd = sbase + FW_Q + (2 * qs + t) * AT_TILE;
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_bf16(tmem + sb * AT_B, operand_desc(qd, 0, k), operand_desc(kd, 0, k), p.idesc_s,
-                     k > 0 ? 1u : 0u);
-          mma_commit(b_sf + 8 * sb);
-          if (j == nk - 1) mma_commit(b_qe);  // Q is free once this item's S MMAs are done
-          if (j >= 1 && !issue_pv(g - 1, j == 1)) { ok = false; break; }
+                for (int k = 0; k < 4; ++k)
+                  mma_bf16(tmem + FW_S_COL + 128 * t, operand_desc(qd, 0, k), operand_desc(kd, 0, k), p.idesc_s,
+                           k > 0 ? 1u : 0u);
+                mma_commit(b_sf + 8 * t);
+                ++ns[t];
+                ++cnt_s[t];
+                progress = true;
+              }
+            }
+            if (np[t] < ns[t] && mbar_test(b_pf + 8 * t, (uint32_t)cnt_pv[t] & 1u)) {
+              tc_fence_after();
+              const int jp = np[t];
+              const uint32_t vd = sbase + FW_KV + ((g + jp) % FW_STAGES) * 2 * AT_TILE + AT_TILE;
+              // A = P_t in TMEM: 16 keys per MMA = 8 columns of bf16 pairs
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk)
+                mma_bf16_tmem_a(tmem + FW_O_COL + 64 * t, tmem + FW_P_COL + 64 * t + kk * 8,
+                                operand_desc(vd, 1, kk), p.idesc_pv, (jp > 0 || kk > 0) ? 1u : 0u);
+              mma_commit(b_pv + 8 * t);
+              ++np[t];
+              ++cnt_pv[t];
+              progress = true;
+            }
+          }
+          if (!q_released && ns[0] == nkt[0] && ns[1] == nkt[1]) {
+            mma_commit(b_qe + 8 * qs);  // this Q set is free once the item's S MMAs are done
+            q_released = true;
+          }
+          // K_j / V_j are no longer read once every tile that uses key tile j has issued PV(j)
+          while (rel < nk && (rel >= nkt[0] || np[0] > rel) && (rel >= nkt[1] || np[1] > rel)) {
+            mma_commit(b_kve + 8 * ((g + rel) % FW_STAGES));
+            ++rel;
+            progress = true;
+          }
+          if (progress) {
+            t_idle = 0;
+          } else {
+            if (*abort_flag) { ok = false; break; }
+            const unsigned long long now = globaltimer_ns();
+            if (t_idle == 0) {
+              t_idle = now;
+            } else if (now - t_idle > WAIT_LIMIT_NS) {
+              if (p.status) atomicOr(p.status, ST_TIMEOUT);
+              *abort_flag = 1;
+              ok = false;
+            }
+          }
         }
-        if (ok && !issue_pv(g - 1, nk == 1)) ok = false;
+        g += nk;
       }
       // every MMA issued by this thread has completed once b_done flips
       mma_commit(b_done);
       mbar_wait_drain(b_done, 0);
     }
   } else {
-    // ---------------- softmax warps 2..9: lane quadrant warp % 4, key half (warp - 2) / 4
-    const int quad = warp & 3, half = (warp - 2) >> 2;
+    // ---------------- softmax warps: query tile t = (warp - 2) / 4, lane quadrant warp % 4
+    const int t = (warp - 2) >> 2, quad = warp & 3;
     const int r = quad * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+    const uint32_t s_col = FW_S_COL + 128 * t, o_col = FW_O_COL + 64 * t, p_col = FW_P_COL + 64 * t;
+    const uint32_t b_sft = b_sf + 8 * t, b_set = b_se + 8 * t, b_pft = b_pf + 8 * t, b_pvt = b_pv + 8 * t;
+    const float2 c2 = make_float2(p.c2, p.c2);
     bool ok = true;
-    int g = 0;  // global tile counter: S / P buffers, barrier parities
-    for (int w = blockIdx.x, it = 0; ok && w < nitems; w += gridDim.x, ++it) {
-      const int qt = p.nq - 1 - w / BH, bh = w % BH, b = bh / a.H, h = bh % a.H;
+    int n_s = 0, n_pv = 0;  // S tiles read and PV MMAs waited for, by this tile's warps
+    for (int w = blockIdx.x; ok && w < nitems; w += gridDim.x) {
+      const int qp = p.nqp - 1 - w / BH, bh = w % BH, b = bh / a.H, h = bh % a.H;
+      const int qt = 2 * qp + t;
+      if (qt >= p.nq) continue;  // this item has no second tile
       const int nk = qt + 1;
       const int qi = qt * AT_B + r;
       float m = -INFINITY, l = 0.f;
-      for (int j = 0; j < nk; ++j, ++g) {
-        const int sb = g & 1;
-        if (!warp_wait(b_sf + 8 * sb, (uint32_t)(g >> 1) & 1u, abort_flag, p.status)) { ok = false; break; }
+      for (int j = 0; j < nk; ++j) {
+        if (!warp_wait(b_sft, (uint32_t)n_s & 1u, abort_flag, p.status)) { ok = false; break; }
         tc_fence_after();
-        uint32_t s0[32], s1[32];
-        tmem_ld32(lane_base + sb * AT_B + half * 64, s0);
-        tmem_ld32(lane_base + sb * AT_B + half * 64 + 32, s1);
-        tmem_ld_wait();
-        tc_fence_before();
-        warp_arrive(b_se + 8 * sb);  // this warp is done reading S
-        float s[64];
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          s[c] = __uint_as_float(s0[c]);
-          s[32 + c] = __uint_as_float(s1[c]);
-        }
-        if (j == qt) {  // diagonal tile: keys after the query are masked
-          const int k0 = j * AT_B + half * 64;
-#pragma unroll
-          for (int c = 0; c < 64; ++c)
-            if (k0 + c > qi) s[c] = -INFINITY;
-        }
-        // Lazy rescaling: the running max m (log2 units) only moves when the row's tile max
-        // exceeds it by more than 8, so p <= 2^8 stays exact in fp32 and bf16; O and l
-        // always share the same m, so the result is unchanged.  The half-row maxima are
-        // exchanged with the partner warp through shared memory (double-buffered slots;
-        // the mbarrier arrive releases the write, the wait acquires the partner's).  The
-        // exponentials are computed speculatively with the current m unless this half
-        // already needs a move, and redone in the rare case the partner's half does.
-        const float hmax = tree_max<64>(s) * p.c2;
-        float* rx = red + (g & 1) * 256;
-        rx[half * 128 + r] = hmax;
-        const uint32_t xb = b_xmax + 8 * (quad * 2 + (g & 1));
-        warp_arrive(xb);
-        bool waited = false;
-        float m_new = m;
-        if (j == 0 || __any_sync(0xffffffffu, hmax > m + 8.0f)) {
-          if (!warp_wait(xb, (uint32_t)(g >> 1) & 1u, abort_flag, p.status)) { ok = false; break; }
-          waited = true;
-          const float tmax = fmaxf(hmax, rx[(half ^ 1) * 128 + r]);
-          if (j == 0 || tmax > m + 8.0f) m_new = fmaxf(m, tmax);
-        }
-        uint32_t pk[32];
-        float lsum = 0.f;
-        for (int pass = 0; pass < 2; ++pass) {
-          const float2 nm = make_float2(-m_new, -m_new), c2 = make_float2(p.c2, p.c2);
-          float2 ps[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-#pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const float2 x = fma2(make_float2(s[2 * c], s[2 * c + 1]), c2, nm);
-            const float2 pr = make_float2(ex2(x.x), ex2(x.y));
-            ps[c & 1] = add2(ps[c & 1], pr);
-            pk[c] = pack_bf16x2(pr.x, pr.y);
-          }
-          lsum = (ps[0].x + ps[0].y) + (ps[1].x + ps[1].y);
-          if (waited) break;
-          // speculation check: does the partner half need the max to move?
-          if (!warp_wait(xb, (uint32_t)(g >> 1) & 1u, abort_flag, p.status)) { ok = false; break; }
-          waited = true;
-          const float tmax = fmaxf(hmax, rx[(half ^ 1) * 128 + r]);
-          const bool mv = tmax > m + 8.0f;
-          if (!__any_sync(0xffffffffu, mv)) break;
-          if (mv) m_new = fmaxf(m, tmax);
-        }
-        if (!ok) break;
-        const bool move = m_new != m;
-        const float alpha = j == 0 ? 0.f : ex2(m - m_new);
-        l = l * alpha + lsum;
-        m = m_new;
-        const bool rescale = j >= 1 && __any_sync(0xffffffffu, move);
-        if (rescale) {
-          // O must be stable: wait for the previous PV (tile g-1), then scale it
-          const uint32_t pb = (g - 1) & 1 ? b_pv2 : b_pv;
-          if (!warp_wait(pb, (uint32_t)((g - 1) >> 1) & 1u, abort_flag, p.status)) { ok = false; break; }
-          tc_fence_after();
-          uint32_t o[32];
-          tmem_ld32(lane_base + AT_O_COL + half * 32, o);
+        float s[128];
+        {
+          uint32_t* u = reinterpret_cast<uint32_t*>(s);
+          tmem_ld32(lane_base + s_col, *reinterpret_cast<uint32_t(*)[32]>(u));
+          tmem_ld32(lane_base + s_col + 32, *reinterpret_cast<uint32_t(*)[32]>(u + 32));
+          tmem_ld32(lane_base + s_col + 64, *reinterpret_cast<uint32_t(*)[32]>(u + 64));
+          tmem_ld32(lane_base + s_col + 96, *reinterpret_cast<uint32_t(*)[32]>(u + 96));
           tmem_ld_wait();
-#pragma unroll
-          for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-          tmem_st32(lane_base + AT_O_COL + half * 32, o);
-        } else if (g >= 2) {
-          // the P buffer of this tile parity was last read by the PV of tile g-2
-          const uint32_t pb = g & 1 ? b_pv2 : b_pv;
-          if (!warp_wait(pb, (uint32_t)((g - 2) >> 1) & 1u, abort_flag, p.status)) { ok = false; break; }
-          tc_fence_after();
         }
-        // P (bf16 pairs) into TMEM: row r, keys half*64 .. +64 = columns half*32 .. +32
-        tmem_st32(lane_base + AT_P_COL + (g & 1) * 64 + half * 32, pk);
+        tc_fence_before();
+        warp_arrive(b_set);  // this warp is done reading S_t
+        ++n_s;
+        const bool diag = j == qt;
+        if (diag) {  // keys after the query are masked
+          const int kmax = qi - j * AT_B;  // key offsets > kmax are masked
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (c > kmax) s[c] = -INFINITY;
+        }
+        // Lazy rescaling: the running max m (log2 units) only moves when the tile's row max
+        // exceeds it by more than 8, so p <= 2^8 stays exact in fp32 and bf16; O and l always
+        // share the same m, so the result is unchanged.
+        const float tmax = row_max128(s) * p.c2;
+        float m_new = m;
+        if (j == 0 || tmax > m + 8.0f) m_new = fmaxf(m, tmax);
+        const bool rescale = j >= 1 && __any_sync(0xffffffffu, m_new != m);
+        const float alpha = j == 0 ? 0.f : ex2(m - m_new);
+        const float2 nm = make_float2(-m_new, -m_new);
+        uint32_t pk[64];
+        float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          const float2 x = fma2(make_float2(s[2 * c], s[2 * c + 1]), c2, nm);
+          const float2 pr = make_float2(ex2(x.x), ex2(x.y));
+          acc[c & 1] = add2(acc[c & 1], pr);
+          pk[c] = pack_bf16x2(pr.x, pr.y);
+        }
+        l = l * alpha + ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y));
+        m = m_new;
+        if (j >= 1) {
+          // PV_t(j-1) must be done: it reads the P buffer this tile overwrites, and O is
+          // rescaled only once that product is in
+          if (!warp_wait(b_pvt, (uint32_t)n_pv & 1u, abort_flag, p.status)) { ok = false; break; }
+          ++n_pv;
+          tc_fence_after();
+          if (rescale) {
+            uint32_t o[64];
+            tmem_ld32(lane_base + o_col, *reinterpret_cast<uint32_t(*)[32]>(o));
+            tmem_ld32(lane_base + o_col + 32, *reinterpret_cast<uint32_t(*)[32]>(o + 32));
+            tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < 64; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+            tmem_st32(lane_base + o_col, *reinterpret_cast<uint32_t(*)[32]>(o));
+            tmem_st32(lane_base + o_col + 32, *reinterpret_cast<uint32_t(*)[32]>(o + 32));
+          }
+        }
+        // P (bf16 pairs) into TMEM: row r, 128 keys = 64 columns
+        tmem_st32(lane_base + p_col, *reinterpret_cast<uint32_t(*)[32]>(pk));
+        tmem_st32(lane_base + p_col + 32, *reinterpret_cast<uint32_t(*)[32]>(pk + 32));
         tmem_st_wait();
         tc_fence_before();
-        warp_arrive(b_pf + 8 * (g & 1));
+        warp_arrive(b_pft);
       }
       if (!ok) break;
-      // epilogue of this item: its last PV (global tile g-1) is done
-      if (!warp_wait((g - 1) & 1 ? b_pv2 : b_pv, (uint32_t)((g - 1) >> 1) & 1u, abort_flag, p.status))
-        break;
+      // epilogue of this tile: its last PV is done
+      if (!warp_wait(b_pvt, (uint32_t)n_pv & 1u, abort_flag, p.status)) break;
+      ++n_pv;
       tc_fence_after();
-      float* rl = red + 512;
-      rl[half * 128 + r] = l;
-      warp_arrive(b_xsum + 8 * quad);
-      if (!warp_wait(b_xsum + 8 * quad, (uint32_t)it & 1u, abort_flag, p.status)) break;
-      const float lt = l + rl[(half ^ 1) * 128 + r];
-      const float inv = 1.0f / lt;
-      uint32_t o[32];
-      tmem_ld32(lane_base + AT_O_COL + half * 32, o);
+      uint32_t o[64];
+      tmem_ld32(lane_base + o_col, *reinterpret_cast<uint32_t(*)[32]>(o));
+      tmem_ld32(lane_base + o_col + 32, *reinterpret_cast<uint32_t(*)[32]>(o + 32));
       tmem_ld_wait();
       tc_fence_before();  // the next item's first PV overwrites O after this read
       if (qi < a.T) {
-        bf16* dst = static_cast<bf16*>(a.o) + (long long)b * a.osb + (long long)h * a.osh +
-                    (long long)qi * a.ost + half * 32;
+        const float inv = 1.0f / l;
+        bf16* dst = static_cast<bf16*>(a.o) + (long long)b * a.osb + (long long)h * a.osh + (long long)qi * a.ost;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < 8; ++q) {
           uint4 u;
           u.x = pack_bf16x2(__uint_as_float(o[8 * q]) * inv, __uint_as_float(o[8 * q + 1]) * inv);
           u.y = pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv);
@@ -364,7 +382,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
           u.w = pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv);
           *reinterpret_cast<uint4*>(dst + 8 * q) = u;
         }
-        if (half == 0) a.lse[(long long)bh * a.T + qi] = (m + __log2f(lt)) * 0.6931471805599453f;
+        a.lse[(long long)bh * a.T + qi] = (m + __log2f(l)) * 0.6931471805599453f;
       }
     }
   }
@@ -995,6 +1013,7 @@ int attn_fwd_tc(const AttnArgs& a, cudaStream_t s) {
   AtParams p;
   p.a = a;
   p.nq = (a.T + AT_B - 1) / AT_B;
+  p.nqp = (p.nq + 1) / 2;
   p.swap_ht = a.sh < a.st ? 1 : 0;
   p.c2 = a.scale * 1.4426950408889634f;
   p.idesc_s = mma_idesc(AT_B, 0);
@@ -1005,7 +1024,7 @@ int attn_fwd_tc(const AttnArgs& a, cudaStream_t s) {
   if (!make_head_map(&tq, a.q, a, p.swap_ht) || !make_head_map(&tk, a.k, a, p.swap_ht) ||
       !make_head_map(&tv, a.v, a, p.swap_ht))
     return (int)cudaErrorInvalidValue;
-  const long long items = (long long)p.nq * a.B * a.H;
+  const long long items = (long long)p.nqp * a.B * a.H;
   const int grid = (int)(items < num_sms() ? items : num_sms());
   launch_k(k_attn_fwd_tc, grid, AT_THREADS, AT_SMEM, s, tq, tk, tv, p);
   return (int)cudaGetLastError();

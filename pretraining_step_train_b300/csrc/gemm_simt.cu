@@ -75,6 +75,8 @@ __global__ void __launch_bounds__(256) k_gemm_simt(GemmArgs g) {
         case EPI_BIAS_RESID: v += bias[n] + resid[(long long)m * g.ldr + n]; break;
         case EPI_BIAS_GELU: v += bias[n]; D2[o] = gelu_f(v); v = gelu_grad_f(v); break;
         case EPI_GELU_BWD: v *= aux[(long long)m * g.ldaux + n]; break;
+        case EPI_BIAS_GELU_H: v += bias[n]; D2[o] = gelu_f(v); break;
+        case EPI_GELU_BWD_H: v *= gelu_grad_f(aux[(long long)m * g.ldaux + n]); break;
         default: break;
       }
       D[o] = v;

@@ -6,14 +6,22 @@
 //   backward  dX = dY W      A = dY (K-major), B = W  (MN-major)
 //             dW = dY^T X    A = dY (MN-major), B = X (MN-major), split over the rows
 //
-// Structure (one persistent CTA per SM, 18 warps):
-//   warp 0      TMA producer: 128B-swizzled A (128 x 64) and B (256 x 64) tiles
-//               into a 4-stage shared-memory ring, completion on mbarriers;
-//   warp 1      owns 512 TMEM columns (two 128 x 256 fp32 accumulators) and one
-//               thread issues tcgen05.mma (M=128, N=256, K=16) per 16-wide k step,
-//               releasing ring stages and finished accumulators with tcgen05.commit;
-//   warps 2-17  epilogue, four warps per TMEM lane quadrant (one per 64-column
-//               quarter): tcgen05.ld 32 rows x 16 columns at a time, fused bias /
+// Structure: persistent clusters of two CTAs (a CTA pair on two SMs), 18 warps
+// each; a pair computes 256 x 256 output tiles with the pair MMA (cta_group::2):
+//   warp 0      TMA producer of each CTA: its 128 rows of A and its 128 rows of
+//               B (half of the tile's 256 N columns), 128B-swizzled 64-deep k
+//               blocks, into a 6-stage shared-memory ring; both CTAs' copies
+//               complete on the even CTA's barrier of that stage;
+//   warp 1      of each CTA allocates 512 TMEM columns (two 128 x 256 fp32
+//               accumulators per CTA) together with its peer; one thread of the
+//               even CTA issues tcgen05.mma.cta_group::2 (M=256, N=256, K=16) per
+//               16-wide k step, reading A and B halves from both CTAs' shared
+//               memory and accumulating 128 rows in each CTA's tensor memory, and
+//               releases ring stages and finished accumulators in both CTAs with
+//               multicast tcgen05.commit;
+//   warps 2-17  epilogue of each CTA (its 128 rows of the tile), four warps per
+//               TMEM lane quadrant (one per 64-column quarter): tcgen05.ld 32 rows
+//               x 16 columns at a time, fused bias /
 //               residual / GELU / GELU' / cross-entropy statistics, then the
 //               32 x 16 result is staged in 32B-swizzled shared memory and
 //               written by a TMA bulk tensor store (coalesced, asynchronous).
@@ -21,9 +29,12 @@
 //               of the matching 32 x 16 box, one chunk ahead.  Sixteen warps
 //               (four per SM sub-partition) hide the epilogue's latencies.
 // The accumulator double buffer lets the epilogue of tile i overlap the
-// mainloop of tile i+1.  Every wait is bounded (about 2 s of %globaltimer);
-// on expiry the CTA latches ST_TIMEOUT in the status word, the other roles
-// stop, outstanding TMA copies and MMAs are drained and TMEM is freed.
+// mainloop of tile i+1.  Per k block each SM stages 32 KB of operands for a
+// 128 x 256 x 64 share of the MMA (a single-CTA 128 x 256 tile stages 48 KB), so
+// the operand traffic through L2, TMA and shared memory per flop is a third lower.
+// Every wait is bounded (about 2 s of %globaltimer); on expiry the CTA latches
+// ST_TIMEOUT in the status word, the other roles stop, outstanding TMA copies and
+// MMAs are drained, both CTAs meet at a cluster barrier and TMEM is freed.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -33,9 +44,13 @@
 namespace gpt2k {
 
 namespace {
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
-constexpr int A_TILE = BM * BK * 2;  // 16 KB
-constexpr int B_TILE = BN * BK * 2;  // 32 KB
+constexpr int BM = 128;       // accumulator rows per CTA
+constexpr int PM = 2 * BM;     // rows of a pair tile
+constexpr int BN = 256;        // columns of a tile (the pair MMA's N)
+constexpr int BNC = BN / 2;    // B rows (output columns) each CTA stages
+constexpr int BK = 64, STAGES = 6;
+constexpr int A_TILE = BM * BK * 2;   // 16 KB
+constexpr int B_TILE = BNC * BK * 2;  // 16 KB
 constexpr int STAGE_BYTES = A_TILE + B_TILE;
 constexpr int RING_BYTES = STAGES * STAGE_BYTES;
 constexpr int TMEM_COLS = 2 * BN;
@@ -51,7 +66,7 @@ constexpr int SMEM_BYTES = 1024 + RING_BYTES + EPI_WARPS * STG_BYTES + BAR_BYTES
 
 struct TcParams {
   GemmArgs g;
-  int mt, nt, splits, kps, total_kb;
+  int mt, nt, splits, kps, total_kb;  // mt, nt: pair tiles (256 x 256) along M and N
   uint32_t idesc;
   unsigned* status;
   int poison;
@@ -90,13 +105,19 @@ struct Unit {
   int tile, m_t, n_t, sp, kb0, kb1, role, slot;
 };
 
-// First stream-K iteration of CTA c: CTA c owns [sk_lo(c), sk_lo(c + 1)).
+// Work is dealt to CTA pairs: pair (cluster) c = blockIdx.x / 2 of gridDim.x / 2.
+__device__ __forceinline__ int pair_id() { return (int)(blockIdx.x >> 1); }
+__device__ __forceinline__ int num_pairs() { return (int)(gridDim.x >> 1); }
+
+// First stream-K iteration of pair c: pair c owns [sk_lo(c), sk_lo(c + 1)).
 __device__ __forceinline__ long long sk_lo(const TcParams& p, int c) {
-  return p.sk_iters * c / gridDim.x;
+  return p.sk_iters * c / num_pairs();
 }
 
-// The u-th unit of this CTA; false past its last.
-//   Plain schedule: tiles blockIdx.x, + gridDim.x, ... over (split, M tile, N tile).
+// The u-th unit of this CTA's pair; false past its last.  Both CTAs of a pair
+// walk the same units; `slot` is the pair's partial-sum slot (each CTA of the
+// pair owns half of it: physical slot 2 * slot + rank).
+//   Plain schedule: tiles c, c + P, ... (c = pair, P = pairs) over (split, M tile, N tile).
 //   SK_SPLIT: the same walk; split s-1 of a tile (U_FINISH) adds the partial
 //   sums that splits 0 .. s-2 (U_PART, slot = their walk index) left for it and
 //   runs the epilogue.  The walk is split-major, so one wave of CTAs covers the
@@ -111,10 +132,11 @@ __device__ __forceinline__ long long sk_lo(const TcParams& p, int c) {
 // In both, a U_FINISH unit waits only on U_PART units, which wait on nothing.
 __device__ __forceinline__ bool cta_unit(const TcParams& p, int u, Unit& w) {
   int tile;
-  w.slot = blockIdx.x;
+  const int c = pair_id(), np = num_pairs();
+  w.slot = c;
   if (p.sk == SK_STREAM) {
     const int Kb = p.total_kb;
-    const long long s = sk_lo(p, blockIdx.x), e = sk_lo(p, blockIdx.x + 1);
+    const long long s = sk_lo(p, c), e = sk_lo(p, c + 1);
     const int nfrag = e > s ? (int)((e - 1) / Kb - s / Kb) + 1 : 0;
     if (u < nfrag) {
       const int i = (e % Kb) != 0 ? (u == 0 ? nfrag - 1 : u - 1) : u;
@@ -126,7 +148,7 @@ __device__ __forceinline__ bool cta_unit(const TcParams& p, int u, Unit& w) {
       w.role = w.kb1 < Kb ? U_PART : (w.kb0 > 0 ? U_FINISH : U_FULL);
       tile = p.dp_tiles + (int)t;
     } else {
-      tile = blockIdx.x + (u - nfrag) * gridDim.x;
+      tile = c + (u - nfrag) * np;
       if (tile >= p.dp_tiles) return false;
       w.kb0 = 0;
       w.kb1 = Kb;
@@ -134,7 +156,7 @@ __device__ __forceinline__ bool cta_unit(const TcParams& p, int u, Unit& w) {
     }
     tile_coords(p, tile, w.m_t, w.n_t, w.sp);
   } else {
-    tile = blockIdx.x + u * gridDim.x;
+    tile = c + u * np;
     if (tile >= p.mt * p.nt * p.splits) return false;
     tile_coords(p, tile, w.m_t, w.n_t, w.sp);
     w.kb0 = w.sp * p.kps;
@@ -281,29 +303,6 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
-// Hardware tanh (MUFU, PTX tanh.approx.f32): relative error about 2^-11, far
-// below the bf16 rounding of the values it feeds.
-__device__ __forceinline__ float tanh_hw(float x) {
-  float y;
-  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-// tanh-form GELU with the hardware tanh (bf16 epilogues only).
-// gelu and gelu' of a pair of values sharing one hardware tanh each, in packed
-// fp32 pair arithmetic: y = x/2 (1 + th), dy = (1 + th)/2 + x/2 (1 - th^2) du with
-// th = tanh(x (k + k c x^2)), du = k + 3 k c x^2.
-__device__ __forceinline__ void gelu_and_grad2(float2 x, float2& y, float2& dy) {
-  const float2 x2 = mul2(x, x);
-  const float2 u = mul2(x, fma2(x2, make_float2(GELU_K * GELU_C, GELU_K * GELU_C), make_float2(GELU_K, GELU_K)));
-  const float2 th = make_float2(tanh_hw(u.x), tanh_hw(u.y));
-  const float2 hx = mul2(x, make_float2(0.5f, 0.5f));
-  y = fma2(hx, th, hx);
-  const float2 du = fma2(x2, make_float2(3.0f * GELU_K * GELU_C, 3.0f * GELU_K * GELU_C), make_float2(GELU_K, GELU_K));
-  const float2 om = fma2(th, make_float2(-th.x, -th.y), make_float2(1.0f, 1.0f));  // 1 - th^2
-  const float2 half_p = fma2(th, make_float2(0.5f, 0.5f), make_float2(0.5f, 0.5f));   // (1 + th) / 2
-  dy = fma2(mul2(hx, om), du, half_p);
-}
-
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmD2,
@@ -323,15 +322,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const GemmArgs& g = p.g;
+  const uint32_t rank = cluster_ctarank();  // 0: the pair's MMA issuer
+  // the even CTA's barriers, as cluster addresses: ring stages fill there, and
+  // both CTAs' epilogues hand their accumulator halves back there
+  const uint32_t lead_full = mapa_shared(b_full, 0), lead_tempty = mapa_shared(b_tempty, 0);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
-      mbar_init(b_full + 8 * i, 1);
+      mbar_init(b_full + 8 * i, 1);  // the even CTA's producer posts both CTAs' bytes
       mbar_init(b_empty + 8 * i, 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(b_tfull + 8 * i, 1);
-      mbar_init(b_tempty + 8 * i, 32 * EPI_WARPS);
+      mbar_init(b_tempty + 8 * i, 2 * EPI_WARPS);  // one arrival per epilogue warp of either CTA
     }
     mbar_init(b_done, 1);
     for (int i = 0; i < 2 * EPI_WARPS; ++i) mbar_init(b_xload + 8 * i, 1);
@@ -343,12 +346,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmD)) : "memory");
   }
   pdl_wait();  // the predecessor kernel is complete: global memory and TMEM are ours
-  if (warp == 1) {
-    tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), TMEM_COLS);
-    tmem_relinquish();
+  if (warp == 1) {  // one warp of each CTA allocates the pair's columns together
+    tmem_alloc_pair(smem_u32(const_cast<uint32_t*>(tmem_slot)), TMEM_COLS);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync_all();  // both CTAs' barriers are initialised and their TMEM allocated
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -363,29 +366,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       bool first = true;
       Unit w;
       for (int u = 0; cta_unit(p, u, w); ++u) {
-        const int m_t = w.m_t, n_t = w.n_t;
+        const int m0 = w.m_t * PM + (int)rank * BM, n0 = w.n_t * BN + (int)rank * BNC;  // this CTA's halves
         bool stop = false;
         for (int kb = w.kb0; kb < w.kb1; ++kb) {
           if (!mbar_wait(b_empty + 8 * stage, phase ^ 1, abort_flag, p.status)) { stop = true; break; }
           if (!((p.poison & POISON_GEMM_TMA) && first)) {
             const uint32_t sa = s_tiles + stage * STAGE_BYTES, sb = sa + A_TILE;
-            const uint32_t fb = b_full + 8 * stage;
-            mbar_expect_tx(fb, STAGE_BYTES);
+            const uint32_t fb = lead_full + 8 * stage;
+            // Only the even CTA arrives, with the byte count of both CTAs' copies (a local
+            // arrive: a cluster-scope release per stage from each producer cost about 1,500
+            // cycles per k block).  The odd CTA's copies may complete on that barrier before
+            // the arrive; the phase cannot complete while the arrive is pending.
+            if (rank == 0) mbar_expect_tx(b_full + 8 * stage, 2 * STAGE_BYTES);
             if (!g.a_mn) {
-              tma_load_2d(sa, &tmA, fb, kb * BK, m_t * BM);
+              tma_load_2d_pair(sa, &tmA, fb, kb * BK, m0);
             } else if (p.a3d) {
-              tma_load_3d(sa, &tmA, fb, 0, kb * BK, m_t * (BM / 64));
+              tma_load_3d_pair(sa, &tmA, fb, 0, kb * BK, m0 / 64);
             } else {
-              tma_load_2d(sa, &tmA, fb, m_t * BM, kb * BK);
-              tma_load_2d(sa + 8192, &tmA, fb, m_t * BM + 64, kb * BK);
+              tma_load_2d_pair(sa, &tmA, fb, m0, kb * BK);
+              tma_load_2d_pair(sa + 8192, &tmA, fb, m0 + 64, kb * BK);
             }
             if (!g.b_mn) {
-              tma_load_2d(sb, &tmB, fb, kb * BK, n_t * BN);
+              tma_load_2d_pair(sb, &tmB, fb, kb * BK, n0);
             } else if (p.b3d) {
-              tma_load_3d(sb, &tmB, fb, 0, kb * BK, n_t * (BN / 64));
+              tma_load_3d_pair(sb, &tmB, fb, 0, kb * BK, n0 / 64);
             } else {
-#pragma unroll
-              for (int j = 0; j < 4; ++j) tma_load_2d(sb + j * 8192, &tmB, fb, n_t * BN + j * 64, kb * BK);
+              tma_load_2d_pair(sb, &tmB, fb, n0, kb * BK);
+              tma_load_2d_pair(sb + 8192, &tmB, fb, n0 + 64, kb * BK);
             }
             last_par[stage] = (int)phase;
           }
@@ -394,13 +401,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         if (stop) break;
       }
-      // drain: never leave the CTA with bulk copies still landing in its shared memory
+      // drain: never leave with bulk copies still landing in shared memory.  Both
+      // CTAs' copies of a stage complete on the even CTA's barrier, so the even
+      // CTA waits for every stage it filled (the odd CTA filled the same ones);
+      // the cluster barrier at the end keeps the odd CTA resident until then.
+      if (rank == 0) {
 #pragma unroll
-      for (int i = 0; i < STAGES; ++i)
-        if (last_par[i] >= 0) mbar_wait_drain(b_full + 8 * i, (uint32_t)last_par[i]);
+        for (int i = 0; i < STAGES; ++i)
+          if (last_par[i] >= 0) mbar_wait_drain(b_full + 8 * i, (uint32_t)last_par[i]);
+      }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && rank == 0) {
       // ---------------- MMA issuer
       int stage = 0;
       uint32_t phase = 0;
@@ -419,18 +431,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t sa = s_tiles + stage * STAGE_BYTES, sb = sa + A_TILE;
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
-            mma_bf16(d_tmem, operand_desc(sa, g.a_mn, k), operand_desc(sb, g.b_mn, k), p.idesc,
-                     (kb > kb0 || k > 0) ? 1u : 0u);
+            mma_bf16_pair(d_tmem, operand_desc(sa, g.a_mn, k), operand_desc(sb, g.b_mn, k), p.idesc,
+                          (kb > kb0 || k > 0) ? 1u : 0u);
           }
-          mma_commit(b_empty + 8 * stage);
+          mma_commit_pair_mc(b_empty + 8 * stage, 3);  // the stage is free again in both CTAs
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
         if (stop) break;
-        mma_commit(b_tfull + 8 * abuf);
+        mma_commit_pair_mc(b_tfull + 8 * abuf, 3);  // both halves of the accumulator are ready
         if (++abuf == 2) { abuf = 0; aphase ^= 1; }
       }
       // all MMAs issued by this thread have completed once b_done flips
-      mma_commit(b_done);
+      mma_commit_pair(b_done);
       mbar_wait_drain(b_done, 0);
     }
   } else {
@@ -450,12 +462,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     auto warp_origin = [&](bool ok, const Unit& w, int& xb, int& y) {
       if (!ok || w.role == U_PART) { xb = 0; y = g.M; return; }
       xb = w.n_t * BN + qq * WCOLS;
-      y = w.m_t * BM + quad * 32;
+      y = w.m_t * PM + (int)rank * BM + quad * 32;
     };
-    // this warp's region of CTA j's partial-sum slot: chunk c, lane l, 16 floats as
+    // this warp's region of this CTA's half of pair slot j: chunk c, lane l, 16 floats as
     // four float4 at ((c * 4 + q) * 32 + l) * 4
     auto slot_of = [&](int j) {
-      return p.sk_part + (size_t)j * (BM * BN) + (size_t)ew * (NCHUNK * CW * 32);
+      return p.sk_part + (size_t)(2 * j + (int)rank) * (BM * BN) + (size_t)ew * (NCHUNK * CW * 32);
+    };
+    auto flag_of = [&](int j) { return p.sk_flags + (2 * j + (int)rank) * EPI_WARPS + ew; };
+    // hand an accumulator buffer back to the MMA issuer (the even CTA)
+    auto release_acc = [&](int b) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_remote_arrive(lead_tempty + 8 * b);
     };
     // Prefetch the x operand of the chunk at (x, y) into box b (all lanes track the state).
     auto x_issue = [&](int x, int y, int b) {
@@ -467,7 +486,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       xpend |= 1u << b;
     };
-    const bool has_bias = epi == EPI_BIAS || epi == EPI_BIAS_RESID || epi == EPI_BIAS_GELU;
+    const bool has_bias = epi == EPI_BIAS || epi == EPI_BIAS_RESID || epi == EPI_BIAS_GELU || epi == EPI_BIAS_GELU_H;
     Unit nw;
     bool nok = cta_unit(p, 0, nw);
     int nxb, ny;  // origin of the next unit this warp handles
@@ -492,33 +511,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           uint32_t r[16];
           tmem_ld16(tacc + c * CW, r);
           tmem_ld_wait();
-          if (c == NCHUNK - 1) {
-            tc_fence_before();
-            mbar_arrive(b_tempty + 8 * abuf);
-          }
+          if (c == NCHUNK - 1) release_acc(abuf);
 #pragma unroll
           for (int q = 0; q < 4; ++q) st_cg4(slot + ((c * 4 + q) * 32 + lane) * 4, r + 4 * q);
         }
         __threadfence();
         __syncwarp();
-        if (lane == 0 && !(p.poison & POISON_GEMM_FLAG)) st_release_gpu(p.sk_flags + w.slot * EPI_WARPS + ew, 1u);
+        if (lane == 0 && !(p.poison & POISON_GEMM_FLAG)) st_release_gpu(flag_of(w.slot), 1u);
         x_issue(nxb, ny, bx);  // the next unit's first operand chunk
         prev_stored = false;
         if (++abuf == 2) { abuf = 0; aphase ^= 1; }
         continue;
       }
       // finish: the partial sums of this tile sit in slots ps0 + i * pst, i < pn
-      // (SK_STREAM: CTAs [j0, blockIdx.x), skipping CTAs with an empty share;
+      // (SK_STREAM: pairs [j0, this pair), skipping pairs with an empty share;
       // SK_SPLIT: the walk indices of splits 0 .. s-2); wait for each one's flag,
       // then add them in that order
       int ps0 = 0, pn = 0, pst = 1;
       if (w.role == U_FINISH) {
         if (p.sk == SK_STREAM) {
           const long long t0 = (long long)(w.tile - p.dp_tiles) * p.total_kb;
-          int j0 = blockIdx.x;
+          int j0 = pair_id();
           while (j0 > 0 && sk_lo(p, j0) > t0) --j0;
           ps0 = j0;
-          pn = blockIdx.x - j0;
+          pn = pair_id() - j0;
         } else {
           pst = p.mt * p.nt;
           ps0 = w.tile - (p.splits - 1) * pst;
@@ -528,11 +544,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int i = 0; i < pn && ok; ++i) {
           const int j = ps0 + i * pst;
           if (p.sk == SK_STREAM && sk_lo(p, j) == sk_lo(p, j + 1)) continue;
-          ok = flag_wait(p.sk_flags + j * EPI_WARPS + ew, lane, abort_flag, p.status);
+          ok = flag_wait(flag_of(j), lane, abort_flag, p.status);
         }
         if (!ok) break;
       }
-      const int m = m_t * BM + quad * 32 + lane;
+      const int m = m_t * PM + (int)rank * BM + quad * 32 + lane;
       const int tgt = (epi == EPI_CE && m < g.M) ? g.targets[m] : -1;
       float ce_m = -INFINITY, ce_s = 0.f, ce_t = 0.f;
       bool stop = false;
@@ -542,10 +558,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         uint32_t r[16];
         tmem_ld16(tacc + c * CW, r);
         tmem_ld_wait();
-        if (c == NCHUNK - 1) {  // every TMEM read of this accumulator is done: hand it back to the MMA
-          tc_fence_before();
-          mbar_arrive(b_tempty + 8 * abuf);
-        }
+        if (c == NCHUNK - 1) release_acc(abuf);  // every TMEM read of this accumulator is done
         if (pn) {
           float acc[16];
 #pragma unroll
@@ -604,7 +617,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               const float2 t = add2(make_float2(v[j], v[j + 1]), make_float2(xv[j], xv[j + 1]));
               v[j] = t.x; v[j + 1] = t.y;
             }
-          } else {  // EPI_GELU_BWD: dh = da * gelu'(h)
+          } else {  // EPI_GELU_BWD: dh = da * gelu'(h); EPI_GELU_BWD_H: gelu'(h) from the stored h
+            if (epi == EPI_GELU_BWD_H) {
+#pragma unroll
+              for (int j = 0; j < 16; j += 2) {
+                float2 y, dy;
+                gelu_and_grad2(make_float2(xv[j], xv[j + 1]), y, dy);
+                xv[j] = dy.x; xv[j + 1] = dy.y;
+              }
+            }
 #pragma unroll
             for (int j = 0; j < 16; j += 2) {
               const float2 t = mul2(make_float2(v[j], v[j + 1]), make_float2(xv[j], xv[j + 1]));
@@ -665,6 +686,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
         uint32_t w[8];
+        if (epi == EPI_BIAS_GELU_H) {
+          // h rounded to bf16 (D, kept for the backward) and gelu of that rounded h (D2), so a
+          // later recompute from D reproduces D2 exactly
+          pack16_bf16(v, w);
+          float a[16];
+          uint32_t wa[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            float2 y, dy;
+            gelu_and_grad2(make_float2(__uint_as_float(w[j] << 16), __uint_as_float(w[j] & 0xFFFF0000u)), y, dy);
+            a[2 * j] = y.x; a[2 * j + 1] = y.y;
+          }
+          pack16_bf16(a, wa);
+          if (lane == 0) bulk_wait_read<0>();
+          __syncwarp();
+          box_store_row(stg, lane, w);
+          box_store_row(stg + BOX_BYTES, lane, wa);
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(&tmD, stg, x0, y0, 0);
+            tma_store_3d(&tmD2, stg + BOX_BYTES, x0, y0, 0);
+            bulk_commit();
+          }
+          prev_stored = true;
+          continue;
+        }
         if (epi == EPI_BIAS_GELU) {
           // gelu'(h) (D, for the backward) and gelu(h) (D2) from one tanh: both staged boxes
           float a[16];
@@ -714,7 +762,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (pn) {  // the partial sums are consumed: lower the flags for the next launch
         __syncwarp();
         if (lane == 0)
-          for (int i = 0; i < pn; ++i) p.sk_flags[(ps0 + i * pst) * EPI_WARPS + ew] = 0u;
+          for (int i = 0; i < pn; ++i) *flag_of(ps0 + i * pst) = 0u;
       }
       // one statistics partial per row and WCOLS-column quarter tile that starts inside N
       if (epi == EPI_CE && !split && m < g.M && n_t * BN + qq * WCOLS < g.N) {
@@ -735,9 +783,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __syncwarp();
   tc_fence_before();
   __syncthreads();
+  // neither CTA leaves while its peer may still signal its barriers or read its
+  // shared memory; then each frees the pair's columns
+  cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    tmem_dealloc_pair(tmem_base, TMEM_COLS);
   }
 }
 
@@ -840,19 +891,48 @@ int num_sms() {
 
 int gemm_tc_stat_cols() { return WCOLS; }
 
+// CTA pairs of k_gemm_tc that can be resident at once on the current device
+// (queried once per device and context; at most half the SMs).
+static PerDeviceOnce g_smem_attr;  // k_gemm_tc's shared-memory limit, set per device and context
+
+static int gemm_pairs() {
+  static PerDeviceOnce once;
+  static int pairs[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return num_sms() / 2;
+  const unsigned long long id = current_context_id();
+  if (id != 0 && once.ctx[dev] == id && pairs[dev] > 0) return pairs[dev];
+  int n = 0;
+  if (smem_limit_once(reinterpret_cast<const void*>(k_gemm_tc), SMEM_BYTES, &g_smem_attr) != cudaSuccess)
+    (void)cudaGetLastError();
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg = launch_cfg(dim3(2), dim3(NUM_THREADS), SMEM_BYTES, nullptr, attr, true);
+  if (cudaOccupancyMaxActiveClusters(&n, k_gemm_tc, &cfg) != cudaSuccess || n <= 0) {
+    (void)cudaGetLastError();
+    n = num_sms() / 2;
+  }
+  if (n > num_sms() / 2) n = num_sms() / 2;
+  pairs[dev] = n;
+  once.ctx[dev] = current_context_id();
+  return n;
+}
+
+int gemm_tc_pairs() { return gemm_pairs(); }
+
 size_t gemm_tc_ws_bytes(int M, int N, int splits) {
   return splits > 1 ? (size_t)splits * M * N * sizeof(float) : 0;
 }
 
-// Partial-sum slots of the in-kernel schedules: three per SM.
+// Partial-sum slots of the in-kernel schedules: three per SM (a pair slot is two
+// of them, one per CTA).
 static int sk_slots() { return 3 * num_sms(); }
 static size_t sk_flag_bytes() { return ((size_t)sk_slots() * EPI_WARPS * 4 + 1023) / 1024 * 1024; }
 
 size_t gemm_tc_sk_ws_bytes() { return sk_flag_bytes() + (size_t)sk_slots() * BM * BN * sizeof(float); }
 size_t gemm_tc_sk_plane_offset() { return sk_flag_bytes(); }
 
-int gemm_tc_pick_splits(int M, int N, int K, int sms) {
-  const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+int gemm_tc_pick_splits(int M, int N, int K, int sms) {  // sms: CTA pairs
+  const int tiles = ((M + PM - 1) / PM) * ((N + BN - 1) / BN);
   const int total_kb = (K + BK - 1) / BK;
   if (tiles >= sms) return 1;
   int best = 1;
@@ -879,7 +959,7 @@ int gemm_tc_effective_splits(int K, int splits) {
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
-// Schedule for T tiles of Kb k blocks on G SMs (GEMM_TC_STREAM_K):
+// Schedule for T pair tiles of Kb k blocks on G CTA pairs (GEMM_TC_STREAM_K):
 //  - T >= G, last wave part-empty by more than 3%, tiles at least 32 k blocks
 //    deep: SK_STREAM over the leftover tiles (whole waves stay data-parallel).
 //    Shallower tiles are epilogue-bound; cutting them adds epilogues, not speed.
@@ -912,7 +992,7 @@ static int sk_plan(const GemmArgs& g, int T, int Kb, int G, bool force, int& dp,
   if (s > 2 && (g.epi == EPI_STORE || g.epi == EPI_F32) &&
       gemm_tc_ws_bytes(M, N, s) <= (size_t)sk_slots() * BM * BN * sizeof(float))
     return SK_REDUCE;
-  if ((long long)(s - 1) * T > sk_slots()) return SK_NONE;
+  if (2LL * (s - 1) * T > sk_slots()) return SK_NONE;
   return SK_SPLIT;
 }
 
@@ -923,16 +1003,17 @@ int gemm_tc(const GemmArgs& g, int splits, void* ws, size_t ws_bytes, unsigned* 
   if (g.N % 8 || g.lda % 8 || g.ldb % 8 || g.ldd % 8) return (int)cudaErrorInvalidValue;
   if (!aligned16(g.A) || !aligned16(g.B) || !aligned16(g.D)) return (int)cudaErrorInvalidValue;
   if (g.epi == EPI_BIAS_RESID && (g.ldr % 8 || !aligned16(g.resid))) return (int)cudaErrorInvalidValue;
-  if (g.epi == EPI_GELU_BWD && (g.ldaux % 8 || !aligned16(g.aux))) return (int)cudaErrorInvalidValue;
-  if (g.epi == EPI_BIAS_GELU && !aligned16(g.D2)) return (int)cudaErrorInvalidValue;
-  if ((g.epi == EPI_BIAS || g.epi == EPI_BIAS_RESID || g.epi == EPI_BIAS_GELU) && !aligned16(g.bias))
+  const bool gelu_fwd = g.epi == EPI_BIAS_GELU || g.epi == EPI_BIAS_GELU_H;
+  const bool gelu_bwd = g.epi == EPI_GELU_BWD || g.epi == EPI_GELU_BWD_H;
+  if (gelu_bwd && (g.ldaux % 8 || !aligned16(g.aux))) return (int)cudaErrorInvalidValue;
+  if (gelu_fwd && !aligned16(g.D2)) return (int)cudaErrorInvalidValue;
+  if ((g.epi == EPI_BIAS || g.epi == EPI_BIAS_RESID || gelu_fwd) && !aligned16(g.bias))
     return (int)cudaErrorInvalidValue;
-  static PerDeviceOnce attr;
-  cudaError_t ae = smem_limit_once(reinterpret_cast<const void*>(k_gemm_tc), SMEM_BYTES, &attr);
+  cudaError_t ae = smem_limit_once(reinterpret_cast<const void*>(k_gemm_tc), SMEM_BYTES, &g_smem_attr);
   if (ae != cudaSuccess) return (int)ae;
   TcParams p;
   p.g = g;
-  p.mt = (g.M + BM - 1) / BM;
+  p.mt = (g.M + PM - 1) / PM;
   p.nt = (g.N + BN - 1) / BN;
   p.total_kb = (g.K + BK - 1) / BK;
   p.sk = 0;
@@ -943,7 +1024,7 @@ int gemm_tc(const GemmArgs& g, int splits, void* ws, size_t ws_bytes, unsigned* 
   if (splits == GEMM_TC_STREAM_K || splits == GEMM_TC_STREAM_K_FORCE) {
     if (!ws || !aligned16(ws) || ws_bytes < gemm_tc_sk_ws_bytes()) return (int)cudaErrorInvalidValue;
     int dp = 0, skt = 0, ssplit = 1;
-    const int plan = sk_plan(g, p.mt * p.nt, p.total_kb, num_sms(), splits == GEMM_TC_STREAM_K_FORCE, dp, skt,
+    const int plan = sk_plan(g, p.mt * p.nt, p.total_kb, gemm_pairs(), splits == GEMM_TC_STREAM_K_FORCE, dp, skt,
                              ssplit);
     char* slots = static_cast<char*>(ws) + sk_flag_bytes();
     if (plan == SK_REDUCE) {  // plain split-K into the slot area
@@ -974,7 +1055,7 @@ int gemm_tc(const GemmArgs& g, int splits, void* ws, size_t ws_bytes, unsigned* 
   p.status = status;
   p.poison = test_poison();
   p.out_f32 = ((p.splits > 1 && p.sk == SK_NONE) || g.epi == EPI_F32) ? 1 : 0;
-  p.load_x = (g.epi == EPI_BIAS_RESID || g.epi == EPI_GELU_BWD) ? 1 : 0;
+  p.load_x = (g.epi == EPI_BIAS_RESID || gelu_bwd) ? 1 : 0;
   p.m_fast = ((double)g.N * g.K > (double)g.M * g.K) ? 1 : 0;
   CUtensorMap tmA, tmB, tmD, tmD2, tmX;
   p.a3d = (g.a_mn && g.M % 64 == 0) ? 1 : 0;
@@ -982,31 +1063,32 @@ int gemm_tc(const GemmArgs& g, int splits, void* ws, size_t ws_bytes, unsigned* 
   bool ok = p.a3d ? make_tmap_mn3d(&tmA, g.A, g.M, g.K, g.lda, BM / 64)
                   : g.a_mn ? make_tmap(&tmA, g.A, g.M, g.K, g.lda, 64, 64)
                            : make_tmap(&tmA, g.A, g.K, g.M, g.lda, 64, BM);
-  ok = ok && (p.b3d ? make_tmap_mn3d(&tmB, g.B, g.N, g.K, g.ldb, BN / 64)
+  ok = ok && (p.b3d ? make_tmap_mn3d(&tmB, g.B, g.N, g.K, g.ldb, BNC / 64)
                     : g.b_mn ? make_tmap(&tmB, g.B, g.N, g.K, g.ldb, 64, 64)
-                             : make_tmap(&tmB, g.B, g.K, g.N, g.ldb, 64, BN));
+                             : make_tmap(&tmB, g.B, g.K, g.N, g.ldb, 64, BNC));
   if (p.splits > 1 && p.sk == SK_NONE)
     ok = ok && make_box_map(&tmD, ws, 1, g.N, g.M, p.splits, g.N);
   else
     ok = ok && make_box_map(&tmD, g.D, p.out_f32, g.N, g.M, 1, g.ldd);
-  if (g.epi == EPI_BIAS_GELU)
+  if (gelu_fwd)
     ok = ok && make_box_map(&tmD2, g.D2, 0, g.N, g.M, 1, g.ldd);
   else
     tmD2 = tmD;
   if (g.epi == EPI_BIAS_RESID)
     ok = ok && make_x_map(&tmX, g.resid, g.N, g.M, g.ldr);
-  else if (g.epi == EPI_GELU_BWD)
+  else if (gelu_bwd)
     ok = ok && make_x_map(&tmX, g.aux, g.N, g.M, g.ldaux);
   else
     tmX = tmA;
   if (!ok) return (int)cudaErrorInvalidValue;
   // kind::f16 instruction descriptor: D fp32, A/B bf16, operand majors, N >> 3, M >> 4
+  // (the pair MMA: M = 256 rows, 128 from each CTA)
   p.idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)g.a_mn << 15) |
-            ((uint32_t)g.b_mn << 16) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+            ((uint32_t)g.b_mn << 16) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(PM >> 4) << 24);
   const int ntiles = p.mt * p.nt * p.splits;
-  int grid = num_sms();  // a stream-K launch spreads its iterations over every SM
-  if (p.sk != SK_STREAM && grid > ntiles) grid = ntiles;
-  launch_k(k_gemm_tc, grid, NUM_THREADS, SMEM_BYTES, s, tmA, tmB, tmD, tmD2, tmX, p);
+  int pairs = gemm_pairs();  // a stream-K launch spreads its iterations over every pair
+  if (p.sk != SK_STREAM && pairs > ntiles) pairs = ntiles;
+  launch_k_pair(k_gemm_tc, 2 * pairs, NUM_THREADS, SMEM_BYTES, s, tmA, tmB, tmD, tmD2, tmX, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return (int)e;
   if (p.splits > 1 && p.sk == SK_NONE && reduce) {

@@ -93,6 +93,7 @@ namespace {
 
 struct Shape {
   int L, H, C, V, Vpad, T, B, prec;
+  int rc = 0;  // activation recompute: 0 none, 1 GELU output, 2 GELU output and LayerNorm outputs
   int M() const { return B * T; }
   int d() const { return C / H; }
   size_t esz() const { return prec == GPT2_BF16 ? 2 : 4; }
@@ -130,7 +131,7 @@ struct Plan {
   size_t params, grads, master, adam_m, adam_v, grad_acc;
   size_t tokens, targets;
   size_t res, x1, ln1, ln2, ln1_mean, ln1_rstd, ln2_mean, ln2_rstd, qkv, atty, att_lse, fch, fca;
-  size_t lnf, lnf_mean, lnf_rstd, logits, ce_max, ce_sum, ce_tgt, ce_lse, ce_rows, scalars, status, hyper, guard;
+  size_t lnf, lnf_mean, lnf_rstd, rc_stats, logits, ce_max, ce_sum, ce_tgt, ce_lse, ce_rows, scalars, status, hyper, guard;
   size_t dres, dres_b, dbig, dqkv, dsmall, attD, order, lnb_part, colsum_part, norm_part, sk_ws;
   size_t sk_bytes = 0;
   int ce_tiles = 0;
@@ -160,8 +161,10 @@ Plan make_plan(const Shape& s) {
   p.targets = take(cur, M * 4);
   p.res = take(cur, (L + 1) * M * C * e);
   p.x1 = take(cur, L * M * C * e);
-  p.ln1 = take(cur, L * M * C * e);
-  p.ln2 = take(cur, L * M * C * e);
+  // with LayerNorm recompute one buffer holds the LayerNorm output in use (forward: until
+  // the next GEMM has read it; backward: recomputed for the weight-gradient GEMM)
+  p.ln1 = take(cur, (s.rc >= 2 ? 1 : L) * M * C * e);
+  p.ln2 = s.rc >= 2 ? p.ln1 : take(cur, L * M * C * e);
   p.ln1_mean = take(cur, L * M * f);
   p.ln1_rstd = take(cur, L * M * f);
   p.ln2_mean = take(cur, L * M * f);
@@ -170,10 +173,12 @@ Plan make_plan(const Shape& s) {
   p.atty = take(cur, L * M * C * e);
   p.att_lse = take(cur, L * (size_t)s.B * s.H * s.T * f);
   p.fch = take(cur, L * M * 4 * C * e);
-  p.fca = take(cur, L * M * 4 * C * e);
+  // with GELU recompute one buffer holds gelu(h) in use (recomputed in the backward)
+  p.fca = take(cur, (s.rc >= 1 ? 1 : L) * M * 4 * C * e);
   p.lnf = take(cur, M * C * e);
   p.lnf_mean = take(cur, M * f);
   p.lnf_rstd = take(cur, M * f);
+  p.rc_stats = take(cur, 2 * M * f);  // statistics written by a recomputed LayerNorm (not read)
   p.logits = take(cur, M * (size_t)s.Vpad * e);
   p.ce_tiles = (s.Vpad + gemm_tc_stat_cols() - 1) / gemm_tc_stat_cols();
   p.ce_max = take(cur, M * p.ce_tiles * f);
@@ -215,6 +220,7 @@ int validate(const Shape& s) {
   if ((long long)s.B * s.T > 16384) return GPT2_E_UNSUPPORTED;
   if (s.prec == GPT2_BF16 && (s.d() != 64 || s.C > 2048)) return GPT2_E_UNSUPPORTED;
   if (s.prec == GPT2_FP32 && (s.d() > 128 || s.C > 1024)) return GPT2_E_UNSUPPORTED;
+  if (s.rc < 0 || s.rc > 2) return GPT2_E_INVAL;
   return GPT2_OK;
 }
 
@@ -300,12 +306,12 @@ struct Ptrs {
   long long MC() const { return (long long)h->s.M() * h->s.C; }
   T* res(int l) const { return h->at<T>(h->p.res) + l * MC(); }
   T* x1(int l) const { return h->at<T>(h->p.x1) + l * MC(); }
-  T* ln1(int l) const { return h->at<T>(h->p.ln1) + l * MC(); }
-  T* ln2(int l) const { return h->at<T>(h->p.ln2) + l * MC(); }
+  T* ln1(int l) const { return h->at<T>(h->p.ln1) + (h->s.rc >= 2 ? 0 : l) * MC(); }
+  T* ln2(int l) const { return h->at<T>(h->p.ln2) + (h->s.rc >= 2 ? 0 : l) * MC(); }
   T* qkv(int l) const { return h->at<T>(h->p.qkv) + l * 3 * MC(); }
   T* atty(int l) const { return h->at<T>(h->p.atty) + l * MC(); }
   T* fch(int l) const { return h->at<T>(h->p.fch) + l * 4 * MC(); }
-  T* fca(int l) const { return h->at<T>(h->p.fca) + l * 4 * MC(); }
+  T* fca(int l) const { return h->at<T>(h->p.fca) + (h->s.rc >= 1 ? 0 : l) * 4 * MC(); }
   float* stat(size_t region, int l) const { return h->at<float>(region) + (long long)l * h->s.M(); }
   float* att_lse(int l) const {
     return h->at<float>(h->p.att_lse) + (long long)l * h->s.B * h->s.H * h->s.T;
@@ -387,8 +393,9 @@ int forward_impl(gpt2* h) {
                             P.param(P_LN2W, l), P.param(P_LN2B, l), M, C, st));
     g = GemmArgs();
     g.A = P.ln2(l); g.lda = C; g.B = P.param(P_FCW, l); g.ldb = C;
-    g.M = M; g.N = 4 * C; g.K = C; g.epi = EPI_BIAS_GELU; g.D = P.fch(l); g.ldd = 4 * C;
-    g.D2 = P.fca(l); g.bias = P.param(P_FCB, l);
+    // fch keeps gelu'(h) for the backward, or h itself when the backward recomputes
+    g.M = M; g.N = 4 * C; g.K = C; g.epi = s.rc >= 1 ? EPI_BIAS_GELU_H : EPI_BIAS_GELU; g.D = P.fch(l);
+    g.ldd = 4 * C; g.D2 = P.fca(l); g.bias = P.param(P_FCB, l);
     CKI(linear<T>(h, g));
     g = GemmArgs();
     g.A = P.fca(l); g.lda = 4 * C; g.B = P.param(P_FCPW, l); g.ldb = 4 * C;
@@ -465,6 +472,8 @@ int backward_impl(gpt2* h) {
                           P.grad(P_LNFB), L > 0 ? P.grad(P_FCPB, L - 1) : nullptr, lnbp, M, C, 0,
                           st, h->at<unsigned>(h->p.status)));
   for (int l = L - 1; l >= 0; --l) {
+    if (s.rc >= 1)  // gelu(h) for the projection's weight gradient, from the h the forward kept
+      REGION(GPT2_K_RECOMPUTE, 0.0, 2.0 * 4.0 * MC * E, gelu_recompute<T>(P.fca(l), P.fch(l), (long long)4 * M * C, st));
     // MLP projection: x2 = x1 + fca Wfcp^T + b
     g = GemmArgs();
     g.A = dcur; g.lda = C; g.a_mn = 1; g.B = P.fca(l); g.ldb = 4 * C; g.b_mn = 1;
@@ -473,11 +482,16 @@ int backward_impl(gpt2* h) {
     // the fcproj bias gradient (column sum of dcur) came out of the previous LayerNorm backward
     g = GemmArgs();
     g.A = dcur; g.lda = C; g.B = P.param(P_FCPW, l); g.ldb = 4 * C; g.b_mn = 1;
-    g.M = M; g.N = 4 * C; g.K = C; g.epi = EPI_GELU_BWD; g.aux = P.fch(l); g.ldaux = 4 * C;
+    g.M = M; g.N = 4 * C; g.K = C; g.epi = s.rc >= 1 ? EPI_GELU_BWD_H : EPI_GELU_BWD; g.aux = P.fch(l);
+    g.ldaux = 4 * C;
     g.D = dbig; g.ldd = 4 * C;
     if (bf) g.colpart = csp;  // the fc bias gradient's partial column sums come out of this epilogue
     CKI(linear<T>(h, g));
     // MLP up-projection: h = ln2 Wfc^T + b
+    if (s.rc >= 2)
+      REGION(GPT2_K_RECOMPUTE, 0.0, 2.0 * MC * E + 8.0 * M,
+             layernorm_fwd<T>(P.ln2(l), h->at<float>(h->p.rc_stats), h->at<float>(h->p.rc_stats) + M, P.x1(l),
+                              P.param(P_LN2W, l), P.param(P_LN2B, l), M, C, st));
     g = GemmArgs();
     g.A = dbig; g.lda = 4 * C; g.a_mn = 1; g.B = P.ln2(l); g.ldb = C; g.b_mn = 1;
     g.M = 4 * C; g.N = C; g.K = M; g.D = P.grad(P_FCW, l); g.ldd = C;
@@ -520,6 +534,10 @@ int backward_impl(gpt2* h) {
     REGION(GPT2_K_ATTN_BWD, attn_flops, 8.0 * MC * E, e = (bf ? attn_bwd_bf16(a, st) : attn_bwd_f32(a, st)));
     CKI(e);
     // QKV: qkv = ln1 Wqkv^T + b
+    if (s.rc >= 2)
+      REGION(GPT2_K_RECOMPUTE, 0.0, 2.0 * MC * E + 8.0 * M,
+             layernorm_fwd<T>(P.ln1(l), h->at<float>(h->p.rc_stats), h->at<float>(h->p.rc_stats) + M, P.res(l),
+                              P.param(P_LN1W, l), P.param(P_LN1B, l), M, C, st));
     g = GemmArgs();
     g.A = dqkv; g.lda = 3 * C; g.a_mn = 1; g.B = P.ln1(l); g.ldb = C; g.b_mn = 1;
     g.M = 3 * C; g.N = C; g.K = M; g.D = P.grad(P_QKVW, l); g.ldd = C;
@@ -637,17 +655,26 @@ size_t gpt2_num_params(int L, int C, int Vpad, int T) {
   return (size_t)Vpad * C + (size_t)T * C + (size_t)L * (12 * (size_t)C * C + 13 * (size_t)C) + 2 * (size_t)C;
 }
 
-size_t gpt2_arena_bytes(int L, int H, int C, int V, int Vpad, int T, int B, int precision) {
-  Shape s{L, H, C, V, Vpad, T, B, precision};
+size_t gpt2_arena_bytes_r(int L, int H, int C, int V, int Vpad, int T, int B, int precision, int recompute) {
+  Shape s{L, H, C, V, Vpad, T, B, precision, recompute};
   if (validate(s) != GPT2_OK) return 0;
   return make_plan(s).total;
 }
 
+size_t gpt2_arena_bytes(int L, int H, int C, int V, int Vpad, int T, int B, int precision) {
+  return gpt2_arena_bytes_r(L, H, C, V, Vpad, T, B, precision, 0);
+}
+
 int gpt2_create(int L, int H, int C, int V, int Vpad, int T, int B, int precision, void* d_arena,
                 size_t arena_bytes, void* stream, gpt2_t** out) {
+  return gpt2_create_r(L, H, C, V, Vpad, T, B, precision, 0, d_arena, arena_bytes, stream, out);
+}
+
+int gpt2_create_r(int L, int H, int C, int V, int Vpad, int T, int B, int precision, int recompute, void* d_arena,
+                  size_t arena_bytes, void* stream, gpt2_t** out) {
   if (!out) return GPT2_E_INVAL;
   *out = nullptr;
-  Shape s{L, H, C, V, Vpad, T, B, precision};
+  Shape s{L, H, C, V, Vpad, T, B, precision, recompute};
   int v = validate(s);
   if (v != GPT2_OK) return v;
   if (!d_arena || (reinterpret_cast<uintptr_t>(d_arena) & 255)) return GPT2_E_INVAL;
@@ -691,7 +718,7 @@ int gpt2_profile(gpt2_t* h, int on) {
   if (!h) return GPT2_E_INVAL;
   if (on) {
     if (h->evpool.empty()) {
-      h->evpool.resize(8192);
+      h->evpool.resize(65536);  // two events per region: enough for several steps of the 48-layer model
       for (auto& e : h->evpool) CK(cudaEventCreate(&e));
     }
     h->recs.clear();
@@ -1197,7 +1224,7 @@ int gemm_bf16(const void* A, const void* B, void* D, int M, int N, int K, long l
   if (splits < 0) {
     if (!al16(workspace) || workspace_bytes < gemm_tc_sk_ws_bytes()) return GPT2_E_INVAL;
   } else {
-    if (splits == 0) splits = gemm_tc_pick_splits(M, N, K, num_sms());
+    if (splits == 0) splits = gemm_tc_pick_splits(M, N, K, gemm_tc_pairs());
     if (splits > 1 && workspace_bytes < gemm_tc_ws_bytes(M, N, splits)) return GPT2_E_INVAL;
   }
   int e = gemm_tc(g, splits, workspace, workspace_bytes, nullptr, static_cast<cudaStream_t>(stream));
@@ -1207,6 +1234,8 @@ int gemm_bf16(const void* A, const void* B, void* D, int M, int N, int K, long l
 }
 
 size_t gemm_bf16_sk_workspace_bytes(void) { return gemm_tc_sk_ws_bytes(); }
+
+int gemm_bf16_pairs(void) { return gemm_tc_pairs(); }
 
 int gemm_bf16_epilogue(const void* A, const void* B, void* D, void* D2, const void* bias, const void* X,
                        float* colpart, int M, int N, int K, long long lda, long long ldb, long long ldd,

@@ -49,6 +49,9 @@ enum EpiKind {
   EPI_GELU_BWD = 4,    // D = acc * aux[m, n]  (aux = the gelu'(h) the forward stored)
   EPI_CE = 5,          // D = z = acc; per (row, N tile) max / sum exp over n < V; target logit
   EPI_F32 = 6,         // D (float*) = acc
+  // activation recompute: the forward keeps only h, the backward derives gelu'(h) from it
+  EPI_BIAS_GELU_H = 7, // h = round(acc + bias[n]);  D = h, D2 = gelu(h)
+  EPI_GELU_BWD_H = 8,  // D = acc * gelu'(aux[m, n])  (aux = the h the forward stored)
 };
 
 struct GemmArgs {
@@ -63,7 +66,7 @@ struct GemmArgs {
   const void* aux = nullptr; long long ldaux = 0;
   float* ce_max = nullptr; float* ce_sum = nullptr; int ce_ld = 0;
   float* ce_tgt = nullptr; const int32_t* targets = nullptr; int V = 0;
-  // EPI_GELU_BWD, tcgen05 engine only: when set, colpart[(m / 32) * N + n] receives
+  // EPI_GELU_BWD / EPI_GELU_BWD_H, tcgen05 engine only: when set, colpart[(m / 32) * N + n] receives
   // the fp32 sum of D over rows m .. m + 31 (before rounding), ceil(M / 32) x N floats
   float* colpart = nullptr;
 };
@@ -95,7 +98,9 @@ size_t gemm_tc_sk_ws_bytes();
 // Splits the call above will actually use for this K (every split non-empty).
 int gemm_tc_effective_splits(int K, int splits);
 size_t gemm_tc_ws_bytes(int M, int N, int splits);
-int gemm_tc_pick_splits(int M, int N, int K, int num_sms);
+int gemm_tc_pick_splits(int M, int N, int K, int num_pairs);
+// CTA pairs the engine runs on (resident at once on the current device).
+int gemm_tc_pairs();
 // Columns covered by one EPI_CE statistics partial (row m's partial j covers
 // columns [j*cols, (j+1)*cols)).
 int gemm_tc_stat_cols();
@@ -154,6 +159,10 @@ void colsum(T* out, const T* x, int M, int N, long long ld, float* partials, cud
 template <typename T>
 void colsum_reduce(T* out, const float* partials, int nparts, int N, cudaStream_t s);
 size_t colsum_partials_floats(int N);
+// y = gelu(x) over n values with the arithmetic of the GEMM's bias + GELU epilogues
+// (bf16: the packed hardware-tanh form; fp32: gelu_f), so a recomputed activation
+// equals, bit for bit, the one the forward pass fed to the next GEMM.
+template <typename T> void gelu_recompute(T* y, const T* x, long long n, cudaStream_t s);
 template <typename T> void to_storage(T* dst, const float* src, long long n, cudaStream_t s);
 template <typename T> void to_f32(float* dst, const T* src, long long n, cudaStream_t s);
 

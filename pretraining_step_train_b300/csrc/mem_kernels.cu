@@ -8,6 +8,7 @@
 // reproducible run to run.
 #include "common.cuh"
 #include "internal.h"
+#include "tc_ptx.cuh"
 
 #include <math.h>
 
@@ -655,6 +656,40 @@ void colsum(T* out, const T* x, int M, int N, long long ld, float* partials, cud
 }
 
 // ------------------------------------------------------------------ elementwise
+// gelu recompute for activation recompute: bf16 pairs through the same packed
+// hardware-tanh arithmetic as the GEMM epilogue that produced them in the
+// forward pass; fp32 through gelu_f, as the fp32 GEMM epilogue.  16-byte vectors.
+template <typename T>
+__global__ void __launch_bounds__(256) k_gelu_recompute(T* __restrict__ y, const T* __restrict__ x, long long n) {
+  pdl_begin();
+  constexpr int N = V16<T>::N;
+  for (long long i = (blockIdx.x * (long long)blockDim.x + threadIdx.x) * N; i < n;
+       i += (long long)gridDim.x * blockDim.x * N) {
+    if constexpr (sizeof(T) == 2) {
+      const uint4 u = ldg_stream(x + i);
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        float2 g, dg;
+        gelu_and_grad2(make_float2(__uint_as_float(w[q] << 16), __uint_as_float(w[q] & 0xFFFF0000u)), g, dg);
+        __nv_bfloat162 t = __floats2bfloat162_rn(g.x, g.y);
+        o[q] = *reinterpret_cast<uint32_t*>(&t);
+      }
+      *reinterpret_cast<uint4*>(y + i) = make_uint4(o[0], o[1], o[2], o[3]);
+    } else {
+      float v[N];
+      load16(x + i, v);
+#pragma unroll
+      for (int e = 0; e < N; ++e) v[e] = gelu_f(v[e]);
+      store16(y + i, v);
+    }
+  }
+}
+template <typename T> void gelu_recompute(T* y, const T* x, long long n, cudaStream_t s) {
+  launch_k(k_gelu_recompute<T>, grid_for(n / V16<T>::N, 256, 148 * 8), 256, 0, s, y, x, n);
+}
+
 template <typename T>
 __global__ void k_to_storage(T* __restrict__ dst, const float* __restrict__ src, long long n) {
   pdl_begin();
@@ -1374,6 +1409,7 @@ void adamw(float* master, P* param_copy, const G* grad, float* m, float* v, long
                                  unsigned*);                                                        \
   template void colsum<T>(T*, const T*, int, int, long long, float*, cudaStream_t);                \
   template void colsum_reduce<T>(T*, const float*, int, int, cudaStream_t);                        \
+  template void gelu_recompute<T>(T*, const T*, long long, cudaStream_t);                          \
   template void to_storage<T>(T*, const float*, long long, cudaStream_t);                          \
   template void to_f32<T>(float*, const T*, long long, cudaStream_t);                              \
   template void ce_rowstats<T>(const T*, long long, const int32_t*, int, int, float*, float*,      \

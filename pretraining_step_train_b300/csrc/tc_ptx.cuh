@@ -33,6 +33,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Non-blocking probe of a barrier phase (no suspend), for threads that poll several barriers.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n.reg .pred p;\nmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, "
+      "p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 // Bounded wait: false when the CTA aborted or the limit expired (then latches ST_TIMEOUT).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                           unsigned* status) {
@@ -190,6 +201,84 @@ __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// ------------------------------------------------------------------ CTA pairs (cta_group::2)
+// A kernel launched in clusters of two CTAs may run its tensor-core work on the
+// pair: one thread of the even CTA issues each MMA, whose A operand comes half
+// from each CTA's shared memory (128 rows each), whose B operand comes half from
+// each (N/2 columns each), and whose accumulator lands in both CTAs' tensor
+// memory (128 rows each, all N columns).  Every tcgen05 instruction of such a
+// kernel uses .cta_group::2; the allocation is made collectively by one warp of
+// each CTA.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+// Whole-cluster barrier (all threads of both CTAs), release / acquire.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\ntcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, "
+      "%3, p;\n}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive once on the barrier at this shared offset in every CTA of `mask` when the
+// pair MMAs issued so far by this thread have completed.
+__device__ __forceinline__ void mma_commit_pair_mc(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"(mask)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+// Plain (CTA-scope release) arrive on a barrier of another CTA of the cluster.  It
+// orders nothing towards the other CTA's threads: use it where only tcgen05
+// completion must be ordered (tcgen05.wait + tcgen05.fence::before_thread_sync
+// first).  A cluster-scope release here cost about 1,000 cycles per arrive.
+__device__ __forceinline__ void mbar_remote_arrive(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+// TMA loads into this CTA's shared memory whose completion is signalled on a
+// barrier that may sit in the peer CTA of the pair (cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* tm, uint32_t cluster_bar, int x,
+                                                 int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2 [%0], [%1, "
+      "{%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(cluster_bar)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* tm, uint32_t cluster_bar, int c0,
+                                                 int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2 [%0], [%1, "
+      "{%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(cluster_bar)
+      : "memory");
+}
+
 // Packed fp32 pair arithmetic (Blackwell f32x2 FMA pipe: two lanes per instruction).
 __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
   float2 d;
@@ -214,6 +303,29 @@ __device__ __forceinline__ float2 add2(float2 a, float2 b) {
       : "=f"(d.x), "=f"(d.y)
       : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
   return d;
+}
+
+// Hardware tanh (MUFU, PTX tanh.approx.f32): relative error about 2^-11, far
+// below the bf16 rounding of the values it feeds.
+__device__ __forceinline__ float tanh_hw(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// tanh-form GELU with the hardware tanh (bf16 epilogues only).
+// gelu and gelu' of a pair of values sharing one hardware tanh each, in packed
+// fp32 pair arithmetic: y = x/2 (1 + th), dy = (1 + th)/2 + x/2 (1 - th^2) du with
+// th = tanh(x (k + k c x^2)), du = k + 3 k c x^2.
+__device__ __forceinline__ void gelu_and_grad2(float2 x, float2& y, float2& dy) {
+  const float2 x2 = mul2(x, x);
+  const float2 u = mul2(x, fma2(x2, make_float2(GELU_K * GELU_C, GELU_K * GELU_C), make_float2(GELU_K, GELU_K)));
+  const float2 th = make_float2(tanh_hw(u.x), tanh_hw(u.y));
+  const float2 hx = mul2(x, make_float2(0.5f, 0.5f));
+  y = fma2(hx, th, hx);
+  const float2 du = fma2(x2, make_float2(3.0f * GELU_K * GELU_C, 3.0f * GELU_K * GELU_C), make_float2(GELU_K, GELU_K));
+  const float2 om = fma2(th, make_float2(-th.x, -th.y), make_float2(1.0f, 1.0f));  // 1 - th^2
+  const float2 half_p = fma2(th, make_float2(0.5f, 0.5f), make_float2(0.5f, 0.5f));   // (1 + th) / 2
+  dy = fma2(mul2(hx, om), du, half_p);
 }
 
 }  // namespace gpt2k

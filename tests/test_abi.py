@@ -114,3 +114,19 @@ def test_gemm_and_step_extensions_validate_on_host(lib):
     assert epi(1, splits=-1) == binding.GPT2_E_INVAL  # stream-K without a workspace
     assert lib.gpt2_grad_accumulate(None, 1, 0.5) == binding.GPT2_E_INVAL
     assert lib.gpt2_clip_adamw_accumulated(None, 6e-4, 0.9, 0.95, 1e-8, 0.1, 1.0, 1, None) == binding.GPT2_E_INVAL
+
+
+def test_recompute_arena_savings(lib):
+    """Activation recompute: level 1 keeps one gelu(h) buffer instead of L, level 2
+    also keeps one LayerNorm output buffer instead of 2L; invalid levels are refused."""
+    for (L, H, C, V, Vpad, T, B, prec) in [(12, 12, 768, 50257, 50304, 1024, 16, binding.GPT2_BF16),
+                                           (4, 4, 64, 256, 256, 64, 4, binding.GPT2_FP32),
+                                           (48, 25, 1600, 50257, 50304, 1024, 16, binding.GPT2_BF16)]:
+        E = 2 if prec == binding.GPT2_BF16 else 4
+        M = B * T
+        r0, r1, r2 = (lib.gpt2_arena_bytes_r(L, H, C, V, Vpad, T, B, prec, r) for r in (0, 1, 2))
+        assert r0 == lib.gpt2_arena_bytes(L, H, C, V, Vpad, T, B, prec)
+        assert r0 - r1 == (L - 1) * M * 4 * C * E
+        assert r1 - r2 == (2 * L - 1) * M * C * E
+    assert lib.gpt2_arena_bytes_r(2, 2, 64, 256, 256, 64, 2, binding.GPT2_BF16, 3) == 0
+    assert lib.gpt2_arena_bytes_r(2, 2, 64, 256, 256, 64, 2, binding.GPT2_BF16, -1) == 0

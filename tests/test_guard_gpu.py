@@ -92,11 +92,11 @@ def test_nonfinite_step_leaves_weights_untouched():
 
 
 def test_spike_guard_skips_outlier_and_scores_match_the_window():
-    """Window of 4, norm threshold 3: the z-scores are NaN until four finite
-    values are held, then equal (x - mean) / std of the last four (population);
-    an outsized weight makes the norm jump, the update is skipped (weights and
-    moments keep their bits, the step counter stays), and with the checks off
-    the same step is applied."""
+    """Window of 4: the z-scores are NaN until four finite values are held, then
+    equal (x - mean) / std of the last four (population).  With thresholds of 3,
+    an outsized LayerNorm gain makes the loss and the norm jump: the update is
+    skipped (weights and moments keep their bits, the step counter stays), and
+    with the checks off the same step is applied."""
     W = 4
     flat, P = _params(63)
     s = binding.Step(L, H, C, V, Vpad, T, B, precision=binding.GPT2_BF16)
@@ -118,10 +118,16 @@ def test_spike_guard_skips_outlier_and_scores_match_the_window():
                 z = (xs[W] - hist.mean()) / hist.std()
                 assert abs(g[key] - z) <= 1e-3 * max(1.0, abs(z)), (key, g[key], z)
         assert g["skipped_spike"] == 0 and g["last_skipped"] == 0
-    # an outsized fc weight: the gradient norm jumps far outside the window
+    # the final LayerNorm's gain scaled by 50: the logits, the loss and the gradients jump
     spiky = flat.copy()
-    for j in range(16):
-        spiky[_weight_index("fcw", 0, j, j)] = 40.0
+    for c in range(C):
+        spiky[_weight_index("lnfw", c)] *= 50.0
+    s.set_guard(3.0, 3.0, W)  # both checks on; this empties the window, so refill it
+    for i in range(W):
+        s.forward(*_batch(150 + i))
+        s.backward()
+        assert _clip_adamw(s, lr=0.0)[0] == binding.GPT2_OK
+    assert s.guard_read()["skipped_spike"] == 0
     s.set_params(spiky)  # zeroes m, v and the step counter; the guard's window stays
     before = _snapshot(s)
     batch = _batch(200)
@@ -130,7 +136,7 @@ def test_spike_guard_skips_outlier_and_scores_match_the_window():
     st, n = _clip_adamw(s)
     assert st == binding.GPT2_OK
     g = s.guard_read()
-    assert g["z_norm"] > 3.0 and g["skipped_spike"] == 1 and g["last_skipped"] == 1, (n, norms, g)
+    assert max(g["z_loss"], g["z_norm"]) > 3.0 and g["skipped_spike"] == 1 and g["last_skipped"] == 1, (n, norms, g)
     _assert_same(before, _snapshot(s))
     # checks off (the window empties): the same step is applied, with t = 1 from the
     # counter that the skipped step left at 0; a second handle given t = 1 agrees bit for bit

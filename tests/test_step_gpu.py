@@ -56,11 +56,18 @@ def _compare(cfg, P, res, ref, loss_tol, grad_tol, w_tol, flat):
     assert rel_l2(res["master"], ref_flat) < w_tol
     W = synth.unflatten_params(res["master"], L, C, Vpad, T)
     for k in W:
+        g = np.abs(ref["grads"][k])
+        g_rms = np.sqrt(np.mean(g ** 2)) + 1e-30
+        w_rms = np.sqrt(np.mean(np.asarray(P[k], np.float64) ** 2))
         if k in ZERO_INIT:
-            g = np.abs(ref["grads"][k])
-            big = g > 100 * grad_tol * (np.sqrt(np.mean(g ** 2)) + 1e-30)
+            big = g > 100 * grad_tol * g_rms
             if big.any():
                 assert rel_l2(W[k][big], ref["params"][k][big]) < w_tol, k
+        elif LR > 0.1 * w_rms:
+            # the first update (about lr * sign(g)) is over a tenth of the weights: where |g|
+            # sits near the rounding level its sign, and so the update, is not determined
+            keep = g > 0.1 * g_rms
+            assert rel_l2(W[k][keep], ref["params"][k][keep]) < w_tol, k
         else:
             assert rel_l2(W[k], ref["params"][k]) < w_tol, k
     return worst
@@ -140,7 +147,7 @@ def _worker_params(shape, seed):
     return _WORKER_P[key]
 
 
-def _oracle_batch_step(shape, seed, tok, tgt, workers=8):
+def _oracle_batch_step(shape, seed, tok, tgt, workers=4):
     """The oracle's step on B sequences, evaluated one sequence at a time.
 
     The loss is the mean over all B*T positions and every sequence has T of
@@ -225,6 +232,41 @@ def test_step_parity_without_clipping(prec, tol):
     ref = O.train_step(P, tok, tgt, cfg, lr=LR, t=1, beta1=B1, beta2=B2, eps=EPS, wd=WD, max_norm=big)
     assert O.clip_scale(ref["norm"], big) == 1.0 and ref["norm"] > CLIP
     _compare(cfg, P, res, ref, *tol, flat)
+
+
+@pytest.mark.parametrize("rc", [1, 2])
+@pytest.mark.parametrize("prec", [binding.GPT2_BF16, binding.GPT2_FP32])
+def test_activation_recompute_step_parity(rc, prec):
+    """Recompute levels 1 (GELU) and 2 (GELU and LayerNorm outputs): the step
+    matches the oracle at the precision's tolerances, and matches the step that
+    keeps every activation (to fp32 rounding in fp32 mode, where the recomputed
+    values are the kept ones; within bf16 rounding in bf16 mode, where gelu and
+    gelu' come from the rounded h)."""
+    bf = prec == binding.GPT2_BF16
+    L, H, C, V, Vpad, T, B = (2, 2, 128, 1000, 1024, 128, 2) if bf else (2, 2, 64, 256, 256, 64, 2)
+    cfg = O.Config(L, H, C, V, Vpad, T)
+    P = synth.init_params(91 + rc, L, C, V, Vpad, T, bf16_representable=bf)
+    tok, tgt = synth.token_batch(92 + rc, B, T, V)
+    flat = synth.flatten_params(P, L, C, Vpad, T)
+    out = {}
+    for r in (0, rc):
+        s = binding.Step(L, H, C, V, Vpad, T, B, precision=prec, recompute=r)
+        s.set_params(flat)
+        loss = s.forward(to_dev(tok, "i32"), to_dev(tgt, "i32"))
+        s.backward()
+        grads = s.get(binding.GPT2_GRADS)
+        norm = s.clip_adamw(LR, B1, B2, EPS, WD, CLIP, 1)
+        out[r] = dict(loss=loss, grads=grads, norm=norm, master=s.get(binding.GPT2_MASTER))
+        s.close()
+    ref = O.train_step(P, tok, tgt, cfg, lr=LR, t=1, beta1=B1, beta2=B2, eps=EPS, wd=WD, max_norm=CLIP)
+    tol = (1e-2, 3e-2, 1e-2) if bf else (1e-4, 1e-4, 1e-4)
+    _compare(cfg, P, out[rc], ref, *tol, flat)
+    if bf:
+        assert abs(out[rc]["loss"] - out[0]["loss"]) < 1e-3 * abs(out[0]["loss"])
+        assert rel_l2(out[rc]["grads"], out[0]["grads"]) < 1e-2
+    else:
+        assert out[rc]["loss"] == out[0]["loss"]  # the forward pass computes the same values
+        assert rel_l2(out[rc]["grads"], out[0]["grads"]) < 1e-6
 
 
 def test_bf16_step_deterministic():
