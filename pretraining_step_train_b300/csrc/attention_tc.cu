@@ -438,13 +438,14 @@ __device__ __forceinline__ void bw_load(const CUtensorMap* tm, int swap, uint32_
 }
 
 // ------------------------------------------------------------------ dQ
-// smem: Q | dO | O (per item) | K,V ring (4 stages); TMEM: S | dP | dQ | dS double buffer.
+// smem: two sets of Q | dO | O (items alternate, so the next item's tiles load while this one
+// finishes) | K,V ring (4 stages); TMEM: S | dP | dQ | dS double buffer.
 // The compute warps also form D = rowsum(dO * O) for their query rows from the
 // dO and O tiles and store it for the dK/dV kernel, which runs after this one.
 constexpr int DQ_STAGES = 4;
-constexpr int DQ_Q = 0, DQ_DO = AT_TILE, DQ_O = 2 * AT_TILE, DQ_KV = 3 * AT_TILE;
+constexpr int DQ_Q = 0, DQ_DO = AT_TILE, DQ_O = 2 * AT_TILE, DQ_KV = 6 * AT_TILE;  // set s: + 3 s TILE
 constexpr int DQ_BAR = DQ_KV + 2 * DQ_STAGES * AT_TILE;
-constexpr int DQ_NBARS = 17;
+constexpr int DQ_NBARS = 19;
 constexpr int DQ_SMEM = 1024 + DQ_BAR + 8 * (DQ_NBARS + 2);
 
 __global__ void __launch_bounds__(BW_THREADS, 1)
@@ -455,9 +456,9 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + DQ_BAR);
-  // q_full, q_empty, kv_full[4], kv_empty[4], sdp_full, sdp_empty, ds_full[2], dq_done[2], done
-  // (ds_full / dq_done per dS buffer: tile parity)
-  const uint32_t b_qf = smem_u32(bars), b_qe = b_qf + 8, b_kvf = b_qe + 8, b_kve = b_kvf + 8 * DQ_STAGES;
+  // q_full[2], q_empty[2] (per Q/dO/O set), kv_full[4], kv_empty[4], sdp_full, sdp_empty, ds_full[2],
+  // dq_done[2], done (ds_full / dq_done per dS buffer: tile parity)
+  const uint32_t b_qf = smem_u32(bars), b_qe = b_qf + 16, b_kvf = b_qe + 16, b_kve = b_kvf + 8 * DQ_STAGES;
   const uint32_t b_sf = b_kve + 8 * DQ_STAGES, b_se = b_sf + 8, b_dsf = b_se + 8, b_dq = b_dsf + 16;
   const uint32_t b_done = b_dq + 16;
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bars + DQ_NBARS);
@@ -467,8 +468,10 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
   const int BH = a.B * a.H, nitems = p.nq * BH;
 
   if (threadIdx.x == 0) {
-    mbar_init(b_qf, 1);
-    mbar_init(b_qe, 9);  // the MMA thread's commit after the item's last S / dP + the 8 compute warps (D formed)
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(b_qf + 8 * i, 1);
+      mbar_init(b_qe + 8 * i, 9);  // the MMA thread's commit after the item's last S / dP + the 8 compute warps (D formed)
+    }
     for (int i = 0; i < DQ_STAGES; ++i) {
       mbar_init(b_kvf + 8 * i, 1);
       mbar_init(b_kve + 8 * i, 1);
@@ -497,16 +500,19 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      int last_par[DQ_STAGES] = {-1, -1, -1, -1}, q_par = -1, g = 0;
+      int last_par[DQ_STAGES] = {-1, -1, -1, -1}, q_par[2] = {-1, -1}, g = 0;
       bool ok = true;
       for (int w = blockIdx.x, it = 0; ok && w < nitems; w += gridDim.x, ++it) {
         const int qt = p.nq - 1 - w / BH, bh = w % BH, b = bh / a.H, h = bh % a.H;
-        if (it > 0 && !mbar_wait(b_qe, (uint32_t)(it - 1) & 1u, abort_flag, p.status)) break;
-        mbar_expect_tx(b_qf, 3 * AT_TILE);
-        bw_load(&tmQ, p.swap_q, sbase + DQ_Q, b_qf, qt * AT_B, h, b);
-        bw_load(&tmdO, p.swap_o, sbase + DQ_DO, b_qf, qt * AT_B, h, b);
-        bw_load(&tmO, p.swap_o, sbase + DQ_O, b_qf, qt * AT_B, h, b);
-        q_par = it & 1;
+        const int qs = it & 1;
+        const uint32_t qb = sbase + 3 * qs * AT_TILE;
+        // set qs was last read by item it - 2
+        if (it >= 2 && !mbar_wait(b_qe + 8 * qs, (uint32_t)((it - 2) >> 1) & 1u, abort_flag, p.status)) break;
+        mbar_expect_tx(b_qf + 8 * qs, 3 * AT_TILE);
+        bw_load(&tmQ, p.swap_q, qb + DQ_Q, b_qf + 8 * qs, qt * AT_B, h, b);
+        bw_load(&tmdO, p.swap_o, qb + DQ_DO, b_qf + 8 * qs, qt * AT_B, h, b);
+        bw_load(&tmO, p.swap_o, qb + DQ_O, b_qf + 8 * qs, qt * AT_B, h, b);
+        q_par[qs] = (it >> 1) & 1;
         for (int j = 0; j <= qt; ++j, ++g) {
           const int st = g % DQ_STAGES;
           const uint32_t ph = (uint32_t)(g / DQ_STAGES) & 1u;
@@ -519,7 +525,8 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
           last_par[st] = (int)ph;
         }
       }
-      if (q_par >= 0) mbar_wait_drain(b_qf, (uint32_t)q_par);
+      for (int i = 0; i < 2; ++i)
+        if (q_par[i] >= 0) mbar_wait_drain(b_qf + 8 * i, (uint32_t)q_par[i]);
       for (int i = 0; i < DQ_STAGES; ++i)
         if (last_par[i] >= 0) mbar_wait_drain(b_kvf + 8 * i, (uint32_t)last_par[i]);
     }
@@ -543,7 +550,9 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
       int g = 0;
       for (int w = blockIdx.x, it = 0; ok && w < nitems; w += gridDim.x, ++it) {
         const int nk = p.nq - w / BH;
-        if (!mbar_wait(b_qf, (uint32_t)it & 1u, abort_flag, p.status)) break;
+        const int qs = it & 1;
+        const uint32_t qb = sbase + 3 * qs * AT_TILE;
+        if (!mbar_wait(b_qf + 8 * qs, (uint32_t)(it >> 1) & 1u, abort_flag, p.status)) break;
         for (int j = 0; j < nk; ++j, ++g) {
           const int st = g % DQ_STAGES;
           if (!mbar_wait(b_kvf + 8 * st, (uint32_t)(g / DQ_STAGES) & 1u, abort_flag, p.status)) {
@@ -555,14 +564,13 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
           const uint32_t kd = sbase + DQ_KV + st * 2 * AT_TILE;
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_bf16(tmem + C_S, operand_desc(sbase + DQ_Q, 0, k), operand_desc(kd, 0, k), p.idesc_s,
-                     k > 0 ? 1u : 0u);
+            mma_bf16(tmem + C_S, operand_desc(qb + DQ_Q, 0, k), operand_desc(kd, 0, k), p.idesc_s, k > 0 ? 1u : 0u);
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_bf16(tmem + C_DP, operand_desc(sbase + DQ_DO, 0, k), operand_desc(kd + AT_TILE, 0, k),
-                     p.idesc_s, k > 0 ? 1u : 0u);
+            mma_bf16(tmem + C_DP, operand_desc(qb + DQ_DO, 0, k), operand_desc(kd + AT_TILE, 0, k), p.idesc_s,
+                     k > 0 ? 1u : 0u);
           mma_commit(b_sf);
-          if (j == nk - 1) mma_commit(b_qe);
+          if (j == nk - 1) mma_commit(b_qe + 8 * qs);
           if (j >= 1 && !issue_dq(g - 1, j == 1)) { ok = false; break; }
         }
         if (ok && !issue_dq(g - 1, nk == 1)) ok = false;
@@ -584,7 +592,9 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
       const float lse2 = valid ? a.lse[(long long)bh * a.T + qi] * 1.4426950408889634f : 0.f;
       // D = sum over d of dO[q, d] O[q, d] from the staged tiles (row r: 128 B, 16-byte
       // piece c at ((c ^ (r & 7)) << 4), the 128B swizzle), pieces in order
-      if (!warp_wait(b_qf, (uint32_t)it & 1u, abort_flag, p.status)) break;
+      const int qs = it & 1;
+      const uint32_t qb = sbase + 3 * qs * AT_TILE;
+      if (!warp_wait(b_qf + 8 * qs, (uint32_t)(it >> 1) & 1u, abort_flag, p.status)) break;
       float Dr = 0.f;
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
@@ -592,10 +602,10 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
         uint32_t x[4], y[4];
         asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                      : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3])
-                     : "r"(sbase + DQ_DO + off));
+                     : "r"(qb + DQ_DO + off));
         asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                      : "=r"(y[0]), "=r"(y[1]), "=r"(y[2]), "=r"(y[3])
-                     : "r"(sbase + DQ_O + off));
+                     : "r"(qb + DQ_O + off));
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           Dr = fmaf(__uint_as_float(x[e] << 16), __uint_as_float(y[e] << 16), Dr);
@@ -604,7 +614,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
       }
       if (!valid) Dr = 0.f;
       if (valid && half == 0) a.Dbuf[(long long)bh * a.T + qi] = Dr;
-      warp_arrive(b_qe);  // this warp is done with the item's dO and O tiles
+      warp_arrive(b_qe + 8 * qs);  // this warp is done with the item's dO and O tiles
       for (int j = 0; j < nk; ++j, ++g) {
         if (!warp_wait(b_sf, (uint32_t)g & 1u, abort_flag, p.status)) { ok = false; break; }
         tc_fence_after();
@@ -687,12 +697,13 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
 }
 
 // ------------------------------------------------------------------ dK, dV
-// smem: K | V (per item) | Q,dO ring (4 stages) | lse2, D ring (4 x 1 KB);
+// smem: two sets of K | V (items alternate, so the next item's K and V load while this
+// one finishes) | Q,dO ring (4 stages) | lse2, D ring (4 x 1 KB);
 // TMEM: S^T | dP^T | dV | dK | P^T | dS^T
 constexpr int DK_STAGES = 4;
-constexpr int DK_K = 0, DK_V = AT_TILE, DK_QD = 2 * AT_TILE, DK_LD = DK_QD + 2 * DK_STAGES * AT_TILE;
+constexpr int DK_K = 0, DK_V = AT_TILE, DK_QD = 4 * AT_TILE, DK_LD = DK_QD + 2 * DK_STAGES * AT_TILE;  // set s: K, V at + 2 s TILE
 constexpr int DK_BAR = DK_LD + DK_STAGES * 1024;
-constexpr int DK_NBARS = 17;
+constexpr int DK_NBARS = 19;
 constexpr int DK_SMEM = 1024 + DK_BAR + 8 * (DK_NBARS + 2);
 
 __global__ void __launch_bounds__(BW_THREADS, 1)
@@ -705,8 +716,9 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
   // stage s: for each query pair (2i, 2i+1) the float4 {-lse2[2i], -lse2[2i+1], -D[2i], -D[2i+1]}
   float* ldbuf = reinterpret_cast<float*>(smem + DK_LD);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + DK_BAR);
-  // kv_full, kv_empty, qd_full[4], qd_empty[4], sdp_full, sdp_empty, ds_full, mma_done, done
-  const uint32_t b_kvf = smem_u32(bars), b_kve = b_kvf + 8, b_qdf = b_kve + 8, b_qde = b_qdf + 8 * DK_STAGES;
+  // kv_full[2], kv_empty[2] (per K/V set), qd_full[4], qd_empty[4], sdp_full, sdp_empty, ds_full,
+  // mma_done, done
+  const uint32_t b_kvf = smem_u32(bars), b_kve = b_kvf + 16, b_qdf = b_kve + 16, b_qde = b_qdf + 8 * DK_STAGES;
   const uint32_t b_sf = b_qde + 8 * DK_STAGES, b_se = b_sf + 8, b_dsf = b_se + 8, b_mm = b_dsf + 8;
   const uint32_t b_done = b_mm + 8;
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bars + DK_NBARS);
@@ -717,8 +729,10 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
   // work item w: key tile w / BH (tile 0 has the most query tiles), (batch, head) = w % BH
 
   if (threadIdx.x == 0) {
-    mbar_init(b_kvf, 1);
-    mbar_init(b_kve, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(b_kvf + 8 * i, 1);
+      mbar_init(b_kve + 8 * i, 1);
+    }
     for (int i = 0; i < DK_STAGES; ++i) {
       mbar_init(b_qdf + 8 * i, 2);  // the TMA expect_tx arrive + the warp that staged lse2 / D
       mbar_init(b_qde + 8 * i, 1);
@@ -745,17 +759,31 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
 
   if (warp == 0) {
     // ---------------- producer warp: TMA by lane 0, lse2 / D staged by all lanes
-    int last_par[DK_STAGES] = {-1, -1, -1, -1}, kv_par = -1, g = 0;
+    // Each lane's four lse and D values for a query tile are loaded one tile ahead, so
+    // their global-memory latency overlaps the wait for the ring stage.
+    int last_par[DK_STAGES] = {-1, -1, -1, -1}, kv_par[2] = {-1, -1}, g = 0;
     bool ok = true;
+    float nl[4], nd[4];  // lse and D of the next query tile to stage (this lane's 4 queries)
+    auto fetch = [&](int bh, int i) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int q = i * AT_B + lane * 4 + e;
+        const bool v = q < a.T;
+        nl[e] = v ? a.lse[(long long)bh * a.T + q] : INFINITY;
+        nd[e] = v ? a.Dbuf[(long long)bh * a.T + q] : 0.f;
+      }
+    };
+    if (blockIdx.x < nitems) fetch(blockIdx.x % BH, blockIdx.x / BH);
     for (int w = blockIdx.x, it = 0; ok && w < nitems; w += gridDim.x, ++it) {
       const int kt = w / BH, bh = w % BH, b = bh / a.H, h = bh % a.H;
-      if (it > 0 && !warp_wait(b_kve, (uint32_t)(it - 1) & 1u, abort_flag, p.status)) break;
+      const int ks = it & 1;  // K/V set of this item
+      if (it >= 2 && !warp_wait(b_kve + 8 * ks, (uint32_t)((it - 2) >> 1) & 1u, abort_flag, p.status)) break;
       if (lane == 0) {
-        mbar_expect_tx(b_kvf, 2 * AT_TILE);
-        bw_load(&tmK, p.swap_q, sbase + DK_K, b_kvf, kt * AT_B, h, b);
-        bw_load(&tmV, p.swap_q, sbase + DK_V, b_kvf, kt * AT_B, h, b);
+        mbar_expect_tx(b_kvf + 8 * ks, 2 * AT_TILE);
+        bw_load(&tmK, p.swap_q, sbase + DK_K + 2 * ks * AT_TILE, b_kvf + 8 * ks, kt * AT_B, h, b);
+        bw_load(&tmV, p.swap_q, sbase + DK_V + 2 * ks * AT_TILE, b_kvf + 8 * ks, kt * AT_B, h, b);
       }
-      kv_par = it & 1;
+      kv_par[ks] = (it >> 1) & 1;
       for (int i = kt; i < p.nq; ++i, ++g) {
         const int st = g % DK_STAGES;
         const uint32_t ph = (uint32_t)(g / DK_STAGES) & 1u;
@@ -769,18 +797,21 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
         float* lb = ldbuf + st * 256;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int c = lane * 4 + e, q = i * AT_B + c;
-          const bool v = q < a.T;
+          const int c = lane * 4 + e;
           const int slot = (c >> 1) * 4 + (c & 1);
-          lb[slot] = v ? -a.lse[(long long)bh * a.T + q] * 1.4426950408889634f : -INFINITY;
-          lb[slot + 2] = v ? -a.Dbuf[(long long)bh * a.T + q] : 0.f;
+          lb[slot] = -nl[e] * 1.4426950408889634f;  // rows past T: -inf, so P = 0 there
+          lb[slot + 2] = -nd[e];
         }
         warp_arrive(b_qdf + 8 * st);
         if (!((p.poison & POISON_ATTN_DKDV) && g == 0)) last_par[st] = (int)ph;
+        // the next tile's values: this item's next query tile, or the next item's first
+        if (i + 1 < p.nq) fetch(bh, i + 1);
+        else if (w + (int)gridDim.x < nitems) fetch((w + gridDim.x) % BH, (w + gridDim.x) / BH);
       }
     }
     if (lane == 0) {
-      if (kv_par >= 0) mbar_wait_drain(b_kvf, (uint32_t)kv_par);
+      for (int i = 0; i < 2; ++i)
+        if (kv_par[i] >= 0) mbar_wait_drain(b_kvf + 8 * i, (uint32_t)kv_par[i]);
       for (int i = 0; i < DK_STAGES; ++i)
         if (last_par[i] >= 0) mbar_wait_drain(b_qdf + 8 * i, (uint32_t)last_par[i]);
     }
@@ -807,7 +838,9 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
       int g = 0;
       for (int w = blockIdx.x, it = 0; ok && w < nitems; w += gridDim.x, ++it) {
         const int n = p.nq - w / BH;  // query tiles kt .. nq-1
-        if (!mbar_wait(b_kvf, (uint32_t)it & 1u, abort_flag, p.status)) break;
+        const int ks = it & 1;
+        const uint32_t kd = sbase + DK_K + 2 * ks * AT_TILE, vd = sbase + DK_V + 2 * ks * AT_TILE;
+        if (!mbar_wait(b_kvf + 8 * ks, (uint32_t)(it >> 1) & 1u, abort_flag, p.status)) break;
         for (int j = 0; j < n; ++j, ++g) {
           const int st = g % DK_STAGES;
           if (!mbar_wait(b_qdf + 8 * st, (uint32_t)(g / DK_STAGES) & 1u, abort_flag, p.status)) {
@@ -819,17 +852,16 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
           const uint32_t qd = sbase + DK_QD + st * 2 * AT_TILE;
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_bf16(tmem + C_S, operand_desc(sbase + DK_K, 0, k), operand_desc(qd, 0, k), p.idesc_s,
-                     k > 0 ? 1u : 0u);
+            mma_bf16(tmem + C_S, operand_desc(kd, 0, k), operand_desc(qd, 0, k), p.idesc_s, k > 0 ? 1u : 0u);
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_bf16(tmem + C_DP, operand_desc(sbase + DK_V, 0, k), operand_desc(qd + AT_TILE, 0, k),
-                     p.idesc_s, k > 0 ? 1u : 0u);
+            mma_bf16(tmem + C_DP, operand_desc(vd, 0, k), operand_desc(qd + AT_TILE, 0, k), p.idesc_s,
+                     k > 0 ? 1u : 0u);
           mma_commit(b_sf);
           if (j >= 1 && !issue_kv(g - 1, j == 1)) { ok = false; break; }
         }
         if (ok && !issue_kv(g - 1, n == 1)) ok = false;
-        if (ok) mma_commit(b_kve);  // K, V of this item are no longer read
+        if (ok) mma_commit(b_kve + 8 * ks);  // this item's K, V set is no longer read
       }
       mma_commit(b_done);
       mbar_wait_drain(b_done, 0);

@@ -500,6 +500,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int xb = nxb, y0 = ny;
       nok = cta_unit(p, u + 1, nw);
       warp_origin(nok, nw, nxb, ny);
+      // this warp's 64 bias values, two per lane, loaded before the accumulator wait so
+      // their latency is hidden; each chunk gathers its 16 with shuffles
+      uint32_t bias2 = 0;
+      if (has_bias && w.role != U_PART && xb + 2 * lane + 1 < g.N)
+        bias2 = __ldg(reinterpret_cast<const unsigned int*>(static_cast<const bf16*>(g.bias) + xb) + lane);
       if (!mbar_wait(b_tfull + 8 * abuf, aphase, abort_flag, p.status)) break;
       tc_fence_after();
       const uint32_t tacc = tmem_base + ((uint32_t)(quad * 32) << 16) + abuf * BN + qq * WCOLS;
@@ -638,19 +643,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
           }
         }
-        if (has_bias) {
-          const bf16* bias = static_cast<const bf16*>(g.bias);
+        if (has_bias) {  // columns x0 + 2i, x0 + 2i + 1 sit in lane c * 8 + i (zero past N)
 #pragma unroll
-          for (int q = 0; q < 2; ++q) {
-            if (x0 + q * 8 < g.N) {
-              float bb[8];
-              load16<bf16>(bias + x0 + q * 8, bb);
-#pragma unroll
-              for (int i = 0; i < 8; i += 2) {
-                const float2 t = add2(make_float2(v[q * 8 + i], v[q * 8 + i + 1]), make_float2(bb[i], bb[i + 1]));
-                v[q * 8 + i] = t.x; v[q * 8 + i + 1] = t.y;
-              }
-            }
+          for (int i = 0; i < 8; ++i) {
+            const uint32_t bb = __shfl_sync(0xffffffffu, bias2, c * 8 + i);
+            const float2 t = add2(make_float2(v[2 * i], v[2 * i + 1]),
+                                  make_float2(__uint_as_float(bb << 16), __uint_as_float(bb & 0xFFFF0000u)));
+            v[2 * i] = t.x; v[2 * i + 1] = t.y;
           }
         }
         if (epi == EPI_CE) {
@@ -774,8 +773,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       if (++abuf == 2) { abuf = 0; aphase ^= 1; }
     }
-    // never leave with bulk copies still reading or filling this warp's boxes
-    if (lane == 0) bulk_wait_all();
+    // never leave with bulk copies still reading or filling this warp's boxes (the stores'
+    // global writes complete with the kernel; only the reads of shared memory must be done)
+    if (lane == 0) bulk_wait_read<0>();
     for (int b = 0; b < 2; ++b)
       if (xpend & (1u << b)) mbar_wait_drain(xbar + 8 * b, (xpar >> b) & 1u);
     __syncwarp();

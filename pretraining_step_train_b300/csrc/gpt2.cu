@@ -137,7 +137,7 @@ struct Plan {
   int ce_tiles = 0;
 };
 
-constexpr int kNormParts = 1024;
+constexpr int kNormParts = 592;  // one wave of 512-thread blocks on 148 SMs (4 per SM)
 
 size_t take(size_t& cur, size_t bytes) {
   size_t o = cur;

@@ -72,10 +72,10 @@ void check_ids(int32_t* ids, int n, int V, unsigned* status, cudaStream_t s) {
 }
 
 // ------------------------------------------------------------------ LayerNorm forward
-// One warp per row; the row stays in registers in its storage format (16-byte
-// vectors: packed bf16 or fp32) and is unpacked on each of the three passes
-// (mean, biased variance, output), so a warp holds few registers and many warps
-// keep row loads in flight.
+// Each warp normalises two rows; both rows are loaded up front and stay in
+// registers in their storage format (16-byte vectors: packed bf16 or fp32),
+// unpacked on each of the three passes (mean, biased variance, output), so a
+// lane keeps 2 * MAXV loads in flight and a launch fits in about one wave.
 template <typename T>
 __device__ __forceinline__ void unpack16(const uint4& u, float* out) {
   if constexpr (sizeof(T) == 4) {
@@ -91,6 +91,8 @@ __device__ __forceinline__ void unpack16(const uint4& u, float* out) {
   }
 }
 
+constexpr int kLnfRows = 2;  // rows per warp
+
 template <typename T, int MAXV>
 __global__ void __launch_bounds__(256) k_layernorm_fwd(T* __restrict__ y, float* __restrict__ mean,
                                                        float* __restrict__ rstd, const T* __restrict__ x,
@@ -98,61 +100,69 @@ __global__ void __launch_bounds__(256) k_layernorm_fwd(T* __restrict__ y, float*
                                                        int M, int C) {
   pdl_begin();
   constexpr int N = V16<T>::N;
-  const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int row0 = ((blockIdx.x * blockDim.x + threadIdx.x) >> 5) * kLnfRows;
   const int lane = threadIdx.x & 31;
-  if (row >= M) return;
+  if (row0 >= M) return;
   const int nv = C / N;
-  const T* xr = x + (long long)row * C;
-  uint4 raw[MAXV];
+  uint4 raw[kLnfRows][MAXV];
 #pragma unroll
-  for (int j = 0; j < MAXV; ++j) {
-    const int vi = lane + j * 32;
-    if (vi < nv) raw[j] = *reinterpret_cast<const uint4*>(xr + vi * N);
-  }
-  float s = 0.f;
+  for (int rr = 0; rr < kLnfRows; ++rr) {
+    const T* xr = x + (long long)(row0 + rr) * C;
 #pragma unroll
-  for (int j = 0; j < MAXV; ++j) {
-    if (lane + j * 32 < nv) {
-      float v[N];
-      unpack16<T>(raw[j], v);
-#pragma unroll
-      for (int e = 0; e < N; ++e) s += v[e];
+    for (int j = 0; j < MAXV; ++j) {
+      const int vi = lane + j * 32;
+      if (row0 + rr < M && vi < nv) raw[rr][j] = *reinterpret_cast<const uint4*>(xr + vi * N);
     }
   }
-  s = warp_sum(s);
-  const float mu = s / (float)C;
-  float ss = 0.f;
 #pragma unroll
-  for (int j = 0; j < MAXV; ++j) {
-    if (lane + j * 32 < nv) {
-      float v[N];
-      unpack16<T>(raw[j], v);
+  for (int rr = 0; rr < kLnfRows; ++rr) {
+    const int row = row0 + rr;
+    if (row >= M) break;
+    float s = 0.f;
 #pragma unroll
-      for (int e = 0; e < N; ++e) {
-        const float d = v[e] - mu;
-        ss += d * d;
+    for (int j = 0; j < MAXV; ++j) {
+      if (lane + j * 32 < nv) {
+        float v[N];
+        unpack16<T>(raw[rr][j], v);
+#pragma unroll
+        for (int e = 0; e < N; ++e) s += v[e];
       }
     }
-  }
-  ss = warp_sum(ss);
-  const float rs = 1.0f / sqrtf(ss / (float)C + 1e-5f);
-  T* yr = y + (long long)row * C;
+    s = warp_sum(s);
+    const float mu = s / (float)C;
+    float ss = 0.f;
 #pragma unroll
-  for (int j = 0; j < MAXV; ++j) {
-    const int vi = lane + j * 32;
-    if (vi < nv) {
-      float v[N], wv[N], bv[N], o[N];
-      unpack16<T>(raw[j], v);
-      load16(w + vi * N, wv);
-      load16(b + vi * N, bv);
+    for (int j = 0; j < MAXV; ++j) {
+      if (lane + j * 32 < nv) {
+        float v[N];
+        unpack16<T>(raw[rr][j], v);
 #pragma unroll
-      for (int e = 0; e < N; ++e) o[e] = (v[e] - mu) * rs * wv[e] + bv[e];
-      store16(yr + vi * N, o);
+        for (int e = 0; e < N; ++e) {
+          const float d = v[e] - mu;
+          ss += d * d;
+        }
+      }
     }
-  }
-  if (lane == 0) {
-    mean[row] = mu;
-    rstd[row] = rs;
+    ss = warp_sum(ss);
+    const float rs = 1.0f / sqrtf(ss / (float)C + 1e-5f);
+    T* yr = y + (long long)row * C;
+#pragma unroll
+    for (int j = 0; j < MAXV; ++j) {
+      const int vi = lane + j * 32;
+      if (vi < nv) {
+        float v[N], wv[N], bv[N], o[N];
+        unpack16<T>(raw[rr][j], v);
+        load16(w + vi * N, wv);
+        load16(b + vi * N, bv);
+#pragma unroll
+        for (int e = 0; e < N; ++e) o[e] = (v[e] - mu) * rs * wv[e] + bv[e];
+        store16(yr + vi * N, o);
+      }
+    }
+    if (lane == 0) {
+      mean[row] = mu;
+      rstd[row] = rs;
+    }
   }
 }
 
@@ -162,7 +172,8 @@ void layernorm_fwd(T* y, float* mean, float* rstd, const T* x, const T* w, const
   const int nv = C / V16<T>::N;
   const int per = (nv + 31) / 32;
   const int block = 256;
-  const int grid = (M * 32 + block - 1) / block;
+  const long long warps = (M + kLnfRows - 1) / kLnfRows;
+  const int grid = (int)((warps * 32 + block - 1) / block);
   if (per <= 1) launch_k(k_layernorm_fwd<T, 1>, grid, block, 0, s, y, mean, rstd, x, w, b, M, C);
   else if (per <= 2) launch_k(k_layernorm_fwd<T, 2>, grid, block, 0, s, y, mean, rstd, x, w, b, M, C);
   else if (per <= 3) launch_k(k_layernorm_fwd<T, 3>, grid, block, 0, s, y, mean, rstd, x, w, b, M, C);
@@ -1166,6 +1177,8 @@ void splitk_reduce(void* out, int out_f32, long long ldo, const float* ws, int s
 }
 
 // ------------------------------------------------------------------ global norm + AdamW
+// Sum of squares of n gradient values in nparts fixed slices (one partial per
+// block, fixed order).  Each thread keeps four 16-byte loads in flight.
 template <typename G>
 __global__ void __launch_bounds__(512)
     k_sumsq(float* __restrict__ partials, const G* __restrict__ g, long long n, long long chunk) {
@@ -1174,15 +1187,26 @@ __global__ void __launch_bounds__(512)
   __shared__ float sh[32];
   const long long b0 = blockIdx.x * chunk;
   const long long b1 = min(n, b0 + chunk);
-  float s = 0.f;
-  for (long long i = b0 + (long long)threadIdx.x * N; i < b1; i += (long long)blockDim.x * N) {
+  const long long step = (long long)blockDim.x * N;
+  float s[4] = {0.f, 0.f, 0.f, 0.f};
+  long long i = b0 + (long long)threadIdx.x * N;
+  for (; i + 3 * step < b1; i += 4 * step) {
+    float v[4][N];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) load16(g + i + u * step, v[u]);
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int e = 0; e < N; ++e) s[u] = fmaf(v[u][e], v[u][e], s[u]);
+  }
+  for (; i < b1; i += step) {
     float v[N];
     load16(g + i, v);
 #pragma unroll
-    for (int e = 0; e < N; ++e) s += v[e] * v[e];
+    for (int e = 0; e < N; ++e) s[0] = fmaf(v[e], v[e], s[0]);
   }
-  s = block_reduce(s, sh, false);
-  if (threadIdx.x == 0) partials[blockIdx.x] = s;
+  const float t = block_reduce((s[0] + s[1]) + (s[2] + s[3]), sh, false);
+  if (threadIdx.x == 0) partials[blockIdx.x] = t;
 }
 template <typename G>
 void grad_sumsq_partials(float* partials, int nparts, const G* g, long long n, cudaStream_t s) {
