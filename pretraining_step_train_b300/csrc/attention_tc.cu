@@ -10,13 +10,14 @@
 //               the strided q / k / v views, 128B swizzle; rows past T are zeros);
 //   warp 1      owns 512 TMEM columns: per query tile t an S buffer (128 fp32
 //               columns), the O accumulator (64) and a P buffer (64 columns of
-//               bf16 pairs); one thread issues S_t = Q_t K_j^T (M=128, N=128,
-//               K=64) and O_t += P_t V_j (M=128, N=64, K=128, A from TMEM), in
-//               the order S_0(j), S_1(j), PV_0(j-1), PV_1(j-1), ..., so the tensor
+//               bf16 pairs);
+//   warps 1, 2  one MMA issuer per query tile t: S_t = Q_t K_j^T (M=128, N=128,
+//               K=64) and O_t += P_t V_j (M=128, N=64, K=128, A from TMEM), each
+//               issued the moment its own tile's inputs are ready, so the tensor
 //               core works on one tile while the softmax warps work on the other;
-//   warps 2-5   softmax of query tile 0, warps 6-9 of tile 1: each thread owns
-//               one query row (lane quadrant = warp % 4) and all 128 keys of a
-//               tile, so the row max and sum stay in the thread; p =
+//   warps 4-7   softmax of query tile 0, warps 8-11 of tile 1 (warp 3 idles): each
+//               thread owns one query row (lane quadrant = warp % 4) and all 128
+//               keys of a tile, so the row max and sum stay in the thread; p =
 //               2^(s*scale*log2e - m) (ex2.approx: 32 per cycle per SM, so the
 //               32K exponentials of a key tile take fewer cycles than its MMAs);
 //               O is rescaled in TMEM only when the running max has to move by
@@ -35,7 +36,7 @@ namespace {
 constexpr int AT_B = 128;                       // queries per tile = keys per tile
 constexpr int AT_D = 64;                        // head size
 constexpr int AT_TILE = AT_B * AT_D * 2;        // 16 KB: one [128 x 64] bf16 tile
-constexpr int AT_THREADS = 320;
+constexpr int AT_THREADS = 384;
 constexpr int AT_TMEM_COLS = 512;
 // forward: smem two sets of (Q_0 | Q_1) | K,V ring; TMEM S_t at 128 t, O_t at 256 + 64 t,
 // P_t at 384 + 64 t
@@ -45,6 +46,9 @@ constexpr int FW_BAR = FW_KV + 2 * FW_STAGES * AT_TILE;
 constexpr int FW_NBARS = 4 + 2 * FW_STAGES + 8 + 1;
 constexpr int AT_SMEM = 1024 + FW_BAR + 8 * (FW_NBARS + 2);
 constexpr uint32_t FW_S_COL = 0, FW_O_COL = 256, FW_P_COL = 384;
+constexpr int FW_REGS_LAUNCH = 168, FW_REGS_CTRL = 56, FW_REGS_SOFTMAX = 216;
+static_assert(128 * FW_REGS_CTRL + 256 * FW_REGS_SOFTMAX <= AT_THREADS * FW_REGS_LAUNCH,
+              "the register split must fit in the launch's registers");
 
 struct AtParams {
   AttnArgs a;
@@ -122,11 +126,11 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int q = 0; q < 2; ++q) {
       mbar_init(b_qf + 8 * q, 1);
-      mbar_init(b_qe + 8 * q, 1);
+      mbar_init(b_qe + 8 * q, 2);  // one commit per query tile's issuer
     }
     for (int i = 0; i < FW_STAGES; ++i) {
       mbar_init(b_kvf + 8 * i, 1);
-      mbar_init(b_kve + 8 * i, 1);
+      mbar_init(b_kve + 8 * i, 2);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(b_sf + 8 * t, 1);
@@ -134,7 +138,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       mbar_init(b_pf + 8 * t, 4);
       mbar_init(b_pv + 8 * t, 1);
     }
-    mbar_init(b_done, 1);
+    mbar_init(b_done, 2);  // one commit per issuer
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -148,138 +152,126 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-
-  if (warp == 0) {
-    if (lane == 0) {
-      // ---------------- TMA producer
-      int last_par[FW_STAGES] = {-1, -1, -1, -1}, q_par[2] = {-1, -1};
-      int g = 0;  // K/V tiles issued so far (ring position)
-      bool ok = true;
-      for (int w = blockIdx.x, it = 0; ok && w < nitems; w += gridDim.x, ++it) {
-        const int qp = p.nqp - 1 - w / BH, bh = w % BH, b = bh / a.H, h = bh % a.H;
-        const bool has1 = 2 * qp + 1 < p.nq;
-        const int nk = 2 * qp + (has1 ? 2 : 1);
-        auto load = [&](const CUtensorMap* tm, uint32_t dst, uint32_t bar, int t0) {
-          if (p.swap_ht) tma_load_4d(dst, tm, bar, 0, h, t0, b);
-          else tma_load_4d(dst, tm, bar, 0, t0, h, b);
-        };
-        // Q set it % 2 was last read by the S MMAs of item it - 2
-        const int qs = it & 1;
-        if (it >= 2 && !mbar_wait(b_qe + 8 * qs, (uint32_t)((it - 2) >> 1) & 1u, abort_flag, p.status)) break;
-        mbar_expect_tx(b_qf + 8 * qs, (has1 ? 2 : 1) * AT_TILE);
-        load(&tmQ, sbase + FW_Q + 2 * qs * AT_TILE, b_qf + 8 * qs, 2 * qp * AT_B);
-        if (has1) load(&tmQ, sbase + FW_Q + (2 * qs + 1) * AT_TILE, b_qf + 8 * qs, (2 * qp + 1) * AT_B);
-        q_par[qs] = (it >> 1) & 1;
-        for (int j = 0; j < nk; ++j, ++g) {
-          const int st = g % FW_STAGES;
-          const uint32_t ph = (uint32_t)(g / FW_STAGES) & 1u;
-          if (!mbar_wait(b_kve + 8 * st, ph ^ 1u, abort_flag, p.status)) { ok = false; break; }
-          if ((p.poison & POISON_ATTN_FWD) && g == 0) continue;
-          const uint32_t kd = sbase + FW_KV + st * 2 * AT_TILE;
-          mbar_expect_tx(b_kvf + 8 * st, 2 * AT_TILE);
-          load(&tmK, kd, b_kvf + 8 * st, j * AT_B);
-          load(&tmV, kd + AT_TILE, b_kvf + 8 * st, j * AT_B);
-          last_par[st] = (int)ph;
-        }
-      }
-      // never leave with copies still landing in shared memory
-      for (int q = 0; q < 2; ++q)
-        if (q_par[q] >= 0) mbar_wait_drain(b_qf + 8 * q, (uint32_t)q_par[q]);
-      for (int i = 0; i < FW_STAGES; ++i)
-        if (last_par[i] >= 0) mbar_wait_drain(b_kvf + 8 * i, (uint32_t)last_par[i]);
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- MMA issuer
-      // It issues whichever product is ready, so each softmax group starts its next tile as
-      // soon as it finishes one and the two groups drift half a period apart (a fixed order
-      // kept them in step, contending for the exponential unit, each waiting on the other):
-      //   S_t(j)  once K_j has landed and group t has read S_t(j-1) out of TMEM;
-      //   PV_t(j) once group t has written P_t(j);
-      // K_j / V_j's ring stage is released once both tiles' PV(j) are issued.
-      int cnt_s[2] = {0, 0}, cnt_pv[2] = {0, 0};  // S and PV MMAs issued per query tile, all items
-      bool ok = true;
-      int g = 0;  // ring position of the item's key tile 0
-      for (int w = blockIdx.x, it = 0; ok && w < nitems; w += gridDim.x, ++it) {
-        const int qp = p.nqp - 1 - w / BH;
-        const int qt0 = 2 * qp;
-        const bool has1 = qt0 + 1 < p.nq;
-        const int nk = qt0 + (has1 ? 2 : 1);
-        const int nkt[2] = {qt0 + 1, has1 ? qt0 + 2 : 0};  // key tiles per query tile
-        const int qs = it & 1;
-        if (!mbar_wait(b_qf + 8 * qs, (uint32_t)(it >> 1) & 1u, abort_flag, p.status)) break;
-        int ns[2] = {0, 0}, np[2] = {0, 0}, rel = 0;  // this item: S issued, PV issued, stages released
-        bool q_released = false;
-        unsigned long long t_idle = 0;
-        while (ok && (np[0] < nkt[0] || np[1] < nkt[1] || rel < nk)) {
-          bool progress = false;
-          for (int t = 0; t < 2; ++t) {
-            const int j = ns[t];
-            if (j < nkt[t] && ns[t] <= np[t] + 1) {  // at most one S ahead of its PV (one P buffer)
-              const int st = (g + j) % FW_STAGES;
-              if (mbar_test(b_kvf + 8 * st, (uint32_t)((g + j) / FW_STAGES) & 1u) &&
-                  (cnt_s[t] == 0 || mbar_test(b_se + 8 * t, (uint32_t)(cnt_s[t] - 1) & 1u))) {
-                tc_fence_after();
-                const uint32_t kd = sbase + FW_KV + st * 2 * AT_TILE;
-                const uint32_t qd = sbase + FW_Q + (2 * qs + t) * AT_TILE;
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                  mma_bf16(tmem + FW_S_COL + 128 * t, operand_desc(qd, 0, k), operand_desc(kd, 0, k), p.idesc_s,
-                           k > 0 ? 1u : 0u);
-                mma_commit(b_sf + 8 * t);
-                ++ns[t];
-                ++cnt_s[t];
-                progress = true;
-              }
-            }
-            if (np[t] < ns[t] && mbar_test(b_pf + 8 * t, (uint32_t)cnt_pv[t] & 1u)) {
-              tc_fence_after();
-              const int jp = np[t];
-              const uint32_t vd = sbase + FW_KV + ((g + jp) % FW_STAGES) * 2 * AT_TILE + AT_TILE;
-              // A = P_t in TMEM: 16 keys per MMA = 8 columns of bf16 pairs
-#pragma unroll
-              for (int kk = 0; kk < 8; ++kk)
-                mma_bf16_tmem_a(tmem + FW_O_COL + 64 * t, tmem + FW_P_COL + 64 * t + kk * 8,
-                                operand_desc(vd, 1, kk), p.idesc_pv, (jp > 0 || kk > 0) ? 1u : 0u);
-              mma_commit(b_pv + 8 * t);
-              ++np[t];
-              ++cnt_pv[t];
-              progress = true;
-            }
-          }
-          if (!q_released && ns[0] == nkt[0] && ns[1] == nkt[1]) {
-            mma_commit(b_qe + 8 * qs);  // this Q set is free once the item's S MMAs are done
-            q_released = true;
-          }
-          // K_j / V_j are no longer read once every tile that uses key tile j has issued PV(j)
-          while (rel < nk && (rel >= nkt[0] || np[0] > rel) && (rel >= nkt[1] || np[1] > rel)) {
-            mma_commit(b_kve + 8 * ((g + rel) % FW_STAGES));
-            ++rel;
-            progress = true;
-          }
-          if (progress) {
-            t_idle = 0;
-          } else {
-            if (*abort_flag) { ok = false; break; }
-            const unsigned long long now = globaltimer_ns();
-            if (t_idle == 0) {
-              t_idle = now;
-            } else if (now - t_idle > WAIT_LIMIT_NS) {
-              if (p.status) atomicOr(p.status, ST_TIMEOUT);
-              *abort_flag = 1;
-              ok = false;
-            }
+  // registers: 384 threads x 168 at launch = 64512; warps 0-3 keep 56, the softmax
+  // warpgroups take 216 (128 x 56 + 256 x 216 = 62464)
+  if (warp < 4) {
+    regs_lower<FW_REGS_CTRL>();
+    if (warp == 0) {
+      if (lane == 0) {
+        // ---------------- TMA producer
+        int last_par[FW_STAGES] = {-1, -1, -1, -1}, q_par[2] = {-1, -1};
+        int g = 0;  // K/V tiles issued so far (ring position)
+        bool ok = true;
+        for (int w = blockIdx.x, it = 0; ok && w < nitems; w += gridDim.x, ++it) {
+          const int qp = p.nqp - 1 - w / BH, bh = w % BH, b = bh / a.H, h = bh % a.H;
+          const bool has1 = 2 * qp + 1 < p.nq;
+          const int nk = 2 * qp + (has1 ? 2 : 1);
+          auto load = [&](const CUtensorMap* tm, uint32_t dst, uint32_t bar, int t0) {
+            if (p.swap_ht) tma_load_4d(dst, tm, bar, 0, h, t0, b);
+            else tma_load_4d(dst, tm, bar, 0, t0, h, b);
+          };
+          // Q set it % 2 was last read by the S MMAs of item it - 2
+          const int qs = it & 1;
+          if (it >= 2 && !mbar_wait(b_qe + 8 * qs, (uint32_t)((it - 2) >> 1) & 1u, abort_flag, p.status)) break;
+          mbar_expect_tx(b_qf + 8 * qs, (has1 ? 2 : 1) * AT_TILE);
+          load(&tmQ, sbase + FW_Q + 2 * qs * AT_TILE, b_qf + 8 * qs, 2 * qp * AT_B);
+          if (has1) load(&tmQ, sbase + FW_Q + (2 * qs + 1) * AT_TILE, b_qf + 8 * qs, (2 * qp + 1) * AT_B);
+          q_par[qs] = (it >> 1) & 1;
+          for (int j = 0; j < nk; ++j, ++g) {
+            const int st = g % FW_STAGES;
+            const uint32_t ph = (uint32_t)(g / FW_STAGES) & 1u;
+            if (!mbar_wait(b_kve + 8 * st, ph ^ 1u, abort_flag, p.status)) { ok = false; break; }
+            if ((p.poison & POISON_ATTN_FWD) && g == 0) continue;
+            const uint32_t kd = sbase + FW_KV + st * 2 * AT_TILE;
+            mbar_expect_tx(b_kvf + 8 * st, 2 * AT_TILE);
+            load(&tmK, kd, b_kvf + 8 * st, j * AT_B);
+            load(&tmV, kd + AT_TILE, b_kvf + 8 * st, j * AT_B);
+            last_par[st] = (int)ph;
           }
         }
-        g += nk;
+        // never leave with copies still landing in shared memory
+        for (int q = 0; q < 2; ++q)
+          if (q_par[q] >= 0) mbar_wait_drain(b_qf + 8 * q, (uint32_t)q_par[q]);
+        for (int i = 0; i < FW_STAGES; ++i)
+          if (last_par[i] >= 0) mbar_wait_drain(b_kvf + 8 * i, (uint32_t)last_par[i]);
       }
-      // every MMA issued by this thread has completed once b_done flips
-      mma_commit(b_done);
-      mbar_wait_drain(b_done, 0);
+    } else if (warp == 1 || warp == 2) {
+      if (lane == 0) {
+        // ---------------- MMA issuer of query tile t = warp - 1
+        // A tile's products come in a fixed order: S_t(0), then per key tile j, S_t(j+1)
+        // once K_{j+1} has landed and the tile's warps have read S_t(j), and PV_t(j) once
+        // they have written P_t(j).  One issuer per tile blocks on exactly the next event of
+        // its own tile, so neither tile's products wait behind the other tile's events and
+        // no thread polls (a polling thread runs several times slower beside the softmax
+        // warps that share its scheduler).
+        // Releases: the Q set takes one commit per tile after the item's last S, a K/V stage
+        // one per tile after its PV; a tile that does not use a stage, or is absent from the
+        // item, is stood in for by a second commit of the other tile's issuer.
+        const int t = warp - 1;
+        const uint32_t b_sft = b_sf + 8 * t, b_set = b_se + 8 * t, b_pft = b_pf + 8 * t, b_pvt = b_pv + 8 * t;
+        const uint32_t s_acc = tmem + FW_S_COL + 128 * t, o_acc = tmem + FW_O_COL + 64 * t;
+        const uint32_t p_op = tmem + FW_P_COL + 64 * t;
+        int cnt_s = 0, cnt_pv = 0;  // S and PV products issued by this thread, all items
+        bool ok = true;
+        int g = 0;  // ring position of the item's key tile 0
+        for (int w = blockIdx.x, it = 0; ok && w < nitems; w += gridDim.x, ++it) {
+          const int qp = p.nqp - 1 - w / BH;
+          const int qt0 = 2 * qp;
+          const bool has1 = qt0 + 1 < p.nq;
+          const int nk_item = qt0 + (has1 ? 2 : 1);
+          const int qt = qt0 + t;
+          if (qt >= p.nq) {  // this item has no second tile
+            g += nk_item;
+            continue;
+          }
+          const int nk = qt + 1;
+          const int qs = it & 1;
+          const uint32_t qd = sbase + FW_Q + (2 * qs + t) * AT_TILE;
+          if (!mbar_wait(b_qf + 8 * qs, (uint32_t)(it >> 1) & 1u, abort_flag, p.status)) break;
+          auto issue_s = [&](int j) -> bool {
+            const int st = (g + j) % FW_STAGES;
+            if (!mbar_wait(b_kvf + 8 * st, (uint32_t)((g + j) / FW_STAGES) & 1u, abort_flag, p.status)) return false;
+            if (cnt_s > 0 && !mbar_wait(b_set, (uint32_t)(cnt_s - 1) & 1u, abort_flag, p.status)) return false;
+            tc_fence_after();
+            const uint32_t kd = sbase + FW_KV + st * 2 * AT_TILE;
+  #pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma_bf16(s_acc, operand_desc(qd, 0, k), operand_desc(kd, 0, k), p.idesc_s, k > 0 ? 1u : 0u);
+            mma_commit(b_sft);
+            ++cnt_s;
+            if (j == nk - 1) {  // this tile no longer reads the item's Q set
+              mma_commit(b_qe + 8 * qs);
+              if (!has1) mma_commit(b_qe + 8 * qs);
+            }
+            return true;
+          };
+          if (!issue_s(0)) { ok = false; break; }
+          for (int j = 0; j < nk; ++j) {
+            if (j + 1 < nk && !issue_s(j + 1)) { ok = false; break; }
+            if (!mbar_wait(b_pft, (uint32_t)cnt_pv & 1u, abort_flag, p.status)) { ok = false; break; }
+            tc_fence_after();
+            const int st = (g + j) % FW_STAGES;
+            const uint32_t vd = sbase + FW_KV + st * 2 * AT_TILE + AT_TILE;
+            // A = P_t in TMEM: 16 keys per MMA = 8 columns of bf16 pairs
+  #pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_bf16_tmem_a(o_acc, p_op + kk * 8, operand_desc(vd, 1, kk), p.idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(b_pvt);
+            ++cnt_pv;
+            mma_commit(b_kve + 8 * st);
+            if (!has1 || (t == 1 && j == nk - 1)) mma_commit(b_kve + 8 * st);
+          }
+          g += nk_item;
+        }
+        // every product issued by either issuer has completed once b_done flips
+        mma_commit(b_done);
+        mbar_wait_drain(b_done, 0);
+      }
     }
   } else {
-    // ---------------- softmax warps: query tile t = (warp - 2) / 4, lane quadrant warp % 4
-    const int t = (warp - 2) >> 2, quad = warp & 3;
+    regs_raise<FW_REGS_SOFTMAX>();
+    // ---------------- softmax warps: query tile t = (warp - 4) / 4, lane quadrant warp % 4
+    const int t = (warp - 4) >> 2, quad = warp & 3;
     const int r = quad * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
     const uint32_t s_col = FW_S_COL + 128 * t, o_col = FW_O_COL + 64 * t, p_col = FW_P_COL + 64 * t;
