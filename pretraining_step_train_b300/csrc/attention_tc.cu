@@ -394,7 +394,12 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
 // tiles and accumulates dQ over their key tiles, the other owns 128-key tiles
 // and accumulates dK and dV over their query tiles.
 
-constexpr int BW_THREADS = 320;
+constexpr int BW_THREADS = 384;
+// warps 0-3: TMA producer, two MMA issuers, one idle; warps 4-11: compute.  Registers:
+// 384 x 168 at launch = 64512; the control warpgroup keeps 96, the compute warpgroups take 200
+constexpr int BW_REGS_LAUNCH = 168, BW_REGS_CTRL = 96, BW_REGS_COMPUTE = 200;
+static_assert(128 * BW_REGS_CTRL + 256 * BW_REGS_COMPUTE <= BW_THREADS * BW_REGS_LAUNCH,
+              "the register split must fit in the launch's registers");
 
 struct BwParams {
   AttnArgs a;
@@ -474,7 +479,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
       mbar_init(b_dsf + 8 * i, 8);
       mbar_init(b_dq + 8 * i, 1);
     }
-    mbar_init(b_done, 1);
+    mbar_init(b_done, 2);  // one commit per issuer
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -490,88 +495,104 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
   const uint32_t tmem = *tmem_slot;
   constexpr uint32_t C_S = 0, C_DP = 128, C_DQ = 256, C_DS = 320;  // dS buffer b at C_DS + 64 b
 
-  if (warp == 0) {
-    if (lane == 0) {
-      int last_par[DQ_STAGES] = {-1, -1, -1, -1}, q_par[2] = {-1, -1}, g = 0;
-      bool ok = true;
-      for (int w = blockIdx.x, it = 0; ok && w < nitems; w += gridDim.x, ++it) {
-        const int qt = p.nq - 1 - w / BH, bh = w % BH, b = bh / a.H, h = bh % a.H;
-        const int qs = it & 1;
-        const uint32_t qb = sbase + 3 * qs * AT_TILE;
-        // set qs was last read by item it - 2
-        if (it >= 2 && !mbar_wait(b_qe + 8 * qs, (uint32_t)((it - 2) >> 1) & 1u, abort_flag, p.status)) break;
-        mbar_expect_tx(b_qf + 8 * qs, 3 * AT_TILE);
-        bw_load(&tmQ, p.swap_q, qb + DQ_Q, b_qf + 8 * qs, qt * AT_B, h, b);
-        bw_load(&tmdO, p.swap_o, qb + DQ_DO, b_qf + 8 * qs, qt * AT_B, h, b);
-        bw_load(&tmO, p.swap_o, qb + DQ_O, b_qf + 8 * qs, qt * AT_B, h, b);
-        q_par[qs] = (it >> 1) & 1;
-        for (int j = 0; j <= qt; ++j, ++g) {
-          const int st = g % DQ_STAGES;
-          const uint32_t ph = (uint32_t)(g / DQ_STAGES) & 1u;
-          if (!mbar_wait(b_kve + 8 * st, ph ^ 1u, abort_flag, p.status)) { ok = false; break; }
-          if ((p.poison & POISON_ATTN_DQ) && g == 0) continue;
-          const uint32_t kd = sbase + DQ_KV + st * 2 * AT_TILE;
-          mbar_expect_tx(b_kvf + 8 * st, 2 * AT_TILE);
-          bw_load(&tmK, p.swap_q, kd, b_kvf + 8 * st, j * AT_B, h, b);
-          bw_load(&tmV, p.swap_q, kd + AT_TILE, b_kvf + 8 * st, j * AT_B, h, b);
-          last_par[st] = (int)ph;
-        }
-      }
-      for (int i = 0; i < 2; ++i)
-        if (q_par[i] >= 0) mbar_wait_drain(b_qf + 8 * i, (uint32_t)q_par[i]);
-      for (int i = 0; i < DQ_STAGES; ++i)
-        if (last_par[i] >= 0) mbar_wait_drain(b_kvf + 8 * i, (uint32_t)last_par[i]);
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      auto issue_dq = [&](int gp, bool first) -> bool {
-        const int db = gp & 1;
-        if (!mbar_wait(b_dsf + 8 * db, (uint32_t)(gp >> 1) & 1u, abort_flag, p.status)) return false;
-        tc_fence_after();
-        const uint32_t kd = sbase + DQ_KV + (gp % DQ_STAGES) * 2 * AT_TILE;
-        // A = dS in TMEM: 16 keys per MMA = 8 columns of bf16 pairs
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_bf16_tmem_a(tmem + C_DQ, tmem + C_DS + db * 64 + kk * 8, operand_desc(kd, 1, kk), p.idesc_d,
-                          (!first || kk > 0) ? 1u : 0u);
-        mma_commit(b_dq + 8 * db);
-        mma_commit(b_kve + 8 * (gp % DQ_STAGES));
-        return true;
-      };
-      bool ok = true;
-      int g = 0;
-      for (int w = blockIdx.x, it = 0; ok && w < nitems; w += gridDim.x, ++it) {
-        const int nk = p.nq - w / BH;
-        const int qs = it & 1;
-        const uint32_t qb = sbase + 3 * qs * AT_TILE;
-        if (!mbar_wait(b_qf + 8 * qs, (uint32_t)(it >> 1) & 1u, abort_flag, p.status)) break;
-        for (int j = 0; j < nk; ++j, ++g) {
-          const int st = g % DQ_STAGES;
-          if (!mbar_wait(b_kvf + 8 * st, (uint32_t)(g / DQ_STAGES) & 1u, abort_flag, p.status)) {
-            ok = false;
-            break;
+  if (warp < 4) {
+    regs_lower<BW_REGS_CTRL>();
+    if (warp == 0) {
+      if (lane == 0) {
+        int last_par[DQ_STAGES] = {-1, -1, -1, -1}, q_par[2] = {-1, -1}, g = 0;
+        bool ok = true;
+        for (int w = blockIdx.x, it = 0; ok && w < nitems; w += gridDim.x, ++it) {
+          const int qt = p.nq - 1 - w / BH, bh = w % BH, b = bh / a.H, h = bh % a.H;
+          const int qs = it & 1;
+          const uint32_t qb = sbase + 3 * qs * AT_TILE;
+          // set qs was last read by item it - 2
+          if (it >= 2 && !mbar_wait(b_qe + 8 * qs, (uint32_t)((it - 2) >> 1) & 1u, abort_flag, p.status)) break;
+          mbar_expect_tx(b_qf + 8 * qs, 3 * AT_TILE);
+          bw_load(&tmQ, p.swap_q, qb + DQ_Q, b_qf + 8 * qs, qt * AT_B, h, b);
+          bw_load(&tmdO, p.swap_o, qb + DQ_DO, b_qf + 8 * qs, qt * AT_B, h, b);
+          bw_load(&tmO, p.swap_o, qb + DQ_O, b_qf + 8 * qs, qt * AT_B, h, b);
+          q_par[qs] = (it >> 1) & 1;
+          for (int j = 0; j <= qt; ++j, ++g) {
+            const int st = g % DQ_STAGES;
+            const uint32_t ph = (uint32_t)(g / DQ_STAGES) & 1u;
+            if (!mbar_wait(b_kve + 8 * st, ph ^ 1u, abort_flag, p.status)) { ok = false; break; }
+            if ((p.poison & POISON_ATTN_DQ) && g == 0) continue;
+            const uint32_t kd = sbase + DQ_KV + st * 2 * AT_TILE;
+            mbar_expect_tx(b_kvf + 8 * st, 2 * AT_TILE);
+            bw_load(&tmK, p.swap_q, kd, b_kvf + 8 * st, j * AT_B, h, b);
+            bw_load(&tmV, p.swap_q, kd + AT_TILE, b_kvf + 8 * st, j * AT_B, h, b);
+            last_par[st] = (int)ph;
           }
-          if (g >= 1 && !mbar_wait(b_se, (uint32_t)(g - 1) & 1u, abort_flag, p.status)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t kd = sbase + DQ_KV + st * 2 * AT_TILE;
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_bf16(tmem + C_S, operand_desc(qb + DQ_Q, 0, k), operand_desc(kd, 0, k), p.idesc_s, k > 0 ? 1u : 0u);
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_bf16(tmem + C_DP, operand_desc(qb + DQ_DO, 0, k), operand_desc(kd + AT_TILE, 0, k), p.idesc_s,
-                     k > 0 ? 1u : 0u);
-          mma_commit(b_sf);
-          if (j == nk - 1) mma_commit(b_qe + 8 * qs);
-          if (j >= 1 && !issue_dq(g - 1, j == 1)) { ok = false; break; }
         }
-        if (ok && !issue_dq(g - 1, nk == 1)) ok = false;
+        for (int i = 0; i < 2; ++i)
+          if (q_par[i] >= 0) mbar_wait_drain(b_qf + 8 * i, (uint32_t)q_par[i]);
+        for (int i = 0; i < DQ_STAGES; ++i)
+          if (last_par[i] >= 0) mbar_wait_drain(b_kvf + 8 * i, (uint32_t)last_par[i]);
       }
-      mma_commit(b_done);
-      mbar_wait_drain(b_done, 0);
+    } else if (warp == 1) {
+      if (lane == 0) {
+        // ---------------- S / dP issuer: S(g) = Q K_j^T and dP(g) = dO V_j^T once K_j, V_j
+        // have landed and the compute warps have read S(g-1), dP(g-1)
+        bool ok = true;
+        int g = 0;
+        for (int w = blockIdx.x, it = 0; ok && w < nitems; w += gridDim.x, ++it) {
+          const int nk = p.nq - w / BH;
+          const int qs = it & 1;
+          const uint32_t qb = sbase + 3 * qs * AT_TILE;
+          if (!mbar_wait(b_qf + 8 * qs, (uint32_t)(it >> 1) & 1u, abort_flag, p.status)) break;
+          for (int j = 0; j < nk; ++j, ++g) {
+            const int st = g % DQ_STAGES;
+            if (!mbar_wait(b_kvf + 8 * st, (uint32_t)(g / DQ_STAGES) & 1u, abort_flag, p.status)) {
+              ok = false;
+              break;
+            }
+            if (g >= 1 && !mbar_wait(b_se, (uint32_t)(g - 1) & 1u, abort_flag, p.status)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t kd = sbase + DQ_KV + st * 2 * AT_TILE;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma_bf16(tmem + C_S, operand_desc(qb + DQ_Q, 0, k), operand_desc(kd, 0, k), p.idesc_s, k > 0 ? 1u : 0u);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma_bf16(tmem + C_DP, operand_desc(qb + DQ_DO, 0, k), operand_desc(kd + AT_TILE, 0, k), p.idesc_s,
+                       k > 0 ? 1u : 0u);
+            mma_commit(b_sf);
+            if (j == nk - 1) mma_commit(b_qe + 8 * qs);
+          }
+        }
+        mma_commit(b_done);
+        mbar_wait_drain(b_done, 0);
+      }
+    } else if (warp == 2) {
+      if (lane == 0) {
+        // ---------------- dQ issuer: dQ += dS(g) K_j once the compute warps have written
+        // dS(g); its commit also frees K_j / V_j (S(g) and dP(g), the stage's other
+        // readers, were complete before dS(g) could be formed)
+        bool ok = true;
+        int g = 0;
+        for (int w = blockIdx.x; ok && w < nitems; w += gridDim.x) {
+          const int nk = p.nq - w / BH;
+          for (int j = 0; j < nk; ++j, ++g) {
+            const int db = g & 1;
+            if (!mbar_wait(b_dsf + 8 * db, (uint32_t)(g >> 1) & 1u, abort_flag, p.status)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t kd = sbase + DQ_KV + (g % DQ_STAGES) * 2 * AT_TILE;
+            // A = dS in TMEM: 16 keys per MMA = 8 columns of bf16 pairs
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_bf16_tmem_a(tmem + C_DQ, tmem + C_DS + db * 64 + kk * 8, operand_desc(kd, 1, kk), p.idesc_d,
+                              (j > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(b_dq + 8 * db);
+            mma_commit(b_kve + 8 * (g % DQ_STAGES));
+          }
+        }
+        mma_commit(b_done);
+        mbar_wait_drain(b_done, 0);
+      }
     }
   } else {
-    const int quad = warp & 3, half = (warp - 2) >> 2;
+    regs_raise<BW_REGS_COMPUTE>();
+    const int quad = warp & 3, half = (warp - 4) >> 2;
     const int r = quad * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
     bool ok = true;
@@ -733,7 +754,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
     mbar_init(b_se, 8);  // one arrival per compute warp
     mbar_init(b_dsf, 8);
     mbar_init(b_mm, 1);
-    mbar_init(b_done, 1);
+    mbar_init(b_done, 2);  // one commit per issuer
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -749,117 +770,135 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
   const uint32_t tmem = *tmem_slot;
   constexpr uint32_t C_S = 0, C_DP = 128, C_DV = 256, C_DK = 320, C_PT = 384, C_DST = 448;
 
-  if (warp == 0) {
-    // ---------------- producer warp: TMA by lane 0, lse2 / D staged by all lanes
-    // Each lane's four lse and D values for a query tile are loaded one tile ahead, so
-    // their global-memory latency overlaps the wait for the ring stage.
-    int last_par[DK_STAGES] = {-1, -1, -1, -1}, kv_par[2] = {-1, -1}, g = 0;
-    bool ok = true;
-    float nl[4], nd[4];  // lse and D of the next query tile to stage (this lane's 4 queries)
-    auto fetch = [&](int bh, int i) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int q = i * AT_B + lane * 4 + e;
-        const bool v = q < a.T;
-        nl[e] = v ? a.lse[(long long)bh * a.T + q] : INFINITY;
-        nd[e] = v ? a.Dbuf[(long long)bh * a.T + q] : 0.f;
-      }
-    };
-    if (blockIdx.x < nitems) fetch(blockIdx.x % BH, blockIdx.x / BH);
-    for (int w = blockIdx.x, it = 0; ok && w < nitems; w += gridDim.x, ++it) {
-      const int kt = w / BH, bh = w % BH, b = bh / a.H, h = bh % a.H;
-      const int ks = it & 1;  // K/V set of this item
-      if (it >= 2 && !warp_wait(b_kve + 8 * ks, (uint32_t)((it - 2) >> 1) & 1u, abort_flag, p.status)) break;
-      if (lane == 0) {
-        mbar_expect_tx(b_kvf + 8 * ks, 2 * AT_TILE);
-        bw_load(&tmK, p.swap_q, sbase + DK_K + 2 * ks * AT_TILE, b_kvf + 8 * ks, kt * AT_B, h, b);
-        bw_load(&tmV, p.swap_q, sbase + DK_V + 2 * ks * AT_TILE, b_kvf + 8 * ks, kt * AT_B, h, b);
-      }
-      kv_par[ks] = (it >> 1) & 1;
-      for (int i = kt; i < p.nq; ++i, ++g) {
-        const int st = g % DK_STAGES;
-        const uint32_t ph = (uint32_t)(g / DK_STAGES) & 1u;
-        if (!warp_wait(b_qde + 8 * st, ph ^ 1u, abort_flag, p.status)) { ok = false; break; }
-        if (lane == 0 && !((p.poison & POISON_ATTN_DKDV) && g == 0)) {
-          const uint32_t qd = sbase + DK_QD + st * 2 * AT_TILE;
-          mbar_expect_tx(b_qdf + 8 * st, 2 * AT_TILE);
-          bw_load(&tmQ, p.swap_q, qd, b_qdf + 8 * st, i * AT_B, h, b);
-          bw_load(&tmdO, p.swap_o, qd + AT_TILE, b_qdf + 8 * st, i * AT_B, h, b);
-        }
-        float* lb = ldbuf + st * 256;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int c = lane * 4 + e;
-          const int slot = (c >> 1) * 4 + (c & 1);
-          lb[slot] = -nl[e] * 1.4426950408889634f;  // rows past T: -inf, so P = 0 there
-          lb[slot + 2] = -nd[e];
-        }
-        warp_arrive(b_qdf + 8 * st);
-        if (!((p.poison & POISON_ATTN_DKDV) && g == 0)) last_par[st] = (int)ph;
-        // the next tile's values: this item's next query tile, or the next item's first
-        if (i + 1 < p.nq) fetch(bh, i + 1);
-        else if (w + (int)gridDim.x < nitems) fetch((w + gridDim.x) % BH, (w + gridDim.x) / BH);
-      }
-    }
-    if (lane == 0) {
-      for (int i = 0; i < 2; ++i)
-        if (kv_par[i] >= 0) mbar_wait_drain(b_kvf + 8 * i, (uint32_t)kv_par[i]);
-      for (int i = 0; i < DK_STAGES; ++i)
-        if (last_par[i] >= 0) mbar_wait_drain(b_qdf + 8 * i, (uint32_t)last_par[i]);
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      auto issue_kv = [&](int gp, bool first) -> bool {
-        if (!mbar_wait(b_dsf, (uint32_t)gp & 1u, abort_flag, p.status)) return false;
-        tc_fence_after();
-        const uint32_t qd = sbase + DK_QD + (gp % DK_STAGES) * 2 * AT_TILE;
-        // A = P^T / dS^T in TMEM: 16 queries per MMA = 8 columns of bf16 pairs
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_bf16_tmem_a(tmem + C_DV, tmem + C_PT + kk * 8, operand_desc(qd + AT_TILE, 1, kk), p.idesc_d,
-                          (!first || kk > 0) ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_bf16_tmem_a(tmem + C_DK, tmem + C_DST + kk * 8, operand_desc(qd, 1, kk), p.idesc_d,
-                          (!first || kk > 0) ? 1u : 0u);
-        mma_commit(b_mm);
-        mma_commit(b_qde + 8 * (gp % DK_STAGES));
-        return true;
-      };
+  if (warp < 4) {
+    regs_lower<BW_REGS_CTRL>();
+    if (warp == 0) {
+      // ---------------- producer warp: TMA by lane 0, lse2 / D staged by all lanes
+      // Each lane's four lse and D values for a query tile are loaded one tile ahead, so
+      // their global-memory latency overlaps the wait for the ring stage.
+      int last_par[DK_STAGES] = {-1, -1, -1, -1}, kv_par[2] = {-1, -1}, g = 0;
       bool ok = true;
-      int g = 0;
-      for (int w = blockIdx.x, it = 0; ok && w < nitems; w += gridDim.x, ++it) {
-        const int n = p.nq - w / BH;  // query tiles kt .. nq-1
-        const int ks = it & 1;
-        const uint32_t kd = sbase + DK_K + 2 * ks * AT_TILE, vd = sbase + DK_V + 2 * ks * AT_TILE;
-        if (!mbar_wait(b_kvf + 8 * ks, (uint32_t)(it >> 1) & 1u, abort_flag, p.status)) break;
-        for (int j = 0; j < n; ++j, ++g) {
-          const int st = g % DK_STAGES;
-          if (!mbar_wait(b_qdf + 8 * st, (uint32_t)(g / DK_STAGES) & 1u, abort_flag, p.status)) {
-            ok = false;
-            break;
-          }
-          if (g >= 1 && !mbar_wait(b_se, (uint32_t)(g - 1) & 1u, abort_flag, p.status)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t qd = sbase + DK_QD + st * 2 * AT_TILE;
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_bf16(tmem + C_S, operand_desc(kd, 0, k), operand_desc(qd, 0, k), p.idesc_s, k > 0 ? 1u : 0u);
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_bf16(tmem + C_DP, operand_desc(vd, 0, k), operand_desc(qd + AT_TILE, 0, k), p.idesc_s,
-                     k > 0 ? 1u : 0u);
-          mma_commit(b_sf);
-          if (j >= 1 && !issue_kv(g - 1, j == 1)) { ok = false; break; }
+      float nl[4], nd[4];  // lse and D of the next query tile to stage (this lane's 4 queries)
+      auto fetch = [&](int bh, int i) {
+  #pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int q = i * AT_B + lane * 4 + e;
+          const bool v = q < a.T;
+          nl[e] = v ? a.lse[(long long)bh * a.T + q] : INFINITY;
+          nd[e] = v ? a.Dbuf[(long long)bh * a.T + q] : 0.f;
         }
-        if (ok && !issue_kv(g - 1, n == 1)) ok = false;
-        if (ok) mma_commit(b_kve + 8 * ks);  // this item's K, V set is no longer read
+      };
+      if (blockIdx.x < nitems) fetch(blockIdx.x % BH, blockIdx.x / BH);
+      for (int w = blockIdx.x, it = 0; ok && w < nitems; w += gridDim.x, ++it) {
+        const int kt = w / BH, bh = w % BH, b = bh / a.H, h = bh % a.H;
+        const int ks = it & 1;  // K/V set of this item
+        if (it >= 2 && !warp_wait(b_kve + 8 * ks, (uint32_t)((it - 2) >> 1) & 1u, abort_flag, p.status)) break;
+        if (lane == 0) {
+          mbar_expect_tx(b_kvf + 8 * ks, 2 * AT_TILE);
+          bw_load(&tmK, p.swap_q, sbase + DK_K + 2 * ks * AT_TILE, b_kvf + 8 * ks, kt * AT_B, h, b);
+          bw_load(&tmV, p.swap_q, sbase + DK_V + 2 * ks * AT_TILE, b_kvf + 8 * ks, kt * AT_B, h, b);
+        }
+        kv_par[ks] = (it >> 1) & 1;
+        for (int i = kt; i < p.nq; ++i, ++g) {
+          const int st = g % DK_STAGES;
+          const uint32_t ph = (uint32_t)(g / DK_STAGES) & 1u;
+          if (!warp_wait(b_qde + 8 * st, ph ^ 1u, abort_flag, p.status)) { ok = false; break; }
+          if (lane == 0 && !((p.poison & POISON_ATTN_DKDV) && g == 0)) {
+            const uint32_t qd = sbase + DK_QD + st * 2 * AT_TILE;
+            mbar_expect_tx(b_qdf + 8 * st, 2 * AT_TILE);
+            bw_load(&tmQ, p.swap_q, qd, b_qdf + 8 * st, i * AT_B, h, b);
+            bw_load(&tmdO, p.swap_o, qd + AT_TILE, b_qdf + 8 * st, i * AT_B, h, b);
+          }
+          float* lb = ldbuf + st * 256;
+  #pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int c = lane * 4 + e;
+            const int slot = (c >> 1) * 4 + (c & 1);
+            lb[slot] = -nl[e] * 1.4426950408889634f;  // rows past T: -inf, so P = 0 there
+            lb[slot + 2] = -nd[e];
+          }
+          warp_arrive(b_qdf + 8 * st);
+          if (!((p.poison & POISON_ATTN_DKDV) && g == 0)) last_par[st] = (int)ph;
+          // the next tile's values: this item's next query tile, or the next item's first
+          if (i + 1 < p.nq) fetch(bh, i + 1);
+          else if (w + (int)gridDim.x < nitems) fetch((w + gridDim.x) % BH, (w + gridDim.x) / BH);
+        }
       }
-      mma_commit(b_done);
-      mbar_wait_drain(b_done, 0);
+      if (lane == 0) {
+        for (int i = 0; i < 2; ++i)
+          if (kv_par[i] >= 0) mbar_wait_drain(b_kvf + 8 * i, (uint32_t)kv_par[i]);
+        for (int i = 0; i < DK_STAGES; ++i)
+          if (last_par[i] >= 0) mbar_wait_drain(b_qdf + 8 * i, (uint32_t)last_par[i]);
+      }
+    } else if (warp == 1) {
+      if (lane == 0) {
+        // ---------------- S^T / dP^T issuer: S^T(g) = K Q_i^T and dP^T(g) = V dO_i^T once
+        // Q_i, dO_i have landed and the compute warps have read S^T(g-1), dP^T(g-1)
+        bool ok = true;
+        int g = 0;
+        for (int w = blockIdx.x, it = 0; ok && w < nitems; w += gridDim.x, ++it) {
+          const int n = p.nq - w / BH;  // query tiles kt .. nq-1
+          const int ks = it & 1;
+          const uint32_t kd = sbase + DK_K + 2 * ks * AT_TILE, vd = sbase + DK_V + 2 * ks * AT_TILE;
+          if (!mbar_wait(b_kvf + 8 * ks, (uint32_t)(it >> 1) & 1u, abort_flag, p.status)) break;
+          for (int j = 0; j < n; ++j, ++g) {
+            const int st = g % DK_STAGES;
+            if (!mbar_wait(b_qdf + 8 * st, (uint32_t)(g / DK_STAGES) & 1u, abort_flag, p.status)) {
+              ok = false;
+              break;
+            }
+            if (g >= 1 && !mbar_wait(b_se, (uint32_t)(g - 1) & 1u, abort_flag, p.status)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t qd = sbase + DK_QD + st * 2 * AT_TILE;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma_bf16(tmem + C_S, operand_desc(kd, 0, k), operand_desc(qd, 0, k), p.idesc_s, k > 0 ? 1u : 0u);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma_bf16(tmem + C_DP, operand_desc(vd, 0, k), operand_desc(qd + AT_TILE, 0, k), p.idesc_s,
+                       k > 0 ? 1u : 0u);
+            mma_commit(b_sf);
+          }
+        }
+        mma_commit(b_done);
+        mbar_wait_drain(b_done, 0);
+      }
+    } else if (warp == 2) {
+      if (lane == 0) {
+        // ---------------- dV / dK issuer: dV += P^T(g) dO_i, dK += dS^T(g) Q_i once the
+        // compute warps have written P^T(g), dS^T(g).  Its commits free the Q_i / dO_i
+        // stage and, after an item's last query tile, the item's K / V set (the S^T and dP^T
+        // products, their other readers, were complete before dS^T could be formed).
+        bool ok = true;
+        int g = 0;
+        for (int w = blockIdx.x, it = 0; ok && w < nitems; w += gridDim.x, ++it) {
+          const int n = p.nq - w / BH;
+          const int ks = it & 1;
+          for (int j = 0; j < n; ++j, ++g) {
+            if (!mbar_wait(b_dsf, (uint32_t)g & 1u, abort_flag, p.status)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t qd = sbase + DK_QD + (g % DK_STAGES) * 2 * AT_TILE;
+            // A = P^T / dS^T in TMEM: 16 queries per MMA = 8 columns of bf16 pairs
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_bf16_tmem_a(tmem + C_DV, tmem + C_PT + kk * 8, operand_desc(qd + AT_TILE, 1, kk), p.idesc_d,
+                              (j > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_bf16_tmem_a(tmem + C_DK, tmem + C_DST + kk * 8, operand_desc(qd, 1, kk), p.idesc_d,
+                              (j > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(b_mm);
+            mma_commit(b_qde + 8 * (g % DK_STAGES));
+          }
+          if (ok) mma_commit(b_kve + 8 * ks);  // this item's K, V set is no longer read
+        }
+        mma_commit(b_done);
+        mbar_wait_drain(b_done, 0);
+      }
     }
   } else {
-    const int quad = warp & 3, half = (warp - 2) >> 2;
+    regs_raise<BW_REGS_COMPUTE>();
+    const int quad = warp & 3, half = (warp - 4) >> 2;
     const int r = quad * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
     bool ok = true;
