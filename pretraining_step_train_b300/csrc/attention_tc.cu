@@ -433,6 +433,19 @@ __device__ __forceinline__ void bw_load(const CUtensorMap* tm, int swap, uint32_
   if (swap) tma_load_4d(dst, tm, bar, 0, h, t0, b);
   else tma_load_4d(dst, tm, bar, 0, t0, h, b);
 }
+// One [128 rows x 64] bf16 tile from shared memory (128B swizzle) to rows t0.. of head (b, h);
+// rows past T are not written.
+__device__ __forceinline__ void bw_store(const CUtensorMap* tm, int swap, uint32_t src, int t0, int h, int b) {
+  if (swap) tma_store_4d(tm, src, 0, h, t0, b);
+  else tma_store_4d(tm, src, 0, t0, h, b);
+}
+// Stores 16-byte piece c (0..7) of row r of a [128 x 128 B] tile with the 128B swizzle
+// (piece c of row r sits at r * 128 + ((c ^ (r & 7)) << 4)), as TMA reads and writes it.
+__device__ __forceinline__ void st_swizzled(uint32_t tile, int r, int c, uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(tile + (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4))),
+               "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
 
 // ------------------------------------------------------------------ dQ
 // smem: two sets of Q | dO | O (items alternate, so the next item's tiles load while this one
@@ -442,13 +455,14 @@ __device__ __forceinline__ void bw_load(const CUtensorMap* tm, int swap, uint32_
 constexpr int DQ_STAGES = 4;
 constexpr int DQ_Q = 0, DQ_DO = AT_TILE, DQ_O = 2 * AT_TILE, DQ_KV = 6 * AT_TILE;  // set s: + 3 s TILE
 constexpr int DQ_BAR = DQ_KV + 2 * DQ_STAGES * AT_TILE;
-constexpr int DQ_NBARS = 19;
+constexpr int DQ_NBARS = 20;
 constexpr int DQ_SMEM = 1024 + DQ_BAR + 8 * (DQ_NBARS + 2);
 
 __global__ void __launch_bounds__(BW_THREADS, 1)
     k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                     const __grid_constant__ CUtensorMap tmO, const BwParams p) {
+                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                 const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmdQ,
+                 const BwParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -457,7 +471,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
   // dq_done[2], done (ds_full / dq_done per dS buffer: tile parity)
   const uint32_t b_qf = smem_u32(bars), b_qe = b_qf + 16, b_kvf = b_qe + 16, b_kve = b_kvf + 8 * DQ_STAGES;
   const uint32_t b_sf = b_kve + 8 * DQ_STAGES, b_se = b_sf + 8, b_dsf = b_se + 8, b_dq = b_dsf + 16;
-  const uint32_t b_done = b_dq + 16;
+  const uint32_t b_done = b_dq + 16, b_stg = b_done + 8;  // staged: the item's dQ rows are in shared memory
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bars + DQ_NBARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + DQ_NBARS + 1);
   const AttnArgs& a = p.a;
@@ -467,7 +481,9 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(b_qf + 8 * i, 1);
-      mbar_init(b_qe + 8 * i, 9);  // the MMA thread's commit after the item's last S / dP + the 8 compute warps (D formed)
+      // the S / dP issuer's commit after the item's last S / dP, the 8 compute warps (D
+      // formed) and the thread whose tensor store of the item's dQ has read the Q tile
+      mbar_init(b_qe + 8 * i, 10);
     }
     for (int i = 0; i < DQ_STAGES; ++i) {
       mbar_init(b_kvf + 8 * i, 1);
@@ -480,6 +496,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
       mbar_init(b_dq + 8 * i, 1);
     }
     mbar_init(b_done, 2);  // one commit per issuer
+    mbar_init(b_stg, 8);   // one arrival per compute warp
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -597,6 +614,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
     const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
     bool ok = true;
     int g = 0;
+    int pend = -1;  // warp 4: the Q set whose dQ tensor store is in flight
     for (int w = blockIdx.x, it = 0; ok && w < nitems; w += gridDim.x, ++it) {
       const int qt = p.nq - 1 - w / BH, bh = w % BH, b = bh / a.H, h = bh % a.H;
       const int nk = qt + 1;
@@ -639,6 +657,13 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
         tmem_ld_wait();
         tc_fence_before();
         warp_arrive(b_se);
+        if (warp == 4 && pend >= 0) {  // the previous item's dQ store has long finished reading its Q tile
+          if (lane == 0) {
+            bulk_wait_read<0>();
+            mbar_arrive(b_qe + 8 * pend);
+          }
+          pend = -1;
+        }
         const int kmask = j == qt ? qi - j * AT_B - half * 64 : AT_B;  // key offsets > kmask are masked
         const float2 c2 = make_float2(p.c2, p.c2), nl = make_float2(-lse2, -lse2);
         const float2 nd = make_float2(-Dr, -Dr);
@@ -685,20 +710,31 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
         const long long prow = ((long long)b * p.nq + qt) * 4 + quad;
         a.bias_part[prow * 3 * a.H * AT_D + h * AT_D + half * 32 + lane] = cs;
       }
-      if (valid) {
-        bf16* dst = static_cast<bf16*>(a.dq) + (long long)b * a.sb + (long long)h * a.sh +
-                    (long long)qi * a.st + half * 32;
+      // dQ rows go into the item's Q tile, which no product reads any more (the item's last
+      // S completed before its last dS was formed); one thread writes the tile out with a
+      // tensor store (rows past T are not written).
+      const uint32_t qst = qb + DQ_Q;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint4 u;
-          u.x = pack_bf16x2(__uint_as_float(o[8 * q]) * a.scale, __uint_as_float(o[8 * q + 1]) * a.scale);
-          u.y = pack_bf16x2(__uint_as_float(o[8 * q + 2]) * a.scale, __uint_as_float(o[8 * q + 3]) * a.scale);
-          u.z = pack_bf16x2(__uint_as_float(o[8 * q + 4]) * a.scale, __uint_as_float(o[8 * q + 5]) * a.scale);
-          u.w = pack_bf16x2(__uint_as_float(o[8 * q + 6]) * a.scale, __uint_as_float(o[8 * q + 7]) * a.scale);
-          *reinterpret_cast<uint4*>(dst + 8 * q) = u;
+      for (int q = 0; q < 4; ++q) {
+        uint4 u;
+        u.x = pack_bf16x2(__uint_as_float(o[8 * q]) * a.scale, __uint_as_float(o[8 * q + 1]) * a.scale);
+        u.y = pack_bf16x2(__uint_as_float(o[8 * q + 2]) * a.scale, __uint_as_float(o[8 * q + 3]) * a.scale);
+        u.z = pack_bf16x2(__uint_as_float(o[8 * q + 4]) * a.scale, __uint_as_float(o[8 * q + 5]) * a.scale);
+        u.w = pack_bf16x2(__uint_as_float(o[8 * q + 6]) * a.scale, __uint_as_float(o[8 * q + 7]) * a.scale);
+        st_swizzled(qst, r, half * 4 + q, u);
+      }
+      fence_async_smem();
+      warp_arrive(b_stg);
+      if (warp == 4) {
+        if (!warp_wait(b_stg, (uint32_t)it & 1u, abort_flag, p.status)) break;
+        if (lane == 0) {
+          bw_store(&tmdQ, p.swap_q, qst, qt * AT_B, h, b);
+          bulk_commit();
         }
+        pend = qs;
       }
     }
+    if (warp == 4 && lane == 0 && pend >= 0) bulk_wait_all();  // the last item's store is out
   }
   __syncwarp();
   tc_fence_before();
@@ -716,12 +752,13 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
 constexpr int DK_STAGES = 4;
 constexpr int DK_K = 0, DK_V = AT_TILE, DK_QD = 4 * AT_TILE, DK_LD = DK_QD + 2 * DK_STAGES * AT_TILE;  // set s: K, V at + 2 s TILE
 constexpr int DK_BAR = DK_LD + DK_STAGES * 1024;
-constexpr int DK_NBARS = 19;
+constexpr int DK_NBARS = 20;
 constexpr int DK_SMEM = 1024 + DK_BAR + 8 * (DK_NBARS + 2);
 
 __global__ void __launch_bounds__(BW_THREADS, 1)
     k_attn_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                       const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV,
                        const BwParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -730,10 +767,10 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
   float* ldbuf = reinterpret_cast<float*>(smem + DK_LD);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + DK_BAR);
   // kv_full[2], kv_empty[2] (per K/V set), qd_full[4], qd_empty[4], sdp_full, sdp_empty, ds_full,
-  // mma_done, done
+  // mma_done, done, staged (the item's dK / dV rows are in shared memory)
   const uint32_t b_kvf = smem_u32(bars), b_kve = b_kvf + 16, b_qdf = b_kve + 16, b_qde = b_qdf + 8 * DK_STAGES;
   const uint32_t b_sf = b_qde + 8 * DK_STAGES, b_se = b_sf + 8, b_dsf = b_se + 8, b_mm = b_dsf + 8;
-  const uint32_t b_done = b_mm + 8;
+  const uint32_t b_done = b_mm + 8, b_stg = b_done + 8;
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bars + DK_NBARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + DK_NBARS + 1);
   const AttnArgs& a = p.a;
@@ -744,7 +781,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(b_kvf + 8 * i, 1);
-      mbar_init(b_kve + 8 * i, 1);
+      mbar_init(b_kve + 8 * i, 1);  // the epilogue's tensor stores have read the set (it stages dK, dV)
     }
     for (int i = 0; i < DK_STAGES; ++i) {
       mbar_init(b_qdf + 8 * i, 2);  // the TMA expect_tx arrive + the warp that staged lse2 / D
@@ -755,6 +792,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
     mbar_init(b_dsf, 8);
     mbar_init(b_mm, 1);
     mbar_init(b_done, 2);  // one commit per issuer
+    mbar_init(b_stg, 8);   // one arrival per compute warp
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -866,16 +904,15 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
     } else if (warp == 2) {
       if (lane == 0) {
         // ---------------- dV / dK issuer: dV += P^T(g) dO_i, dK += dS^T(g) Q_i once the
-        // compute warps have written P^T(g), dS^T(g).  Its commits free the Q_i / dO_i
-        // stage and, after an item's last query tile, the item's K / V set (the S^T and dP^T
-        // products, their other readers, were complete before dS^T could be formed).
+        // compute warps have written P^T(g), dS^T(g).  Its commit frees the Q_i / dO_i stage
+        // (the S^T and dP^T products, its other readers, were complete before dS^T could be
+        // formed).
         bool ok = true;
         int g = 0;
-        for (int w = blockIdx.x, it = 0; ok && w < nitems; w += gridDim.x, ++it) {
-          const int n = p.nq - w / BH;
-          const int ks = it & 1;
-          for (int j = 0; j < n; ++j, ++g) {
-            if (!mbar_wait(b_dsf, (uint32_t)g & 1u, abort_flag, p.status)) { ok = false; break; }
+        for (int w = blockIdx.x; ok && w < nitems; w += gridDim.x) {
+        const int n = p.nq - w / BH;
+        for (int j = 0; j < n; ++j, ++g) {
+        if (!mbar_wait(b_dsf, (uint32_t)g & 1u, abort_flag, p.status)) { ok = false; break; }
             tc_fence_after();
             const uint32_t qd = sbase + DK_QD + (g % DK_STAGES) * 2 * AT_TILE;
             // A = P^T / dS^T in TMEM: 16 queries per MMA = 8 columns of bf16 pairs
@@ -889,9 +926,8 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
                               (j > 0 || kk > 0) ? 1u : 0u);
             mma_commit(b_mm);
             mma_commit(b_qde + 8 * (g % DK_STAGES));
-          }
-          if (ok) mma_commit(b_kve + 8 * ks);  // this item's K, V set is no longer read
-        }
+            }
+            }
         mma_commit(b_done);
         mbar_wait_drain(b_done, 0);
       }
@@ -903,6 +939,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
     const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
     bool ok = true;
     int g = 0;
+    int pend = -1;  // warp 4: the K/V set whose tensor stores are in flight
     for (int w = blockIdx.x, it = 0; ok && w < nitems; w += gridDim.x, ++it) {
       const int kt = w / BH, bh = w % BH, b = bh / a.H, h = bh % a.H;
       const int kr = kt * AT_B + r;
@@ -923,6 +960,13 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
         tmem_ld_wait();
         tc_fence_before();
         warp_arrive(b_se);
+        if (warp == 4 && pend >= 0) {  // the previous item's stores have long finished reading its set
+          if (lane == 0) {
+            bulk_wait_read<0>();
+            mbar_arrive(b_kve + 8 * pend);
+          }
+          pend = -1;
+        }
         const float4* ld4 = reinterpret_cast<const float4*>(ldbuf + st * 256) + half * 32;
         const float2 c2 = make_float2(p.c2, p.c2);
         uint32_t pp[32], pd[32];
@@ -976,26 +1020,39 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
         cs = colsum_32x32(v, lane);
         a.bias_part[prow * 3 * C + 2 * C + h * AT_D + half * 32 + lane] = cs;
       }
-      if (kr < a.T) {
-        const long long off = (long long)b * a.sb + (long long)h * a.sh + (long long)kr * a.st + half * 32;
-        bf16* dvd = static_cast<bf16*>(a.dv) + off;
-        bf16* dkd = static_cast<bf16*>(a.dk) + off;
+      // dK (scaled) and dV rows go into the item's K / V tiles, which no product reads any
+      // more (the item's last S^T / dP^T completed before its last dS^T was formed); one
+      // thread writes both tiles out with tensor stores (rows past T are not written), and
+      // the set goes back to the producer once those stores have read it.
+      const int ks = it & 1;
+      const uint32_t kst = sbase + DK_K + 2 * ks * AT_TILE, vst = sbase + DK_V + 2 * ks * AT_TILE;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint4 u, k;
-          u.x = pack_bf16x2(__uint_as_float(ov[8 * q]), __uint_as_float(ov[8 * q + 1]));
-          u.y = pack_bf16x2(__uint_as_float(ov[8 * q + 2]), __uint_as_float(ov[8 * q + 3]));
-          u.z = pack_bf16x2(__uint_as_float(ov[8 * q + 4]), __uint_as_float(ov[8 * q + 5]));
-          u.w = pack_bf16x2(__uint_as_float(ov[8 * q + 6]), __uint_as_float(ov[8 * q + 7]));
-          k.x = pack_bf16x2(__uint_as_float(ok_[8 * q]) * a.scale, __uint_as_float(ok_[8 * q + 1]) * a.scale);
-          k.y = pack_bf16x2(__uint_as_float(ok_[8 * q + 2]) * a.scale, __uint_as_float(ok_[8 * q + 3]) * a.scale);
-          k.z = pack_bf16x2(__uint_as_float(ok_[8 * q + 4]) * a.scale, __uint_as_float(ok_[8 * q + 5]) * a.scale);
-          k.w = pack_bf16x2(__uint_as_float(ok_[8 * q + 6]) * a.scale, __uint_as_float(ok_[8 * q + 7]) * a.scale);
-          *reinterpret_cast<uint4*>(dvd + 8 * q) = u;
-          *reinterpret_cast<uint4*>(dkd + 8 * q) = k;
+      for (int q = 0; q < 4; ++q) {
+        uint4 u, k;
+        u.x = pack_bf16x2(__uint_as_float(ov[8 * q]), __uint_as_float(ov[8 * q + 1]));
+        u.y = pack_bf16x2(__uint_as_float(ov[8 * q + 2]), __uint_as_float(ov[8 * q + 3]));
+        u.z = pack_bf16x2(__uint_as_float(ov[8 * q + 4]), __uint_as_float(ov[8 * q + 5]));
+        u.w = pack_bf16x2(__uint_as_float(ov[8 * q + 6]), __uint_as_float(ov[8 * q + 7]));
+        k.x = pack_bf16x2(__uint_as_float(ok_[8 * q]) * a.scale, __uint_as_float(ok_[8 * q + 1]) * a.scale);
+        k.y = pack_bf16x2(__uint_as_float(ok_[8 * q + 2]) * a.scale, __uint_as_float(ok_[8 * q + 3]) * a.scale);
+        k.z = pack_bf16x2(__uint_as_float(ok_[8 * q + 4]) * a.scale, __uint_as_float(ok_[8 * q + 5]) * a.scale);
+        k.w = pack_bf16x2(__uint_as_float(ok_[8 * q + 6]) * a.scale, __uint_as_float(ok_[8 * q + 7]) * a.scale);
+        st_swizzled(vst, r, half * 4 + q, u);
+        st_swizzled(kst, r, half * 4 + q, k);
+      }
+      fence_async_smem();
+      warp_arrive(b_stg);
+      if (warp == 4) {
+        if (!warp_wait(b_stg, (uint32_t)it & 1u, abort_flag, p.status)) break;
+        if (lane == 0) {
+          bw_store(&tmdK, p.swap_q, kst, kt * AT_B, h, b);
+          bw_store(&tmdV, p.swap_q, vst, kt * AT_B, h, b);
+          bulk_commit();
         }
+        pend = ks;
       }
     }
+    if (warp == 4 && lane == 0 && pend >= 0) bulk_wait_all();  // the last item's stores are out
   }
   __syncwarp();
   tc_fence_before();
@@ -1117,16 +1174,17 @@ int attn_bwd_tc(const AttnArgs& a, cudaStream_t s) {
   p.poison = test_poison();
   AttnArgs ao = a;  // dO shares the o strides
   ao.st = a.ost; ao.sh = a.osh; ao.sb = a.osb;
-  CUtensorMap tq, tk, tv, tdo, to;
+  CUtensorMap tq, tk, tv, tdo, to, tdk, tdv, tdq;
   if (!make_head_map(&tq, a.q, a, p.swap_q) || !make_head_map(&tk, a.k, a, p.swap_q) ||
       !make_head_map(&tv, a.v, a, p.swap_q) || !make_head_map(&tdo, a.dO, ao, p.swap_o) ||
-      !make_head_map(&to, a.o, ao, p.swap_o))
+      !make_head_map(&to, a.o, ao, p.swap_o) || !make_head_map(&tdk, a.dk, a, p.swap_q) ||
+      !make_head_map(&tdv, a.dv, a, p.swap_q) || !make_head_map(&tdq, a.dq, a, p.swap_q))
     return (int)cudaErrorInvalidValue;
   const long long items = (long long)p.nq * a.B * a.H;
   const int grid = (int)(items < num_sms() ? items : num_sms());
   // dQ first: it also writes D = rowsum(dO * O), which the dK/dV kernel reads
-  launch_k(k_attn_bwd_dq_tc, grid, BW_THREADS, DQ_SMEM, s, tq, tk, tv, tdo, to, p);
-  launch_k(k_attn_bwd_dkdv_tc, grid, BW_THREADS, DK_SMEM, s, tq, tk, tv, tdo, p);
+  launch_k(k_attn_bwd_dq_tc, grid, BW_THREADS, DQ_SMEM, s, tq, tk, tv, tdo, to, tdq, p);
+  launch_k(k_attn_bwd_dkdv_tc, grid, BW_THREADS, DK_SMEM, s, tq, tk, tv, tdo, tdk, tdv, p);
   return (int)cudaGetLastError();
 }
 
