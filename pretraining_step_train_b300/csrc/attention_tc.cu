@@ -43,7 +43,7 @@ constexpr int AT_TMEM_COLS = 512;
 constexpr int FW_STAGES = 4;
 constexpr int FW_Q = 0, FW_KV = 4 * AT_TILE;  // Q set q: tile t at FW_Q + (2 q + t) TILE; stage s: K at FW_KV + 2 s TILE, V after
 constexpr int FW_BAR = FW_KV + 2 * FW_STAGES * AT_TILE;
-constexpr int FW_NBARS = 4 + 2 * FW_STAGES + 8 + 1;
+constexpr int FW_NBARS = 4 + 2 * FW_STAGES + 8 + 1 + 2;
 constexpr int AT_SMEM = 1024 + FW_BAR + 8 * (FW_NBARS + 2);
 constexpr uint32_t FW_S_COL = 0, FW_O_COL = 256, FW_P_COL = 384;
 constexpr int FW_REGS_LAUNCH = 168, FW_REGS_CTRL = 56, FW_REGS_SOFTMAX = 216;
@@ -54,7 +54,8 @@ struct AtParams {
   AttnArgs a;
   int nq;        // query tiles per (batch, head)
   int nqp;       // query-tile pairs per (batch, head): ceil(nq / 2)
-  int swap_ht;   // tensor maps index (d, h, t, b) instead of (d, t, h, b)
+  int swap_ht;   // the q / k / v tensor maps index (d, h, t, b) instead of (d, t, h, b)
+  int swap_o;    // the same for the o tensor map
   float c2;      // scale * log2(e)
   uint32_t idesc_s, idesc_pv;
   unsigned* status;
@@ -100,9 +101,18 @@ __device__ __forceinline__ float row_max128(const float* v) {
   return max3(m[0], m[1], fmaxf(m[2], m[3]));
 }
 
+// Stores 16-byte piece c (0..7) of row r of a [128 x 128 B] tile with the 128B swizzle
+// (piece c of row r sits at r * 128 + ((c ^ (r & 7)) << 4)), as TMA reads and writes it.
+__device__ __forceinline__ void st_swizzled(uint32_t tile, int r, int c, uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(tile + (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4))),
+               "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
 __global__ void __launch_bounds__(AT_THREADS, 1)
     k_attn_fwd_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV, const AtParams p) {
+              const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+              const AtParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -111,7 +121,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   // pv_done[2] (per query tile), done
   const uint32_t b_qf = smem_u32(bars), b_qe = b_qf + 16, b_kvf = b_qe + 16, b_kve = b_kvf + 8 * FW_STAGES;
   const uint32_t b_sf = b_kve + 8 * FW_STAGES, b_se = b_sf + 16, b_pf = b_se + 16, b_pv = b_pf + 16;
-  const uint32_t b_done = b_pv + 16;
+  const uint32_t b_done = b_pv + 16, b_stg = b_done + 8;  // staged[2]: a tile's O rows are in shared memory
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bars + FW_NBARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + FW_NBARS + 1);
 
@@ -126,7 +136,10 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int q = 0; q < 2; ++q) {
       mbar_init(b_qf + 8 * q, 1);
-      mbar_init(b_qe + 8 * q, 2);  // one commit per query tile's issuer
+      // per query tile: its issuer's commit after the item's last S and the thread whose
+      // tensor store of the tile's O has read the Q tile (both doubled for tile 0 when the
+      // item has no tile 1)
+      mbar_init(b_qe + 8 * q, 4);
     }
     for (int i = 0; i < FW_STAGES; ++i) {
       mbar_init(b_kvf + 8 * i, 1);
@@ -139,6 +152,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       mbar_init(b_pv + 8 * t, 1);
     }
     mbar_init(b_done, 2);  // one commit per issuer
+    for (int t = 0; t < 2; ++t) mbar_init(b_stg + 8 * t, 4);  // one arrival per softmax warp of the tile
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -279,10 +293,14 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     const float2 c2 = make_float2(p.c2, p.c2);
     bool ok = true;
     int n_s = 0, n_pv = 0;  // S tiles read and PV MMAs waited for, by this tile's warps
-    for (int w = blockIdx.x; ok && w < nitems; w += gridDim.x) {
+    int n_it = 0;           // items of this tile so far
+    int pend = -1, pend_n = 0;  // quad-0 warp: the Q set whose O store is in flight, arrivals owed
+    for (int w = blockIdx.x, it = 0; ok && w < nitems; w += gridDim.x, ++it) {
       const int qp = p.nqp - 1 - w / BH, bh = w % BH, b = bh / a.H, h = bh % a.H;
       const int qt = 2 * qp + t;
       if (qt >= p.nq) continue;  // this item has no second tile
+      const bool has1 = 2 * qp + 1 < p.nq;
+      const int qs = it & 1;
       const int nk = qt + 1;
       const int qi = qt * AT_B + r;
       float m = -INFINITY, l = 0.f;
@@ -301,6 +319,13 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         tc_fence_before();
         warp_arrive(b_set);  // this warp is done reading S_t
         ++n_s;
+        if (quad == 0 && pend >= 0) {  // the previous item's O store has long finished reading its Q tile
+          if (lane == 0) {
+            bulk_wait_read<0>();
+            for (int i = 0; i < pend_n; ++i) mbar_arrive(b_qe + 8 * pend);
+          }
+          pend = -1;
+        }
         const bool diag = j == qt;
         if (diag) {  // keys after the query are masked
           const int kmax = qi - j * AT_B;  // key offsets > kmax are masked
@@ -362,21 +387,36 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       tmem_ld32(lane_base + o_col + 32, *reinterpret_cast<uint32_t(*)[32]>(o + 32));
       tmem_ld_wait();
       tc_fence_before();  // the next item's first PV overwrites O after this read
-      if (qi < a.T) {
-        const float inv = 1.0f / l;
-        bf16* dst = static_cast<bf16*>(a.o) + (long long)b * a.osb + (long long)h * a.osh + (long long)qi * a.ost;
+      // O / l rows go into this tile's Q tile, which no product reads any more (the tile's
+      // last S completed before it was read); one thread writes the tile out with a tensor
+      // store (rows past T are not written)
+      const float inv = 1.0f / l;
+      const uint32_t ost = sbase + FW_Q + (2 * qs + t) * AT_TILE;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          uint4 u;
-          u.x = pack_bf16x2(__uint_as_float(o[8 * q]) * inv, __uint_as_float(o[8 * q + 1]) * inv);
-          u.y = pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv);
-          u.z = pack_bf16x2(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv);
-          u.w = pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv);
-          *reinterpret_cast<uint4*>(dst + 8 * q) = u;
-        }
-        a.lse[(long long)bh * a.T + qi] = (m + __log2f(l)) * 0.6931471805599453f;
+      for (int q = 0; q < 8; ++q) {
+        uint4 u;
+        u.x = pack_bf16x2(__uint_as_float(o[8 * q]) * inv, __uint_as_float(o[8 * q + 1]) * inv);
+        u.y = pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv);
+        u.z = pack_bf16x2(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv);
+        u.w = pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv);
+        st_swizzled(ost, r, q, u);
       }
+      fence_async_smem();
+      warp_arrive(b_stg + 8 * t);
+      if (qi < a.T) a.lse[(long long)bh * a.T + qi] = (m + __log2f(l)) * 0.6931471805599453f;
+      if (quad == 0) {
+        if (!warp_wait(b_stg + 8 * t, (uint32_t)n_it & 1u, abort_flag, p.status)) break;
+        if (lane == 0) {
+          if (p.swap_o) tma_store_4d(&tmO, ost, 0, h, qt * AT_B, b);
+          else tma_store_4d(&tmO, ost, 0, qt * AT_B, h, b);
+          bulk_commit();
+        }
+        pend = qs;
+        pend_n = has1 ? 1 : 2;
+      }
+      ++n_it;
     }
+    if (quad == 0 && lane == 0 && pend >= 0) bulk_wait_all();  // the last item's store is out
   }
   __syncwarp();
   tc_fence_before();
@@ -438,13 +478,6 @@ __device__ __forceinline__ void bw_load(const CUtensorMap* tm, int swap, uint32_
 __device__ __forceinline__ void bw_store(const CUtensorMap* tm, int swap, uint32_t src, int t0, int h, int b) {
   if (swap) tma_store_4d(tm, src, 0, h, t0, b);
   else tma_store_4d(tm, src, 0, t0, h, b);
-}
-// Stores 16-byte piece c (0..7) of row r of a [128 x 128 B] tile with the 128B swizzle
-// (piece c of row r sits at r * 128 + ((c ^ (r & 7)) << 4)), as TMA reads and writes it.
-__device__ __forceinline__ void st_swizzled(uint32_t tile, int r, int c, uint4 v) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(tile + (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4))),
-               "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-               : "memory");
 }
 
 // ------------------------------------------------------------------ dQ
@@ -1135,18 +1168,21 @@ int attn_fwd_tc(const AttnArgs& a, cudaStream_t s) {
   p.nq = (a.T + AT_B - 1) / AT_B;
   p.nqp = (p.nq + 1) / 2;
   p.swap_ht = a.sh < a.st ? 1 : 0;
+  p.swap_o = a.osh < a.ost ? 1 : 0;
   p.c2 = a.scale * 1.4426950408889634f;
   p.idesc_s = mma_idesc(AT_B, 0);
   p.idesc_pv = mma_idesc(AT_D, 1);
   p.status = a.status;
   p.poison = test_poison();
-  CUtensorMap tq, tk, tv;
+  AttnArgs ao = a;  // o has its own strides
+  ao.st = a.ost; ao.sh = a.osh; ao.sb = a.osb;
+  CUtensorMap tq, tk, tv, to;
   if (!make_head_map(&tq, a.q, a, p.swap_ht) || !make_head_map(&tk, a.k, a, p.swap_ht) ||
-      !make_head_map(&tv, a.v, a, p.swap_ht))
+      !make_head_map(&tv, a.v, a, p.swap_ht) || !make_head_map(&to, a.o, ao, p.swap_o))
     return (int)cudaErrorInvalidValue;
   const long long items = (long long)p.nqp * a.B * a.H;
   const int grid = (int)(items < num_sms() ? items : num_sms());
-  launch_k(k_attn_fwd_tc, grid, AT_THREADS, AT_SMEM, s, tq, tk, tv, p);
+  launch_k(k_attn_fwd_tc, grid, AT_THREADS, AT_SMEM, s, tq, tk, tv, to, p);
   return (int)cudaGetLastError();
 }
 
