@@ -11,10 +11,11 @@
 //   warp 1      owns 512 TMEM columns: per query tile t an S buffer (128 fp32
 //               columns), the O accumulator (64) and a P buffer (64 columns of
 //               bf16 pairs);
-//   warps 1, 2  one MMA issuer per query tile t: S_t = Q_t K_j^T (M=128, N=128,
-//               K=64) and O_t += P_t V_j (M=128, N=64, K=128, A from TMEM), each
-//               issued the moment its own tile's inputs are ready, so the tensor
-//               core works on one tile while the softmax warps work on the other;
+//   warps 1, 2  MMA issuers: warp 1 issues S_t = Q_t K_j^T (M=128, N=128, K=64) for
+//               both query tiles, warp 2 O_t += P_t V_j (M=128, N=64, K=128, A from
+//               TMEM); each product goes as soon as its own inputs are ready, and an S
+//               never waits behind PV issue, so the tensor core works on one tile's
+//               products while the softmax warps work on the other's;
 //   warps 4-7   softmax of query tile 0, warps 8-11 of tile 1 (warp 3 idles): each
 //               thread owns one query row (lane quadrant = warp % 4) and all 128
 //               keys of a tile, so the row max and sum stay in the thread; p =
@@ -46,7 +47,7 @@ constexpr int FW_BAR = FW_KV + 2 * FW_STAGES * AT_TILE;
 constexpr int FW_NBARS = 4 + 2 * FW_STAGES + 8 + 1 + 2;
 constexpr int AT_SMEM = 1024 + FW_BAR + 8 * (FW_NBARS + 2);
 constexpr uint32_t FW_S_COL = 0, FW_O_COL = 256, FW_P_COL = 384;
-constexpr int FW_REGS_LAUNCH = 168, FW_REGS_CTRL = 56, FW_REGS_SOFTMAX = 216;
+constexpr int FW_REGS_LAUNCH = 168, FW_REGS_CTRL = 64, FW_REGS_SOFTMAX = 216;
 static_assert(128 * FW_REGS_CTRL + 256 * FW_REGS_SOFTMAX <= AT_THREADS * FW_REGS_LAUNCH,
               "the register split must fit in the launch's registers");
 
@@ -136,14 +137,14 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int q = 0; q < 2; ++q) {
       mbar_init(b_qf + 8 * q, 1);
-      // per query tile: its issuer's commit after the item's last S and the thread whose
-      // tensor store of the tile's O has read the Q tile (both doubled for tile 0 when the
-      // item has no tile 1)
-      mbar_init(b_qe + 8 * q, 4);
+      // the S issuer's commit after the item's last S, and per query tile the thread whose
+      // tensor store of the tile's O has read its Q tile (tile 0's twice when the item has no
+      // tile 1)
+      mbar_init(b_qe + 8 * q, 3);
     }
     for (int i = 0; i < FW_STAGES; ++i) {
       mbar_init(b_kvf + 8 * i, 1);
-      mbar_init(b_kve + 8 * i, 2);
+      mbar_init(b_kve + 8 * i, 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(b_sf + 8 * t, 1);
@@ -166,8 +167,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // registers: 384 threads x 168 at launch = 64512; warps 0-3 keep 56, the softmax
-  // warpgroups take 216 (128 x 56 + 256 x 216 = 62464)
+  // registers: 384 threads x 168 at launch = 64512; warps 0-3 keep 64, the softmax
+  // warpgroups take 216 (128 x 64 + 256 x 216 = 63488)
   if (warp < 4) {
     regs_lower<FW_REGS_CTRL>();
     if (warp == 0) {
@@ -209,75 +210,87 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         for (int i = 0; i < FW_STAGES; ++i)
           if (last_par[i] >= 0) mbar_wait_drain(b_kvf + 8 * i, (uint32_t)last_par[i]);
       }
-    } else if (warp == 1 || warp == 2) {
+    } else if (warp == 1) {
       if (lane == 0) {
-        // ---------------- MMA issuer of query tile t = warp - 1
-        // A tile's products come in a fixed order: S_t(0), then per key tile j, S_t(j+1)
-        // once K_{j+1} has landed and the tile's warps have read S_t(j), and PV_t(j) once
-        // they have written P_t(j).  One issuer per tile blocks on exactly the next event of
-        // its own tile, so neither tile's products wait behind the other tile's events and
-        // no thread polls (a polling thread runs several times slower beside the softmax
-        // warps that share its scheduler).
-        // Releases: the Q set takes one commit per tile after the item's last S, a K/V stage
-        // one per tile after its PV; a tile that does not use a stage, or is absent from the
-        // item, is stood in for by a second commit of the other tile's issuer.
-        const int t = warp - 1;
-        const uint32_t b_sft = b_sf + 8 * t, b_set = b_se + 8 * t, b_pft = b_pf + 8 * t, b_pvt = b_pv + 8 * t;
-        const uint32_t s_acc = tmem + FW_S_COL + 128 * t, o_acc = tmem + FW_O_COL + 64 * t;
-        const uint32_t p_op = tmem + FW_P_COL + 64 * t;
-        int cnt_s = 0, cnt_pv = 0;  // S and PV products issued by this thread, all items
+        // ---------------- S issuer: S_t(j) = Q_t K_j^T for both query tiles, in the order
+        // S_0(0), S_1(0), S_0(1), S_1(1), ...; S_t(j) once K_j has landed and tile t's
+        // warps have read S_t(j-1).  The PV products come from another thread: an MMA issue
+        // blocks while the tensor core is busy, and S_t(j+1) must not sit behind the PV
+        // issue of the previous key tile (its tile would wait for it).
+        int cnt_s[2] = {0, 0};  // S products issued per tile, all items
         bool ok = true;
         int g = 0;  // ring position of the item's key tile 0
         for (int w = blockIdx.x, it = 0; ok && w < nitems; w += gridDim.x, ++it) {
-          const int qp = p.nqp - 1 - w / BH;
-          const int qt0 = 2 * qp;
+          const int qt0 = 2 * (p.nqp - 1 - w / BH);
           const bool has1 = qt0 + 1 < p.nq;
-          const int nk_item = qt0 + (has1 ? 2 : 1);
-          const int qt = qt0 + t;
-          if (qt >= p.nq) {  // this item has no second tile
-            g += nk_item;
-            continue;
-          }
-          const int nk = qt + 1;
+          const int nk_item = qt0 + (has1 ? 2 : 1);  // tile t uses key tiles 0 .. qt0 + t
           const int qs = it & 1;
-          const uint32_t qd = sbase + FW_Q + (2 * qs + t) * AT_TILE;
           if (!mbar_wait(b_qf + 8 * qs, (uint32_t)(it >> 1) & 1u, abort_flag, p.status)) break;
-          auto issue_s = [&](int j) -> bool {
+          for (int j = 0; ok && j < nk_item; ++j) {
             const int st = (g + j) % FW_STAGES;
-            if (!mbar_wait(b_kvf + 8 * st, (uint32_t)((g + j) / FW_STAGES) & 1u, abort_flag, p.status)) return false;
-            if (cnt_s > 0 && !mbar_wait(b_set, (uint32_t)(cnt_s - 1) & 1u, abort_flag, p.status)) return false;
-            tc_fence_after();
-            const uint32_t kd = sbase + FW_KV + st * 2 * AT_TILE;
-  #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              mma_bf16(s_acc, operand_desc(qd, 0, k), operand_desc(kd, 0, k), p.idesc_s, k > 0 ? 1u : 0u);
-            mma_commit(b_sft);
-            ++cnt_s;
-            if (j == nk - 1) {  // this tile no longer reads the item's Q set
-              mma_commit(b_qe + 8 * qs);
-              if (!has1) mma_commit(b_qe + 8 * qs);
+            if (!mbar_wait(b_kvf + 8 * st, (uint32_t)((g + j) / FW_STAGES) & 1u, abort_flag, p.status)) {
+              ok = false;
+              break;
             }
-            return true;
-          };
-          if (!issue_s(0)) { ok = false; break; }
-          for (int j = 0; j < nk; ++j) {
-            if (j + 1 < nk && !issue_s(j + 1)) { ok = false; break; }
-            if (!mbar_wait(b_pft, (uint32_t)cnt_pv & 1u, abort_flag, p.status)) { ok = false; break; }
-            tc_fence_after();
-            const int st = (g + j) % FW_STAGES;
-            const uint32_t vd = sbase + FW_KV + st * 2 * AT_TILE + AT_TILE;
-            // A = P_t in TMEM: 16 keys per MMA = 8 columns of bf16 pairs
-  #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              mma_bf16_tmem_a(o_acc, p_op + kk * 8, operand_desc(vd, 1, kk), p.idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
-            mma_commit(b_pvt);
-            ++cnt_pv;
-            mma_commit(b_kve + 8 * st);
-            if (!has1 || (t == 1 && j == nk - 1)) mma_commit(b_kve + 8 * st);
+            const uint32_t kd = sbase + FW_KV + st * 2 * AT_TILE;
+            for (int t = 0; t < 2; ++t) {
+              if (j > qt0 + t || (t == 1 && !has1)) continue;
+              if (cnt_s[t] > 0 && !mbar_wait(b_se + 8 * t, (uint32_t)(cnt_s[t] - 1) & 1u, abort_flag, p.status)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint32_t qd = sbase + FW_Q + (2 * qs + t) * AT_TILE;
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                mma_bf16(tmem + FW_S_COL + 128 * t, operand_desc(qd, 0, k), operand_desc(kd, 0, k), p.idesc_s,
+                         k > 0 ? 1u : 0u);
+              mma_commit(b_sf + 8 * t);
+              ++cnt_s[t];
+            }
           }
+          if (ok) mma_commit(b_qe + 8 * qs);  // no product reads the item's Q set any more
           g += nk_item;
         }
         // every product issued by either issuer has completed once b_done flips
+        mma_commit(b_done);
+        mbar_wait_drain(b_done, 0);
+      }
+    } else if (warp == 2) {
+      if (lane == 0) {
+        // ---------------- PV issuer: O_t += P_t(j) V_j once tile t's warps have written
+        // P_t(j), in the order PV_0(0), PV_1(0), PV_0(1), ...  After key tile j's last PV its
+        // commit releases K_j / V_j's ring stage (the S products that read K_j were complete
+        // before any P_t(j) could be formed).
+        int cnt_pv[2] = {0, 0};  // PV products issued per tile, all items
+        bool ok = true;
+        int g = 0;
+        for (int w = blockIdx.x; ok && w < nitems; w += gridDim.x) {
+          const int qt0 = 2 * (p.nqp - 1 - w / BH);
+          const bool has1 = qt0 + 1 < p.nq;
+          const int nk_item = qt0 + (has1 ? 2 : 1);
+          for (int j = 0; ok && j < nk_item; ++j) {
+            const int st = (g + j) % FW_STAGES;
+            const uint32_t vd = sbase + FW_KV + st * 2 * AT_TILE + AT_TILE;
+            for (int t = 0; t < 2; ++t) {
+              if (j > qt0 + t || (t == 1 && !has1)) continue;
+              if (!mbar_wait(b_pf + 8 * t, (uint32_t)cnt_pv[t] & 1u, abort_flag, p.status)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              // A = P_t in TMEM: 16 keys per MMA = 8 columns of bf16 pairs
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk)
+                mma_bf16_tmem_a(tmem + FW_O_COL + 64 * t, tmem + FW_P_COL + 64 * t + kk * 8,
+                                operand_desc(vd, 1, kk), p.idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+              mma_commit(b_pv + 8 * t);
+              ++cnt_pv[t];
+            }
+            if (ok) mma_commit(b_kve + 8 * st);
+          }
+          g += nk_item;
+        }
         mma_commit(b_done);
         mbar_wait_drain(b_done, 0);
       }
