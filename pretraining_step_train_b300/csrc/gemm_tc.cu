@@ -9,9 +9,9 @@
 // Structure: persistent clusters of two CTAs (a CTA pair on two SMs), 18 warps
 // each; a pair computes 256 x 256 output tiles with the pair MMA (cta_group::2):
 //   warp 0      TMA producer of each CTA: its 128 rows of A and its 128 rows of
-//               B (half of the tile's 256 N columns), 128B-swizzled 64-deep k
-//               blocks, into a 6-stage shared-memory ring; both CTAs' copies
-//               complete on the even CTA's barrier of that stage;
+//               B (half of the tile's 256 N columns), 128-deep k blocks as two
+//               128B-swizzled 64-deep slabs, into a 3-stage shared-memory ring;
+//               both CTAs' copies complete on the even CTA's barrier of that stage;
 //   warp 1      of each CTA allocates 512 TMEM columns (two 128 x 256 fp32
 //               accumulators per CTA) together with its peer; one thread of the
 //               even CTA issues tcgen05.mma.cta_group::2 (M=256, N=256, K=16) per
@@ -29,7 +29,7 @@
 //               of the matching 32 x 16 box, one chunk ahead.  Sixteen warps
 //               (four per SM sub-partition) hide the epilogue's latencies.
 // The accumulator double buffer lets the epilogue of tile i overlap the
-// mainloop of tile i+1.  Per k block each SM stages 32 KB of operands for a
+// mainloop of tile i+1.  Per 64 of K each SM stages 32 KB of operands for a
 // 128 x 256 x 64 share of the MMA (a single-CTA 128 x 256 tile stages 48 KB), so
 // the operand traffic through L2, TMA and shared memory per flop is a third lower.
 // Every wait is bounded (about 2 s of %globaltimer); on expiry the CTA latches
@@ -48,9 +48,15 @@ constexpr int BM = 128;       // accumulator rows per CTA
 constexpr int PM = 2 * BM;     // rows of a pair tile
 constexpr int BN = 256;        // columns of a tile (the pair MMA's N)
 constexpr int BNC = BN / 2;    // B rows (output columns) each CTA stages
-constexpr int BK = 64, STAGES = 6;
-constexpr int A_TILE = BM * BK * 2;   // 16 KB
-constexpr int B_TILE = BNC * BK * 2;  // 16 KB
+// A stage holds a 128-deep k block as two 64-deep slabs (the 128B swizzle's width) per
+// operand: one wait and one commit of the MMA thread per 8 MMAs.  Its control path runs
+// beside 16 busy epilogue warps and costs about 300 cycles per wait / commit round, a
+// third of the time at 64-deep stages (512 cycles of MMAs).
+constexpr int KS = 64, SLABS = 2, BK = KS * SLABS, STAGES = 3;
+constexpr int A_SLAB = BM * KS * 2;   // 16 KB
+constexpr int B_SLAB = BNC * KS * 2;  // 16 KB
+constexpr int A_TILE = SLABS * A_SLAB;
+constexpr int B_TILE = SLABS * B_SLAB;
 constexpr int STAGE_BYTES = A_TILE + B_TILE;
 constexpr int RING_BYTES = STAGES * STAGE_BYTES;
 constexpr int TMEM_COLS = 2 * BN;
@@ -378,21 +384,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // cycles per k block).  The odd CTA's copies may complete on that barrier before
             // the arrive; the phase cannot complete while the arrive is pending.
             if (rank == 0) mbar_expect_tx(b_full + 8 * stage, 2 * STAGE_BYTES);
-            if (!g.a_mn) {
-              tma_load_2d_pair(sa, &tmA, fb, kb * BK, m0);
-            } else if (p.a3d) {
-              tma_load_3d_pair(sa, &tmA, fb, 0, kb * BK, m0 / 64);
-            } else {
-              tma_load_2d_pair(sa, &tmA, fb, m0, kb * BK);
-              tma_load_2d_pair(sa + 8192, &tmA, fb, m0 + 64, kb * BK);
-            }
-            if (!g.b_mn) {
-              tma_load_2d_pair(sb, &tmB, fb, kb * BK, n0);
-            } else if (p.b3d) {
-              tma_load_3d_pair(sb, &tmB, fb, 0, kb * BK, n0 / 64);
-            } else {
-              tma_load_2d_pair(sb, &tmB, fb, n0, kb * BK);
-              tma_load_2d_pair(sb + 8192, &tmB, fb, n0 + 64, kb * BK);
+            // each 64-deep slab lands in its own region; a slab past K reads zeros
+            #pragma unroll
+            for (int sl = 0; sl < SLABS; ++sl) {
+              const int kk = kb * BK + sl * KS;
+              const uint32_t da = sa + sl * A_SLAB, db = sb + sl * B_SLAB;
+              if (!g.a_mn) {
+                tma_load_2d_pair(da, &tmA, fb, kk, m0);
+              } else if (p.a3d) {
+                tma_load_3d_pair(da, &tmA, fb, 0, kk, m0 / 64);
+              } else {
+                tma_load_2d_pair(da, &tmA, fb, m0, kk);
+                tma_load_2d_pair(da + 8192, &tmA, fb, m0 + 64, kk);
+              }
+              if (!g.b_mn) {
+                tma_load_2d_pair(db, &tmB, fb, kk, n0);
+              } else if (p.b3d) {
+                tma_load_3d_pair(db, &tmB, fb, 0, kk, n0 / 64);
+              } else {
+                tma_load_2d_pair(db, &tmB, fb, n0, kk);
+                tma_load_2d_pair(db + 8192, &tmB, fb, n0 + 64, kk);
+              }
             }
             last_par[stage] = (int)phase;
           }
@@ -431,8 +443,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t sa = s_tiles + stage * STAGE_BYTES, sb = sa + A_TILE;
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
-            mma_bf16_pair(d_tmem, operand_desc(sa, g.a_mn, k), operand_desc(sb, g.b_mn, k), p.idesc,
-                          (kb > kb0 || k > 0) ? 1u : 0u);
+            const int sl = k / (KS / 16), ks = k % (KS / 16);
+            mma_bf16_pair(d_tmem, operand_desc(sa + sl * A_SLAB, g.a_mn, ks), operand_desc(sb + sl * B_SLAB, g.b_mn, ks),
+                          p.idesc, (kb > kb0 || k > 0) ? 1u : 0u);
           }
           mma_commit_pair_mc(b_empty + 8 * stage, 3);  // the stage is free again in both CTAs
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -939,7 +952,7 @@ int gemm_tc_pick_splits(int M, int N, int K, int sms) {  // sms: CTA pairs
   double best_score = -1.0;
   for (int s = 1; s <= 16; ++s) {
     const int kps = (total_kb + s - 1) / s;
-    if (s > 1 && kps < 4) break;
+    if (s > 1 && kps * BK < 256) break;  // at least 256 of K per split
     const int work = tiles * s;
     const int waves = (work + sms - 1) / sms;
     const double eff = (double)work / ((double)waves * sms);
@@ -960,8 +973,8 @@ int gemm_tc_effective_splits(int K, int splits) {
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 // Schedule for T pair tiles of Kb k blocks on G CTA pairs (GEMM_TC_STREAM_K):
-//  - T >= G, last wave part-empty by more than 3%, tiles at least 32 k blocks
-//    deep: SK_STREAM over the leftover tiles (whole waves stay data-parallel).
+//  - T >= G, last wave part-empty by more than 3%, tiles at least 2048 deep in
+//    K: SK_STREAM over the leftover tiles (whole waves stay data-parallel).
 //    Shallower tiles are epilogue-bound; cutting them adds epilogues, not speed.
 //  - T < G: s = the split count of gemm_tc_pick_splits.  Two splits: SK_SPLIT
 //    (the second split adds the first's sums).  More: the finishing CTAs would
@@ -979,7 +992,7 @@ static int sk_plan(const GemmArgs& g, int T, int Kb, int G, bool force, int& dp,
     return SK_STREAM;
   }
   if (T >= G) {
-    if (rem == 0 || Kb < 32) return SK_NONE;
+    if (rem == 0 || Kb * BK < 2048) return SK_NONE;
     const double eff = (double)T / ((double)(T / G + 1) * G);
     if (eff >= 0.97) return SK_NONE;
     dp = T - rem;
