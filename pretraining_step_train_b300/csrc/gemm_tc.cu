@@ -430,6 +430,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t phase = 0;
       int abuf = 0;
       uint32_t aphase = 0;
+      // Descriptors of stage 0's first k step; another stage, slab or k step only moves the
+      // start address (bits 0-13, in 16-byte units, no carry for shared-memory offsets).
+      const uint64_t da0 = operand_desc(s_tiles, g.a_mn, 0), db0 = operand_desc(s_tiles + A_TILE, g.b_mn, 0);
+      const uint32_t ka = g.a_mn ? 2048 : 32, kb16 = g.b_mn ? 2048 : 32;  // bytes per 16-wide k step
       Unit w;
       for (int u = 0; cta_unit(p, u, w); ++u) {
         const int kb0 = w.kb0, kb1 = w.kb1;
@@ -438,13 +442,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t d_tmem = tmem_base + abuf * BN;
         bool stop = false;
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait(b_full + 8 * stage, phase, abort_flag, p.status)) { stop = true; break; }
+          // a non-blocking probe first: the stage is usually full already
+          if (!mbar_test(b_full + 8 * stage, phase) && !mbar_wait(b_full + 8 * stage, phase, abort_flag, p.status)) {
+            stop = true;
+            break;
+          }
           tc_fence_after();
-          const uint32_t sa = s_tiles + stage * STAGE_BYTES, sb = sa + A_TILE;
-#pragma unroll
+          const uint64_t so = (uint64_t)((stage * STAGE_BYTES) >> 4);
+          #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
             const int sl = k / (KS / 16), ks = k % (KS / 16);
-            mma_bf16_pair(d_tmem, operand_desc(sa + sl * A_SLAB, g.a_mn, ks), operand_desc(sb + sl * B_SLAB, g.b_mn, ks),
+            mma_bf16_pair(d_tmem, da0 + so + ((sl * A_SLAB + ks * ka) >> 4), db0 + so + ((sl * B_SLAB + ks * kb16) >> 4),
                           p.idesc, (kb > kb0 || k > 0) ? 1u : 0u);
           }
           mma_commit_pair_mc(b_empty + 8 * stage, 3);  // the stage is free again in both CTAs
