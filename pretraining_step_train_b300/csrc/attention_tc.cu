@@ -39,8 +39,8 @@ constexpr int AT_D = 64;                        // head size
 constexpr int AT_TILE = AT_B * AT_D * 2;        // 16 KB: one [128 x 64] bf16 tile
 constexpr int AT_THREADS = 384;
 constexpr int AT_TMEM_COLS = 512;
-// forward: smem two sets of (Q_0 | Q_1) | K,V ring; TMEM S_t at 128 t, O_t at 256 + 64 t,
-// P_t at 384 + 64 t
+// forward: smem two sets of (Q_0 | Q_1) (a Q_t tile then stages tile t's O for its tensor
+// store) | K,V ring; TMEM S_t at 128 t, O_t at 256 + 64 t, P_t at 384 + 64 t
 constexpr int FW_STAGES = 4;
 constexpr int FW_Q = 0, FW_KV = 4 * AT_TILE;  // Q set q: tile t at FW_Q + (2 q + t) TILE; stage s: K at FW_KV + 2 s TILE, V after
 constexpr int FW_BAR = FW_KV + 2 * FW_STAGES * AT_TILE;
@@ -495,7 +495,8 @@ __device__ __forceinline__ void bw_store(const CUtensorMap* tm, int swap, uint32
 
 // ------------------------------------------------------------------ dQ
 // smem: two sets of Q | dO | O (items alternate, so the next item's tiles load while this one
-// finishes) | K,V ring (4 stages); TMEM: S | dP | dQ | dS double buffer.
+// finishes; a set's Q tile then stages the item's dQ for its tensor store) | K,V ring
+// (4 stages); TMEM: S | dP | dQ | dS double buffer.
 // The compute warps also form D = rowsum(dO * O) for their query rows from the
 // dO and O tiles and store it for the dK/dV kernel, which runs after this one.
 constexpr int DQ_STAGES = 4;
@@ -793,7 +794,8 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
 
 // ------------------------------------------------------------------ dK, dV
 // smem: two sets of K | V (items alternate, so the next item's K and V load while this
-// one finishes) | Q,dO ring (4 stages) | lse2, D ring (4 x 1 KB);
+// one finishes; a set then stages the item's dK | dV for the tensor stores) | Q,dO ring
+// (4 stages) | lse2, D ring (4 x 1 KB);
 // TMEM: S^T | dP^T | dV | dK | P^T | dS^T
 constexpr int DK_STAGES = 4;
 constexpr int DK_K = 0, DK_V = AT_TILE, DK_QD = 4 * AT_TILE, DK_LD = DK_QD + 2 * DK_STAGES * AT_TILE;  // set s: K, V at + 2 s TILE
