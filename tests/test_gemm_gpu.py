@@ -119,8 +119,8 @@ def test_gemm_in_kernel_partials(a_mn, b_mn, M, N, K):
 
 
 @pytest.mark.parametrize("M,N,K,a_mn,b_mn", [
-    (16384, 768, 3072, 0, 1),   # 384 output tiles: two whole waves + 88 tiles cut along K
-    (768, 3072, 16384, 1, 1),   # 72 tiles, two K splits finished in-kernel
+    (16384, 768, 3072, 0, 1),   # 192 pair tiles on 74 pairs: two whole waves + 44 tiles cut along K
+    (768, 3072, 16384, 1, 1),   # 36 pair tiles, two K splits finished in-kernel
 ])
 def test_gemm_stream_k_step_shapes(M, N, K, a_mn, b_mn):
     """The schedule the training step takes (-1) on two of its GEMM shapes: equal to
@@ -178,9 +178,9 @@ def _epilogue_case(seed, M, N, K, a_mn, b_mn, epi, splits):
 
 
 @pytest.mark.parametrize("M,N,K,a_mn,b_mn,splits", [
-    (640, 264, 2112, 0, 0, -2),     # 10 tiles cut along K over all SMs: 2-3 k blocks per CTA, ragged N
+    (640, 264, 2112, 0, 0, -2),     # 6 pair tiles cut along K over all pairs: 1-2 k blocks each, ragged N and K
     (640, 264, 2112, 0, 1, -1),     # fewer tiles than SMs: K splits finished in-kernel
-    (4160, 1280, 2048, 0, 1, -1),   # 165 tiles: one whole wave + a stream-K tail of 17 tiles
+    (4160, 1280, 2048, 0, 1, -1),   # 85 pair tiles: one whole wave + a stream-K tail of 11 tiles
     (300, 520, 200, 0, 0, 1),       # plain schedule, ragged M and K
 ])
 @pytest.mark.parametrize("epi", [1, 2, 3, 4])
