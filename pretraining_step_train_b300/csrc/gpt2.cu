@@ -1,6 +1,6 @@
-// GPT-2 step driver and C ABI (see include/gpt2.h).
+// GPT-2 step sequencing and C ABI (see include/gpt2.h).
 //
-// The driver carves one caller-owned device arena into parameters, AdamW
+// The host code here carves one caller-owned device arena into parameters, AdamW
 // state, every activation the backward pass needs and its scratch, then issues
 // a fixed kernel sequence on the caller's stream.  Nothing is allocated after
 // gpt2_create and no call synchronises unless a host output is requested, so
