@@ -113,8 +113,10 @@ def test_gemm_in_kernel_partials(a_mn, b_mn, M, N, K):
             np.testing.assert_allclose(got, ref, rtol=0, atol=2e-5 * np.sqrt(K) * 4)
         else:
             assert rel_l2(got, ref) < 4e-3
+    # the flags sit in front of the partial-sum slots (three per SM, 128 x 256 fp32 each)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    flags = to_np(ws[:3 * sms * 16 * 4].view(torch.int32))
+    flag_bytes = binding.lib().gemm_bf16_sk_workspace_bytes() - 3 * sms * 128 * 256 * 4
+    flags = to_np(ws[:flag_bytes].view(torch.int32))
     assert not flags.any()
 
 
